@@ -1,0 +1,429 @@
+"""Plain CPU oracle for the FreeToken MoE-layer hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It shares no code,
+tables or constants with the CUDA library, and the library never calls it.
+
+It is written for a reader checking it against the pages, not for speed:
+every decision is a total order written out directly, expert maths runs in
+float64 on decoded weights, and numpy matmul/sort are the only library steps.
+
+Sources (cited by page title and section):
+  [FT]  "FreeToken 完全拆解：带宽自适应执行，让 8GB 笔记本跑 35B、单卡工作站跑 753B 的边缘 MoE 服务系统"
+  [FT2] "개인 장치에서 MoE 모델을 서빙하는 FreeToken" (no section headings; cited by paragraph topic)
+  [P3]  "OSDI'26 | 双路 CPU + 两张 5090，本地跑满血 671B DeepSeek：云端 SLO 是怎么在消费级硬件上达成的"
+
+Readings taken where the pages are silent or garbled (each is listed in the
+design notes with its reason):
+  * q* is rounded half-up, computed in integers over bandwidths in MB/s.
+  * F is the first q misses in ascending logical id; C is the rest.
+  * Hit slots are never victims, so q <= S - |H|.
+  * One global clock ticks once per layer-step; LRU ties break by slot index.
+  * The C set leaves residency and recency untouched.
+  * Router gates are a softmax over the k selected logits; ties pick the lower id.
+  * FP8 blocks are 1x128 along the reduction dimension of each output row.
+  * The output sums, per token, the shared expert first and then the k pair
+    rows in ascending expert id.
+
+Parity unpinned: none of the functions here; the pins live in tests/.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+FT_CPU = -1          # rewritten pair id meaning "evaluated on the host (C set)"
+FP8_BLOCK = 128
+
+
+# ============================================================== q* miss split
+def mbps(gbps: float) -> int:
+    """Bandwidth in GB/s -> integer MB/s, nearest, halves away from zero."""
+    v = gbps * 1000.0
+    return int(math.floor(v + 0.5)) if v >= 0 else -int(math.floor(-v + 0.5))
+
+
+def split_misses(m: int, bp_mbs: int, bh_mbs: int, evictable: int) -> int:
+    """Number q of the m misses to fill over the host link.
+
+    [FT, "q* 策略"]: fills stream at B_P while the host executes the other
+    m-q misses on the residual bandwidth B_H-B_P; equal branch times give
+    q* = m*B_P/B_H.  [FT2, paragraph on the miss split]: the residual is
+    max(B_H-B_P, 0), so with B_H <= B_P every miss is filled.  q* is rounded
+    and at least one fill is kept whenever there is a miss.  The fill count
+    cannot exceed the slots that are not hits of this step (evictable).
+
+    Rounding: half up, i.e. floor(m*bp/bh + 1/2) = (2*m*bp + bh) // (2*bh).
+    """
+    if m <= 0:
+        return 0
+    if bh_mbs <= bp_mbs:
+        q = m
+    else:
+        q = (2 * m * bp_mbs + bh_mbs) // (2 * bh_mbs)
+        q = max(q, 1)
+    return max(0, min(q, m, evictable))
+
+
+# ===================================================================== router
+def route(logits: np.ndarray, k: int):
+    """Top-k router with softmax gates.
+
+    For each token the k experts with the largest logits are chosen (equal
+    logits: the lower expert id first), listed in ascending expert id; the
+    gates are a softmax over those k logits, computed in float64 and stored
+    as float32.  [FT, "Device-side 缓存控制"] (routing precedes dedupe).
+    """
+    B, E = logits.shape
+    sel = np.empty((B, k), dtype=np.int64)
+    gates = np.empty((B, k), dtype=np.float32)
+    ids = np.arange(E)
+    for t in range(B):
+        z = logits[t].astype(np.float64)
+        order = np.lexsort((ids, -z))          # primary: logit desc; secondary: id asc
+        chosen = np.sort(order[:k])
+        zs = z[chosen]
+        w = np.exp(zs - zs.max())
+        sel[t] = chosen
+        gates[t] = (w / w.sum()).astype(np.float32)
+    return sel, gates
+
+
+def dedupe(sel: np.ndarray, layer: int, n_experts: int) -> list[int]:
+    """Sorted unique logical ids u = layer*E + e over the whole batch.
+
+    [FT, "Device-side 缓存控制"]; logical id form from [FT, "FTW 权重格式与平台适配"].
+    """
+    return sorted({layer * n_experts + int(e) for e in sel.reshape(-1)})
+
+
+# ========================================================== slot-pool cache
+@dataclass
+class StepRecord:
+    layer: int
+    clock: int
+    A: list
+    H: list
+    M: list
+    q: int
+    victims: list
+    F: list
+    C: list
+    slot_of_pair: np.ndarray     # [B, k]: slot id, or FT_CPU
+
+
+@dataclass
+class Counters:
+    hits: int = 0
+    misses: int = 0
+    fills: int = 0
+    cpu_execs: int = 0
+    evictions: int = 0
+
+
+class SlotCache:
+    """Global slot-pool LRU shared by every MoE layer.
+
+    [FT, "语义感知专家缓存"]: one LRU residency space for all layers; a hit
+    refreshes recency, a fill admits the newly chosen expert, an eviction
+    removes the expert unused for longest.  [FT2, paragraph on the two-tier
+    memory]: a slot holds every tensor of one (layer, expert).
+
+    State: res[u] = slot holding logical expert u or -1; owner[s] = logical
+    id in slot s or -1; stamp[s] = clock of the last step that used slot s
+    (0 for a slot never used).  One clock for all layers, starting at 0.
+    """
+
+    def __init__(self, n_slots: int, n_logical: int):
+        self.S = int(n_slots)
+        self.res = np.full(n_logical, -1, dtype=np.int64)
+        self.owner = np.full(self.S, -1, dtype=np.int64)
+        self.stamp = np.zeros(self.S, dtype=np.int64)
+        self.clock = 0
+        self.cnt = Counters()
+        self.buffers: list | None = None
+        self.prefill_next_layer: int | None = None
+
+    # -------------------------------------------------------------- decode
+    def lru_candidates(self, K: int) -> list[int]:
+        """One scan for the K least recently used slots that are not hits of
+        this step (stamp < clock), ascending by (stamp, slot).
+
+        [FT, "Device-side 缓存控制"]: a single pass yields K candidates and the
+        miss path consumes the first q <= K of them.
+        """
+        cand = np.nonzero(self.stamp < self.clock)[0]
+        order = np.lexsort((cand, self.stamp[cand]))
+        return [int(s) for s in cand[order[:K]]]
+
+    def decode_step(self, layer: int, n_experts: int, sel: np.ndarray,
+                    bp_mbs: int, bh_mbs: int) -> StepRecord:
+        """Cache decisions of one decode layer-step.
+
+        [FT, "Device-side 缓存控制"]: dedupe -> classify against the residency
+        table -> fill count q -> victims -> rewrite ids to slots or FT_CPU.
+        [FT, "q* 策略"]: F is admitted to the cache; C is executed on the host
+        and leaves residency unchanged.
+        """
+        B, k = sel.shape
+        A = dedupe(sel, layer, n_experts)
+        self.clock += 1
+        H = [u for u in A if self.res[u] >= 0]
+        M = [u for u in A if self.res[u] < 0]
+        for u in H:
+            self.stamp[self.res[u]] = self.clock
+        self.cnt.hits += len(H)
+        self.cnt.misses += len(M)
+        q = split_misses(len(M), bp_mbs, bh_mbs, self.S - len(H))
+        K = min(B * k, n_experts)
+        victims = self.lru_candidates(K) if q > 0 else []
+        for i in range(q):
+            v = victims[i]
+            old = self.owner[v]
+            if old >= 0:
+                self.res[old] = -1
+                self.cnt.evictions += 1
+            self.owner[v] = M[i]
+            self.res[M[i]] = v
+            self.stamp[v] = self.clock
+            self.cnt.fills += 1
+        F, C = M[:q], M[q:]
+        self.cnt.cpu_execs += len(C)
+        slot_of_pair = np.empty((B, k), dtype=np.int64)
+        for t in range(B):
+            for r in range(k):
+                s = self.res[layer * n_experts + int(sel[t, r])]
+                slot_of_pair[t, r] = s if s >= 0 else FT_CPU
+        self.prefill_next_layer = None
+        return StepRecord(layer, self.clock, A, H, M, q, victims, F, C, slot_of_pair)
+
+    # ------------------------------------------------------------- prefill
+    def prefill_layer(self, layer: int, n_experts: int, n_layers: int) -> list[int]:
+        """Residency effect of one prefill layer with full-layer double buffering.
+
+        [FT, "全层双缓冲"] and [FT2, paragraph on the double buffer]: two
+        full-layer buffers are taken from the shared slot pool; layer l is
+        computed from one while layer l+1 streams, whole, into the other.
+        Reading used here: a chunk starts at a call that does not continue the
+        previous prefill layer; it takes the 2E least recently used slots
+        (ascending (stamp, slot)); the first E are buffer 0, the next E buffer
+        1, and their occupants leave the cache.  Layer l goes to buffer
+        (l - first layer) mod 2, expert e of it into the buffer's e-th slot;
+        the slot's previous occupant leaves, an older resident copy of the
+        same expert is invalidated (slot emptied, stamp 0), and every expert of
+        the layer is stamped with this step's clock.  What the last two layers
+        leave behind seeds decode.  Prefill is not counted as hits or misses.
+        Returns the buffer's slot list (slot of expert e).
+        """
+        E = n_experts
+        if self.S < 2 * E:
+            raise ValueError("prefill double buffering needs at least 2E slots")
+        if self.prefill_next_layer != layer or self.buffers is None:
+            order = np.lexsort((np.arange(self.S), self.stamp))
+            bufs = [int(s) for s in order[:2 * E]]
+            for v in bufs:
+                if self.owner[v] >= 0:
+                    self.res[self.owner[v]] = -1
+                    self.owner[v] = -1
+                    self.stamp[v] = 0
+            self.buffers = [bufs[:E], bufs[E:]]
+            self.prefill_first = layer
+        self.clock += 1
+        buf = self.buffers[(layer - self.prefill_first) % 2]
+        for e in range(E):
+            u = layer * E + e
+            v = buf[e]
+            if self.owner[v] >= 0 and self.owner[v] != u:
+                self.res[self.owner[v]] = -1
+            old = self.res[u]
+            if old >= 0 and old != v:
+                self.owner[old] = -1
+                self.stamp[old] = 0
+            self.owner[v] = u
+            self.res[u] = v
+            self.stamp[v] = self.clock
+        self.prefill_next_layer = layer + 1 if layer + 1 < n_layers else None
+        return list(buf)
+
+    # -------------------------------------------------------------- resize
+    def resize(self, new_slots: int) -> list[tuple[int, int]]:
+        """Safe-point resize of the expert cache.
+
+        [FT, "挑战三"] and [FT2, paragraph on the memory budget]: the cache
+        can shrink or grow at run time and the outputs do not change, because
+        the host pool stays the source of truth.  Reading used here: growing
+        appends empty slots; shrinking keeps the new_slots most recent entries
+        by (stamp desc, slot asc), drops the rest, and moves each kept entry
+        that sits at a slot >= new_slots into the free slots below new_slots,
+        both taken in ascending slot order.  Returns the (from, to) moves.
+        """
+        n = int(new_slots)
+        if n < 0:
+            raise ValueError("negative size")
+        if n >= self.S:
+            self.owner = np.concatenate([self.owner, np.full(n - self.S, -1, dtype=np.int64)])
+            self.stamp = np.concatenate([self.stamp, np.zeros(n - self.S, dtype=np.int64)])
+            self.S = n
+            return []
+        occ = np.nonzero(self.owner >= 0)[0]
+        order = np.lexsort((occ, -self.stamp[occ]))
+        keep = set(int(s) for s in occ[order[:n]])
+        for s in occ:
+            if int(s) not in keep:
+                self.res[self.owner[s]] = -1
+                self.owner[s] = -1
+                self.stamp[s] = 0
+        movers = sorted(s for s in keep if s >= n)
+        free = [s for s in range(n) if s not in keep]
+        moves = list(zip(movers, free))
+        for src, dst in moves:
+            u = self.owner[src]
+            self.owner[dst] = u
+            self.stamp[dst] = self.stamp[src]
+            self.res[u] = dst
+        self.owner = self.owner[:n].copy()
+        self.stamp = self.stamp[:n].copy()
+        self.S = n
+        self.buffers = None
+        self.prefill_next_layer = None
+        return moves
+
+
+# ================================================================ expert maths
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64: the upper half of a float32."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def _e4m3_value(code: int) -> float:
+    """One E4M3FN code: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0
+    is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity.
+    [P3, §4.1] names the format; the definition is the OCP 8-bit float one."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def matvec_post_scaled(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """FP8 rows times x, one scale per 1x128 block of each row applied after the block's dot.
+
+    [P3, §4.2]: the block's dot product is formed first and multiplied by the
+    block scale once (scale*sum(w*x) = sum(scale*w*x)).
+    """
+    R, K = codes.shape
+    nb = K // FP8_BLOCK
+    w = e4m3_to_f64(codes).reshape(R, nb, FP8_BLOCK)
+    xb = np.asarray(x, dtype=np.float64).reshape(nb, FP8_BLOCK)
+    block_dots = np.einsum("rbk,bk->rb", w, xb)
+    return (block_dots * scales.astype(np.float64)).sum(axis=1)
+
+
+def swiglu_expert(expert: dict, x: np.ndarray, fp8: bool) -> np.ndarray:
+    """One SwiGLU expert on one token, float64: y = W_d (silu(W_g x) * (W_u x)).
+
+    Bank layout (per expert, row-major): gate [I][H], up [I][H], down [H][I];
+    FP8 scales gate_scale/up_scale [I][H/128], down_scale [H][I/128].
+    [FT2, paragraph on the double buffer] / [P3, §4.3] (gate, up, down projections).
+    """
+    if fp8:
+        a = matvec_post_scaled(expert["gate"], expert["gate_scale"], x)
+        b = matvec_post_scaled(expert["up"], expert["up_scale"], x)
+        h = silu(a) * b
+        return matvec_post_scaled(expert["down"], expert["down_scale"], h)
+    a = bf16_to_f64(expert["gate"]) @ x
+    b = bf16_to_f64(expert["up"]) @ x
+    h = silu(a) * b
+    return bf16_to_f64(expert["down"]) @ h
+
+
+def pair_row(expert: dict, x: np.ndarray, gate: float, fp8: bool) -> np.ndarray:
+    """Gate-weighted output row of one (token, expert) pair, float64."""
+    return np.float64(np.float32(gate)) * swiglu_expert(expert, x, fp8)
+
+
+def combine(shared_row, rows: list) -> np.ndarray:
+    """Fixed-order merge: shared expert first, then the k pair rows in rank
+    (= ascending expert id) order.  [FT, "q* 策略"] (exact merge of the GPU
+    and host partial sums)."""
+    out = np.zeros_like(np.asarray(rows[0], dtype=np.float64)) if shared_row is None \
+        else np.asarray(shared_row, dtype=np.float64).copy()
+    for r in rows:
+        out = out + np.asarray(r, dtype=np.float64)
+    return out
+
+
+def decode_layer_outputs(rec: StepRecord, sel, gates, x_bits, c_partial, expert_of, shared=None,
+                         fp8=False, tokens=None, n_experts=None):
+    """Layer output rows [len(tokens), H] for a decode step.
+
+    Pair (t, r) in G = H u F (slot_of_pair >= 0) is evaluated here from the
+    expert weights; a C pair takes its row from c_partial[t][r].
+    [FT, "执行顺序与工程细节"]: grouped evaluation of G, host partials for C,
+    then the merge.
+    """
+    B, k = sel.shape
+    tokens = range(B) if tokens is None else tokens
+    outs = []
+    for t in tokens:
+        x = bf16_to_f64(x_bits[t])
+        rows = []
+        for r in range(k):
+            if rec.slot_of_pair[t, r] >= 0:
+                u = rec.layer * n_experts + int(sel[t, r])
+                rows.append(pair_row(expert_of(u), x, gates[t, r], fp8))
+            else:
+                rows.append(np.asarray(c_partial[t, r], dtype=np.float64))
+        srow = swiglu_expert(shared, x, fp8) if shared is not None else None
+        outs.append(combine(srow, rows))
+    return np.stack(outs)
+
+
+def all_pair_rows(layer, sel, gates, x_bits, expert_of, n_experts, fp8=False) -> np.ndarray:
+    """Every pair's gate-weighted row, float64 [B, k, H]: what a host executor
+    would return for any C pair."""
+    B, k = sel.shape
+    rows = []
+    for t in range(B):
+        x = bf16_to_f64(x_bits[t])
+        rows.append([pair_row(expert_of(layer * n_experts + int(sel[t, r])), x, gates[t, r], fp8)
+                     for r in range(k)])
+    return np.asarray(rows)
+
+
+def prefill_outputs(layer, sel, gates, x_bits, expert_of, n_experts, tokens, shared=None, fp8=False):
+    """Prefill output rows for the given tokens: every pair runs on the GPU side."""
+    outs = []
+    for t in tokens:
+        x = bf16_to_f64(x_bits[t])
+        rows = [pair_row(expert_of(layer * n_experts + int(sel[t, r])), x, gates[t, r], fp8)
+                for r in range(sel.shape[1])]
+        srow = swiglu_expert(shared, x, fp8) if shared is not None else None
+        outs.append(combine(srow, rows))
+    return np.stack(outs)
+
+
+def rel_err_rows(y: np.ndarray, ref: np.ndarray) -> float:
+    """max over rows of max_j |y - ref| / max_j |ref|."""
+    y = np.atleast_2d(np.asarray(y, dtype=np.float64))
+    ref = np.atleast_2d(np.asarray(ref, dtype=np.float64))
+    num = np.abs(y - ref).max(axis=1)
+    den = np.maximum(np.abs(ref).max(axis=1), 1e-30)
+    return float((num / den).max())
