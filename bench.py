@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE-layer expert-cache hot path on one GB300 (or N replicas).
+
+Workload (decode): 40 MoE layers of the 35B-A3B expert shape (H 2048, I 512,
+256 routed experts top-8 + one shared expert, BF16), batch 1, a routing trace with
+temporal locality (p = 0.7 reuse, Zipf(1.1) redraws), slot cache = 37% of the
+routed pool (3788 slots), B_P:B_H = 52.7:77.3.  One step = one token through all
+40 layers (control -> fill -> gate/up GEMV -> down GEMV + combine per layer),
+replayed as one CUDA graph.  Inputs are synthetic and seeded; the expert weights
+read per token (2.27 GB) exceed L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tok/s + expert-weight HBM GB/s; prefill-chunk tok/s vs TC peak"
+FALLBACK_HBM = 6800.0
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = _env_int("WORLD_SIZE", 1)
+        self.rank = _env_int("RANK", 0)
+        self.local = _env_int("LOCAL_RANK", 0)
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() and \
+            self.pg.get_backend() == "nccl" else torch.device("cpu")
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() and \
+            self.pg.get_backend() == "nccl" else torch.device("cpu")
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, d: Dist) -> tuple[float, float]:
+    """Whole-job throughput: units summed over ranks / the slowest rank's time."""
+    total = d.sum(units_per_rank)
+    tmax = d.max(seconds_per_rank)
+    return total / tmax, tmax
+
+
+# ------------------------------------------------------------------ inputs
+_OVERRIDE: dict = {}
+
+
+def _workload():
+    import synth
+
+    w = synth.decode_bf16()
+    if _OVERRIDE.get("layers"):
+        w = w.with_(n_layers=_OVERRIDE["layers"], cache_slots=synth.capacity_slots(0.37, _OVERRIDE["layers"], 256))
+    if _OVERRIDE.get("slots"):
+        w = w.with_(cache_slots=_OVERRIDE["slots"])
+    return w
+
+
+def _config_desc(w) -> dict:
+    name = "decode_bf16_35B-A3B-shape" if not (_OVERRIDE.get("layers") or _OVERRIDE.get("slots")) \
+        else "decode_bf16_35B-A3B-shape (reduced, profiling only)"
+    return {"workload": name, "n_layers": w.n_layers, "hidden": w.hidden,
+            "expert_inter": w.inter, "n_experts": w.n_experts, "top_k": w.top_k, "shared_expert": w.has_shared,
+            "weights": "bf16", "global_batch": w.batch, "cache_slots": w.cache_slots,
+            "cache_fraction": round(w.cache_slots / w.n_logical, 4), "bp_bh_gbps": [w.bp_gbps, w.bh_gbps],
+            "trace": "p=0.7 reuse, Zipf(1.1) redraw, 512-step cycle",
+            "l2": "inputs larger than L2 (2.27 GB of expert weights per token), no flush"}
+
+
+def _pool_banks(w, d: Dist):
+    """Host expert pool.  Replicas on one node share one copy in /dev/shm."""
+    import synth
+
+    pool = synth.ExpertPool(w)
+    if d.world == 1:
+        return pool, pool.routed_banks(), pool.shared_banks()
+    tag = f"/dev/shm/ftmoe_pool_{w.seed}"
+    banks = {}
+    if d.rank == 0:
+        for k, shp in pool.shapes.items():
+            banks[k] = np.memmap(f"{tag}_{k}", dtype=pool.dtypes[k], mode="w+", shape=(w.n_logical,) + shp)
+        pool.fill_banks(banks, 0)
+        for a in banks.values():
+            a.flush()
+    d.barrier()
+    if d.rank != 0:
+        for k, shp in pool.shapes.items():
+            banks[k] = np.memmap(f"{tag}_{k}", dtype=pool.dtypes[k], mode="r+", shape=(w.n_logical,) + shp)
+    return pool, banks, pool.shared_banks()
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode_eval.cu",):
+        with open(os.path.join(ROOT, "serving_router_top_dedupe_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        t = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel)
+    if not e or e.get("source_hash") != _kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def _peaks():
+    try:
+        p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM, "fallback"
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_decode_tokens(w, banks, shared, trace, n_tokens, time_budget_s):
+    """Time the CPU oracle on a bounded sample: whole tokens (all layers) of the same
+    trace, cache simulation included.  Returns (tokens, seconds, cpu_seconds)."""
+    import oracle as O
+    import synth
+
+    sim = O.SlotCache(w.cache_slots, w.n_logical)
+    bp, bh = O.mbps(w.bp_gbps), O.mbps(w.bh_gbps)
+    expert = lambda u: {k: v[u] for k, v in banks.items()}
+    c0, t0 = time.process_time(), time.perf_counter()
+    done = 0
+    for s in range(n_tokens):
+        for l in range(w.n_layers):
+            xb = synth.decode_x(w, s % w.steps, l)
+            z = synth.decode_logits(w, s % w.steps, l, trace)
+            sel, gates = O.route(z, w.top_k)
+            rec = sim.decode_step(l, w.n_experts, sel, bp, bh)
+            cp = np.zeros((w.batch, w.top_k, w.hidden), dtype=np.float32)
+            sh = {k: v[l] for k, v in shared.items()} if shared is not None else None
+            O.decode_layer_outputs(rec, sel, gates, xb, cp, expert, shared=sh, n_experts=w.n_experts)
+        done += 1
+        if time.perf_counter() - t0 > time_budget_s:
+            break
+    return done, time.perf_counter() - t0, time.process_time() - c0
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, d: Dist) -> dict | None:
+    import torch
+
+    import synth
+    from serving_router_top_dedupe_gb300 import build as B
+
+    B.build()
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    w = _workload()
+    L, Bt, H, E, k = w.n_layers, w.batch, w.hidden, w.n_experts, w.top_k
+    t_setup = time.perf_counter()
+    pool, banks, shared = _pool_banks(w, d)
+    trace = synth.routing_trace(w)
+    n_tr = w.steps
+    xs = np.empty((n_tr, L, Bt, H), dtype=np.uint16)
+    zs = np.empty((n_tr, L, Bt, E), dtype=np.float32)
+    for s in range(n_tr):
+        for l in range(L):
+            xs[s, l] = synth.decode_x(w, s, l)
+            zs[s, l] = synth.decode_logits(w, s, l, trace)
+    stream = torch.cuda.Stream(device=dev)
+    cfg = F.make_config(L, H, w.inter, E, k, w.has_shared, F.FT_W_BF16, Bt, w.cache_slots, w.bp_gbps, w.bh_gbps,
+                        device=d.local, compute_stream=stream.cuda_stream)
+    h = F.ft_moe_init(cfg, banks, shared)
+    bp_measured = F.ft_bench_bw(256 << 20, 8)
+    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
+    z_all = torch.from_numpy(zs).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    # host-side partial rows of C pairs: synthetic stand-ins (content does not change the work)
+    cp_all = (torch.randn((n_tr, L, Bt, k, H), device=dev, generator=gen) * 0.01).float()
+    x_s = torch.empty((L, Bt, H), dtype=torch.int16, device=dev)
+    z_s = torch.empty((L, Bt, E), dtype=torch.float32, device=dev)
+    c_s = torch.empty((L, Bt, k, H), dtype=torch.float32, device=dev)
+    o_s = torch.empty((L, Bt, H), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+    g = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
+    setup_s = time.perf_counter() - t_setup
+
+    def load(i):
+        s = i % n_tr
+        x_s.copy_(x_all[s])
+        z_s.copy_(z_all[s])
+        c_s.copy_(cp_all[s])
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            load(i)
+            F.ft_graph_launch(g)
+        stream.synchronize()
+        st0 = F.ft_moe_get_stats(h)
+        clocks = ClockSampler(d.local)
+        d.barrier()
+        torch.cuda.synchronize(dev)
+        clocks.start()
+        time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.warmup, args.warmup + args.steps):
+            load(i)
+            F.ft_graph_launch(g)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize(dev)
+        d.barrier()
+        clk = clocks.stop()
+        ms = e0.elapsed_time(e1)
+        st1 = F.ft_moe_get_stats(h)
+    value, tmax = aggregate(args.steps * Bt, ms * 1e-3, d)
+    layer_steps = (st1.decode_steps - st0.decode_steps)
+    miss = st1.misses - st0.misses
+    acts = (st1.hits - st0.hits) + miss
+    cache = {"miss_rate": miss / max(1, acts), "fills_per_token": (st1.fills - st0.fills) / args.steps,
+             "host_pairs_per_token": (st1.cpu_execs - st0.cpu_execs) / args.steps,
+             "gpu_experts_per_token": (st1.eval_entries - st0.eval_entries) / args.steps,
+             "fill_gb_per_token": (st1.fills - st0.fills) / args.steps * 6 * H * w.inter / 1e9,
+             "error_word": st1.error_word}
+
+    # kernel profile over a window of the same trace (events on each kernel's own stream)
+    n_prof = min(args.profile_steps, n_tr)
+    F.ft_moe_set_profiling(h, 1)
+    F.ft_moe_get_profile(h, reset=True)
+    sp0 = F.ft_moe_get_stats(h)
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            j = args.warmup + args.steps + i
+            load(j)
+            F.ft_moe_decode_layers(h, 0, L, Bt, x_s, z_s, c_s, o_s)
+    prof = F.ft_moe_get_profile(h, reset=True)
+    sp1 = F.ft_moe_get_stats(h)
+    F.ft_moe_set_profiling(h, 0)
+    ent = sp1.eval_entries - sp0.eval_entries
+    prs = sp1.eval_pairs - sp0.eval_pairs
+    esz = 2
+    gate_up_bytes = ent * 2 * w.inter * H * esz + prs * (H * 2 + w.inter * 4)
+    down_bytes = ent * H * w.inter * esz + prs * (w.inter * 4 + H * 4) + n_prof * L * Bt * H * 4 * (k + 2)
+    tot_ms = sum(v[1] for v in prof.values())
+    kernels = {}
+    for name, (n, msum) in prof.items():
+        if n:
+            kernels[name] = {"launches": n, "avg_us": round(1e3 * msum / n, 3), "share": round(msum / tot_ms, 4)}
+    peak, peak_kind = _peaks()
+    gu_n, gu_ms = prof["gate_up"]
+    dn_n, dn_ms = prof["down_combine"]
+    ach_gu = gate_up_bytes / (gu_ms * 1e-3) / 1e9 if gu_ms else None
+    ach_dn = down_bytes / (dn_ms * 1e-3) / 1e9 if dn_ms else None
+    ach_both = (gate_up_bytes + down_bytes) / ((gu_ms + dn_ms) * 1e-3) / 1e9 if gu_ms else None
+    kernels.get("gate_up", {})["achieved_gbs"] = round(ach_gu, 1) if ach_gu else None
+    kernels.get("down_combine", {})["achieved_gbs"] = round(ach_dn, 1) if ach_dn else None
+    tr = _traffic("gate_up")
+    roofline = {"kernel": "gate_up (expert GEMV phase 1: gate+up rows, SwiGLU)", "bound": "hbm",
+                "achieved": round(ach_gu, 1) if ach_gu else None, "peak": peak, "unit": "GB/s",
+                "frac": round(ach_gu / peak, 4) if ach_gu else None, "peak_source": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": round(gate_up_bytes / max(1, gu_n)),
+                "traffic": tr}
+
+    # end to end through the host-buffer C-ABI call (H2D inputs, D2H outputs, every step)
+    n_e2e = min(args.e2e_steps, args.steps)
+    xh = torch.empty((L, Bt, H), dtype=torch.int16).pin_memory()
+    zh = torch.empty((L, Bt, E), dtype=torch.float32).pin_memory()
+    ch = torch.empty((L, Bt, k, H), dtype=torch.float32).pin_memory()
+    oh = torch.empty((L, Bt, H), dtype=torch.float32).pin_memory()
+    cp_host = cp_all[: min(n_tr, 64)].cpu()
+    F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)   # capture the cached graph
+    t_e2e = 0.0
+    for i in range(n_e2e):
+        s = (args.warmup + args.steps + n_prof + i) % n_tr
+        xh.copy_(torch.from_numpy(xs[s].view(np.int16)))
+        zh.copy_(torch.from_numpy(zs[s]))
+        ch.copy_(cp_host[s % cp_host.shape[0]])
+        t0 = time.perf_counter()
+        F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)
+        t_e2e += time.perf_counter() - t0
+    e2e_v, _ = aggregate(n_e2e * Bt, t_e2e, d)
+    h2d = L * Bt * (H * 2 + E * 4 + k * H * 4)
+    d2h = L * Bt * H * 4
+    e2e = {"value": round(e2e_v, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n_e2e, "api": "ft_moe_decode_layers_host (pinned host buffers, cached graph)"}
+    F.ft_graph_destroy(g)
+    F.ft_moe_destroy(h)
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see DESIGN.md)",
+           "config": {**_config_desc(w), "parallelism": f"replicas x{d.world}" if d.world > 1 else "single GPU"},
+           "hbm_gbs_expert_weights": {"gate_up": roofline["achieved"],
+                                      "down_combine": round(ach_dn, 1) if ach_dn else None,
+                                      "both": round(ach_both, 1) if ach_both else None},
+           "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * L * 4, "clocks": clk,
+           "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1),
+           "setup_s": round(setup_s, 1)}
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, args.cpu_tokens, args.cpu_budget)
+        out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
+                               "kind": "oracle",
+                               "sample": f"{n} tokens x {L} layers of the same trace (float64 numpy oracle, "
+                                         f"cache simulation included), {sec:.1f} s on {os.cpu_count()} host cores"}
+    return out
+
+
+# -------------------------------------------------------------- reference
+def run_reference(args, d: Dist) -> dict | None:
+    if d.rank != 0:
+        return None
+    import synth
+
+    w = _workload()
+    pool = synth.ExpertPool(w)
+    banks, shared = pool.routed_banks(), pool.shared_banks()
+    trace = synth.routing_trace(w)
+    n_tok = max(1, min(args.steps, args.ref_tokens))
+    if args.warmup:
+        oracle_decode_tokens(w, banks, shared, trace, 1, 1e9)
+    n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, n_tok, args.cpu_budget)
+    v = n / sec
+    return {"metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": d.world, "steps": n,
+            "warmup": min(args.warmup, 1), "ms_per_step": round(sec * 1e3 / n, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": _config_desc(w), "impl": "reference",
+            "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
+                             "kind": "oracle",
+                             "sample": f"{n} tokens x {w.n_layers} layers (bounded sample of the decode trace)"},
+            "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--profile-steps", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=128)
+    ap.add_argument("--cpu-tokens", type=int, default=16)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer MoE layers")
+    ap.add_argument("--slots", type=int, default=0, help="profiling only: other cache size")
+    args = ap.parse_args()
+    _OVERRIDE.update(layers=args.layers, slots=args.slots)
+    d = Dist()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        d.init("gloo")
+        out = run_reference(args, d)
+    else:
+        d.init("nccl")
+        out = run_ours(args, d)
+    if d.rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    d.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,265 @@
+/*
+ * ft_moe.h -- C ABI of libftmoe: the MoE-layer hot path of a FreeToken-style
+ * edge-serving system, on one GB300 (sm_103a).
+ *
+ * What the library computes (sources cited by page title and section):
+ *   [FT]  "FreeToken 完全拆解：带宽自适应执行，让 8GB 笔记本跑 35B、单卡工作站跑 753B 的边缘 MoE 服务系统"
+ *   [FT2] "개인 장치에서 MoE 모델을 서빙하는 FreeToken" (paragraph topics, no headings)
+ *   [P3]  "OSDI'26 | 双路 CPU + 两张 5090，本地跑满血 671B DeepSeek：云端 SLO 是怎么在消费级硬件上达成的"
+ *
+ *  - A slot pool in HBM holds whole experts; one global LRU over all MoE layers,
+ *    addressed by the logical id u = layer*E + expert ([FT] "语义感知专家缓存",
+ *    [FT] "FTW 权重格式与平台适配").
+ *  - Per decode layer-step, one control kernel routes (top-k softmax), dedupes the
+ *    batch's experts, classifies hits/misses against the residency table, computes
+ *    the fill count q, finds the K least recently used victims in one pass and
+ *    rewrites routed ids to slots or FT_CPU ([FT] "Device-side 缓存控制").
+ *  - q = round(m * B_P / B_H), at least one fill when m > 0 ([FT] "q* 策略").
+ *    The F set is copied host->slots on the transfer stream; the C set's
+ *    gate-weighted rows are an INPUT (c_partial): no host executor lives here.
+ *  - G = H u F is evaluated by SwiGLU GEMV kernels (BF16, or FP8 E4M3 with one
+ *    FP32 scale per 1x128 block applied after the block's dot product, [P3] §4.2),
+ *    then a combine sums, per token, the shared expert and the k pair rows in
+ *    ascending expert id (fixed order), so outputs do not depend on cache size or
+ *    on the F/C split ([FT] "q* 策略").
+ *  - Prefill chunks stream whole layers into two pool buffers while the previous
+ *    layer runs a tcgen05 grouped GEMM ([FT] "全层双缓冲").
+ *
+ * Conventions for every entry point:
+ *  - Return FT_OK or an ft_status; ft_last_error() gives a thread-local message.
+ *  - Argument errors are returned synchronously and change no state.
+ *  - Decode/prefill calls only enqueue work on the library's compute stream (no
+ *    host synchronisation), except where a function says it synchronises.
+ *    Errors found by kernels (bad ids in inputs, NaN logits, a wait that timed
+ *    out) set bits in a device error word, read by ft_moe_get_stats().
+ *  - "dev" pointers are device (HBM) addresses owned by the caller; "host"
+ *    pointers are host addresses owned by the caller.
+ *  - BF16 values are passed as raw 16-bit patterns (uint16_t storage).
+ */
+#ifndef FT_MOE_H
+#define FT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FT_OK = 0,
+  FT_ERR_INVALID = 1,   /* bad argument or configuration */
+  FT_ERR_CUDA = 2,      /* a CUDA runtime/driver call failed */
+  FT_ERR_NOMEM = 3,     /* device or host allocation failed */
+  FT_ERR_PIN = 4,       /* the host pool could not be pinned/registered; no fallback */
+  FT_ERR_CAPACITY = 5,  /* the slot pool is too small for the request */
+  FT_ERR_STATE = 6,     /* call not allowed in the current state (e.g. during capture) */
+  FT_ERR_TIMEOUT = 7,   /* a bounded device-side wait gave up */
+  FT_ERR_DEVICE = 8     /* the device error word is non-zero */
+} ft_status;
+
+typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1 } ft_wtype;
+
+/* How a decode step moves F-set experts from the host pool into their slots.
+ * FT_FILL_KERNEL: one fixed-shape copy kernel on the transfer stream reads the
+ *   device-resident copy list and pulls bytes from the mapped host pool; the
+ *   whole step can be captured into a CUDA graph.
+ * FT_FILL_MEMCPY: the host waits for the control kernel, reads the copy list and
+ *   issues one cudaMemcpyAsync per bank per filled expert on the transfer stream.
+ *   One host synchronisation per layer; not capturable. */
+typedef enum { FT_FILL_KERNEL = 0, FT_FILL_MEMCPY = 1 } ft_fill_mode;
+
+/* Rewritten pair id of a C-set pair (executed on the host; row taken from c_partial). */
+#define FT_CPU (-1)
+
+/* Bits of the device error word. */
+#define FT_DEVERR_NAN_LOGIT 0x1u   /* a NaN router logit (treated as -inf) */
+#define FT_DEVERR_BAD_STATE 0x2u   /* residency table inconsistent (should never happen) */
+#define FT_DEVERR_TIMEOUT 0x4u     /* a bounded wait gave up */
+#define FT_DEVERR_CAPACITY 0x8u    /* a work list overflowed its fixed shape */
+
+typedef struct {
+  int n_layers;           /* L: MoE layers */
+  int hidden;             /* H: model width (multiple of 256; FP8: of 128) */
+  int inter;              /* I: expert intermediate width (multiple of 128) */
+  int n_experts;          /* E: routed experts per layer (<= 1024) */
+  int top_k;              /* k (<= 16, <= E) */
+  int has_shared;         /* 1: one always-on shared expert per layer (weight 1) */
+  int wtype;              /* ft_wtype */
+  int max_batch;          /* largest decode batch B (<= 64) */
+  int max_prefill_tokens; /* largest prefill chunk T (0: no prefill) */
+  int cache_slots;        /* S: slots in the HBM pool */
+  double bp_gbps;         /* B_P, pinned host -> HBM GB/s; <= 0: measured at init */
+  double bh_gbps;         /* B_H, host-side expert processing GB/s (supplied) */
+  int fill_mode;          /* ft_fill_mode */
+  int device;             /* CUDA device ordinal */
+  void* compute_stream;   /* cudaStream_t, or NULL for a library-created stream */
+  void* transfer_stream;  /* cudaStream_t, or NULL for a library-created stream */
+} ft_moe_config;
+
+/* Host expert banks ([FT] "FTW 权重格式与平台适配": first dimension of every bank is
+ * the logical id; rows with the same id form one expert).  Row-major:
+ *   gate, up   [L*E][I][H]        BF16 bits (uint16) or E4M3 codes (uint8)
+ *   down       [L*E][H][I]
+ *   gate_scale, up_scale [L*E][I][H/128] FP32 (FP8 only; NULL for BF16)
+ *   down_scale [L*E][H][I/128]           FP32 (FP8 only)
+ * For the shared-expert banks the first dimension is L (one per layer). */
+typedef struct {
+  const void* gate;
+  const void* up;
+  const void* down;
+  const float* gate_scale;
+  const float* up_scale;
+  const float* down_scale;
+} ft_banks;
+
+typedef struct ft_moe ft_moe;
+typedef struct ft_graph ft_graph;
+
+typedef struct {
+  uint64_t hits, misses, fills, cpu_execs, evictions;
+  uint64_t decode_steps, prefill_layers;
+  uint64_t eval_entries;  /* decode: experts evaluated on the GPU (G entries + shared), summed over steps */
+  uint64_t eval_pairs;    /* decode: (expert, token) pairs evaluated on the GPU, summed over steps */
+  uint32_t error_word;  /* FT_DEVERR_* bits */
+  uint32_t clock;       /* global LRU clock (one tick per layer-step) */
+  double bp_gbps, bh_gbps;
+  int cache_slots;
+} ft_stats;
+
+/* Last decode layer-step's decisions, for parity checks.  The caller provides
+ * host arrays of the stated sizes (K = min(max_batch*top_k, n_experts)); any
+ * pointer may be NULL to skip that array. */
+typedef struct {
+  int layer, batch, q, n_active, n_hit, n_miss, n_victims, n_cpu;
+  uint32_t clock;
+  int32_t* sel;          /* [batch*top_k] expert ids, ascending per token */
+  float* gates;          /* [batch*top_k] softmax over the token's k logits */
+  int32_t* slot_of_pair; /* [batch*top_k] slot id, or FT_CPU */
+  int32_t* active;       /* [K] A: sorted unique logical ids */
+  int32_t* hit;          /* [K] H, ascending */
+  int32_t* miss;         /* [K] M, ascending; F = first q, C = the rest */
+  int32_t* victims;      /* [K] LRU candidates, ascending (stamp, slot); first q used */
+} ft_step_trace;
+
+/* Per-kernel CUDA-event timing collected while profiling is on. */
+typedef struct {
+  uint64_t launches[6];  /* 0 control, 1 fill, 2 gemv phase 1, 3 gemv phase 2 + combine,
+                            4 prefill route, 5 prefill grouped GEMM */
+  double total_ms[6];
+} ft_profile;
+
+/* Create the library state: allocates the slot pool (S * slot bytes) and the work
+ * buffers in HBM, copies the shared experts to HBM, and registers (pins + maps)
+ * each host bank with cudaHostRegister unless it is already pinned.
+ *   cfg      configuration (copied)
+ *   host_pool routed-expert banks, caller-owned, must outlive the handle
+ *   shared   shared-expert banks (first dim L) or NULL when cfg->has_shared == 0
+ *   out      receives the handle
+ * Errors: FT_ERR_INVALID (shape limits above), FT_ERR_NOMEM, FT_ERR_PIN (no
+ * fallback path), FT_ERR_CUDA.  Synchronises. */
+ft_status ft_moe_init(const ft_moe_config* cfg, const ft_banks* host_pool, const ft_banks* shared,
+                      ft_moe** out);
+
+/* One decode layer-step ([FT] "执行顺序与工程细节", "Device-side 缓存控制").
+ *   layer     0 <= layer < L
+ *   batch     1 <= batch <= max_batch tokens
+ *   x_bf16    dev [batch][H] BF16 activations
+ *   logits    dev [batch][E] FP32 router logits
+ *   c_partial dev [batch][top_k][H] FP32 gate-weighted rows of host-executed pairs;
+ *             row (t, r) is read only if that pair lands in the C set.  May be NULL
+ *             only when B_H <= B_P (every miss is filled).
+ *   out       dev [batch][H] FP32 layer output
+ *   rows_out  optional dev [batch][top_k][H] FP32: GPU pair rows (g_r * expert(x_t));
+ *             rows of C pairs are left untouched.
+ * Enqueues on the compute stream; graph-capturable with FT_FILL_KERNEL. */
+ft_status ft_moe_decode_step(ft_moe* h, int layer, int batch, const void* x_bf16, const float* logits,
+                             const float* c_partial, float* out, float* rows_out);
+
+/* n_layers consecutive decode layer-steps (layers first_layer .. first_layer+n-1,
+ * one token batch), with per-layer inputs packed layer-major:
+ * x [n][batch][H], logits [n][batch][E], c_partial [n][batch][k][H], out [n][batch][H],
+ * rows_out [n][batch][k][H] or NULL.  Same semantics as n calls of ft_moe_decode_step. */
+ft_status ft_moe_decode_layers(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_bf16,
+                               const float* logits, const float* c_partial, float* out, float* rows_out);
+
+/* Same as ft_moe_decode_layers with HOST buffers: copies the inputs into library
+ * staging buffers (H2D), runs the layers (through a cached CUDA graph when
+ * use_graph != 0 and fill_mode == FT_FILL_KERNEL), copies out back (D2H) and
+ * synchronises.  out_host may be NULL (no D2H). */
+ft_status ft_moe_decode_layers_host(ft_moe* h, int first_layer, int n_layers, int batch,
+                                    const void* x_host, const float* logits_host,
+                                    const float* c_partial_host, float* out_host, int use_graph);
+
+/* Capture ft_moe_decode_layers(...) with these exact device buffers into a CUDA
+ * graph (requires FT_FILL_KERNEL).  Replays re-read the buffers' current contents. */
+ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, int batch,
+                                      const void* x_bf16, const float* logits, const float* c_partial,
+                                      float* out, float* rows_out, ft_graph** g);
+ft_status ft_graph_launch(ft_graph* g);  /* enqueue one replay on the compute stream */
+ft_status ft_graph_destroy(ft_graph* g);
+
+/* One prefill layer of a chunk ([FT] "全层双缓冲"): a call that does not continue
+ * the previous prefill layer starts a chunk and takes the 2E least recently used
+ * slots as two full-layer buffers (host-synchronising once).  Layer l's experts are
+ * in buffer (l - first) mod 2; the whole of layer l+1 is copied into the other
+ * buffer with cudaMemcpyAsync on the transfer stream while layer l's routing and
+ * grouped GEMM run on the compute stream.  All pairs run on the GPU.
+ *   n_tokens  1 <= T <= max_prefill_tokens
+ *   x_bf16    dev [T][H] BF16;  logits dev [T][E] FP32;  out dev [T][H] FP32
+ * Errors: FT_ERR_CAPACITY when S < 2E (the on-demand path is not built). */
+ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x_bf16, const float* logits,
+                               float* out);
+
+/* Safe-point resize of the slot pool ([FT] "挑战三"; [FT2] paragraph on the memory
+ * budget).  Growing adds empty slots.  Shrinking keeps the new_slots most recently
+ * used experts (stamp desc, slot asc), drops the rest and moves kept experts from
+ * slots >= new_slots into the free slots below, in ascending order.  Outputs of
+ * later steps do not change (the host pool stays authoritative).  Synchronises;
+ * reallocates the pool when growing.  Errors: FT_ERR_INVALID (new_slots < 1),
+ * FT_ERR_NOMEM, FT_ERR_STATE (called while a graph of this handle is being captured). */
+ft_status ft_cache_resize(ft_moe* h, int new_slots);
+
+/* Host mirror of the device split rule ([FT] "q* 策略"; [FT2] paragraph on the miss
+ * split): q = clamp(round_half_up(m * bp / bh), 1, m) for m > 0, with bp, bh rounded
+ * to integer MB/s; q = m when bh <= bp; then q <= evictable.  No GPU needed.
+ * Errors: FT_ERR_INVALID (m < 0, evictable < 0, bandwidths <= 0, q_out NULL). */
+ft_status ft_split_misses(int m, double bp_gbps, double bh_gbps, int evictable, int* q_out);
+
+/* Pinned host -> HBM copy bandwidth with cudaMemcpyAsync on the current device,
+ * timed with CUDA events over `iters` copies of `bytes` (the calibration step,
+ * [FT] "q* 策略", "ft bench bw").  Allocates and frees its own buffers; synchronises. */
+ft_status ft_bench_bw(size_t bytes, int iters, double* bp_gbps);
+
+/* Counters, error word, clock.  Synchronises the library's streams. */
+ft_status ft_moe_get_stats(ft_moe* h, ft_stats* out);
+
+/* Decisions of the last decode layer-step (see ft_step_trace).  Synchronises. */
+ft_status ft_moe_get_step_trace(ft_moe* h, ft_step_trace* out);
+
+/* Copy of the residency state: res [L*E], owner [S], stamp [S] (host arrays, any may
+ * be NULL), clock.  Synchronises. */
+ft_status ft_moe_get_state(ft_moe* h, int32_t* res, int32_t* owner, uint32_t* stamp, uint32_t* clock);
+
+/* Turn per-kernel CUDA-event timing on (1) or off (0); ft_moe_get_profile reads and
+ * (reset != 0) clears the totals.  Timing events are recorded on the stream each
+ * kernel is launched on.  Synchronises. */
+ft_status ft_moe_set_profiling(ft_moe* h, int enable);
+ft_status ft_moe_get_profile(ft_moe* h, ft_profile* out, int reset);
+
+/* Replace the compute stream (e.g. to follow a framework's current stream). */
+ft_status ft_moe_set_stream(ft_moe* h, void* compute_stream);
+
+/* Wait for all work the handle has enqueued. */
+ft_status ft_moe_synchronize(ft_moe* h);
+
+/* Release device memory, streams and host registrations.  Synchronises. */
+ft_status ft_moe_destroy(ft_moe* h);
+
+/* Thread-local message describing the last error of this thread ("" if none). */
+const char* ft_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_MOE_H */

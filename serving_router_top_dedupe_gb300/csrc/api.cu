@@ -1,0 +1,937 @@
+// Host runtime of libftmoe: the C ABI declared in include/ft_moe.h.
+//
+// Owns the HBM slot pool, the residency state, the fixed-shape work lists, the
+// compute and transfer streams, cached CUDA graphs and the host-pool registrations.
+// Every routing-dependent decision runs in kernels (control.cu); this file only
+// validates arguments, enqueues work and moves bytes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "ft_internal.cuh"
+#include "ft_prefill.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ft_status fail(ft_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define FT_CUDA(call)                                                                        \
+  do {                                                                                       \
+    cudaError_t e_ = (call);                                                                 \
+    if (e_ != cudaSuccess)                                                                   \
+      return fail(e_ == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA, "%s: %s (%s:%d)", \
+                  #call, cudaGetErrorString(e_), __FILE__, __LINE__);                        \
+  } while (0)
+
+long long to_mbps(double gbps) { return (long long)std::floor(gbps * 1000.0 + 0.5); }
+
+struct HostBank {
+  const uint8_t* host = nullptr;  // caller's pointer
+  const uint8_t* dev = nullptr;   // device-visible alias
+  size_t row = 0;                 // bytes per logical id
+  size_t bytes = 0;
+  bool registered = false;        // registered by us (unregister at destroy)
+};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct ft_graph {
+  ft_moe* owner = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+struct ft_moe {
+  ft_moe_config cfg{};
+  int dev = 0, n_sm = 0;
+  cudaStream_t cs = nullptr, ts = nullptr;
+  bool own_cs = false, own_ts = false;
+  ft::SlotLayout lay{};
+  int S = 0, L = 0, E = 0, K = 0, H = 0, I = 0, kcap = 0;
+  long long bp_mbs = 0, bh_mbs = 0;
+  double bp_gbps = 0, bh_gbps = 0;
+  HostBank bank[6];
+  int n_banks = 3;
+  uint8_t* pool = nullptr;
+  uint8_t* shared_w = nullptr;
+  int32_t* res = nullptr;
+  int32_t* owner = nullptr;
+  uint32_t* stamp = nullptr;
+  ft::DevState* st = nullptr;
+  ft::DecodeWork w{};
+  std::vector<void*> allocs;  // work-list allocations
+  int32_t* counts_host = nullptr;  // pinned mirror (memcpy fill mode)
+  int32_t* copy_host = nullptr;    // pinned [2*kcap]
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_ctrl = nullptr;
+  int grid_eval = 0, grid_fill = 0;
+  // host-buffer staging (lazy)
+  uint16_t* stg_x = nullptr;
+  float *stg_logits = nullptr, *stg_cp = nullptr, *stg_out = nullptr;
+  std::map<std::tuple<int, int, int>, ft_graph*> host_graphs;
+  // profiling
+  bool prof = false;
+  std::vector<ProfRec> prof_live;
+  std::vector<cudaEvent_t> ev_free;
+  ft_profile prof_acc{};
+  // prefill (lazy)
+  ft::PrefillState* pf = nullptr;
+  std::vector<ft_graph*> graphs;
+};
+
+namespace ft {
+
+SlotLayout make_layout(int wtype, int H, int I) {
+  SlotLayout l{};
+  const size_t esz = wtype == FT_W_BF16 ? 2 : 1;
+  l.gate_b = (size_t)I * H * esz;
+  l.down_b = (size_t)H * I * esz;
+  l.gate = 0;
+  l.up = l.gate_b;
+  l.down = 2 * l.gate_b;
+  size_t end = l.down + l.down_b;
+  if (wtype == FT_W_FP8_E4M3_B128) {
+    l.gs_b = (size_t)I * (H / 128) * 4;
+    l.ds_b = (size_t)H * (I / 128) * 4;
+    l.gs = end;
+    l.us = l.gs + l.gs_b;
+    l.ds = l.us + l.gs_b;
+    end = l.ds + l.ds_b;
+  } else {
+    l.gs = l.us = l.ds = end;
+  }
+  l.used = end;
+  l.stride = (end + 255) / 256 * 256;
+  return l;
+}
+
+}  // namespace ft
+
+namespace {
+
+ft_status prof_begin(ft_moe* h, cudaStream_t s, cudaEvent_t* out) {
+  *out = nullptr;
+  if (!h->prof) return FT_OK;
+  cudaEvent_t e;
+  if (!h->ev_free.empty()) {
+    e = h->ev_free.back();
+    h->ev_free.pop_back();
+  } else {
+    FT_CUDA(cudaEventCreate(&e));
+  }
+  FT_CUDA(cudaEventRecord(e, s));
+  *out = e;
+  return FT_OK;
+}
+
+ft_status prof_end(ft_moe* h, int kind, cudaStream_t s, cudaEvent_t a) {
+  if (!h->prof || !a) return FT_OK;
+  cudaEvent_t e;
+  if (!h->ev_free.empty()) {
+    e = h->ev_free.back();
+    h->ev_free.pop_back();
+  } else {
+    FT_CUDA(cudaEventCreate(&e));
+  }
+  FT_CUDA(cudaEventRecord(e, s));
+  h->prof_live.push_back({kind, a, e});
+  return FT_OK;
+}
+
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &st);
+  return st != cudaStreamCaptureStatusNone;
+}
+
+ft_status alloc_dev(ft_moe* h, void** p, size_t bytes) {
+  cudaError_t e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+  if (e != cudaSuccess) return fail(FT_ERR_NOMEM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  h->allocs.push_back(*p);
+  return FT_OK;
+}
+
+ft_status register_bank(HostBank& b, const void* p, size_t row, size_t n_rows) {
+  b.host = static_cast<const uint8_t*>(p);
+  b.row = row;
+  b.bytes = row * n_rows;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return fail(FT_ERR_INVALID, "host bank not 16-byte aligned");
+  cudaPointerAttributes at{};
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  bool pinned = e == cudaSuccess && at.type == cudaMemoryTypeHost;
+  cudaGetLastError();
+  if (!pinned) {
+    e = cudaHostRegister(const_cast<void*>(p), b.bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(FT_ERR_PIN, "cudaHostRegister(%zu bytes) failed: %s (no fallback path)", b.bytes,
+                  cudaGetErrorString(e));
+    }
+    b.registered = true;
+  }
+  void* d = nullptr;
+  e = cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FT_ERR_PIN, "host bank is pinned but not mapped: %s", cudaGetErrorString(e));
+  }
+  b.dev = static_cast<const uint8_t*>(d);
+  return FT_OK;
+}
+
+ft_status check_cfg(const ft_moe_config* c) {
+  if (!c) return fail(FT_ERR_INVALID, "null config");
+  if (c->n_layers < 1 || c->n_experts < 1 || c->n_experts > ft::kMaxE)
+    return fail(FT_ERR_INVALID, "n_layers >= 1 and 1 <= n_experts <= %d required", ft::kMaxE);
+  if (c->top_k < 1 || c->top_k > ft::kMaxK || c->top_k > c->n_experts)
+    return fail(FT_ERR_INVALID, "1 <= top_k <= min(%d, n_experts) required", ft::kMaxK);
+  if (c->wtype != FT_W_BF16 && c->wtype != FT_W_FP8_E4M3_B128) return fail(FT_ERR_INVALID, "unknown wtype");
+  const int hmul = c->wtype == FT_W_BF16 ? 256 : 512;
+  if (c->hidden < hmul || c->hidden % hmul) return fail(FT_ERR_INVALID, "hidden must be a multiple of %d", hmul);
+  if (c->inter < 128 || c->inter % 128) return fail(FT_ERR_INVALID, "inter must be a multiple of 128");
+  if (c->max_batch < 1 || c->max_batch > ft::kMaxBatch)
+    return fail(FT_ERR_INVALID, "1 <= max_batch <= %d required", ft::kMaxBatch);
+  if (c->cache_slots < 1 || c->cache_slots > (1 << 20))
+    return fail(FT_ERR_INVALID, "1 <= cache_slots <= 2^20 required");
+  if (c->bh_gbps <= 0) return fail(FT_ERR_INVALID, "bh_gbps must be > 0");
+  if (c->fill_mode != FT_FILL_KERNEL && c->fill_mode != FT_FILL_MEMCPY) return fail(FT_ERR_INVALID, "fill_mode");
+  if (c->max_prefill_tokens < 0) return fail(FT_ERR_INVALID, "max_prefill_tokens < 0");
+  if ((long long)c->n_layers * c->n_experts > (1LL << 30)) return fail(FT_ERR_INVALID, "too many experts");
+  return FT_OK;
+}
+
+ft_status alloc_work(ft_moe* h) {
+  const int B = h->cfg.max_batch, k = h->K, kc = h->kcap;
+  const size_t npair = (size_t)B * k, nent = (size_t)kc + 1, ngp = npair + B;
+  ft::DecodeWork& w = h->w;
+  ft_status s;
+#define A(ptr, n)                                                     \
+  if ((s = alloc_dev(h, (void**)&(ptr), (n) * sizeof(*(ptr)))) != FT_OK) return s;
+  A(w.sel, npair);
+  A(w.gates, npair);
+  A(w.slot_of_pair, npair);
+  A(w.active, (size_t)kc);
+  A(w.hit, (size_t)kc);
+  A(w.miss, (size_t)kc);
+  A(w.victims, (size_t)kc);
+  A(w.copy_u, (size_t)kc);
+  A(w.copy_slot, (size_t)kc);
+  A(w.counts, (size_t)ft::C_NCOUNTS);
+  A(w.g_w, nent);
+  A(w.g_off, nent + 1);
+  A(w.g_pair, ngp);
+  A(w.h, ngp * h->I);
+  A(w.rows, npair * h->H);
+  A(w.shared_rows, (size_t)B * h->H);
+  A(w.blk_count, (size_t)h->H / ft::kRowsPerItem2);
+#undef A
+  w.kmax = kc;
+  FT_CUDA(cudaMemset(w.blk_count, 0, sizeof(uint32_t) * (h->H / ft::kRowsPerItem2)));
+  FT_CUDA(cudaMemset(w.counts, 0, sizeof(int32_t) * ft::C_NCOUNTS));
+  return FT_OK;
+}
+
+// Enqueue one decode layer-step (control -> fill -> gate/up -> down+combine).
+ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const float* logits,
+                        const float* cpart, float* out, float* rows_out) {
+  cudaStream_t cs = h->cs, ts = h->ts;
+  ft::CtrlParams cp{};
+  cp.logits = logits;
+  cp.B = batch;
+  cp.E = h->E;
+  cp.k = h->K;
+  cp.layer = layer;
+  cp.S = h->S;
+  cp.kcap = std::min(batch * h->K, h->E);
+  cp.has_shared = h->cfg.has_shared;
+  cp.bp_mbs = h->bp_mbs;
+  cp.bh_mbs = h->bh_mbs;
+  cp.res = h->res;
+  cp.owner = h->owner;
+  cp.stamp = h->stamp;
+  cp.st = h->st;
+  cp.w = h->w;
+  cp.pool = h->pool;
+  cp.slot_stride = h->lay.stride;
+  cp.shared_w = h->cfg.has_shared ? h->shared_w + (size_t)layer * h->lay.stride : nullptr;
+  cudaEvent_t pa;
+  ft_status s;
+  if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
+  FT_CUDA(ft::launch_control(cp, cs));
+  if ((s = prof_end(h, 0, cs, pa)) != FT_OK) return s;
+
+  // fill on the transfer stream (fork / join with events)
+  FT_CUDA(cudaEventRecord(h->ev_fork, cs));
+  FT_CUDA(cudaStreamWaitEvent(ts, h->ev_fork, 0));
+  if (h->cfg.fill_mode == FT_FILL_KERNEL) {
+    ft::FillParams fp{};
+    fp.counts = h->w.counts;
+    fp.copy_u = h->w.copy_u;
+    fp.copy_slot = h->w.copy_slot;
+    fp.pool = h->pool;
+    fp.lay = h->lay;
+    fp.n_banks = h->n_banks;
+    for (int j = 0; j < h->n_banks; ++j) {
+      fp.src[j] = h->bank[j].dev;
+      fp.src_row[j] = h->bank[j].row;
+    }
+    if ((s = prof_begin(h, ts, &pa)) != FT_OK) return s;
+    FT_CUDA(ft::launch_fill(fp, h->grid_fill, ts));
+    if ((s = prof_end(h, 1, ts, pa)) != FT_OK) return s;
+  } else {
+    // host-driven cudaMemcpyAsync fills: read the copy list, then one copy per bank
+    FT_CUDA(cudaMemcpyAsync(h->counts_host, h->w.counts, sizeof(int32_t) * ft::C_NCOUNTS,
+                            cudaMemcpyDeviceToHost, ts));
+    FT_CUDA(cudaMemcpyAsync(h->copy_host, h->w.copy_u, sizeof(int32_t) * h->kcap, cudaMemcpyDeviceToHost, ts));
+    FT_CUDA(cudaMemcpyAsync(h->copy_host + h->kcap, h->w.copy_slot, sizeof(int32_t) * h->kcap,
+                            cudaMemcpyDeviceToHost, ts));
+    FT_CUDA(cudaStreamSynchronize(ts));
+    const int q = h->counts_host[ft::C_Q];
+    const size_t seg[6] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds};
+    if ((s = prof_begin(h, ts, &pa)) != FT_OK) return s;
+    for (int i = 0; i < q; ++i) {
+      const int u = h->copy_host[i], slot = h->copy_host[h->kcap + i];
+      uint8_t* dst = h->pool + (size_t)slot * h->lay.stride;
+      for (int j = 0; j < h->n_banks; ++j)
+        FT_CUDA(cudaMemcpyAsync(dst + seg[j], h->bank[j].host + (size_t)u * h->bank[j].row, h->bank[j].row,
+                                cudaMemcpyHostToDevice, ts));
+    }
+    if ((s = prof_end(h, 1, ts, pa)) != FT_OK) return s;
+  }
+  FT_CUDA(cudaEventRecord(h->ev_join, ts));
+  FT_CUDA(cudaStreamWaitEvent(cs, h->ev_join, 0));
+
+  ft::EvalParams ep{};
+  ep.counts = h->w.counts;
+  ep.g_w = h->w.g_w;
+  ep.g_off = h->w.g_off;
+  ep.g_pair = h->w.g_pair;
+  ep.gates = h->w.gates;
+  ep.slot_of_pair = h->w.slot_of_pair;
+  ep.x = static_cast<const uint16_t*>(x);
+  ep.h = h->w.h;
+  ep.rows = rows_out ? rows_out : h->w.rows;
+  ep.shared_rows = h->w.shared_rows;
+  ep.c_partial = cpart;
+  ep.out = out;
+  ep.blk_count = h->w.blk_count;
+  ep.error_word = &h->st->error_word;
+  ep.lay = h->lay;
+  ep.H = h->H;
+  ep.I = h->I;
+  ep.k = h->K;
+  ep.B = batch;
+  ep.has_shared = h->cfg.has_shared;
+  if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
+  FT_CUDA(ft::launch_gate_up(ep, h->cfg.wtype, h->grid_eval, cs));
+  if ((s = prof_end(h, 2, cs, pa)) != FT_OK) return s;
+  if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
+  FT_CUDA(ft::launch_down_combine(ep, h->cfg.wtype, h->grid_eval, cs));
+  if ((s = prof_end(h, 3, cs, pa)) != FT_OK) return s;
+  return FT_OK;
+}
+
+ft_status check_step(ft_moe* h, int layer, int batch, const void* x, const float* logits, const float* cpart,
+                     const float* out) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (layer < 0 || layer >= h->L) return fail(FT_ERR_INVALID, "layer %d out of range", layer);
+  if (batch < 1 || batch > h->cfg.max_batch) return fail(FT_ERR_INVALID, "batch %d out of range", batch);
+  if (!x || !logits || !out) return fail(FT_ERR_INVALID, "null x/logits/out");
+  if (!cpart && h->bh_mbs > h->bp_mbs)
+    return fail(FT_ERR_INVALID, "c_partial may be NULL only when B_H <= B_P (every miss filled)");
+  if (h->pf) ft::prefill_interrupt(h->pf);
+  return FT_OK;
+}
+
+}  // namespace
+
+// ============================================================ ABI entry points
+extern "C" {
+
+const char* ft_last_error(void) { return g_last_error.c_str(); }
+
+ft_status ft_split_misses(int m, double bp_gbps, double bh_gbps, int evictable, int* q_out) {
+  if (!q_out || m < 0 || evictable < 0 || !(bp_gbps > 0) || !(bh_gbps > 0))
+    return fail(FT_ERR_INVALID, "ft_split_misses: bad argument");
+  const long long bp = to_mbps(bp_gbps), bh = to_mbps(bh_gbps);
+  long long q;
+  if (m == 0) {
+    q = 0;
+  } else if (bh <= bp) {
+    q = m;
+  } else {
+    q = (2LL * m * bp + bh) / (2LL * bh);
+    if (q < 1) q = 1;
+  }
+  q = std::min<long long>({q, (long long)m, (long long)evictable});
+  *q_out = (int)q;
+  return FT_OK;
+}
+
+ft_status ft_bench_bw(size_t bytes, int iters, double* bp_gbps) {
+  if (!bp_gbps || bytes < 1024 || iters < 1) return fail(FT_ERR_INVALID, "ft_bench_bw: bad argument");
+  void *hbuf = nullptr, *dbuf = nullptr;
+  cudaStream_t s = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ft_status st = FT_OK;
+  float ms = 0.f;
+  if (cudaHostAlloc(&hbuf, bytes, cudaHostAllocDefault) != cudaSuccess) {
+    st = fail(FT_ERR_PIN, "cudaHostAlloc(%zu) failed", bytes);
+    goto done;
+  }
+  if (cudaMalloc(&dbuf, bytes) != cudaSuccess) {
+    st = fail(FT_ERR_NOMEM, "cudaMalloc(%zu) failed", bytes);
+    goto done;
+  }
+  memset(hbuf, 1, bytes);
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess || cudaEventCreate(&a) != cudaSuccess ||
+      cudaEventCreate(&b) != cudaSuccess) {
+    st = fail(FT_ERR_CUDA, "stream/event creation failed");
+    goto done;
+  }
+  cudaMemcpyAsync(dbuf, hbuf, bytes, cudaMemcpyHostToDevice, s);  // warm-up
+  cudaEventRecord(a, s);
+  for (int i = 0; i < iters; ++i) cudaMemcpyAsync(dbuf, hbuf, bytes, cudaMemcpyHostToDevice, s);
+  cudaEventRecord(b, s);
+  if (cudaEventSynchronize(b) != cudaSuccess || cudaEventElapsedTime(&ms, a, b) != cudaSuccess || ms <= 0.f) {
+    st = fail(FT_ERR_CUDA, "timing failed: %s", cudaGetErrorString(cudaGetLastError()));
+    goto done;
+  }
+  *bp_gbps = (double)bytes * iters / (ms * 1e-3) / 1e9;
+done:
+  if (a) cudaEventDestroy(a);
+  if (b) cudaEventDestroy(b);
+  if (s) cudaStreamDestroy(s);
+  if (dbuf) cudaFree(dbuf);
+  if (hbuf) cudaFreeHost(hbuf);
+  return st;
+}
+
+static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* host_pool, const ft_banks* shared) {
+  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128;
+  ft_status s;
+  h->cfg = *cfg;
+  h->dev = cfg->device;
+  FT_CUDA(cudaSetDevice(h->dev));
+  FT_CUDA(cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev));
+  h->L = cfg->n_layers;
+  h->E = cfg->n_experts;
+  h->K = cfg->top_k;
+  h->H = cfg->hidden;
+  h->I = cfg->inter;
+  h->S = cfg->cache_slots;
+  h->kcap = std::min(cfg->max_batch * cfg->top_k, cfg->n_experts);
+  h->lay = ft::make_layout(cfg->wtype, h->H, h->I);
+  h->n_banks = fp8 ? 6 : 3;
+  h->grid_eval = h->n_sm * 4;
+  h->grid_fill = h->n_sm * 2;
+  if (cfg->compute_stream) {
+    h->cs = (cudaStream_t)cfg->compute_stream;
+  } else {
+    FT_CUDA(cudaStreamCreateWithFlags(&h->cs, cudaStreamNonBlocking));
+    h->own_cs = true;
+  }
+  if (cfg->transfer_stream) {
+    h->ts = (cudaStream_t)cfg->transfer_stream;
+  } else {
+    FT_CUDA(cudaStreamCreateWithFlags(&h->ts, cudaStreamNonBlocking));
+    h->own_ts = true;
+  }
+  FT_CUDA(cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming));
+  FT_CUDA(cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming));
+  FT_CUDA(cudaEventCreateWithFlags(&h->ev_ctrl, cudaEventDisableTiming));
+
+  // bandwidths for the split rule (integer MB/s on the device)
+  h->bh_gbps = cfg->bh_gbps;
+  h->bp_gbps = cfg->bp_gbps;
+  if (!(h->bp_gbps > 0) && (s = ft_bench_bw((size_t)256 << 20, 8, &h->bp_gbps)) != FT_OK) return s;
+  h->bp_mbs = to_mbps(h->bp_gbps);
+  h->bh_mbs = to_mbps(h->bh_gbps);
+
+  // host pool: pin + map every bank
+  const size_t nlog = (size_t)h->L * h->E;
+  const void* bp[6] = {host_pool->gate, host_pool->up, host_pool->down,
+                       host_pool->gate_scale, host_pool->up_scale, host_pool->down_scale};
+  const size_t rows[6] = {h->lay.gate_b, h->lay.gate_b, h->lay.down_b, h->lay.gs_b, h->lay.gs_b, h->lay.ds_b};
+  for (int j = 0; j < h->n_banks; ++j) {
+    if (rows[j] % 16) return fail(FT_ERR_INVALID, "bank row bytes not a multiple of 16");
+    if ((s = register_bank(h->bank[j], bp[j], rows[j], nlog)) != FT_OK) return s;
+  }
+
+  // HBM: slot pool, shared experts, state, work lists
+  {
+    cudaError_t e = cudaMalloc(&h->pool, (size_t)h->S * h->lay.stride);
+    if (e != cudaSuccess)
+      return fail(FT_ERR_NOMEM, "slot pool of %d x %zu bytes: %s", h->S, h->lay.stride, cudaGetErrorString(e));
+  }
+  if (cfg->has_shared) {
+    FT_CUDA(cudaMalloc(&h->shared_w, (size_t)h->L * h->lay.stride));
+    const void* sp[6] = {shared->gate, shared->up, shared->down, shared->gate_scale, shared->up_scale,
+                         shared->down_scale};
+    const size_t seg[6] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds};
+    for (int l = 0; l < h->L; ++l)
+      for (int j = 0; j < h->n_banks; ++j)
+        FT_CUDA(cudaMemcpy(h->shared_w + (size_t)l * h->lay.stride + seg[j],
+                           static_cast<const uint8_t*>(sp[j]) + (size_t)l * rows[j], rows[j], cudaMemcpyHostToDevice));
+  }
+  if ((s = alloc_dev(h, (void**)&h->res, sizeof(int32_t) * nlog)) != FT_OK) return s;
+  if ((s = alloc_dev(h, (void**)&h->owner, sizeof(int32_t) * h->S)) != FT_OK) return s;
+  if ((s = alloc_dev(h, (void**)&h->stamp, sizeof(uint32_t) * h->S)) != FT_OK) return s;
+  if ((s = alloc_dev(h, (void**)&h->st, sizeof(ft::DevState))) != FT_OK) return s;
+  FT_CUDA(cudaMemset(h->res, 0xff, sizeof(int32_t) * nlog));
+  FT_CUDA(cudaMemset(h->owner, 0xff, sizeof(int32_t) * h->S));
+  FT_CUDA(cudaMemset(h->stamp, 0, sizeof(uint32_t) * h->S));
+  FT_CUDA(cudaMemset(h->st, 0, sizeof(ft::DevState)));
+  if ((s = alloc_work(h)) != FT_OK) return s;
+  FT_CUDA(cudaHostAlloc((void**)&h->counts_host, sizeof(int32_t) * ft::C_NCOUNTS, cudaHostAllocDefault));
+  FT_CUDA(cudaHostAlloc((void**)&h->copy_host, sizeof(int32_t) * 2 * h->kcap, cudaHostAllocDefault));
+  FT_CUDA(ft::prepare_kernels(h->cfg.wtype, h->H, h->I));
+  FT_CUDA(cudaDeviceSynchronize());
+  return FT_OK;
+}
+
+ft_status ft_moe_init(const ft_moe_config* cfg, const ft_banks* host_pool, const ft_banks* shared, ft_moe** out) {
+  ft_status s = check_cfg(cfg);
+  if (s != FT_OK) return s;
+  if (!out || !host_pool || !host_pool->gate || !host_pool->up || !host_pool->down)
+    return fail(FT_ERR_INVALID, "null host pool / out");
+  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128;
+  if (fp8 && (!host_pool->gate_scale || !host_pool->up_scale || !host_pool->down_scale))
+    return fail(FT_ERR_INVALID, "FP8 banks need scale arrays");
+  if (cfg->has_shared && (!shared || !shared->gate || !shared->up || !shared->down ||
+                          (fp8 && (!shared->gate_scale || !shared->up_scale || !shared->down_scale))))
+    return fail(FT_ERR_INVALID, "has_shared set but shared banks missing");
+  *out = nullptr;
+  ft_moe* h = new ft_moe();
+  s = init_body(h, cfg, host_pool, shared);
+  if (s != FT_OK) {
+    std::string keep = g_last_error;
+    ft_moe_destroy(h);
+    g_last_error = keep;
+    return s;
+  }
+  *out = h;
+  return FT_OK;
+}
+
+ft_status ft_moe_decode_step(ft_moe* h, int layer, int batch, const void* x_bf16, const float* logits,
+                             const float* c_partial, float* out, float* rows_out) {
+  ft_status s = check_step(h, layer, batch, x_bf16, logits, c_partial, out);
+  if (s != FT_OK) return s;
+  if (h->cfg.fill_mode == FT_FILL_MEMCPY && capturing(h->cs))
+    return fail(FT_ERR_STATE, "FT_FILL_MEMCPY steps cannot be captured into a graph");
+  FT_CUDA(cudaSetDevice(h->dev));
+  return enqueue_layer(h, layer, batch, x_bf16, logits, c_partial, out, rows_out);
+}
+
+ft_status ft_moe_decode_layers(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_bf16,
+                               const float* logits, const float* c_partial, float* out, float* rows_out) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > h->L)
+    return fail(FT_ERR_INVALID, "layer range [%d, %d) out of range", first_layer, first_layer + n_layers);
+  const size_t H = h->H, E = h->E, K = h->K;
+  for (int i = 0; i < n_layers; ++i) {
+    const size_t b = (size_t)i * batch;
+    ft_status s = ft_moe_decode_step(
+        h, first_layer + i, batch, static_cast<const uint16_t*>(x_bf16) + b * H, logits + b * E,
+        c_partial ? c_partial + b * K * H : nullptr, out + b * H, rows_out ? rows_out + b * K * H : nullptr);
+    if (s != FT_OK) return s;
+  }
+  return FT_OK;
+}
+
+ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_bf16,
+                                      const float* logits, const float* c_partial, float* out, float* rows_out,
+                                      ft_graph** g) {
+  if (!h || !g) return fail(FT_ERR_INVALID, "null handle/graph");
+  if (h->cfg.fill_mode != FT_FILL_KERNEL) return fail(FT_ERR_STATE, "graph capture needs FT_FILL_KERNEL");
+  if (h->prof) return fail(FT_ERR_STATE, "turn profiling off before capturing");
+  FT_CUDA(cudaSetDevice(h->dev));
+  std::unique_ptr<ft_graph> gr(new ft_graph());
+  gr->owner = h;
+  FT_CUDA(cudaStreamBeginCapture(h->cs, cudaStreamCaptureModeThreadLocal));
+  ft_status s = ft_moe_decode_layers(h, first_layer, n_layers, batch, x_bf16, logits, c_partial, out, rows_out);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->cs, &graph);
+  if (s != FT_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return s;
+  }
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "capture failed: %s", cudaGetErrorString(e));
+  gr->graph = graph;
+  e = cudaGraphInstantiate(&gr->exec, graph, 0);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  *g = gr.release();
+  h->graphs.push_back(*g);
+  return FT_OK;
+}
+
+ft_status ft_graph_launch(ft_graph* g) {
+  if (!g || !g->exec) return fail(FT_ERR_INVALID, "null graph");
+  if (g->owner->pf) ft::prefill_interrupt(g->owner->pf);
+  FT_CUDA(cudaGraphLaunch(g->exec, g->owner->cs));
+  return FT_OK;
+}
+
+ft_status ft_graph_destroy(ft_graph* g) {
+  if (!g) return FT_OK;
+  if (g->owner) {
+    auto& v = g->owner->graphs;
+    v.erase(std::remove(v.begin(), v.end(), g), v.end());
+  }
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+  return FT_OK;
+}
+
+ft_status ft_moe_decode_layers_host(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_host,
+                                    const float* logits_host, const float* c_partial_host, float* out_host,
+                                    int use_graph) {
+  if (!h || !x_host || !logits_host) return fail(FT_ERR_INVALID, "null argument");
+  if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > h->L)
+    return fail(FT_ERR_INVALID, "layer range out of range");
+  if (batch < 1 || batch > h->cfg.max_batch) return fail(FT_ERR_INVALID, "batch out of range");
+  FT_CUDA(cudaSetDevice(h->dev));
+  const size_t L = h->L, B = h->cfg.max_batch, H = h->H, E = h->E, K = h->K;
+  if (!h->stg_x) {
+    ft_status s;
+    if ((s = alloc_dev(h, (void**)&h->stg_x, sizeof(uint16_t) * L * B * H)) != FT_OK) return s;
+    if ((s = alloc_dev(h, (void**)&h->stg_logits, sizeof(float) * L * B * E)) != FT_OK) return s;
+    if ((s = alloc_dev(h, (void**)&h->stg_cp, sizeof(float) * L * B * K * H)) != FT_OK) return s;
+    if ((s = alloc_dev(h, (void**)&h->stg_out, sizeof(float) * L * B * H)) != FT_OK) return s;
+  }
+  const size_t nb = (size_t)n_layers * batch;
+  FT_CUDA(cudaMemcpyAsync(h->stg_x, x_host, sizeof(uint16_t) * nb * H, cudaMemcpyHostToDevice, h->cs));
+  FT_CUDA(cudaMemcpyAsync(h->stg_logits, logits_host, sizeof(float) * nb * E, cudaMemcpyHostToDevice, h->cs));
+  if (c_partial_host)
+    FT_CUDA(cudaMemcpyAsync(h->stg_cp, c_partial_host, sizeof(float) * nb * K * H, cudaMemcpyHostToDevice, h->cs));
+  const float* cp = c_partial_host ? h->stg_cp : nullptr;
+  ft_status s;
+  if (use_graph && h->cfg.fill_mode == FT_FILL_KERNEL && !h->prof) {
+    auto key = std::make_tuple(first_layer, n_layers, batch * 2 + (cp ? 1 : 0));
+    auto it = h->host_graphs.find(key);
+    ft_graph* g = nullptr;
+    if (it == h->host_graphs.end()) {
+      s = ft_moe_graph_capture_decode(h, first_layer, n_layers, batch, h->stg_x, h->stg_logits, cp, h->stg_out,
+                                      nullptr, &g);
+      if (s != FT_OK) return s;
+      h->host_graphs[key] = g;
+    } else {
+      g = it->second;
+    }
+    if ((s = ft_graph_launch(g)) != FT_OK) return s;
+  } else {
+    s = ft_moe_decode_layers(h, first_layer, n_layers, batch, h->stg_x, h->stg_logits, cp, h->stg_out, nullptr);
+    if (s != FT_OK) return s;
+  }
+  if (out_host)
+    FT_CUDA(cudaMemcpyAsync(out_host, h->stg_out, sizeof(float) * nb * H, cudaMemcpyDeviceToHost, h->cs));
+  FT_CUDA(cudaStreamSynchronize(h->cs));
+  return FT_OK;
+}
+
+ft_status ft_moe_synchronize(ft_moe* h) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  FT_CUDA(cudaSetDevice(h->dev));
+  FT_CUDA(cudaStreamSynchronize(h->ts));
+  FT_CUDA(cudaStreamSynchronize(h->cs));
+  return FT_OK;
+}
+
+ft_status ft_moe_get_stats(ft_moe* h, ft_stats* out) {
+  if (!h || !out) return fail(FT_ERR_INVALID, "null argument");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  ft::DevState d{};
+  FT_CUDA(cudaMemcpy(&d, h->st, sizeof d, cudaMemcpyDeviceToHost));
+  out->hits = d.hits;
+  out->misses = d.misses;
+  out->fills = d.fills;
+  out->cpu_execs = d.cpu_execs;
+  out->evictions = d.evictions;
+  out->decode_steps = d.decode_steps;
+  out->prefill_layers = d.prefill_layers;
+  out->eval_entries = d.eval_entries;
+  out->eval_pairs = d.eval_pairs;
+  out->error_word = d.error_word;
+  out->clock = d.clock;
+  out->bp_gbps = h->bp_gbps;
+  out->bh_gbps = h->bh_gbps;
+  out->cache_slots = h->S;
+  return FT_OK;
+}
+
+ft_status ft_moe_get_step_trace(ft_moe* h, ft_step_trace* t) {
+  if (!h || !t) return fail(FT_ERR_INVALID, "null argument");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  int32_t c[ft::C_NCOUNTS];
+  FT_CUDA(cudaMemcpy(c, h->w.counts, sizeof c, cudaMemcpyDeviceToHost));
+  t->layer = c[ft::C_LAYER];
+  t->batch = c[ft::C_BATCH];
+  t->q = c[ft::C_Q];
+  t->n_active = c[ft::C_NACTIVE];
+  t->n_hit = c[ft::C_NHIT];
+  t->n_miss = c[ft::C_NMISS];
+  t->n_victims = c[ft::C_NVICT];
+  t->n_cpu = c[ft::C_NMISS] - c[ft::C_Q];
+  t->clock = (uint32_t)c[ft::C_CLOCK];
+  const size_t np = (size_t)t->batch * h->K;
+  if (t->sel) FT_CUDA(cudaMemcpy(t->sel, h->w.sel, np * 4, cudaMemcpyDeviceToHost));
+  if (t->gates) FT_CUDA(cudaMemcpy(t->gates, h->w.gates, np * 4, cudaMemcpyDeviceToHost));
+  if (t->slot_of_pair) FT_CUDA(cudaMemcpy(t->slot_of_pair, h->w.slot_of_pair, np * 4, cudaMemcpyDeviceToHost));
+  if (t->active && t->n_active) FT_CUDA(cudaMemcpy(t->active, h->w.active, (size_t)t->n_active * 4, cudaMemcpyDeviceToHost));
+  if (t->hit && t->n_hit) FT_CUDA(cudaMemcpy(t->hit, h->w.hit, (size_t)t->n_hit * 4, cudaMemcpyDeviceToHost));
+  if (t->miss && t->n_miss) FT_CUDA(cudaMemcpy(t->miss, h->w.miss, (size_t)t->n_miss * 4, cudaMemcpyDeviceToHost));
+  if (t->victims && t->n_victims)
+    FT_CUDA(cudaMemcpy(t->victims, h->w.victims, (size_t)t->n_victims * 4, cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+ft_status ft_moe_get_state(ft_moe* h, int32_t* res, int32_t* owner, uint32_t* stamp, uint32_t* clock) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  if (res) FT_CUDA(cudaMemcpy(res, h->res, sizeof(int32_t) * h->L * h->E, cudaMemcpyDeviceToHost));
+  if (owner) FT_CUDA(cudaMemcpy(owner, h->owner, sizeof(int32_t) * h->S, cudaMemcpyDeviceToHost));
+  if (stamp) FT_CUDA(cudaMemcpy(stamp, h->stamp, sizeof(uint32_t) * h->S, cudaMemcpyDeviceToHost));
+  if (clock) {
+    ft::DevState d{};
+    FT_CUDA(cudaMemcpy(&d, h->st, sizeof d, cudaMemcpyDeviceToHost));
+    *clock = d.clock;
+  }
+  return FT_OK;
+}
+
+ft_status ft_moe_set_profiling(ft_moe* h, int enable) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  h->prof = enable != 0;
+  return FT_OK;
+}
+
+ft_status ft_moe_get_profile(ft_moe* h, ft_profile* out, int reset) {
+  if (!h || !out) return fail(FT_ERR_INVALID, "null argument");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  for (auto& r : h->prof_live) {
+    float ms = 0.f;
+    FT_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+    h->prof_acc.launches[r.kind] += 1;
+    h->prof_acc.total_ms[r.kind] += ms;
+    h->ev_free.push_back(r.a);
+    h->ev_free.push_back(r.b);
+  }
+  h->prof_live.clear();
+  *out = h->prof_acc;
+  if (reset) h->prof_acc = ft_profile{};
+  return FT_OK;
+}
+
+ft_status ft_moe_set_stream(ft_moe* h, void* compute_stream) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  if (h->own_cs && h->cs) cudaStreamDestroy(h->cs);
+  if (compute_stream) {
+    h->cs = (cudaStream_t)compute_stream;
+    h->own_cs = false;
+  } else {
+    FT_CUDA(cudaStreamCreateWithFlags(&h->cs, cudaStreamNonBlocking));
+    h->own_cs = true;
+  }
+  return FT_OK;
+}
+
+ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x_bf16, const float* logits,
+                               float* out) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (layer < 0 || layer >= h->L) return fail(FT_ERR_INVALID, "layer %d out of range", layer);
+  if (n_tokens < 1 || n_tokens > h->cfg.max_prefill_tokens)
+    return fail(FT_ERR_INVALID, "n_tokens %d outside [1, max_prefill_tokens=%d]", n_tokens, h->cfg.max_prefill_tokens);
+  if (!x_bf16 || !logits || !out) return fail(FT_ERR_INVALID, "null x/logits/out");
+  if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
+  if (h->S < 2 * h->E)
+    return fail(FT_ERR_CAPACITY, "prefill double buffering needs >= 2E = %d slots (have %d)", 2 * h->E, h->S);
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
+  FT_CUDA(cudaSetDevice(h->dev));
+  ft::PrefillCtx c{};
+  c.cs = h->cs;
+  c.ts = h->ts;
+  c.L = h->L;
+  c.E = h->E;
+  c.K = h->K;
+  c.H = h->H;
+  c.I = h->I;
+  c.S = h->S;
+  c.has_shared = h->cfg.has_shared;
+  c.max_tokens = h->cfg.max_prefill_tokens;
+  c.n_sm = h->n_sm;
+  c.lay = h->lay;
+  c.pool = h->pool;
+  c.shared_w = h->shared_w;
+  c.res = h->res;
+  c.owner = h->owner;
+  c.stamp = h->stamp;
+  c.st = h->st;
+  for (int j = 0; j < 3; ++j) {
+    c.bank_host[j] = h->bank[j].host;
+    c.bank_row[j] = h->bank[j].row;
+  }
+  c.prof = h->prof;
+  if (!h->pf) {
+    cudaError_t e = ft::prefill_create(&h->pf, c);
+    if (e != cudaSuccess) return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA,
+                                      "prefill buffers: %s", cudaGetErrorString(e));
+  }
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev;
+  std::string err;
+  cudaError_t e = ft::prefill_layer(h->pf, c, layer, n_tokens, static_cast<const uint16_t*>(x_bf16), logits, out,
+                                    h->prof ? &ev : nullptr, &err);
+  for (auto& r : ev) h->prof_live.push_back({r.first, r.second.first, r.second.second});
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill layer %d: %s %s", layer, cudaGetErrorString(e), err.c_str());
+  return FT_OK;
+}
+
+ft_status ft_cache_resize(ft_moe* h, int new_slots) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (new_slots < 1 || new_slots > (1 << 20)) return fail(FT_ERR_INVALID, "new_slots out of range");
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "resize during capture");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  if (h->pf) ft::prefill_interrupt(h->pf), ft_moe_synchronize(h);
+  const int S = h->S, n = new_slots;
+  const size_t nlog = (size_t)h->L * h->E;
+  std::vector<int32_t> res(nlog), owner(S);
+  std::vector<uint32_t> stamp(S);
+  FT_CUDA(cudaMemcpy(res.data(), h->res, nlog * 4, cudaMemcpyDeviceToHost));
+  FT_CUDA(cudaMemcpy(owner.data(), h->owner, (size_t)S * 4, cudaMemcpyDeviceToHost));
+  FT_CUDA(cudaMemcpy(stamp.data(), h->stamp, (size_t)S * 4, cudaMemcpyDeviceToHost));
+  const size_t stride = h->lay.stride;
+  if (n >= S) {
+    uint8_t* np = nullptr;
+    cudaError_t e = cudaMalloc(&np, (size_t)n * stride);
+    if (e != cudaSuccess) return fail(FT_ERR_NOMEM, "grow pool to %d slots: %s", n, cudaGetErrorString(e));
+    FT_CUDA(cudaMemcpy(np, h->pool, (size_t)S * stride, cudaMemcpyDeviceToDevice));
+    cudaFree(h->pool);
+    h->pool = np;
+    owner.resize(n, -1);
+    stamp.resize(n, 0u);
+  } else {
+    // keep the n most recent entries (stamp desc, slot asc)
+    std::vector<int> occ;
+    for (int sl = 0; sl < S; ++sl)
+      if (owner[sl] >= 0) occ.push_back(sl);
+    std::stable_sort(occ.begin(), occ.end(), [&](int a, int b) {
+      return stamp[a] != stamp[b] ? stamp[a] > stamp[b] : a < b;
+    });
+    std::vector<char> keep(S, 0);
+    for (size_t i = 0; i < occ.size() && (int)i < n; ++i) keep[occ[i]] = 1;
+    for (int sl = 0; sl < S; ++sl)
+      if (owner[sl] >= 0 && !keep[sl]) {
+        res[owner[sl]] = -1;
+        owner[sl] = -1;
+        stamp[sl] = 0;
+      }
+    std::vector<int> movers, freeb;
+    for (int sl = n; sl < S; ++sl)
+      if (keep[sl]) movers.push_back(sl);
+    for (int sl = 0; sl < n; ++sl)
+      if (!keep[sl]) freeb.push_back(sl);
+    for (size_t i = 0; i < movers.size(); ++i) {
+      const int src = movers[i], dst = freeb[i];
+      FT_CUDA(cudaMemcpyAsync(h->pool + (size_t)dst * stride, h->pool + (size_t)src * stride, h->lay.used,
+                              cudaMemcpyDeviceToDevice, h->cs));
+      owner[dst] = owner[src];
+      stamp[dst] = stamp[src];
+      res[owner[dst]] = dst;
+    }
+    owner.resize(n);
+    stamp.resize(n);
+    FT_CUDA(cudaStreamSynchronize(h->cs));
+  }
+  int32_t* nowner = nullptr;
+  uint32_t* nstamp = nullptr;
+  FT_CUDA(cudaMalloc(&nowner, (size_t)n * 4));
+  FT_CUDA(cudaMalloc(&nstamp, (size_t)n * 4));
+  FT_CUDA(cudaMemcpy(nowner, owner.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  FT_CUDA(cudaMemcpy(nstamp, stamp.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
+  FT_CUDA(cudaMemcpy(h->res, res.data(), nlog * 4, cudaMemcpyHostToDevice));
+  for (auto& p : h->allocs) {
+    if (p == h->owner) p = nowner;
+    if (p == h->stamp) p = nstamp;
+  }
+  cudaFree(h->owner);
+  cudaFree(h->stamp);
+  h->owner = nowner;
+  h->stamp = nstamp;
+  h->S = n;
+  h->cfg.cache_slots = n;
+  // graphs captured earlier hold old pointers and sizes: drop them
+  for (auto& kv : h->host_graphs) ft_graph_destroy(kv.second);
+  h->host_graphs.clear();
+  for (ft_graph* g : h->graphs) g->owner = nullptr;
+  h->graphs.clear();
+  if (h->pf) {
+    ft::prefill_destroy(h->pf);
+    h->pf = nullptr;
+  }
+  return FT_OK;
+}
+
+ft_status ft_moe_destroy(ft_moe* h) {
+  if (!h) return FT_OK;
+  cudaSetDevice(h->dev);
+  if (h->cs) cudaStreamSynchronize(h->cs);
+  if (h->ts) cudaStreamSynchronize(h->ts);
+  for (auto& kv : h->host_graphs) ft_graph_destroy(kv.second);
+  for (ft_graph* g : h->graphs) g->owner = nullptr;
+  if (h->pf) ft::prefill_destroy(h->pf);
+  for (auto& r : h->prof_live) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : h->ev_free) cudaEventDestroy(e);
+  for (void* p : h->allocs) cudaFree(p);
+  if (h->pool) cudaFree(h->pool);
+  if (h->shared_w) cudaFree(h->shared_w);
+  if (h->counts_host) cudaFreeHost(h->counts_host);
+  if (h->copy_host) cudaFreeHost(h->copy_host);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->ev_ctrl) cudaEventDestroy(h->ev_ctrl);
+  for (auto& b : h->bank)
+    if (b.registered) cudaHostUnregister(const_cast<uint8_t*>(b.host));
+  if (h->own_cs && h->cs) cudaStreamDestroy(h->cs);
+  if (h->own_ts && h->ts) cudaStreamDestroy(h->ts);
+  delete h;
+  return FT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,451 @@
+// Per-layer decode control kernel: one CTA does every routing-dependent decision of
+// a decode layer-step on the device, so the step needs no host synchronisation and
+// can replay inside a CUDA graph.
+//
+// Order of work ("FreeToken 完全拆解", section "Device-side 缓存控制"):
+//   route (top-k softmax per token) -> dedupe over the batch -> classify against the
+//   residency table -> fill count q -> one scan for the K least recently used slots
+//   -> install the first q misses in the first q victims -> rewrite routed ids to
+//   slots or FT_CPU -> fixed-shape evaluation lists with device-resident counts.
+// Split rule: "FreeToken 完全拆解", section "q* 策略"; residual bandwidth
+// max(B_H-B_P, 0): "개인 장치에서 MoE 모델을 서빙하는 FreeToken", paragraph on the miss split.
+#include <cfloat>
+#include <climits>
+
+#include "ft_internal.cuh"
+
+namespace ft {
+namespace {
+
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  // total order: larger logit first, then lower expert id
+  return v > bv || (v == bv && e < be);
+}
+
+// Fill count: q = clamp(floor(m*bp/bh + 1/2), 1, m) for m > 0; all misses when the
+// residual bandwidth B_H - B_P is not positive; never more than `evictable`.
+__device__ __forceinline__ int split_q(int m, long long bp, long long bh, int evictable) {
+  if (m <= 0) return 0;
+  long long q;
+  if (bh <= bp) {
+    q = m;
+  } else {
+    q = (2LL * m * bp + bh) / (2LL * bh);
+    if (q < 1) q = 1;
+  }
+  if (q > m) q = m;
+  if (q > evictable) q = evictable;
+  return q < 0 ? 0 : (int)q;
+}
+
+template <int NPL>  // logits held per lane: E <= 32*NPL
+__device__ void route_token(const CtrlParams& p, int t, int lane, int* s_sel, uint32_t* s_bitmap,
+                            uint32_t* s_err) {
+  const float* z = p.logits + (size_t)t * p.E;
+  float v[NPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    int e = lane + 32 * j;
+    float x = -INFINITY;
+    if (e < p.E) {
+      x = __ldg(z + e);
+      if (x != x) {  // NaN: ranked as -inf, reported
+        x = -INFINITY;
+        atomicOr(s_err, FT_DEVERR_NAN_LOGIT);
+      }
+    } else {
+      taken |= 1u << j;  // not an expert
+    }
+    v[j] = x;
+  }
+  int my_e = INT_MAX;
+  float my_z = -INFINITY, zmax = -INFINITY;
+  for (int r = 0; r < p.k; ++r) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      int e = lane + 32 * j;
+      if (!(taken & (1u << j)) && better(v[j], e, bv, be)) {
+        bv = v[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == r) {
+      my_e = be;
+      my_z = bv;
+    }
+    if (r == 0) zmax = bv;
+  }
+  // rank of this lane's id among the k chosen ids -> ascending-id position
+  int rank = 0;
+  for (int j = 0; j < p.k; ++j) {
+    int oe = __shfl_sync(0xffffffffu, my_e, j);
+    if (lane < p.k && oe < my_e) ++rank;
+  }
+  float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < p.k) {
+    int idx = t * p.k + rank;
+    p.w.sel[idx] = my_e;
+    p.w.gates[idx] = ex / sum;
+    s_sel[idx] = my_e;
+    atomicOr(&s_bitmap[my_e >> 5], 1u << (my_e & 31));
+  }
+}
+
+__global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) {
+  __shared__ uint32_t s_bitmap[kMaxE / 32];
+  __shared__ int s_sel[kMaxPairs];
+  __shared__ int s_active[kMaxE];
+  __shared__ int s_hit[kMaxE];
+  __shared__ int s_miss[kMaxE];
+  __shared__ int s_gidx[kMaxE];
+  __shared__ int s_victims[kMaxE];
+  __shared__ unsigned long long s_vkeys[kMaxE];
+  __shared__ uint32_t s_hist[256];
+  __shared__ int s_gcount[kMaxE + 1];
+  __shared__ uint32_t s_err;
+  __shared__ uint32_t s_clock;
+  __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand;
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_kk;
+  __shared__ uint32_t s_lo, s_hi;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E, k = p.k, B = p.B, S = p.S;
+  const int base_u = p.layer * E;
+
+  for (int i = tid; i < kMaxE / 32; i += blockDim.x) s_bitmap[i] = 0;
+  for (int i = tid; i < E; i += blockDim.x) s_gidx[i] = -1;
+  if (tid == 0) {
+    s_err = 0;
+    s_clock = p.st->clock + 1u;
+    s_evict = 0;
+    s_nv = 0;
+    s_lo = UINT_MAX;
+    s_hi = 0;
+    s_ncand = 0;
+  }
+  __syncthreads();
+  const uint32_t clock = s_clock;
+
+  // ---- 1. route: one warp per token
+  for (int t = warp; t < B; t += blockDim.x / 32) {
+    if (E <= 32) route_token<1>(p, t, lane, s_sel, s_bitmap, &s_err);
+    else if (E <= 64) route_token<2>(p, t, lane, s_sel, s_bitmap, &s_err);
+    else if (E <= 128) route_token<4>(p, t, lane, s_sel, s_bitmap, &s_err);
+    else if (E <= 256) route_token<8>(p, t, lane, s_sel, s_bitmap, &s_err);
+    else if (E <= 512) route_token<16>(p, t, lane, s_sel, s_bitmap, &s_err);
+    else route_token<32>(p, t, lane, s_sel, s_bitmap, &s_err);
+  }
+  __syncthreads();
+
+  // ---- 2. dedupe + classify (warp 0; A is at most min(B*k, E) ids)
+  if (warp == 0) {
+    const int nwords = (E + 31) / 32;
+    uint32_t word = lane < nwords ? s_bitmap[lane] : 0u;
+    int cnt = __popc(word), incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int pos = incl - cnt;
+    while (word) {
+      int b = __ffs(word) - 1;
+      word &= word - 1;
+      s_active[pos++] = base_u + lane * 32 + b;
+    }
+    const int nact = __shfl_sync(0xffffffffu, incl, 31);
+    int nh = 0, nm = 0;
+    for (int c = 0; c < nact; c += 32) {
+      int i = c + lane;
+      int u = i < nact ? s_active[i] : -1;
+      int slot = u >= 0 ? p.res[u] : -1;
+      if (slot >= S) {  // cannot happen with a consistent table
+        atomicOr(&s_err, FT_DEVERR_BAD_STATE);
+        slot = -1;
+      }
+      bool valid = i < nact, hit = valid && slot >= 0;
+      uint32_t hb = __ballot_sync(0xffffffffu, hit);
+      uint32_t mb = __ballot_sync(0xffffffffu, valid && !hit);
+      uint32_t lt = (1u << lane) - 1u;
+      if (hit) {
+        s_hit[nh + __popc(hb & lt)] = u;
+        p.stamp[slot] = clock;  // hit refreshes recency
+      } else if (valid) {
+        s_miss[nm + __popc(mb & lt)] = u;
+      }
+      nh += __popc(hb);
+      nm += __popc(mb);
+    }
+    if (lane == 0) {
+      s_nactive = nact;
+      s_nhit = nh;
+      s_nmiss = nm;
+      s_q = split_q(nm, p.bp_mbs, p.bh_mbs, S - nh);
+    }
+  }
+  __syncthreads();
+
+  const int q = s_q;
+  const int kcap = p.kcap;
+
+  // ---- 3. one-pass K-LRU victim scan over slots not hit in this step
+  if (q > 0) {
+    // range of candidate stamps and their count
+    uint32_t lo = UINT_MAX, hi = 0;
+    int nc = 0;
+    for (int s = tid; s < S; s += blockDim.x) {
+      uint32_t st = p.stamp[s];
+      if (st < clock) {
+        lo = min(lo, st);
+        hi = max(hi, st);
+        ++nc;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      nc += __shfl_xor_sync(0xffffffffu, nc, o);
+    }
+    if (lane == 0) {
+      atomicMin(&s_lo, lo);
+      atomicMax(&s_hi, hi);
+      atomicAdd(&s_ncand, nc);
+    }
+    __syncthreads();
+    const uint32_t st_lo = s_lo;
+    const int ncand = s_ncand;
+    const int want = min(kcap, ncand);
+    const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
+    const uint32_t range = s_hi - st_lo;
+    const int width = (range ? 32 - __clz(range) : 0) + sbits;
+    auto key_of = [&](int s, uint32_t st) -> unsigned long long {
+      return ((unsigned long long)(st - st_lo) << sbits) | (unsigned long long)s;
+    };
+    unsigned long long thresh = ~0ull;
+    if (want < ncand) {
+      // radix select of the want-th smallest key, 8 bits per pass, most significant first
+      const int passes = (width + 7) / 8;
+      if (tid == 0) {
+        s_prefix = 0;
+        s_kk = want;
+      }
+      __syncthreads();
+      for (int ps = passes - 1; ps >= 0; --ps) {
+        const int shift = ps * 8;
+        for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0;
+        __syncthreads();
+        const unsigned long long pre = s_prefix;
+        for (int s = tid; s < S; s += blockDim.x) {
+          uint32_t st = p.stamp[s];
+          if (st < clock) {
+            unsigned long long key = key_of(s, st);
+            if ((key >> (shift + 8)) == pre) atomicAdd(&s_hist[(key >> shift) & 255], 1u);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t h8[8], sum = 0;
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            h8[b] = s_hist[lane * 8 + b];
+            sum += h8[b];
+          }
+          uint32_t incl = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const uint32_t kk = (uint32_t)s_kk;
+          const uint32_t excl = incl - sum;
+          bool mine = excl < kk && incl >= kk;
+          if (mine) {
+            uint32_t run = excl;
+            int d = 0;
+            for (int b = 0; b < 8; ++b) {
+              if (run + h8[b] >= kk) {
+                d = b;
+                break;
+              }
+              run += h8[b];
+            }
+            s_prefix = (pre << 8) | (unsigned long long)(lane * 8 + d);
+            s_kk = (int)(kk - run);
+          }
+        }
+        __syncthreads();
+      }
+      thresh = s_prefix;
+    }
+    // collect the `want` smallest keys (keys are unique), then order them
+    for (int s = tid; s < S; s += blockDim.x) {
+      uint32_t st = p.stamp[s];
+      if (st < clock) {
+        unsigned long long key = key_of(s, st);
+        if (key <= thresh) {
+          int i = atomicAdd(&s_nv, 1);
+          if (i < kMaxE) s_vkeys[i] = key;
+        }
+      }
+    }
+    __syncthreads();
+    const int nv = min(s_nv, want);
+    const unsigned long long smask = (1ull << sbits) - 1ull;
+    for (int i = tid; i < nv; i += blockDim.x) {
+      unsigned long long ki = s_vkeys[i];
+      int rank = 0;
+      for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
+      s_victims[rank] = (int)(ki & smask);
+    }
+    if (tid == 0) s_nv = nv;
+    __syncthreads();
+
+    // ---- 4. install F = first q misses into the first q victims
+    for (int i = tid; i < q; i += blockDim.x) {
+      int v = s_victims[i];
+      int u = s_miss[i];
+      int old = p.owner[v];
+      if (old >= 0) {
+        p.res[old] = -1;
+        atomicAdd(&s_evict, 1);
+      }
+      p.owner[v] = u;
+      p.res[u] = v;
+      p.stamp[v] = clock;
+      p.w.copy_u[i] = u;
+      p.w.copy_slot[i] = v;
+    }
+  }
+  __syncthreads();
+
+  // ---- 5. G = resident part of A (ascending u): evaluation entries
+  if (warp == 0) {
+    const int nact = s_nactive;
+    int ng = 0;
+    for (int c = 0; c < nact; c += 32) {
+      int i = c + lane;
+      int u = i < nact ? s_active[i] : -1;
+      int slot = u >= 0 ? p.res[u] : -1;
+      bool in = slot >= 0;
+      uint32_t b = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        int g = ng + __popc(b & ((1u << lane) - 1u));
+        s_gidx[u - base_u] = g;
+        p.w.g_w[g] = p.pool + (size_t)slot * p.slot_stride;
+      }
+      ng += __popc(b);
+    }
+    if (lane == 0) s_ng = ng;
+  }
+  for (int i = tid; i <= kMaxE; i += blockDim.x) s_gcount[i] = 0;
+  __syncthreads();
+  const int ng = s_ng;
+
+  // rewrite pairs to slots / FT_CPU and count pairs per entry
+  const int npairs = B * k;
+  for (int pi = tid; pi < npairs; pi += blockDim.x) {
+    int e = s_sel[pi];
+    int g = s_gidx[e];
+    p.w.slot_of_pair[pi] = g >= 0 ? p.res[base_u + e] : FT_CPU;
+    if (g >= 0) atomicAdd(&s_gcount[g], 1);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of per-entry pair counts -> g_off
+    int carry = 0;
+    for (int c = 0; c < ng; c += 32) {
+      int i = c + lane;
+      int v = i < ng ? s_gcount[i] : 0, incl = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (i < ng) {
+        p.w.g_off[i] = carry + incl - v;
+        s_gcount[i] = carry + incl - v;  // becomes the offset
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      p.w.g_off[ng] = carry;
+      s_gcount[ng] = carry;
+      int ne = ng;
+      if (p.has_shared) {
+        p.w.g_w[ng] = p.shared_w;
+        p.w.g_off[ng + 1] = carry + B;
+        ne = ng + 1;
+      }
+      int* cnt = p.w.counts;
+      cnt[C_NACTIVE] = s_nactive;
+      cnt[C_NHIT] = s_nhit;
+      cnt[C_NMISS] = s_nmiss;
+      cnt[C_Q] = q;
+      cnt[C_NVICT] = q > 0 ? s_nv : 0;
+      cnt[C_NG] = ng;
+      cnt[C_NENTRIES] = ne;
+      cnt[C_NGPAIRS] = carry;
+      cnt[C_LAYER] = p.layer;
+      cnt[C_BATCH] = B;
+      cnt[C_CLOCK] = (int)clock;
+      cnt[C_EVICT] = s_evict;
+    }
+  }
+  __syncthreads();
+  // place pairs: within an entry, ascending pair id
+  for (int pi = tid; pi < npairs; pi += blockDim.x) {
+    int e = s_sel[pi];
+    int g = s_gidx[e];
+    if (g < 0) continue;
+    int pos = 0;
+    for (int j = 0; j < pi; ++j) pos += (s_sel[j] == e);
+    p.w.g_pair[s_gcount[g] + pos] = pi;
+  }
+  if (p.has_shared) {
+    const int base = s_gcount[ng];
+    for (int t = tid; t < B; t += blockDim.x) p.w.g_pair[base + t] = t;
+  }
+  // lists for traces
+  for (int i = tid; i < s_nactive; i += blockDim.x) p.w.active[i] = s_active[i];
+  for (int i = tid; i < s_nhit; i += blockDim.x) p.w.hit[i] = s_hit[i];
+  for (int i = tid; i < s_nmiss; i += blockDim.x) p.w.miss[i] = s_miss[i];
+  if (q > 0)
+    for (int i = tid; i < s_nv; i += blockDim.x) p.w.victims[i] = s_victims[i];
+  if (tid == 0) {
+    DevState* st = p.st;
+    st->clock = clock;
+    st->hits += (unsigned long long)s_nhit;
+    st->misses += (unsigned long long)s_nmiss;
+    st->fills += (unsigned long long)q;
+    st->cpu_execs += (unsigned long long)(s_nmiss - q);
+    st->evictions += (unsigned long long)s_evict;
+    st->decode_steps += 1ull;
+    st->eval_entries += (unsigned long long)(s_ng + (p.has_shared ? 1 : 0));
+    st->eval_pairs += (unsigned long long)(s_gcount[s_ng] + (p.has_shared ? B : 0));
+    if (s_err) atomicOr(&st->error_word, s_err);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_control(const CtrlParams& p, cudaStream_t s) {
+  control_kernel<<<1, kCtrlThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ft

@@ -1,0 +1,447 @@
+// Decode-side data movement and expert evaluation.
+//
+//  fill_kernel        F-set fill: copies whole experts (every bank) from the mapped
+//                     host pool into their victim slots, driven by the device copy
+//                     list and its valid count ("FreeToken 完全拆解", section
+//                     "Device-side 缓存控制": one fixed-shape launch across all banks).
+//  gate_up_kernel     h = silu(W_g x) * (W_u x) for every (entry, token) of G = H u F
+//                     plus the shared expert.
+//  down_combine_kernel y = W_d h, pair row = g * y, and per row block the last CTA to
+//                     finish sums shared + the k pair rows (GPU row, or the caller's
+//                     c_partial row for C pairs) in ascending expert id.
+//
+// GEMV design for HBM: every weight byte is read once with 16-byte streaming loads,
+// one warp per row, all of a row's loads issued before any arithmetic.  The reduction
+// order of each (token, expert) dot product is fixed (lane-strided chunks, then an xor
+// butterfly), independent of slot, batch composition or split, so outputs are identical
+// across cache capacities.  FP8 E4M3 rows are decoded with the hardware e4m3x2->f16x2
+// conversion; each 128-element block's partial dot is multiplied by its FP32 scale once
+// ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2, post-scaling).
+#include <cuda_fp16.h>
+
+#include "ft_internal.cuh"
+
+namespace ft {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// acc += w.lo*x.lo + w.hi*x.hi, BF16 operands, FP32 accumulation (exact products).
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// acc += w.lo*x.lo + w.hi*x.hi, F16 operands, FP32 accumulation (exact products).
+__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// two E4M3 codes (low byte = element 0) -> f16x2 (element 0 in the low half)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}" : "=r"(r) : "r"(two));
+  return r;
+}
+
+// 16 bytes of BF16 weights (8 elements) . 8 BF16 activations
+__device__ __forceinline__ float dot_bf16_bf16(uint4 w, uint4 x, float acc) {
+  acc = fma2_bf16(w.x, x.x, acc);
+  acc = fma2_bf16(w.y, x.y, acc);
+  acc = fma2_bf16(w.z, x.z, acc);
+  acc = fma2_bf16(w.w, x.w, acc);
+  return acc;
+}
+
+// 16 bytes of BF16 weights (8 elements) . 8 FP32 values
+__device__ __forceinline__ float dot_bf16_f32(uint4 w, const float* v, float acc) {
+  const float4 a = *reinterpret_cast<const float4*>(v);
+  const float4 b = *reinterpret_cast<const float4*>(v + 4);
+  acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
+  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
+  acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
+  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
+  acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
+  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
+  acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
+  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+  return acc;
+}
+
+// one 32-bit word of E4M3 codes (4 elements) . 4 F16 values (as two f16x2 words)
+__device__ __forceinline__ float dot4_e4m3_f16(uint32_t w, uint32_t x01, uint32_t x23, float acc) {
+  acc = fma2_f16(e4m3x2_to_f16x2(w & 0xffffu), x01, acc);
+  acc = fma2_f16(e4m3x2_to_f16x2(w >> 16), x23, acc);
+  return acc;
+}
+
+// 16 bytes of E4M3 weights (16 elements) . 16 F16 values -> partial (not scaled)
+__device__ __forceinline__ float dot_e4m3_f16(uint4 w, uint4 xa, uint4 xb) {
+  float d = 0.f;
+  d = dot4_e4m3_f16(w.x, xa.x, xa.y, d);
+  d = dot4_e4m3_f16(w.y, xa.z, xa.w, d);
+  d = dot4_e4m3_f16(w.z, xb.x, xb.y, d);
+  d = dot4_e4m3_f16(w.w, xb.z, xb.w, d);
+  return d;
+}
+
+// 16 bytes of E4M3 weights . 16 FP32 values -> partial (not scaled)
+__device__ __forceinline__ float dot_e4m3_f32(uint4 w, const float* v) {
+  float d = 0.f;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 xv = *reinterpret_cast<const float4*>(v + 4 * q);
+    uint32_t p01 = e4m3x2_to_f16x2(ws[q] & 0xffffu), p23 = e4m3x2_to_f16x2(ws[q] >> 16);
+    float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&p01));
+    float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&p23));
+    d = fmaf(f01.x, xv.x, d);
+    d = fmaf(f01.y, xv.y, d);
+    d = fmaf(f23.x, xv.z, d);
+    d = fmaf(f23.y, xv.w, d);
+  }
+  return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.0f + expf(-a)) * b; }
+
+// ------------------------------------------------------------------------- fill
+__global__ void __launch_bounds__(256) fill_kernel(FillParams p) {
+  const int q = p.counts[C_Q];
+  if (q <= 0) return;
+  const int G = gridDim.x, b = blockIdx.x;
+  int first, step, part, nparts;
+  if (q >= G) {
+    first = b;
+    step = G;
+    part = 0;
+    nparts = 1;
+  } else {
+    first = b % q;
+    step = q;  // one expert per CTA: the loop body runs once
+    part = b / q;
+    nparts = (G - 1 - first) / q + 1;
+  }
+  size_t seg_off[6] = {p.lay.gate, p.lay.up, p.lay.down, p.lay.gs, p.lay.us, p.lay.ds};
+  for (int i = first; i < q; i += step) {
+    const int u = p.copy_u[i];
+    uint8_t* dst_slot = p.pool + (size_t)p.copy_slot[i] * p.lay.stride;
+    for (int j = 0; j < p.n_banks; ++j) {
+      const size_t nbytes = p.src_row[j];
+      const uint4* src = reinterpret_cast<const uint4*>(p.src[j] + (size_t)u * nbytes);
+      uint4* dst = reinterpret_cast<uint4*>(dst_slot + seg_off[j]);
+      const size_t n16 = nbytes / 16;
+      const size_t stride = (size_t)nparts * blockDim.x;
+      size_t c = (size_t)part * blockDim.x + threadIdx.x;
+      for (; c + 3 * stride < n16; c += 4 * stride) {
+        uint4 v0 = ld_stream(src + c), v1 = ld_stream(src + c + stride);
+        uint4 v2 = ld_stream(src + c + 2 * stride), v3 = ld_stream(src + c + 3 * stride);
+        dst[c] = v0;
+        dst[c + stride] = v1;
+        dst[c + 2 * stride] = v2;
+        dst[c + 3 * stride] = v3;
+      }
+      for (; c < n16; c += stride) dst[c] = ld_stream(src + c);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- gate / up
+// Work item = (entry, block of 8 rows of I): warp w computes row 8*rb + w for every
+// token of the entry.  Tokens are staged in shared memory TG at a time.
+template <int WT, int SEG, int TG>
+__global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int ne = p.counts[C_NENTRIES];
+  const int I = p.I, H = p.H;
+  const int rbs = I / 8;
+  const int n_items = ne * rbs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
+  constexpr int EPC = 16 / ESZ;  // elements per 16-byte chunk
+  const int row_chunks = H / EPC;
+  // x tile: BF16 path keeps raw bf16 (2 B); FP8 path keeps f16 (2 B) -> H*2 bytes per token
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int g = item / rbs, rb = item - g * rbs;
+    const int i = rb * 8 + warp;
+    const uint8_t* W = p.g_w[g];
+    const uint8_t* wg = W + p.lay.gate + (size_t)i * H * ESZ;
+    const uint8_t* wu = W + p.lay.up + (size_t)i * H * ESZ;
+    const float* sg = reinterpret_cast<const float*>(W + p.lay.gs) + (size_t)i * (H / 128);
+    const float* su = reinterpret_cast<const float*>(W + p.lay.us) + (size_t)i * (H / 128);
+    const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
+    const bool shared_entry = p.has_shared && g == ne - 1;
+    for (int t0 = 0; t0 < np; t0 += TG) {
+      const int nt = min(TG, np - t0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < nt * (H / 8); idx += blockDim.x) {
+        const int tt = idx / (H / 8), c8 = idx - tt * (H / 8);
+        const int pr = p.g_pair[p0 + t0 + tt];
+        const int tok = shared_entry ? pr : pr / p.k;
+        uint4 v = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + c8 * 8);
+        if (WT == FT_W_FP8_E4M3_B128) {  // bf16 -> f16 (exact for the f16 normal range)
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float lo = __uint_as_float(in[q] << 16), hi = __uint_as_float(in[q] & 0xffff0000u);
+            __half2 hh = __floats2half2_rn(lo, hi);
+            o[q] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          v = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4*>(xs + (size_t)tt * H + c8 * 8) = v;
+      }
+      __syncthreads();
+      float acc_a[TG], acc_b[TG];
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) acc_a[tt] = acc_b[tt] = 0.f;
+      for (int c0 = 0; c0 < row_chunks; c0 += 32 * SEG) {
+        uint4 wa[SEG], wb[SEG];
+#pragma unroll
+        for (int s = 0; s < SEG; ++s) {
+          const int c = c0 + s * 32 + lane;
+          if (c < row_chunks) {
+            wa[s] = ld_stream(wg + (size_t)c * 16);
+            wb[s] = ld_stream(wu + (size_t)c * 16);
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < SEG; ++s) {
+          const int c = c0 + s * 32 + lane;
+          if (c < row_chunks) {
+            if (WT == FT_W_BF16) {
+#pragma unroll
+              for (int tt = 0; tt < TG; ++tt) {
+                if (tt < nt) {
+                  const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)tt * H + c * 8);
+                  acc_a[tt] = dot_bf16_bf16(wa[s], xv, acc_a[tt]);
+                  acc_b[tt] = dot_bf16_bf16(wb[s], xv, acc_b[tt]);
+                }
+              }
+            } else {
+              const float scg = __ldg(sg + c / 8), scu = __ldg(su + c / 8);
+#pragma unroll
+              for (int tt = 0; tt < TG; ++tt) {
+                if (tt < nt) {
+                  const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)tt * H + c * 16);
+                  const uint4 xa = xp[0], xb = xp[1];
+                  acc_a[tt] = fmaf(dot_e4m3_f16(wa[s], xa, xb), scg, acc_a[tt]);
+                  acc_b[tt] = fmaf(dot_e4m3_f16(wb[s], xa, xb), scu, acc_b[tt]);
+                }
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < TG; ++tt) {
+        const float a = warp_sum(acc_a[tt]);
+        const float b = warp_sum(acc_b[tt]);
+        if (lane == 0 && tt < nt) p.h[(size_t)(p0 + t0 + tt) * I + i] = silu_mul(a, b);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ down + combine
+// Work item = (entry, block of 32 output rows): warp w computes rows 32*rb + 4w .. +3.
+template <int WT, int RPW, int TG>
+__global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+  const int ne = p.counts[C_NENTRIES];
+  const int I = p.I, H = p.H, k = p.k, B = p.B;
+  constexpr int R2 = 8 * RPW;
+  static_assert(R2 == kRowsPerItem2, "row block");
+  const int nrb = H / R2;
+  const int n_items = ne * nrb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
+  constexpr int EPC = 16 / ESZ;
+  const int row_chunks = I / EPC;
+  float* hs = reinterpret_cast<float*>(smem);  // [TG][I]
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int g = item / nrb, rb = item - g * nrb;
+    const uint8_t* W = p.g_w[g];
+    const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
+    const bool shared_entry = p.has_shared && g == ne - 1;
+    const int j0 = rb * R2 + warp * RPW;
+    for (int t0 = 0; t0 < np; t0 += TG) {
+      const int nt = min(TG, np - t0);
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < nt * (I / 4); idx += blockDim.x) {
+        const int tt = idx / (I / 4), c4 = idx - tt * (I / 4);
+        *reinterpret_cast<float4*>(hs + (size_t)tt * I + c4 * 4) =
+            *reinterpret_cast<const float4*>(p.h + (size_t)(p0 + t0 + tt) * I + c4 * 4);
+      }
+      __syncthreads();
+      float acc[RPW][TG];
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int tt = 0; tt < TG; ++tt) acc[r][tt] = 0.f;
+      constexpr int SEG = ESZ == 2 ? 2 : 4;
+      for (int c0 = 0; c0 < row_chunks; c0 += 32 * SEG) {
+        uint4 wv[RPW][SEG];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+          for (int s = 0; s < SEG; ++s) {
+            const int c = c0 + s * 32 + lane;
+            if (c < row_chunks)
+              wv[r][s] = ld_stream(W + p.lay.down + ((size_t)(j0 + r) * I) * ESZ + (size_t)c * 16);
+          }
+#pragma unroll
+        for (int s = 0; s < SEG; ++s) {
+          const int c = c0 + s * 32 + lane;
+          if (c < row_chunks) {
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+              if (WT == FT_W_BF16) {
+#pragma unroll
+                for (int tt = 0; tt < TG; ++tt)
+                  if (tt < nt) acc[r][tt] = dot_bf16_f32(wv[r][s], hs + (size_t)tt * I + c * 8, acc[r][tt]);
+              } else {
+                const float sc = __ldg(reinterpret_cast<const float*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 128) + c / 8);
+#pragma unroll
+                for (int tt = 0; tt < TG; ++tt)
+                  if (tt < nt) acc[r][tt] = fmaf(dot_e4m3_f32(wv[r][s], hs + (size_t)tt * I + c * 16), sc, acc[r][tt]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int tt = 0; tt < TG; ++tt) {
+          const float y = warp_sum(acc[r][tt]);
+          if (lane == 0 && tt < nt) {
+            const int pr = p.g_pair[p0 + t0 + tt];
+            if (shared_entry) p.shared_rows[(size_t)pr * H + j0 + r] = y;
+            else p.rows[(size_t)pr * H + j0 + r] = p.gates[pr] * y;
+          }
+        }
+    }
+    // arrival at this row block; the last entry to arrive combines it
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t prev = atomicAdd(p.blk_count + rb, 1u);
+      s_last = prev == (uint32_t)(ne - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      for (int idx = threadIdx.x; idx < B * R2; idx += blockDim.x) {
+        const int t = idx / R2, j = rb * R2 + (idx - t * R2);
+        float o = p.has_shared ? ld_cg_f32(p.shared_rows + (size_t)t * H + j) : 0.f;
+        for (int r = 0; r < k; ++r) {
+          const int pr = t * k + r;
+          if (p.slot_of_pair[pr] >= 0) {
+            o += ld_cg_f32(p.rows + (size_t)pr * H + j);
+          } else if (p.c_partial) {
+            o += p.c_partial[(size_t)pr * H + j];
+          } else if (j == 0) {
+            atomicOr(p.error_word, FT_DEVERR_CAPACITY);
+          }
+        }
+        p.out[(size_t)t * H + j] = o;
+      }
+      if (threadIdx.x == 0) p.blk_count[rb] = 0u;
+    }
+  }
+}
+
+template <int WT, int SEG, int TG>
+cudaError_t gate_up_launch(const EvalParams& p, int grid, cudaStream_t s) {
+  gate_up_kernel<WT, SEG, TG><<<grid, kEvalThreads, (size_t)TG * p.H * 2, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int WT, int TG>
+cudaError_t down_launch(const EvalParams& p, int grid, cudaStream_t s) {
+  down_combine_kernel<WT, 4, TG><<<grid, kEvalThreads, (size_t)TG * p.I * 4, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename F>
+cudaError_t set_smem(F f, size_t bytes) {
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
+  fill_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
+  const bool one = p.B == 1;
+  if (wtype == FT_W_BF16) {
+    return one ? gate_up_launch<FT_W_BF16, 8, 1>(p, grid, s) : gate_up_launch<FT_W_BF16, 8, 4>(p, grid, s);
+  }
+  return one ? gate_up_launch<FT_W_FP8_E4M3_B128, 7, 1>(p, grid, s)
+             : gate_up_launch<FT_W_FP8_E4M3_B128, 7, 4>(p, grid, s);
+}
+
+cudaError_t prepare_kernels(int wtype, int H, int I) {
+  cudaError_t e = cudaSuccess;
+  const size_t gu1 = (size_t)H * 2, gu4 = 4 * gu1, dn1 = (size_t)I * 4, dn4 = 4 * dn1;
+  if (wtype == FT_W_BF16) {
+    if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 1>, gu1)) != cudaSuccess) return e;
+    if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 4>, gu4)) != cudaSuccess) return e;
+    if ((e = set_smem(down_combine_kernel<FT_W_BF16, 4, 1>, dn1)) != cudaSuccess) return e;
+    e = set_smem(down_combine_kernel<FT_W_BF16, 4, 4>, dn4);
+  } else {
+    if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 1>, gu1)) != cudaSuccess) return e;
+    if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 4>, gu4)) != cudaSuccess) return e;
+    if ((e = set_smem(down_combine_kernel<FT_W_FP8_E4M3_B128, 4, 1>, dn1)) != cudaSuccess) return e;
+    e = set_smem(down_combine_kernel<FT_W_FP8_E4M3_B128, 4, 4>, dn4);
+  }
+  return e;
+}
+
+cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
+  const bool one = p.B == 1;
+  if (wtype == FT_W_BF16) return one ? down_launch<FT_W_BF16, 1>(p, grid, s) : down_launch<FT_W_BF16, 4>(p, grid, s);
+  return one ? down_launch<FT_W_FP8_E4M3_B128, 1>(p, grid, s) : down_launch<FT_W_FP8_E4M3_B128, 4>(p, grid, s);
+}
+
+}  // namespace ft

@@ -1,0 +1,123 @@
+// Internal definitions of libftmoe (device structs, limits, kernel entry points).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "ft_moe.h"
+
+namespace ft {
+
+constexpr int kMaxE = 1024;           // routed experts per layer
+constexpr int kMaxK = 16;             // top-k
+constexpr int kMaxBatch = 64;         // decode tokens per step
+constexpr int kMaxPairs = kMaxBatch * kMaxK;
+constexpr int kCtrlThreads = 1024;
+constexpr int kEvalThreads = 256;     // GEMV CTAs: 8 warps
+constexpr int kRowsPerItem2 = 32;     // down-projection rows per work item (= combine block)
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Device-resident counters and clock of one handle.
+struct DevState {
+  uint32_t clock;
+  uint32_t error_word;
+  unsigned long long hits, misses, fills, cpu_execs, evictions;
+  unsigned long long decode_steps, prefill_layers;
+  unsigned long long eval_entries, eval_pairs;  // G entries (+shared) and (entry, token) pairs evaluated
+};
+
+// Indices into DecodeWork::counts (written by the control kernel, read by the
+// fill / evaluation kernels and by the host for traces).
+enum CountIdx {
+  C_NACTIVE = 0, C_NHIT, C_NMISS, C_Q, C_NVICT, C_NG, C_NENTRIES, C_NGPAIRS,
+  C_LAYER, C_BATCH, C_CLOCK, C_EVICT, C_NCOUNTS = 16
+};
+
+// Fixed-shape work lists of a decode layer-step.  One set per handle; every
+// layer-step overwrites it, and the valid counts tell kernels how much is live.
+struct DecodeWork {
+  int32_t* sel;            // [maxB*k] expert ids, ascending per token
+  float* gates;            // [maxB*k]
+  int32_t* slot_of_pair;   // [maxB*k] slot, or FT_CPU
+  int32_t* active;         // [Kmax] A (logical ids)
+  int32_t* hit;            // [Kmax]
+  int32_t* miss;           // [Kmax]
+  int32_t* victims;        // [Kmax]
+  int32_t* copy_u;         // [Kmax] F: logical id to fill
+  int32_t* copy_slot;      // [Kmax] F: destination slot
+  int32_t* counts;         // [C_NCOUNTS]
+  // Evaluation entries: 0..n_g-1 are G = H u F in ascending logical id; entry
+  // n_g is the shared expert when the model has one.
+  const uint8_t** g_w;     // [Kmax+1] base address of the entry's weights
+  int32_t* g_off;          // [Kmax+2] prefix offsets into g_pair
+  int32_t* g_pair;         // [maxB*k + maxB] routed: pair id t*k+r; shared: token t
+  float* h;                // [(maxB*k + maxB) * I] intermediate, indexed like g_pair
+  float* rows;             // [maxB*k*H] GPU pair rows when the caller gives no rows_out
+  float* shared_rows;      // [maxB*H]
+  uint32_t* blk_count;     // [H / kRowsPerItem2] combine arrival counters (self-resetting)
+  int kmax;                // capacity of the per-expert lists
+};
+
+// Byte layout of one slot: gate | up | down [| gate_scale | up_scale | down_scale].
+struct SlotLayout {
+  size_t gate, up, down, gs, us, ds;  // byte offsets
+  size_t gate_b, down_b, gs_b, ds_b;  // byte sizes (up == gate, us == gs)
+  size_t used, stride;                // bytes used, slot stride (256-aligned)
+};
+
+SlotLayout make_layout(int wtype, int H, int I);
+
+struct CtrlParams {
+  const float* logits;
+  int B, E, k, layer, S, kcap, has_shared;
+  long long bp_mbs, bh_mbs;
+  int32_t* res;
+  int32_t* owner;
+  uint32_t* stamp;
+  DevState* st;
+  DecodeWork w;
+  const uint8_t* pool;
+  size_t slot_stride;
+  const uint8_t* shared_w;  // shared expert of this layer, or nullptr
+};
+
+struct FillParams {
+  const int32_t* counts;
+  const int32_t* copy_u;
+  const int32_t* copy_slot;
+  uint8_t* pool;
+  SlotLayout lay;
+  const uint8_t* src[6];    // device-visible addresses of the host banks
+  size_t src_row[6];        // bytes per logical id in each bank
+  int n_banks;
+};
+
+struct EvalParams {
+  const int32_t* counts;
+  const uint8_t* const* g_w;
+  const int32_t* g_off;
+  const int32_t* g_pair;
+  const float* gates;
+  const int32_t* slot_of_pair;
+  const uint16_t* x;        // [B][H] bf16
+  float* h;
+  float* rows;              // [B*k][H]
+  float* shared_rows;       // [B][H]
+  const float* c_partial;   // [B*k][H] or nullptr
+  float* out;               // [B][H]
+  uint32_t* blk_count;
+  uint32_t* error_word;
+  SlotLayout lay;
+  int H, I, k, B, has_shared;
+};
+
+// Kernel launchers (stream-ordered, no synchronisation).
+cudaError_t launch_control(const CtrlParams& p, cudaStream_t s);
+cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
+cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s);
+cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s);
+// Set the dynamic shared-memory limits of every evaluation kernel (call once, before capture).
+cudaError_t prepare_kernels(int wtype, int H, int I);
+
+}  // namespace ft

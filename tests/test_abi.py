@@ -1,0 +1,89 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point the
+header declares, the host split mirror agrees with the oracle, and argument
+errors come back as status codes."""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+
+    g.build()
+    from serving_router_top_dedupe_gb300 import ftmoe
+
+    return ftmoe
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        names |= set(re.findall(r"^\s*(?:ft_status|const char\*)\s+(ft_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol(F):
+    declared = _declared()
+    assert len(declared) >= 20
+    import ctypes
+
+    lib = ctypes.CDLL(F.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(F.EXPORTED)
+
+
+def test_split_host_mirror_matches_oracle(F):
+    rng = random.Random(3)
+    for _ in range(2000):
+        m = rng.randint(0, 300)
+        bp = round(rng.uniform(0.5, 400), 3)
+        bh = round(rng.uniform(0.5, 400), 3)
+        ev = rng.randint(0, 400)
+        assert F.ft_split_misses(m, bp, bh, ev) == O.split_misses(m, O.mbps(bp), O.mbps(bh), ev)
+    assert F.ft_split_misses(4, 11.8, 47.5, 99) == 1
+    assert F.ft_split_misses(4, 52.7, 77.3, 99) == 3
+
+
+def test_split_rejects_bad_arguments(F):
+    for args in [(-1, 1.0, 1.0, 1), (1, 0.0, 1.0, 1), (1, 1.0, -2.0, 1), (1, 1.0, 1.0, -1)]:
+        with pytest.raises(F.FtError) as e:
+            F.ft_split_misses(*args)
+        assert e.value.status == F.FT_ERR_INVALID
+
+
+def test_init_rejects_bad_config_without_touching_the_gpu(F):
+    banks = {"gate": np.zeros(16, np.uint16), "up": np.zeros(16, np.uint16), "down": np.zeros(16, np.uint16)}
+    bad = [
+        dict(hidden=100),           # not a multiple of 256
+        dict(top_k=0), dict(top_k=17), dict(n_experts=2000), dict(max_batch=65), dict(cache_slots=0),
+        dict(inter=100), dict(bh_gbps=0.0), dict(wtype=7),
+    ]
+    base = dict(n_layers=2, hidden=256, inter=128, n_experts=16, top_k=2, has_shared=False, wtype=F.FT_W_BF16,
+                max_batch=1, cache_slots=8, bp_gbps=11.8, bh_gbps=47.5)
+    for b in bad:
+        with pytest.raises(F.FtError) as e:
+            F.ft_moe_init(F.make_config(**{**base, **b}), banks)
+        assert e.value.status == F.FT_ERR_INVALID
+    with pytest.raises(F.FtError) as e:  # FP8 without scale banks
+        F.ft_moe_init(F.make_config(**{**base, "wtype": F.FT_W_FP8_E4M3_B128, "hidden": 512}), banks)
+    assert e.value.status == F.FT_ERR_INVALID
+
+
+def test_null_handle_calls_fail_cleanly(F):
+    with pytest.raises(F.FtError):
+        F.ft_moe_decode_step(None, 0, 1, 1, 1, 1, 1)
+    with pytest.raises(F.FtError):
+        F.ft_cache_resize(None, 4)
+    with pytest.raises(F.FtError):
+        F.ft_moe_get_stats(None)
+    F.ft_moe_destroy(None)
