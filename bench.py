@@ -321,6 +321,7 @@ def run_ours(args, d: Dist) -> dict | None:
         clk = clocks.stop()
         ms = e0.elapsed_time(e1)
         st1 = F.ft_moe_get_stats(h)
+    bp_after = F.ft_bench_bw(256 << 20, 8)
     value, tmax = aggregate(args.steps * Bt, ms * 1e-3, d)
     layer_steps = (st1.decode_steps - st0.decode_steps)
     miss = st1.misses - st0.misses
@@ -331,19 +332,24 @@ def run_ours(args, d: Dist) -> dict | None:
              "fill_gb_per_token": (st1.fills - st0.fills) / args.steps * 6 * H * w.inter / 1e9,
              "error_word": st1.error_word}
 
-    # kernel profile over a window of the same trace (events on each kernel's own stream)
+    # kernel profile: replays of a graph captured with timing events as nodes (events on
+    # each kernel's own stream), read after every replay; same trace, continuing state
     n_prof = min(args.profile_steps, n_tr)
     F.ft_moe_set_profiling(h, 1)
+    gp = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
     F.ft_moe_get_profile(h, reset=True)
     sp0 = F.ft_moe_get_stats(h)
     with torch.cuda.stream(stream):
         for i in range(n_prof):
-            j = args.warmup + args.steps + i
-            load(j)
-            F.ft_moe_decode_layers(h, 0, L, Bt, x_s, z_s, c_s, o_s)
+            load(args.warmup + args.steps + i)
+            F.ft_graph_launch(gp)
+            F.ft_moe_get_profile(h, reset=False)
     prof = F.ft_moe_get_profile(h, reset=True)
     sp1 = F.ft_moe_get_stats(h)
+    F.ft_graph_destroy(gp)
     F.ft_moe_set_profiling(h, 0)
+    fill_bytes_prof = (sp1.fills - sp0.fills) * 6 * H * w.inter
+    fill_gbs = fill_bytes_prof / (prof["fill"][1] * 1e-3) / 1e9 if prof["fill"][1] else None
     ent = sp1.eval_entries - sp0.eval_entries
     prs = sp1.eval_pairs - sp0.eval_pairs
     esz = 2
@@ -402,7 +408,8 @@ def run_ours(args, d: Dist) -> dict | None:
                                       "down_combine": round(ach_dn, 1) if ach_dn else None,
                                       "both": round(ach_both, 1) if ach_both else None},
            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * L * 4, "clocks": clk,
-           "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1),
+           "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1), "bp_after_timed_gbps": round(bp_after, 1),
+           "fill_observed_gbs": round(fill_gbs, 1) if fill_gbs else None,
            "setup_s": round(setup_s, 1)}
     if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
         n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, args.cpu_tokens, args.cpu_budget)

@@ -243,7 +243,9 @@ ft_status ft_moe_get_state(ft_moe* h, int32_t* res, int32_t* owner, uint32_t* st
 
 /* Turn per-kernel CUDA-event timing on (1) or off (0); ft_moe_get_profile reads and
  * (reset != 0) clears the totals.  Timing events are recorded on the stream each
- * kernel is launched on.  Synchronises. */
+ * kernel is launched on.  A graph captured while profiling is on carries its timing
+ * events as graph nodes: reading the profile after a replay adds that replay's kernel
+ * times (read after every replay; earlier replays are overwritten).  Synchronises. */
 ft_status ft_moe_set_profiling(ft_moe* h, int enable);
 ft_status ft_moe_get_profile(ft_moe* h, ft_profile* out, int reset);
 

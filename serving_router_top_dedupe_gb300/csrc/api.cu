@@ -64,6 +64,8 @@ struct ft_graph {
   ft_moe* owner = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  std::vector<ProfRec> prof;  // timing events captured as graph nodes (profiling on at capture)
+  uint64_t pending = 0;       // replays since the profile was last read
 };
 
 struct ft_moe {
@@ -133,6 +135,14 @@ SlotLayout make_layout(int wtype, int H, int I) {
 
 namespace {
 
+bool capturing(cudaStream_t s);
+
+// Inside a capture an event becomes an event-record graph node only when recorded as
+// external; otherwise it is a capture-internal dependency with no timestamp.
+cudaError_t record_timing_event(cudaEvent_t e, cudaStream_t s) {
+  return capturing(s) ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal) : cudaEventRecord(e, s);
+}
+
 ft_status prof_begin(ft_moe* h, cudaStream_t s, cudaEvent_t* out) {
   *out = nullptr;
   if (!h->prof) return FT_OK;
@@ -143,7 +153,7 @@ ft_status prof_begin(ft_moe* h, cudaStream_t s, cudaEvent_t* out) {
   } else {
     FT_CUDA(cudaEventCreate(&e));
   }
-  FT_CUDA(cudaEventRecord(e, s));
+  FT_CUDA(record_timing_event(e, s));
   *out = e;
   return FT_OK;
 }
@@ -157,7 +167,7 @@ ft_status prof_end(ft_moe* h, int kind, cudaStream_t s, cudaEvent_t a) {
   } else {
     FT_CUDA(cudaEventCreate(&e));
   }
-  FT_CUDA(cudaEventRecord(e, s));
+  FT_CUDA(record_timing_event(e, s));
   h->prof_live.push_back({kind, a, e});
   return FT_OK;
 }
@@ -569,10 +579,10 @@ ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, 
                                       ft_graph** g) {
   if (!h || !g) return fail(FT_ERR_INVALID, "null handle/graph");
   if (h->cfg.fill_mode != FT_FILL_KERNEL) return fail(FT_ERR_STATE, "graph capture needs FT_FILL_KERNEL");
-  if (h->prof) return fail(FT_ERR_STATE, "turn profiling off before capturing");
   FT_CUDA(cudaSetDevice(h->dev));
   std::unique_ptr<ft_graph> gr(new ft_graph());
   gr->owner = h;
+  const size_t n_prof0 = h->prof_live.size();
   FT_CUDA(cudaStreamBeginCapture(h->cs, cudaStreamCaptureModeThreadLocal));
   ft_status s = ft_moe_decode_layers(h, first_layer, n_layers, batch, x_bf16, logits, c_partial, out, rows_out);
   cudaGraph_t graph = nullptr;
@@ -583,6 +593,8 @@ ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, 
   }
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "capture failed: %s", cudaGetErrorString(e));
   gr->graph = graph;
+  gr->prof.assign(h->prof_live.begin() + n_prof0, h->prof_live.end());
+  h->prof_live.resize(n_prof0);
   e = cudaGraphInstantiate(&gr->exec, graph, 0);
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
   *g = gr.release();
@@ -592,8 +604,10 @@ ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, 
 
 ft_status ft_graph_launch(ft_graph* g) {
   if (!g || !g->exec) return fail(FT_ERR_INVALID, "null graph");
+  if (!g->owner) return fail(FT_ERR_STATE, "graph belongs to a resized or destroyed handle");
   if (g->owner->pf) ft::prefill_interrupt(g->owner->pf);
   FT_CUDA(cudaGraphLaunch(g->exec, g->owner->cs));
+  ++g->pending;
   return FT_OK;
 }
 
@@ -605,6 +619,10 @@ ft_status ft_graph_destroy(ft_graph* g) {
   }
   if (g->exec) cudaGraphExecDestroy(g->exec);
   if (g->graph) cudaGraphDestroy(g->graph);
+  for (auto& r : g->prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
   delete g;
   return FT_OK;
 }
@@ -749,6 +767,17 @@ ft_status ft_moe_get_profile(ft_moe* h, ft_profile* out, int reset) {
     h->ev_free.push_back(r.b);
   }
   h->prof_live.clear();
+  // graphs captured with profiling on: their event nodes hold the last replay's times
+  for (ft_graph* g : h->graphs) {
+    if (!g->pending || g->prof.empty()) continue;
+    for (auto& r : g->prof) {
+      float ms = 0.f;
+      FT_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+      h->prof_acc.launches[r.kind] += 1;
+      h->prof_acc.total_ms[r.kind] += ms;
+    }
+    g->pending = 0;
+  }
   *out = h->prof_acc;
   if (reset) h->prof_acc = ft_profile{};
   return FT_OK;

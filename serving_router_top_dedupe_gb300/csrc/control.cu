@@ -38,6 +38,10 @@ __device__ __forceinline__ int split_q(int m, long long bp, long long bh, int ev
   return q < 0 ? 0 : (int)q;
 }
 
+constexpr int kRegJ = 16;      // stamps per thread held in registers (S <= 16K)
+constexpr int kDigit = 11;     // radix-select digit
+constexpr int kBins = 1 << kDigit;
+
 template <int NPL>  // logits held per lane: E <= 32*NPL
 __device__ void route_token(const CtrlParams& p, int t, int lane, int* s_sel, uint32_t* s_bitmap,
                             uint32_t* s_err) {
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   __shared__ int s_gidx[kMaxE];
   __shared__ int s_victims[kMaxE];
   __shared__ unsigned long long s_vkeys[kMaxE];
-  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_hist[kBins];
   __shared__ int s_gcount[kMaxE + 1];
   __shared__ uint32_t s_err;
   __shared__ uint32_t s_clock;
@@ -207,17 +211,31 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
 
   // ---- 3. one-pass K-LRU victim scan over slots not hit in this step
   if (q > 0) {
+    // Stamps stay in registers for S <= 16K slots (read from global once).
+    uint32_t rs[kRegJ];
+    const bool in_reg = S <= kRegJ * kCtrlThreads;
+#pragma unroll
+    for (int j = 0; j < kRegJ; ++j) {
+      const int s = tid + j * kCtrlThreads;
+      rs[j] = (in_reg && s < S) ? p.stamp[s] : UINT_MAX;
+    }
+#define FOR_CANDIDATES(...)                                          \
+  if (in_reg) {                                                      \
+    _Pragma("unroll") for (int j = 0; j < kRegJ; ++j) {              \
+      const int s = tid + j * kCtrlThreads;                          \
+      const uint32_t st = rs[j];                                     \
+      if (s < S && st < clock) { __VA_ARGS__ }                       \
+    }                                                                \
+  } else {                                                           \
+    for (int s = tid; s < S; s += kCtrlThreads) {                    \
+      const uint32_t st = p.stamp[s];                                \
+      if (st < clock) { __VA_ARGS__ }                                \
+    }                                                                \
+  }
     // range of candidate stamps and their count
     uint32_t lo = UINT_MAX, hi = 0;
     int nc = 0;
-    for (int s = tid; s < S; s += blockDim.x) {
-      uint32_t st = p.stamp[s];
-      if (st < clock) {
-        lo = min(lo, st);
-        hi = max(hi, st);
-        ++nc;
-      }
-    }
+    FOR_CANDIDATES(lo = min(lo, st); hi = max(hi, st); ++nc;)
     for (int o = 16; o > 0; o >>= 1) {
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
@@ -234,59 +252,49 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     const int want = min(kcap, ncand);
     const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
     const uint32_t range = s_hi - st_lo;
-    const int width = (range ? 32 - __clz(range) : 0) + sbits;
-    auto key_of = [&](int s, uint32_t st) -> unsigned long long {
-      return ((unsigned long long)(st - st_lo) << sbits) | (unsigned long long)s;
-    };
+    const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
+    // key = (stamp - lowest stamp, slot): unique, ordered like (stamp, slot)
+#define KEY_OF(s, st) ((((unsigned long long)((st) - st_lo)) << sbits) | (unsigned long long)(s))
     unsigned long long thresh = ~0ull;
     if (want < ncand) {
-      // radix select of the want-th smallest key, 8 bits per pass, most significant first
-      const int passes = (width + 7) / 8;
+      // radix select of the want-th smallest key, kDigit bits per pass, most significant first
+      const int passes = (width + kDigit - 1) / kDigit;
       if (tid == 0) {
         s_prefix = 0;
         s_kk = want;
       }
-      __syncthreads();
       for (int ps = passes - 1; ps >= 0; --ps) {
-        const int shift = ps * 8;
-        for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0;
+        const int shift = ps * kDigit;
+        for (int i = tid; i < kBins; i += kCtrlThreads) s_hist[i] = 0;
         __syncthreads();
         const unsigned long long pre = s_prefix;
-        for (int s = tid; s < S; s += blockDim.x) {
-          uint32_t st = p.stamp[s];
-          if (st < clock) {
-            unsigned long long key = key_of(s, st);
-            if ((key >> (shift + 8)) == pre) atomicAdd(&s_hist[(key >> shift) & 255], 1u);
-          }
-        }
+        FOR_CANDIDATES(const unsigned long long key = KEY_OF(s, st);
+                       if ((key >> (shift + kDigit)) == pre) atomicAdd(&s_hist[(key >> shift) & (kBins - 1)], 1u);)
         __syncthreads();
         if (warp == 0) {
-          uint32_t h8[8], sum = 0;
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            h8[b] = s_hist[lane * 8 + b];
-            sum += h8[b];
-          }
+          constexpr int per = kBins / 32;
+          uint32_t sum = 0;
+          for (int b = 0; b < per; ++b) sum += s_hist[lane * per + ((b + lane) & (per - 1))];  // bank-skewed
           uint32_t incl = sum;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
           }
           const uint32_t kk = (uint32_t)s_kk;
           const uint32_t excl = incl - sum;
-          bool mine = excl < kk && incl >= kk;
-          if (mine) {
+          if (excl < kk && incl >= kk) {  // exactly one lane
             uint32_t run = excl;
-            int d = 0;
-            for (int b = 0; b < 8; ++b) {
-              if (run + h8[b] >= kk) {
+            int d = per - 1;
+            for (int b = 0; b < per; ++b) {
+              const uint32_t hb = s_hist[lane * per + b];
+              if (run + hb >= kk) {
                 d = b;
                 break;
               }
-              run += h8[b];
+              run += hb;
             }
-            s_prefix = (pre << 8) | (unsigned long long)(lane * 8 + d);
+            s_prefix = (pre << kDigit) | (unsigned long long)(lane * per + d);
             s_kk = (int)(kk - run);
           }
         }
@@ -295,21 +303,17 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
       thresh = s_prefix;
     }
     // collect the `want` smallest keys (keys are unique), then order them
-    for (int s = tid; s < S; s += blockDim.x) {
-      uint32_t st = p.stamp[s];
-      if (st < clock) {
-        unsigned long long key = key_of(s, st);
-        if (key <= thresh) {
-          int i = atomicAdd(&s_nv, 1);
-          if (i < kMaxE) s_vkeys[i] = key;
-        }
-      }
-    }
+    FOR_CANDIDATES(const unsigned long long key = KEY_OF(s, st); if (key <= thresh) {
+      const int i = atomicAdd(&s_nv, 1);
+      if (i < kMaxE) s_vkeys[i] = key;
+    })
+#undef FOR_CANDIDATES
+#undef KEY_OF
     __syncthreads();
     const int nv = min(s_nv, want);
     const unsigned long long smask = (1ull << sbits) - 1ull;
-    for (int i = tid; i < nv; i += blockDim.x) {
-      unsigned long long ki = s_vkeys[i];
+    for (int i = tid; i < nv; i += kCtrlThreads) {
+      const unsigned long long ki = s_vkeys[i];
       int rank = 0;
       for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
       s_victims[rank] = (int)(ki & smask);

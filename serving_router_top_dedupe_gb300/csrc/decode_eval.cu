@@ -32,6 +32,12 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// Host-pool reads (mapped pinned memory over the host link): plain coherent loads with
+// evict-first L2 policy.  The read-only .nc path is far slower for host memory.
+__device__ __forceinline__ uint4 ld_host(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
 __device__ __forceinline__ float ld_cg_f32(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
@@ -137,43 +143,54 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.0f + expf(-a)) * b; }
 
 // ------------------------------------------------------------------------- fill
+// Work = q experts x n_banks contiguous segments.  CTA b copies a share of segment
+// b mod nseg (addresses computed once per segment), issuing FILL_UNROLL 16-byte loads
+// from the mapped host pool before storing any, so the grid keeps several MB of host
+// reads in flight: one 6 MB expert then moves at the host link's rate.
+constexpr int FILL_UNROLL = 8;
+
+__device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16,
+                                             size_t first, size_t stride) {
+  for (size_t base = first; base < n16; base += stride * FILL_UNROLL) {
+    uint4 v[FILL_UNROLL];
+#pragma unroll
+    for (int u = 0; u < FILL_UNROLL; ++u) {
+      const size_t c = base + u * stride;
+      if (c < n16) v[u] = ld_host(src + c);
+    }
+#pragma unroll
+    for (int u = 0; u < FILL_UNROLL; ++u) {
+      const size_t c = base + u * stride;
+      if (c < n16) dst[c] = v[u];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) fill_kernel(FillParams p) {
   const int q = p.counts[C_Q];
   if (q <= 0) return;
-  const int G = gridDim.x, b = blockIdx.x;
-  int first, step, part, nparts;
-  if (q >= G) {
-    first = b;
-    step = G;
-    part = 0;
-    nparts = 1;
-  } else {
-    first = b % q;
-    step = q;  // one expert per CTA: the loop body runs once
-    part = b / q;
-    nparts = (G - 1 - first) / q + 1;
-  }
-  size_t seg_off[6] = {p.lay.gate, p.lay.up, p.lay.down, p.lay.gs, p.lay.us, p.lay.ds};
-  for (int i = first; i < q; i += step) {
-    const int u = p.copy_u[i];
-    uint8_t* dst_slot = p.pool + (size_t)p.copy_slot[i] * p.lay.stride;
-    for (int j = 0; j < p.n_banks; ++j) {
-      const size_t nbytes = p.src_row[j];
-      const uint4* src = reinterpret_cast<const uint4*>(p.src[j] + (size_t)u * nbytes);
-      uint4* dst = reinterpret_cast<uint4*>(dst_slot + seg_off[j]);
-      const size_t n16 = nbytes / 16;
-      const size_t stride = (size_t)nparts * blockDim.x;
-      size_t c = (size_t)part * blockDim.x + threadIdx.x;
-      for (; c + 3 * stride < n16; c += 4 * stride) {
-        uint4 v0 = ld_stream(src + c), v1 = ld_stream(src + c + stride);
-        uint4 v2 = ld_stream(src + c + 2 * stride), v3 = ld_stream(src + c + 3 * stride);
-        dst[c] = v0;
-        dst[c + stride] = v1;
-        dst[c + 2 * stride] = v2;
-        dst[c + 3 * stride] = v3;
-      }
-      for (; c < n16; c += stride) dst[c] = ld_stream(src + c);
+  const int nseg = q * p.n_banks;
+  const int G = gridDim.x;
+  for (int sgi = nseg >= G ? blockIdx.x : blockIdx.x % nseg; sgi < nseg; sgi += G) {
+    const int i = sgi / p.n_banks, j = sgi - i * p.n_banks;
+    // CTAs sharing this segment: those with the same residue mod nseg (all of them when nseg < G)
+    const int part = nseg >= G ? 0 : blockIdx.x / nseg;
+    const int nparts = nseg >= G ? 1 : (G - 1 - sgi) / nseg + 1;
+    size_t nbytes, doff;
+    const uint8_t* sb;
+    switch (j) {
+      case 0: nbytes = p.src_row[0]; doff = p.lay.gate; sb = p.src[0]; break;
+      case 1: nbytes = p.src_row[1]; doff = p.lay.up; sb = p.src[1]; break;
+      case 2: nbytes = p.src_row[2]; doff = p.lay.down; sb = p.src[2]; break;
+      case 3: nbytes = p.src_row[3]; doff = p.lay.gs; sb = p.src[3]; break;
+      case 4: nbytes = p.src_row[4]; doff = p.lay.us; sb = p.src[4]; break;
+      default: nbytes = p.src_row[5]; doff = p.lay.ds; sb = p.src[5]; break;
     }
+    const int uid = p.copy_u[i];
+    const uint4* src = reinterpret_cast<const uint4*>(sb + (size_t)uid * nbytes);
+    uint4* dst = reinterpret_cast<uint4*>(p.pool + (size_t)p.copy_slot[i] * p.lay.stride + doff);
+    copy_segment(src, dst, nbytes / 16, (size_t)part * blockDim.x + threadIdx.x, (size_t)nparts * blockDim.x);
+    if (nseg < G) break;  // one segment share per CTA
   }
 }
 
