@@ -258,6 +258,38 @@ ft_status ft_moe_synchronize(ft_moe* h);
 /* Release device memory, streams and host registrations.  Synchronises. */
 ft_status ft_moe_destroy(ft_moe* h);
 
+/* Allocation-free layer evaluation.  The pages have no counterpart: this entry point is
+ * for callers that cannot call cudaMalloc, such as an engine that reserved all device
+ * memory for its own pool at start-up and forbids further allocation, or a plug-in host
+ * that only lets a library use memory it was handed.  It evaluates one decode MoE layer
+ * whose E routed experts all sit in device memory owned by the caller: top-k softmax
+ * routing, grouped SwiGLU evaluation of every routed pair, and the fixed-order combine
+ * (shared expert first, then the k rows in ascending expert id).  The result equals what
+ * ft_moe_decode_step returns for a cache that holds the whole layer.
+ *   experts_dev  dev, E slots of stride S_b = round_up(used, 256) bytes, each laid out
+ *                gate [I][H] | up [I][H] | down [H][I] (BF16, 2 B/elem; or E4M3 codes,
+ *                1 B/elem, followed by gate_scale [I][H/128] | up_scale [I][H/128] |
+ *                down_scale [H][I/128] FP32), used = the sum of those sizes
+ *   shared_dev   dev, one slot in the same layout, or NULL (no shared expert)
+ *   x_bf16 [batch][H] BF16, logits [batch][E] FP32, out [batch][H] FP32 (dev);
+ *   rows_out     optional dev [batch][top_k][H] FP32 gate-weighted pair rows
+ *   stream       cudaStream_t to enqueue on (NULL: legacy default stream)
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  All intermediates live
+ * in one file-scope device array of 8 MiB that every GPU loading the library holds until
+ * the process exits; a request whose intermediates do not fit returns FT_ERR_CAPACITY
+ * (e.g. batch * top_k * H * 4 bytes of pair rows alone must stay well below 8 MiB).
+ * The first call on a device, with that device current, looks up the array's device
+ * address and sets kernel launch limits; make that first call before any stream capture.
+ * Every call shares the array and the array keeps the last call's contents (the call
+ * resets what must start fresh), so calls that overlap on the GPU -- on different streams,
+ * or from several threads -- race with each other: serialise them.
+ * Other errors: FT_ERR_INVALID (the ft_moe_init shape limits; batch <= 64), FT_ERR_CUDA.
+ * Returns after enqueueing; no error message is stored for ft_last_error. */
+ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, int hidden, int inter, int wtype,
+                                         const void* experts_dev, const void* shared_dev, int batch,
+                                         const void* x_bf16, const float* logits, float* out,
+                                         float* rows_out, void* stream);
+
 /* Thread-local message describing the last error of this thread ("" if none). */
 const char* ft_last_error(void);
 

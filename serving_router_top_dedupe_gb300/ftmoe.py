@@ -90,6 +90,8 @@ _SIGS = {
     "ft_moe_set_stream": [_P, _P],
     "ft_moe_synchronize": [_P],
     "ft_moe_destroy": [_P],
+    "ft_moe_decode_resident_noalloc": [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, _P, C.c_int, _P, _P, _P, _P,
+                                       _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -239,6 +241,17 @@ def ft_moe_synchronize(h) -> None:
 
 def ft_moe_destroy(h) -> None:
     _check(_lib.ft_moe_destroy(h))
+
+
+def ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, experts_dev, shared_dev, batch, x_bf16,
+                                   logits, out, rows_out=None, stream=None) -> None:
+    """Allocation-free layer evaluation (see include/ft_moe.h): every intermediate lives in
+    the library's fixed 8 MiB device scratch array; nothing is allocated by the call."""
+    st = _lib.ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, _ptr(experts_dev),
+                                             _ptr(shared_dev), batch, _ptr(x_bf16), _ptr(logits), _ptr(out),
+                                             _ptr(rows_out), stream)
+    if st != FT_OK:
+        raise FtError(st, "ft_moe_decode_resident_noalloc failed")
 
 
 def make_config(n_layers, hidden, inter, n_experts, top_k, has_shared, wtype, max_batch, cache_slots,
