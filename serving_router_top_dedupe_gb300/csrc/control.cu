@@ -13,14 +13,11 @@
 #include <climits>
 
 #include "ft_internal.cuh"
+#include "ft_route.cuh"
 
 namespace ft {
 namespace {
 
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  // total order: larger logit first, then lower expert id
-  return v > bv || (v == bv && e < be);
-}
 
 // Fill count: q = clamp(floor(m*bp/bh + 1/2), 1, m) for m > 0; all misses when the
 // residual bandwidth B_H - B_P is not positive; never more than `evictable`.
@@ -41,75 +38,6 @@ __device__ __forceinline__ int split_q(int m, long long bp, long long bh, int ev
 constexpr int kRegJ = 16;      // stamps per thread held in registers (S <= 16K)
 constexpr int kDigit = 11;     // radix-select digit
 constexpr int kBins = 1 << kDigit;
-
-template <int NPL>  // logits held per lane: E <= 32*NPL
-__device__ void route_token(const CtrlParams& p, int t, int lane, int* s_sel, uint32_t* s_bitmap,
-                            uint32_t* s_err) {
-  const float* z = p.logits + (size_t)t * p.E;
-  float v[NPL];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    int e = lane + 32 * j;
-    float x = -INFINITY;
-    if (e < p.E) {
-      x = __ldg(z + e);
-      if (x != x) {  // NaN: ranked as -inf, reported
-        x = -INFINITY;
-        atomicOr(s_err, FT_DEVERR_NAN_LOGIT);
-      }
-    } else {
-      taken |= 1u << j;  // not an expert
-    }
-    v[j] = x;
-  }
-  int my_e = INT_MAX;
-  float my_z = -INFINITY, zmax = -INFINITY;
-  for (int r = 0; r < p.k; ++r) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
-#pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-      int e = lane + 32 * j;
-      if (!(taken & (1u << j)) && better(v[j], e, bv, be)) {
-        bv = v[j];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == r) {
-      my_e = be;
-      my_z = bv;
-    }
-    if (r == 0) zmax = bv;
-  }
-  // rank of this lane's id among the k chosen ids -> ascending-id position
-  int rank = 0;
-  for (int j = 0; j < p.k; ++j) {
-    int oe = __shfl_sync(0xffffffffu, my_e, j);
-    if (lane < p.k && oe < my_e) ++rank;
-  }
-  float ex = lane < p.k ? expf(my_z - zmax) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < p.k) {
-    int idx = t * p.k + rank;
-    p.w.sel[idx] = my_e;
-    p.w.gates[idx] = ex / sum;
-    s_sel[idx] = my_e;
-    atomicOr(&s_bitmap[my_e >> 5], 1u << (my_e & 31));
-  }
-}
 
 __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) {
   __shared__ uint32_t s_bitmap[kMaxE / 32];
@@ -149,12 +77,13 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
 
   // ---- 1. route: one warp per token
   for (int t = warp; t < B; t += blockDim.x / 32) {
-    if (E <= 32) route_token<1>(p, t, lane, s_sel, s_bitmap, &s_err);
-    else if (E <= 64) route_token<2>(p, t, lane, s_sel, s_bitmap, &s_err);
-    else if (E <= 128) route_token<4>(p, t, lane, s_sel, s_bitmap, &s_err);
-    else if (E <= 256) route_token<8>(p, t, lane, s_sel, s_bitmap, &s_err);
-    else if (E <= 512) route_token<16>(p, t, lane, s_sel, s_bitmap, &s_err);
-    else route_token<32>(p, t, lane, s_sel, s_bitmap, &s_err);
+    route_token_any(p.logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
+      const int idx = t * k + rank;
+      p.w.sel[idx] = e;
+      p.w.gates[idx] = g;
+      s_sel[idx] = e;
+      atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
+    });
   }
   __syncthreads();
 

@@ -24,6 +24,32 @@ struct PrefillCtx {
   bool prof;
 };
 
+// Arguments of the grouped GEMM (prefill_gemm.cu).  Entries 0..E-1 are the layer's
+// routed experts (weights in pool slots buf_slots[e]); entry E, when present, is the
+// shared expert (weights in the shared-expert array, row block `layer`).
+struct GemmDesc {
+  int n_entries, E, layer, I, H;
+  int mt;                    // M tiles per entry: gate/up I/64, down H/128
+  int kb;                    // K steps of 64: gate/up H/64, down I/64
+  const int32_t* entry_off;  // [n_entries+1] first pair of each entry (pairs sorted by entry, token)
+  const int32_t* tile_off;   // [n_entries+1] prefix of N tiles per entry
+  const int32_t* buf_slots;  // [E]
+  const int32_t* pair_tok;   // [P] token of each pair
+  const float* pair_gate;    // [P] gate of each pair (1 for the shared expert)
+  uint16_t* h;               // [P][I] BF16 (gate/up output)
+  uint16_t* rows;            // [P][H] BF16 (down output)
+  uint32_t* error_word;
+};
+
+// Tensor maps and launch of the grouped GEMM.  mode 0: gate/up + SwiGLU from x (token
+// rows gathered); mode 1: down + gate weighting from h.
+struct GemmMaps;
+cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
+                             int I, const uint16_t* h_buf, int max_pairs);
+void gemm_maps_destroy(GemmMaps* m);
+cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, int T, const GemmDesc& d, int grid,
+                                cudaStream_t s);
+
 struct PrefillState;
 
 using ProfEvents = std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>>;

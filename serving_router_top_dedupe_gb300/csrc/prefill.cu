@@ -1,25 +1,521 @@
-// Prefill path: full-layer double buffering and the grouped GEMM.
+// Prefill path: full-layer double buffering from the shared slot pool, routing of a
+// whole chunk, the grouped GEMMs (prefill_gemm.cu) and the fixed-order combine.
+//
+// "FreeToken 完全拆解", section "全层双缓冲": two full-layer buffers come from the same
+// global slot pool as the decode cache; while layer l is computed from one, a transfer
+// stream copies every expert of layer l+1 into the other without waiting for routing;
+// what the last layers leave behind seeds decode.  Reading used here (the pages fix no
+// finer policy): a chunk starts at a prefill call that does not continue the previous
+// prefill layer and takes the 2E least recently used slots (ascending (stamp, slot)),
+// evicting their occupants; layer l uses buffer (l - first) mod 2, expert e in its e-th
+// slot; installing a layer drops the buffer's previous occupants, invalidates any older
+// resident copy of the layer's experts and stamps every expert of the layer with that
+// step's clock.  Prefill does not count as hits or misses.
+#include <algorithm>
+#include <cstring>
+
 #include "ft_prefill.cuh"
+#include "ft_route.cuh"
 
 namespace ft {
+namespace {
+
+constexpr int kPickThreads = 1024;
+constexpr int kPickMaxSlots = 16384;  // slots sorted in shared memory when a chunk starts
+constexpr int kTileN = 256;
+
+// Sorts all slots by (stamp, slot) in shared memory (bitonic), writes the 2E least
+// recently used to out[] in order and evicts their occupants.
+__global__ void __launch_bounds__(kPickThreads) pick_buffers_kernel(int32_t* res, int32_t* owner, uint32_t* stamp,
+                                                                   int S, int n_pick, int32_t* out) {
+  extern __shared__ unsigned long long keys[];
+  int n2 = 1;
+  while (n2 < S) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    keys[i] = i < S ? (((unsigned long long)stamp[i] << 32) | (unsigned)i) : ~0ull;
+  __syncthreads();
+  for (int kk = 2; kk <= n2; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool up = (i & kk) == 0;
+          const unsigned long long a = keys[i], b = keys[ixj];
+          if ((a > b) == up) {
+            keys[i] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n_pick; i += blockDim.x) {
+    const int v = (int)(keys[i] & 0xffffffffu);
+    out[i] = v;
+    const int o = owner[v];
+    if (o >= 0) res[o] = -1;
+    owner[v] = -1;
+    stamp[v] = 0u;
+  }
+}
+
+// Residency effect of computing layer `layer` from buffer `buf` (one CTA).
+__global__ void __launch_bounds__(1024) install_layer_kernel(int layer, int E, const int32_t* buf, int32_t* res,
+                                                            int32_t* owner, uint32_t* stamp, DevState* st) {
+  __shared__ uint32_t s_clock;
+  if (threadIdx.x == 0) s_clock = st->clock + 1u;
+  // phase 1: read previous occupants and older copies
+  int prev[4], old[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = threadIdx.x + j * blockDim.x;
+    prev[j] = old[j] = -1;
+    if (e < E) {
+      prev[j] = owner[buf[e]];
+      old[j] = res[layer * E + e];
+    }
+  }
+  __syncthreads();
+  const uint32_t clock = s_clock;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = threadIdx.x + j * blockDim.x;
+    if (e >= E) continue;
+    const int u = layer * E + e, v = buf[e];
+    if (prev[j] >= 0 && prev[j] != u) res[prev[j]] = -1;
+    if (old[j] >= 0 && old[j] != v) {
+      owner[old[j]] = -1;
+      stamp[old[j]] = 0u;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = threadIdx.x + j * blockDim.x;
+    if (e >= E) continue;
+    const int u = layer * E + e, v = buf[e];
+    owner[v] = u;
+    res[u] = v;
+    stamp[v] = clock;
+  }
+  if (threadIdx.x == 0) {
+    st->clock = clock;
+    st->prefill_layers += 1ull;
+  }
+}
+
+// One warp per token: top-k softmax, then the token's bit in each chosen expert's mask.
+__global__ void __launch_bounds__(256) prefill_route_kernel(const float* logits, int T, int E, int k, int W,
+                                                           int32_t* sel, float* gates, uint32_t* masks,
+                                                           uint32_t* error_word) {
+  __shared__ uint32_t s_err;
+  if (threadIdx.x == 0) s_err = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t < T) {
+    route_token_any(logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
+      sel[(size_t)t * k + rank] = e;
+      gates[(size_t)t * k + rank] = g;
+      atomicOr(masks + (size_t)e * W + (t >> 5), 1u << (t & 31));
+    });
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && s_err) atomicOr(error_word, s_err);
+}
+
+// Per expert: exclusive prefix of popcounts over its mask words (token order), its
+// pair count; then pair offsets and N-tile offsets over entries (one CTA).
+__global__ void __launch_bounds__(1024) prefill_scan_kernel(const uint32_t* masks, int W, int E, int T,
+                                                           int has_shared, int32_t* wpre, int32_t* entry_off,
+                                                           int32_t* tile_off) {
+  __shared__ int s_cnt[kMaxE + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int per = (W + 31) / 32;  // contiguous words per lane
+  for (int e = warp; e < E; e += nw) {
+    const uint32_t* m = masks + (size_t)e * W;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int w = lane * per + i;
+      if (w < W) local += __popc(m[w]);
+    }
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int w = lane * per + i;
+      if (w < W) {
+        wpre[(size_t)e * W + w] = run;
+        run += __popc(m[w]);
+      }
+    }
+    if (lane == 31) s_cnt[e] = incl;
+  }
+  if (threadIdx.x == 0 && has_shared) s_cnt[E] = T;
+  __syncthreads();
+  if (warp == 0) {
+    const int n = E + (has_shared ? 1 : 0);
+    int carry_p = 0, carry_t = 0;
+    for (int c = 0; c < n; c += 32) {
+      const int i = c + lane;
+      const int v = i < n ? s_cnt[i] : 0;
+      const int nt = (v + kTileN - 1) / kTileN;
+      int ip = v, it = nt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yp = __shfl_up_sync(0xffffffffu, ip, o), yt = __shfl_up_sync(0xffffffffu, it, o);
+        if (lane >= o) {
+          ip += yp;
+          it += yt;
+        }
+      }
+      if (i < n) {
+        entry_off[i] = carry_p + ip - v;
+        tile_off[i] = carry_t + it - nt;
+      }
+      carry_p += __shfl_sync(0xffffffffu, ip, 31);
+      carry_t += __shfl_sync(0xffffffffu, it, 31);
+    }
+    if (lane == 0) {
+      entry_off[n] = carry_p;
+      tile_off[n] = carry_t;
+    }
+  }
+}
+
+// Pair (t, r) -> its position in the expert-sorted pair list (tokens ascending within
+// an expert); shared-expert pairs follow all routed pairs, one per token.
+__global__ void prefill_place_kernel(const int32_t* sel, const float* gates, const uint32_t* masks,
+                                     const int32_t* wpre, const int32_t* entry_off, int T, int k, int E, int W,
+                                     int has_shared, int32_t* pair_tok, float* pair_gate, int32_t* pos_of) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < T * k) {
+    const int t = i / k;
+    const int e = sel[i];
+    const int w = t >> 5;
+    const uint32_t below = masks[(size_t)e * W + w] & ((1u << (t & 31)) - 1u);
+    const int pos = entry_off[e] + wpre[(size_t)e * W + w] + __popc(below);
+    pair_tok[pos] = t;
+    pair_gate[pos] = gates[i];
+    pos_of[i] = pos;
+  } else if (has_shared && i < T * k + T) {
+    const int t = i - T * k;
+    const int pos = entry_off[E] + t;
+    pair_tok[pos] = t;
+    pair_gate[pos] = 1.0f;
+  }
+}
+
+// out[t] = shared row (if any) + the k pair rows in rank order (ascending expert id).
+__global__ void prefill_combine_kernel(const uint16_t* rows, const int32_t* pos_of, const int32_t* entry_off, int T,
+                                       int k, int H, int E, int has_shared, float* out) {
+  const int per_tok = H / 8;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)T * per_tok) return;
+  const int t = (int)(i / per_tok), j0 = (int)(i - (size_t)t * per_tok) * 8;
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  auto add_row = [&](int p) {
+    const uint4 v = *reinterpret_cast<const uint4*>(rows + (size_t)p * H + j0);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] += __uint_as_float(w[q] << 16);
+      acc[2 * q + 1] += __uint_as_float(w[q] & 0xffff0000u);
+    }
+  };
+  if (has_shared) add_row(entry_off[E] + t);
+  for (int r = 0; r < k; ++r) add_row(pos_of[(size_t)t * k + r]);
+  float4* o = reinterpret_cast<float4*>(out + (size_t)t * H + j0);
+  o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
 
 struct PrefillState {
-  int dummy = 0;
+  int T_max = 0, E = 0, K = 0, H = 0, I = 0, L = 0, S = 0, W = 0, has_shared = 0, n_sm = 0;
+  // routing and GEMM buffers
+  int32_t *sel = nullptr, *wpre = nullptr, *entry_off = nullptr, *tile_off = nullptr;
+  int32_t *pair_tok = nullptr, *pos_of = nullptr, *buf_dev = nullptr, *pick_dev = nullptr, *pick_host = nullptr;
+  float *gates = nullptr, *pair_gate = nullptr;
+  uint32_t* masks = nullptr;
+  uint16_t *h = nullptr, *rows = nullptr;
+  GemmMaps* maps = nullptr;
+  // chunk state (host)
+  bool active = false;
+  int first = 0, next_layer = -1, pending = -1;
+  std::vector<int> buf[2];
+  cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr}, ev_restore = nullptr;
+  bool free_recorded[2] = {false, false};
+  cudaStream_t cs = nullptr, ts = nullptr;
+  // what a restore copy needs
+  uint8_t* pool = nullptr;
+  SlotLayout lay{};
+  const uint8_t* bank_host[3] = {nullptr, nullptr, nullptr};
+  size_t bank_row[3] = {0, 0, 0};
 };
 
-cudaError_t prefill_create(PrefillState** out, const PrefillCtx&) {
-  *out = new PrefillState();
+namespace {
+
+// Copy every expert of `layer` from the host banks into the slots `slots` (on ts).
+// Runs of consecutive slots become one 2-D copy per bank.
+cudaError_t copy_layer(PrefillState* p, int layer, const std::vector<int>& slots, cudaStream_t ts) {
+  const size_t seg[3] = {p->lay.gate, p->lay.up, p->lay.down};
+  const int E = p->E;
+  int e = 0;
+  while (e < E) {
+    int run = 1;
+    while (e + run < E && slots[e + run] == slots[e] + run) ++run;
+    for (int j = 0; j < 3; ++j) {
+      const uint8_t* src = p->bank_host[j] + ((size_t)layer * E + e) * p->bank_row[j];
+      uint8_t* dst = p->pool + (size_t)slots[e] * p->lay.stride + seg[j];
+      cudaError_t err = run == 1 ? cudaMemcpyAsync(dst, src, p->bank_row[j], cudaMemcpyHostToDevice, ts)
+                                 : cudaMemcpy2DAsync(dst, p->lay.stride, src, p->bank_row[j], p->bank_row[j], run,
+                                                     cudaMemcpyHostToDevice, ts);
+      if (err != cudaSuccess) return err;
+    }
+    e += run;
+  }
   return cudaSuccess;
 }
 
-void prefill_destroy(PrefillState* p) { delete p; }
+// Enqueue the load of `layer` into buffer b on the transfer stream, after the compute
+// that last used buffer b.
+cudaError_t load_buffer(PrefillState* p, int layer, int b, ProfEvents* prof) {
+  cudaError_t e;
+  if (p->free_recorded[b] && (e = cudaStreamWaitEvent(p->ts, p->ev_free[b], 0)) != cudaSuccess) return e;
+  cudaEvent_t a = nullptr, z = nullptr;
+  if (prof) {
+    cudaEventCreate(&a);
+    cudaEventCreate(&z);
+    cudaEventRecord(a, p->ts);
+  }
+  if ((e = copy_layer(p, layer, p->buf[b], p->ts)) != cudaSuccess) return e;
+  if (prof) {
+    cudaEventRecord(z, p->ts);
+    prof->push_back({7, {a, z}});
+  }
+  return cudaEventRecord(p->ev_loaded[b], p->ts);
+}
 
-void prefill_interrupt(PrefillState*) {}
+template <typename T>
+cudaError_t dev_alloc(T** ptr, size_t n) {
+  return cudaMalloc(reinterpret_cast<void**>(ptr), (n ? n : 1) * sizeof(T));
+}
 
-cudaError_t prefill_layer(PrefillState*, const PrefillCtx&, int, int, const uint16_t*, const float*, float*,
-                          ProfEvents*, std::string* err) {
-  if (err) *err = "prefill grouped GEMM not built yet";
-  return cudaErrorNotSupported;
+}  // namespace
+
+cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
+  if (c.S > kPickMaxSlots) return cudaErrorInvalidValue;
+  if (c.lay.stride != c.lay.used || c.H % 128 || c.I % 64) return cudaErrorInvalidValue;
+  PrefillState* p = new PrefillState();
+  p->T_max = c.max_tokens;
+  p->E = c.E;
+  p->K = c.K;
+  p->H = c.H;
+  p->I = c.I;
+  p->L = c.L;
+  p->S = c.S;
+  p->W = (c.max_tokens + 31) / 32;
+  p->has_shared = c.has_shared;
+  p->n_sm = c.n_sm;
+  p->pool = c.pool;
+  p->lay = c.lay;
+  for (int j = 0; j < 3; ++j) {
+    p->bank_host[j] = c.bank_host[j];
+    p->bank_row[j] = c.bank_row[j];
+  }
+  const size_t T = c.max_tokens, k = c.K, P = T * k + (c.has_shared ? T : 0);
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = dev_alloc(&p->sel, T * k);
+  if (e == cudaSuccess) e = dev_alloc(&p->gates, T * k);
+  if (e == cudaSuccess) e = dev_alloc(&p->masks, (size_t)c.E * p->W);
+  if (e == cudaSuccess) e = dev_alloc(&p->wpre, (size_t)c.E * p->W);
+  if (e == cudaSuccess) e = dev_alloc(&p->entry_off, (size_t)c.E + 2);
+  if (e == cudaSuccess) e = dev_alloc(&p->tile_off, (size_t)c.E + 2);
+  if (e == cudaSuccess) e = dev_alloc(&p->pair_tok, P);
+  if (e == cudaSuccess) e = dev_alloc(&p->pair_gate, P);
+  if (e == cudaSuccess) e = dev_alloc(&p->pos_of, T * k);
+  if (e == cudaSuccess) e = dev_alloc(&p->h, P * c.I);
+  if (e == cudaSuccess) e = dev_alloc(&p->rows, P * c.H);
+  if (e == cudaSuccess) e = dev_alloc(&p->buf_dev, (size_t)2 * c.E);
+  if (e == cudaSuccess) e = dev_alloc(&p->pick_dev, (size_t)2 * c.E);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->pick_host), sizeof(int32_t) * 2 * c.E, 0);
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    e = cudaEventCreateWithFlags(&p->ev_loaded[b], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_free[b], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_restore, cudaEventDisableTiming);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pick_buffers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPickMaxSlots * (int)sizeof(unsigned long long));
+  if (e == cudaSuccess) e = gemm_maps_create(&p->maps, c.pool, c.S, c.shared_w, c.L, c.H, c.I, p->h, (int)P);
+  if (e != cudaSuccess) {
+    prefill_destroy(p);
+    return e;
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+void prefill_destroy(PrefillState* p) {
+  if (!p) return;
+  prefill_interrupt(p);
+  if (p->cs) cudaStreamSynchronize(p->cs);
+  if (p->ts) cudaStreamSynchronize(p->ts);
+  void* bufs[] = {p->sel, p->gates, p->masks, p->wpre, p->entry_off, p->tile_off, p->pair_tok,
+                  p->pair_gate, p->pos_of, p->h, p->rows, p->buf_dev, p->pick_dev};
+  for (void* b : bufs)
+    if (b) cudaFree(b);
+  if (p->pick_host) cudaFreeHost(p->pick_host);
+  for (int b = 0; b < 2; ++b) {
+    if (p->ev_loaded[b]) cudaEventDestroy(p->ev_loaded[b]);
+    if (p->ev_free[b]) cudaEventDestroy(p->ev_free[b]);
+  }
+  if (p->ev_restore) cudaEventDestroy(p->ev_restore);
+  gemm_maps_destroy(p->maps);
+  delete p;
+}
+
+void prefill_interrupt(PrefillState* p) {
+  if (!p || !p->active) return;
+  if (p->pending >= 0) {
+    // buffer of the streaming layer still holds (in the residency table) the layer two
+    // before it: copy that layer's weights back so data and table agree again
+    const int b = (p->pending - p->first) & 1;
+    const int back = p->pending - 2;
+    if (back >= p->first) {
+      copy_layer(p, back, p->buf[b], p->ts);
+    }
+    cudaEventRecord(p->ev_restore, p->ts);
+    cudaStreamWaitEvent(p->cs, p->ev_restore, 0);
+  }
+  p->active = false;
+  p->pending = -1;
+  p->next_layer = -1;
+}
+
+cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T, const uint16_t* x,
+                          const float* logits, float* out, ProfEvents* prof, std::string* err) {
+  cudaError_t e;
+  p->cs = c.cs;
+  p->ts = c.ts;
+  const int E = p->E, k = p->K;
+  auto timed = [&](int kind, auto&& body) -> cudaError_t {
+    cudaEvent_t a = nullptr, z = nullptr;
+    if (prof) {
+      cudaEventCreate(&a);
+      cudaEventCreate(&z);
+      cudaEventRecord(a, c.cs);
+    }
+    cudaError_t r = body();
+    if (prof) {
+      cudaEventRecord(z, c.cs);
+      prof->push_back({kind, {a, z}});
+    }
+    return r;
+  };
+
+  // ---- chunk start: take the 2E least recently used slots as the two buffers
+  if (!p->active || p->next_layer != layer) {
+    prefill_interrupt(p);
+    pick_buffers_kernel<<<1, kPickThreads, kPickMaxSlots * sizeof(unsigned long long), c.cs>>>(
+        c.res, c.owner, c.stamp, c.S, 2 * E, p->pick_dev);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaMemcpyAsync(p->buf_dev, p->pick_dev, sizeof(int32_t) * 2 * E, cudaMemcpyDeviceToDevice, c.cs)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaMemcpyAsync(p->pick_host, p->pick_dev, sizeof(int32_t) * 2 * E, cudaMemcpyDeviceToHost, c.cs)) !=
+        cudaSuccess)
+      return e;
+    if ((e = cudaStreamSynchronize(c.cs)) != cudaSuccess) return e;
+    p->buf[0].assign(p->pick_host, p->pick_host + E);
+    p->buf[1].assign(p->pick_host + E, p->pick_host + 2 * E);
+    p->active = true;
+    p->first = layer;
+    p->pending = -1;
+    p->free_recorded[0] = p->free_recorded[1] = false;
+  }
+  const int b = (layer - p->first) & 1;
+
+  // ---- this layer's weights: already streaming (prefetched) or load now
+  if (p->pending != layer && (e = load_buffer(p, layer, b, prof)) != cudaSuccess) return e;
+  p->pending = -1;
+  if ((e = cudaStreamWaitEvent(c.cs, p->ev_loaded[b], 0)) != cudaSuccess) return e;
+  install_layer_kernel<<<1, 1024, 0, c.cs>>>(layer, E, p->buf_dev + (size_t)b * E, c.res, c.owner, c.stamp, c.st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  // ---- stream the whole next layer into the other buffer while this one computes
+  if (layer + 1 < p->L) {
+    if ((e = load_buffer(p, layer + 1, b ^ 1, prof)) != cudaSuccess) return e;
+    p->pending = layer + 1;
+  }
+
+  // ---- route the chunk and sort its pairs by expert
+  e = timed(4, [&]() -> cudaError_t {
+    cudaError_t r = cudaMemsetAsync(p->masks, 0, sizeof(uint32_t) * (size_t)E * p->W, c.cs);
+    if (r != cudaSuccess) return r;
+    prefill_route_kernel<<<(T + 7) / 8, 256, 0, c.cs>>>(logits, T, E, k, p->W, p->sel, p->gates, p->masks,
+                                                        &c.st->error_word);
+    prefill_scan_kernel<<<1, 1024, 0, c.cs>>>(p->masks, p->W, E, T, p->has_shared, p->wpre, p->entry_off,
+                                              p->tile_off);
+    const int n_pl = T * k + (p->has_shared ? T : 0);
+    prefill_place_kernel<<<(n_pl + 255) / 256, 256, 0, c.cs>>>(p->sel, p->gates, p->masks, p->wpre, p->entry_off, T,
+                                                               k, E, p->W, p->has_shared, p->pair_tok, p->pair_gate,
+                                                               p->pos_of);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return e;
+
+  // ---- grouped GEMMs on the tensor cores
+  GemmDesc d{};
+  d.n_entries = E + (p->has_shared ? 1 : 0);
+  d.E = E;
+  d.layer = layer;
+  d.I = p->I;
+  d.H = p->H;
+  d.entry_off = p->entry_off;
+  d.tile_off = p->tile_off;
+  d.buf_slots = p->buf_dev + (size_t)b * E;
+  d.pair_tok = p->pair_tok;
+  d.pair_gate = p->pair_gate;
+  d.h = p->h;
+  d.rows = p->rows;
+  d.error_word = &c.st->error_word;
+  e = timed(5, [&]() -> cudaError_t {
+    d.mt = p->I / 64;
+    d.kb = p->H / 64;
+    cudaError_t r = launch_grouped_gemm(0, p->maps, x, T, d, p->n_sm, c.cs);
+    if (r != cudaSuccess) return r;
+    d.mt = p->H / 128;
+    d.kb = p->I / 64;
+    return launch_grouped_gemm(1, p->maps, x, T, d, p->n_sm, c.cs);
+  });
+  if (e != cudaSuccess) {
+    if (err) *err = "grouped GEMM launch";
+    return e;
+  }
+  e = timed(6, [&]() -> cudaError_t {
+    const size_t n = (size_t)T * (p->H / 8);
+    prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, c.cs>>>(p->rows, p->pos_of, p->entry_off, T, k,
+                                                                          p->H, E, p->has_shared, out);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return e;
+  if ((e = cudaEventRecord(p->ev_free[b], c.cs)) != cudaSuccess) return e;
+  p->free_recorded[b] = true;
+  if (layer + 1 < p->L) {
+    p->next_layer = layer + 1;
+  } else {
+    p->active = false;
+    p->next_layer = -1;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace ft

@@ -1,1 +1,482 @@
-// Grouped GEMM for prefill (filled in with the tcgen05 kernel).
+// Prefill grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMA + TMEM).
+//
+// A prefill chunk routes thousands of tokens, so nearly every expert of a layer gets
+// ~T*k/E tokens ("FreeToken 完全拆解", section "挑战一"): the expert evaluation is a real
+// dense contraction per expert.  Both projections use the weight-stationary ("swap-AB")
+// form D[m, n] = sum_k W[m, k] * X[n, k]: the M side is 128 weight rows, the N side is up
+// to 256 of the expert's tokens (a multiple of 16), so ragged token counts pad only to 16.
+//
+//  mode 0 (gate/up + SwiGLU): one 128-row M tile holds 64 gate rows and the same 64 up
+//    rows of the expert (two TMA boxes), K = H.  The N operand gathers the expert's token
+//    rows of x with TMA tile::gather4.  Epilogue: h[p][i] = silu(g) * u as BF16.
+//  mode 1 (down + gate weighting): M tile = 128 rows of W_down, K = I, the N operand is
+//    the expert's contiguous rows of h.  Epilogue: rows[p][j] = BF16(gate_p * y).
+//
+// One CTA per SM, persistent over tiles.  Warp 0 issues TMA into a 4-stage shared-memory
+// ring, warp 1 issues tcgen05.mma (one thread) into one of two TMEM accumulators, warps
+// 2-5 drain the other accumulator (tcgen05.ld) while the next tile accumulates.  Every
+// mbarrier wait is bounded: on timeout the kernel records FT_DEVERR_TIMEOUT, stops
+// issuing work, drains its outstanding copies (bounded) and frees TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "ft_prefill.cuh"
+
+namespace ft {
+namespace {
+
+constexpr int BM = 128, BK = 64, BN_MAX = 256, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = BN_MAX * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_COLS = 16;               // TMEM columns drained per step
+constexpr int STG_PITCH = EPI_COLS + 1;    // staging row pitch (floats), bank-conflict free
+constexpr int GEMM_THREADS = 192;
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with parity `parity` to complete.  On timeout sets the
+// error word and the CTA's abort flag and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* error_word) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  atomicOr(error_word, FT_DEVERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Four rows (r0..r3) of `map`, each `box width` elements from column x, one row high.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                            int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile, rows of 128 bytes with the 128-byte
+// swizzle, 8-row atoms 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: BF16 A and B, FP32 accumulator, both K-major.
+__device__ __forceinline__ uint32_t bf16_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 16 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  uint32_t b = __float_as_uint(f);
+  b += 0x7FFFu + ((b >> 16) & 1u);  // round to nearest even (inputs are finite)
+  return (uint16_t)(b >> 16);
+}
+
+struct TileInfo {
+  int e, m, nvalid, N, pbase;
+};
+
+// Global tile g -> (entry, M tile, N range).  M tiles are innermost so consecutive tiles
+// of one CTA reuse the same token rows through L2.  An entry with n_e tokens is split
+// into ceil(n_e/256) N tiles of equal size rounded up to 16.
+__device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int g) {
+  TileInfo t;
+  t.m = g % d.mt;
+  const int q = g / d.mt;
+  int lo = 0, hi = d.n_entries;  // tile_off[lo] <= q < tile_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(d.tile_off + mid) <= q) lo = mid;
+    else hi = mid;
+  }
+  t.e = lo;
+  const int p0 = __ldg(d.entry_off + lo), ne = __ldg(d.entry_off + lo + 1) - p0;
+  const int t0 = __ldg(d.tile_off + lo), nt = __ldg(d.tile_off + lo + 1) - t0;
+  const int tsize = ((ne + nt - 1) / nt + 15) & ~15;
+  const int n0 = (q - t0) * tsize;
+  t.nvalid = min(tsize, ne - n0);
+  t.N = (t.nvalid + 15) & ~15;
+  t.pbase = p0 + n0;
+  return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
+                        const __grid_constant__ CUtensorMap tmB, const GemmDesc d) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + BM * STG_PITCH * 4);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* done = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(tfull + b), 1);
+      mbar_init(smem_u32(tempty + b), 128);
+    }
+    mbar_init(smem_u32(done), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {  // 512 TMEM columns: two 256-column FP32 accumulators
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = d.mt * __ldg(d.tile_off + d.n_entries);
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    int last_par[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const TileInfo t = decode_tile(d, g);
+      if (t.nvalid <= 0) continue;
+      const bool sh = t.e >= d.E;
+      const CUtensorMap* mA = sh ? &tmAs : &tmA;
+      const int wbase = sh ? d.layer : __ldg(d.buf_slots + t.e);
+      int arow0, arow1 = 0;
+      if (MODE == 0) {
+        arow0 = wbase * 3 * d.I + t.m * 64;  // gate rows
+        arow1 = arow0 + d.I;                 // up rows
+      } else {
+        arow0 = wbase * 3 * d.H + 2 * d.H + t.m * BM;  // down rows
+      }
+      int rows[8];
+      const int ngroups = t.N / 4;
+      if (MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int gi = lane + 32 * j;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int n = min(4 * gi + r, t.nvalid - 1);
+            rows[4 * j + r] = gi < ngroups ? __ldg(d.pair_tok + t.pbase + n) : 0;
+          }
+        }
+      }
+      bool ok = true;
+      for (int kb = 0; kb < d.kb; ++kb) {
+        int w_ok = lane == 0 ? (int)mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag, d.error_word) : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_dst = smem_base + stage * STAGE_BYTES, b_dst = a_dst + A_BYTES;
+        const uint32_t fb = smem_u32(full + stage);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, A_BYTES + (MODE == 0 ? t.N * 128 : B_BYTES));
+          if (MODE == 0) {
+            tma_load_2d(a_dst, mA, kb * BK, arow0, fb);
+            tma_load_2d(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb);
+          } else {
+            tma_load_2d(a_dst, mA, kb * BK, arow0, fb);
+            tma_load_2d(b_dst, &tmB, kb * BK, t.pbase, fb);
+          }
+        }
+        __syncwarp();
+        if (MODE == 0) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int gi = lane + 32 * j;
+            if (gi < ngroups)
+              tma_gather4(b_dst + gi * 512, &tmB, kb * BK, rows[4 * j], rows[4 * j + 1], rows[4 * j + 2],
+                          rows[4 * j + 3], fb);
+          }
+        }
+        last_par[stage] = (int)phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && lane == 0) {  // drain copies still in flight before the CTA exits
+      for (int s = 0; s < STAGES; ++s)
+        if (last_par[s] >= 0)
+          for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(smem_u32(full + s), (uint32_t)last_par[s]); ++i) {
+          }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+        const TileInfo t = decode_tile(d, g);
+        if (t.nvalid <= 0) continue;
+        if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag, d.error_word)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
+        const uint32_t idesc = bf16_idesc(BM, t.N);
+        for (int kb = 0; kb < d.kb; ++kb) {
+          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, d.error_word)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + stage * STAGE_BYTES, b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), idesc, (kb | k) != 0);
+          umma_commit(smem_u32(empty + stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(tfull + acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued above has completed once `done` flips
+      umma_commit(smem_u32(done));
+      for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(smem_u32(done), 0u); ++i) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 64;       // 0..127
+    const int q4 = warp & 3;               // TMEM lane quarter this warp may access
+    const int m = 32 * q4 + lane;          // accumulator row (TMEM lane)
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const TileInfo t = decode_tile(d, g);
+      if (t.nvalid <= 0) continue;
+      if (!mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, d.error_word)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * BN_MAX);
+      for (int c0 = 0; c0 < t.N; c0 += EPI_COLS) {
+        float v[EPI_COLS];
+        tmem_ld16(tbase + c0, v);
+        if (MODE == 0) {
+#pragma unroll
+          for (int c = 0; c < EPI_COLS; ++c) stg[m * STG_PITCH + c] = v[c];
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          const int i = et & 63, cb = (et >> 6) * (EPI_COLS / 2);
+#pragma unroll
+          for (int c = 0; c < EPI_COLS / 2; ++c) {
+            const int n = c0 + cb + c;
+            if (n < t.nvalid) {
+              const float gv = stg[i * STG_PITCH + cb + c], uv = stg[(64 + i) * STG_PITCH + cb + c];
+              const float hv = gv / (1.0f + expf(-gv)) * uv;
+              d.h[(size_t)(t.pbase + n) * d.I + t.m * 64 + i] = f2bf(hv);
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        } else {
+#pragma unroll
+          for (int c = 0; c < EPI_COLS; ++c) {
+            const int n = c0 + c;
+            if (n < t.nvalid) {
+              const int p = t.pbase + n;
+              d.rows[(size_t)p * d.H + t.m * BM + m] = f2bf(__ldg(d.pair_gate + p) * v[c]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(tempty + acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------ host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// 2-D BF16 tensor [outer][inner] with row pitch row_bytes, 128-byte swizzled boxes.
+cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                     uint32_t box_inner, uint32_t box_outer) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + BM * STG_PITCH * 4 + 16 * 8 + 16; }
+
+}  // namespace
+
+struct GemmMaps {
+  CUtensorMap a_gu, a_gu_sh;    // weight rows of width H (gate, up): pool / shared experts
+  CUtensorMap a_dn, a_dn_sh;    // weight rows of width I (down)
+  CUtensorMap h_map;            // h [P][I]
+  int H, I;
+  bool attr_set = false;
+};
+
+cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
+                             int I, const uint16_t* h_buf, int max_pairs) {
+  GemmMaps* m = new GemmMaps();
+  m->H = H;
+  m->I = I;
+  // a slot is gate [I][H] | up [I][H] | down [H][I]: 3I rows of width H, or 3H rows of width I
+  cudaError_t e = make_map(&m->a_gu, pool, H, (uint64_t)S * 3 * I, (uint64_t)H * 2, BK, 64);
+  if (e == cudaSuccess) e = make_map(&m->a_dn, pool, I, (uint64_t)S * 3 * H, (uint64_t)I * 2, BK, BM);
+  const void* sh = shared_w ? (const void*)shared_w : (const void*)pool;
+  const uint64_t sh_rows = shared_w ? (uint64_t)L : (uint64_t)S;
+  if (e == cudaSuccess) e = make_map(&m->a_gu_sh, sh, H, sh_rows * 3 * I, (uint64_t)H * 2, BK, 64);
+  if (e == cudaSuccess) e = make_map(&m->a_dn_sh, sh, I, sh_rows * 3 * H, (uint64_t)I * 2, BK, BM);
+  if (e == cudaSuccess) e = make_map(&m->h_map, h_buf, I, (uint64_t)max_pairs, (uint64_t)I * 2, BK, BN_MAX);
+  if (e == cudaSuccess) {
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)gemm_smem_bytes());
+  }
+  if (e != cudaSuccess) {
+    delete m;
+    return e;
+  }
+  *out = m;
+  return cudaSuccess;
+}
+
+void gemm_maps_destroy(GemmMaps* m) { delete m; }
+
+cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, int T, const GemmDesc& d, int grid,
+                                cudaStream_t s) {
+  if (mode == 0) {
+    CUtensorMap xm;  // token rows of x, one row per gather4 row
+    cudaError_t e = make_map(&xm, x, m->H, (uint64_t)T, (uint64_t)m->H * 2, BK, 1);
+    if (e != cudaSuccess) return e;
+    grouped_gemm_kernel<0><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_gu, m->a_gu_sh, xm, d);
+  } else {
+    grouped_gemm_kernel<1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_dn, m->a_dn_sh, m->h_map, d);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ft

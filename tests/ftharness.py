@@ -136,3 +136,30 @@ class Run:
             (c.hits, c.misses, c.fills, c.cpu_execs, c.evictions)
         assert s.error_word == 0
         return s
+
+
+def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None):
+    """One prefill layer on both sides; compares residency state, and outputs of
+    `check_tokens` (all when None) against the float64 oracle."""
+    F, w = r.F, r.w
+    xb = synth.prefill_x(w, chunk, layer, T)
+    z = synth.prefill_logits(w, chunk, layer, T)
+    r.sim.prefill_layer(layer, w.n_experts, w.n_layers)
+    x_d = torch.from_numpy(xb.view(np.int16)).to(r.dev)
+    z_d = torch.from_numpy(z).to(r.dev)
+    out_d = torch.empty((T, w.hidden), dtype=torch.float32, device=r.dev)
+    F.ft_moe_prefill_chunk(r.h, layer, T, x_d, z_d, out_d)
+    st = F.ft_moe_get_state(r.h, w.n_logical, r.sim.S)
+    assert st["clock"] == r.sim.clock
+    assert np.array_equal(st["res"], r.sim.res), f"prefill layer {layer}: residency table"
+    assert np.array_equal(st["owner"], r.sim.owner), f"prefill layer {layer}: slot owners"
+    assert np.array_equal(st["stamp"].astype(np.int64), r.sim.stamp), f"prefill layer {layer}: stamps"
+    out = out_d.cpu().numpy()
+    tokens = range(T) if check_tokens is None else check_tokens
+    sel, gates = O.route(z, w.top_k)
+    ref = O.prefill_outputs(layer, sel, gates, xb, r.expert, w.n_experts, tokens=list(tokens),
+                            shared=r.shared_expert(layer))
+    err = O.rel_err_rows(out[list(tokens)], ref)
+    r.max_err = max(r.max_err, err)
+    assert err <= OUT_TOL, f"prefill layer {layer}: relative error {err:.3e}"
+    return out

@@ -1,0 +1,81 @@
+"""GPU parity of the prefill path: full-layer double buffering from the shared slot pool
+(residency compared with the oracle after every layer), routing of the chunk, the
+tcgen05 grouped GEMMs and the fixed-order combine (outputs vs the float64 oracle)."""
+import numpy as np
+import pytest
+
+import synth
+from ftharness import Run, prefill_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__ as g
+
+    g.build()
+
+
+def test_prefill_small_every_token_and_decode_after():
+    """4 layers, 16 experts, top-2, 200 tokens (ragged tiles), 40 slots; then decode."""
+    w = synth.prefill().with_(n_layers=4, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=40,
+                              prefill_tokens=200)
+    with Run(w, max_prefill_tokens=256) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 200)
+        # decode afterwards uses what prefill left resident
+        dw = w.with_(logits="normal")
+        r.w = dw
+        for s in range(4):
+            for l in range(w.n_layers):
+                r.step(s, l, check_out=True)
+        r.compare_state()
+        print("max rel err", r.max_err)
+
+
+def test_prefill_chunk_break_restores_streamed_buffer():
+    """A decode step while layer 3 streams into the buffer that still holds layer 1."""
+    w = synth.prefill().with_(n_layers=6, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=48,
+                              prefill_tokens=64)
+    with Run(w, max_prefill_tokens=64) as r:
+        for l in range(3):
+            prefill_step(r, 0, l, 64)
+        dw = w.with_(logits="normal")
+        r.w = dw
+        for l in range(w.n_layers):
+            r.step(0, l, check_out=True)        # layer 1's experts must still be intact
+        r.w = w
+        for l in range(2, 6):                   # new chunk starting mid-model
+            prefill_step(r, 1, l, 64)
+        r.compare_state()
+
+
+def test_prefill_35b_expert_shape_sampled_tokens():
+    """H 2048, I 512, 256 experts top-8, 1024 tokens, 3 layers: sampled token rows."""
+    w = synth.prefill().with_(n_layers=3, cache_slots=700, prefill_tokens=1024)
+    rng = np.random.default_rng(0)
+    with Run(w, max_prefill_tokens=1024) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 1024, check_tokens=sorted(rng.choice(1024, 24, replace=False)))
+        print("max rel err", r.max_err)
+
+
+def test_prefill_with_shared_expert():
+    w = synth.decode_bf16().with_(n_layers=3, n_experts=32, cache_slots=70, logits="uniform", prefill_tokens=300)
+    with Run(w, max_prefill_tokens=300) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 300, check_tokens=list(range(0, 300, 7)))
+
+
+def test_prefill_rejects_small_pool():
+    w = synth.prefill().with_(n_layers=2, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=31)
+    with Run(w, max_prefill_tokens=64) as r:
+        import torch
+
+        x = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
+        z = torch.zeros((8, 16), dtype=torch.float32, device="cuda")
+        o = torch.empty((8, 256), dtype=torch.float32, device="cuda")
+        with pytest.raises(r.F.FtError) as e:
+            r.F.ft_moe_prefill_chunk(r.h, 0, 8, x, z, o)
+        assert e.value.status == r.F.FT_ERR_CAPACITY
