@@ -399,6 +399,21 @@ def run_ours(args, d: Dist) -> dict | None:
            "steps": n_e2e, "api": "ft_moe_decode_layers_host (pinned host buffers, cached graph)"}
     F.ft_graph_destroy(g)
     F.ft_moe_destroy(h)
+    del x_all, z_all, cp_all
+    cpu_baseline = None
+    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
+        n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, args.cpu_tokens, args.cpu_budget)
+        cpu_baseline = {"value": round(n / sec, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
+                        "kind": "oracle",
+                        "sample": f"{n} tokens x {L} layers of the same trace (float64 numpy oracle, "
+                                  f"cache simulation included), {sec:.1f} s on {os.cpu_count()} host cores"}
+    prefill = None
+    if not args.no_prefill:
+        banks = shared = pool = None
+        import gc
+
+        gc.collect()
+        prefill = run_prefill(args, d, dev, stream)
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5), "higher_is_better": True,
@@ -407,17 +422,98 @@ def run_ours(args, d: Dist) -> dict | None:
            "hbm_gbs_expert_weights": {"gate_up": roofline["achieved"],
                                       "down_combine": round(ach_dn, 1) if ach_dn else None,
                                       "both": round(ach_both, 1) if ach_both else None},
-           "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * L * 4, "clocks": clk,
+           "roofline": roofline, "prefill": prefill, "e2e": e2e, "gpu_launches": args.steps * L * 4, "clocks": clk,
            "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1), "bp_after_timed_gbps": round(bp_after, 1),
            "fill_observed_gbs": round(fill_gbs, 1) if fill_gbs else None,
            "setup_s": round(setup_s, 1)}
-    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
-        n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, args.cpu_tokens, args.cpu_budget)
-        out["cpu_baseline"] = {"value": round(n / sec, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
-                               "kind": "oracle",
-                               "sample": f"{n} tokens x {L} layers of the same trace (float64 numpy oracle, "
-                                         f"cache simulation included), {sec:.1f} s on {os.cpu_count()} host cores"}
+    if cpu_baseline is not None:
+        out["cpu_baseline"] = cpu_baseline
     return out
+
+
+# ---------------------------------------------------------------- prefill
+def run_prefill(args, d: Dist, dev, stream) -> dict:
+    """Prefill chunks of the 35B-A3B shape: T = 8192 tokens x 40 layers, 256 experts top-8,
+    uniform router logits, full-layer double buffering from the pinned host pool."""
+    import gc
+
+    import torch
+
+    import synth
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
+    w = synth.prefill()
+    if args.prefill_layers or args.prefill_tokens:   # profiling captures only: smaller chunk
+        nl = args.prefill_layers or w.n_layers
+        w = w.with_(n_layers=nl, prefill_tokens=args.prefill_tokens or w.prefill_tokens,
+                    cache_slots=max(2 * w.n_experts, synth.capacity_slots(0.37, nl, w.n_experts)))
+    L, T, H, E, I, k = w.n_layers, w.prefill_tokens, w.hidden, w.n_experts, w.inter, w.top_k
+    pool = synth.ExpertPool(w)
+    banks = pool.routed_banks()
+    cfg = F.make_config(L, H, I, E, k, False, F.FT_W_BF16, 1, w.cache_slots, w.bp_gbps, w.bh_gbps,
+                        max_prefill_tokens=T, device=d.local, compute_stream=stream.cuda_stream)
+    h = F.ft_moe_init(cfg, banks)
+    # activations: two distinct layers' x, reused alternately (routing, which sets the work,
+    # uses every layer's own logits)
+    x = torch.from_numpy(np.stack([synth.prefill_x(w, 0, l, T) for l in range(2)]).view(np.int16)).to(dev)
+    z = torch.stack([torch.from_numpy(synth.prefill_logits(w, 0, l, T)) for l in range(L)]).to(dev)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+    def chunk():
+        for l in range(L):
+            F.ft_moe_prefill_chunk(h, l, T, x[l % 2], z[l], out)
+
+    with torch.cuda.stream(stream):
+        chunk()                                       # warm-up chunk
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.prefill_chunks):
+            chunk()
+        e1.record(stream)
+        e1.synchronize()
+        F.ft_moe_synchronize(h)
+        chunk_s = e0.elapsed_time(e1) * 1e-3 / args.prefill_chunks
+        F.ft_moe_set_profiling(h, 1)
+        F.ft_moe_get_profile(h, reset=True)
+        chunk()
+        prof = F.ft_moe_get_profile(h, reset=True)
+        F.ft_moe_set_profiling(h, 0)
+    st = F.ft_moe_get_stats(h)
+    F.ft_moe_destroy(h)
+    del banks, pool
+    gc.collect()
+    flop_layer = T * k * 6.0 * I * H                  # gate+up (4IH) and down (2IH) per routed pair
+    gu_ms, dn_ms = prof["prefill_gemm_gate_up"][1], prof["prefill_gemm_down"][1]
+    gemm_ms = gu_ms + dn_ms
+    copy_n, copy_ms = prof["prefill_copy"]
+    stream_bytes = L * E * 6.0 * I * H                # whole pool streamed per chunk
+    try:
+        pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        tc_peak, tc_src = float(pk["bf16_tflops_sustained"]), "measured bf16_tflops_sustained"
+    except (OSError, ValueError, KeyError):
+        tc_peak, tc_src = 1700.0, "fallback sustained"
+    gemm_tflops = L * flop_layer / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    bp = F.ft_bench_bw(256 << 20, 8)
+    hbm, _ = _peaks()
+    bound_s = {"tensor": L * flop_layer / (tc_peak * 1e12), "hbm_weights": stream_bytes / (hbm * 1e9),
+               "host_link": stream_bytes / (bp * 1e9)}
+    return {"workload": "prefill_chunk_35B-A3B-shape: T 8192 x 40 layers, H 2048, I 512, E 256 top-8, "
+                        "uniform logits, 3788 slots, full-layer double buffer",
+            "value": round(T / chunk_s, 1), "unit": "tok/s", "chunk_s": round(chunk_s, 4),
+            "chunks": args.prefill_chunks,
+            "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None, "peak": tc_peak,
+                             "frac": round(gemm_tflops / tc_peak, 4) if gemm_tflops else None,
+                             "peak_source": tc_src, "bound": "tensor",
+                             "flop_per_layer": flop_layer, "avg_us_per_layer": round(1e3 * gemm_ms / L, 2),
+                             "gate_up_tflops": round(L * T * k * 4.0 * I * H / (gu_ms * 1e-3) / 1e12, 1) if gu_ms else None,
+                             "down_tflops": round(L * T * k * 2.0 * I * H / (dn_ms * 1e-3) / 1e12, 1) if dn_ms else None},
+            "layer_copy_gbs": round(stream_bytes / (copy_ms * 1e-3) / 1e9, 1) if copy_ms else None,
+            "bp_gbps": round(bp, 1),
+            "chunk_bound_s": {kk: round(v, 4) for kk, v in bound_s.items()},
+            "frac_of_chunk_bound": round(max(bound_s.values()) / chunk_s, 4),
+            "kernels_ms_per_chunk": {kk: round(v[1], 3) for kk, v in prof.items() if v[0] and kk.startswith("prefill")},
+            "error_word": st.error_word}
 
 
 # -------------------------------------------------------------- reference
@@ -457,6 +553,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-chunks", type=int, default=2)
+    ap.add_argument("--prefill-only", action="store_true", help="profiling: run only the prefill measurement")
+    ap.add_argument("--prefill-layers", type=int, default=0, help="profiling only: fewer layers")
+    ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling only: fewer tokens")
     ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer MoE layers")
     ap.add_argument("--slots", type=int, default=0, help="profiling only: other cache size")
     args = ap.parse_args()
@@ -467,6 +568,16 @@ def main():
     if args.impl == "reference":
         d.init("gloo")
         out = run_reference(args, d)
+    elif args.prefill_only:
+        import torch
+
+        from serving_router_top_dedupe_gb300 import build as B
+
+        B.build()
+        torch.cuda.set_device(d.local)
+        dev = torch.device("cuda", d.local)
+        out = {"metric": METRIC, "prefill": run_prefill(args, d, dev, torch.cuda.Stream(device=dev)),
+               "note": "prefill-only profiling run"}
     else:
         d.init("nccl")
         out = run_ours(args, d)

@@ -144,10 +144,11 @@ typedef struct {
 
 /* Per-kernel CUDA-event timing collected while profiling is on. */
 typedef struct {
-  uint64_t launches[8];  /* 0 control, 1 fill, 2 gemv phase 1 (gate/up), 3 gemv phase 2 (down)
+  uint64_t launches[9];  /* 0 control, 1 fill, 2 gemv phase 1 (gate/up), 3 gemv phase 2 (down)
                             + combine, 4 prefill routing (route, scan, place), 5 prefill grouped
-                            GEMMs (both projections), 6 prefill combine, 7 prefill layer copy */
-  double total_ms[8];
+                            GEMM gate/up + SwiGLU, 6 prefill combine, 7 prefill layer copy,
+                            8 prefill grouped GEMM down + gate weighting */
+  double total_ms[9];
 } ft_profile;
 
 /* Create the library state: allocates the slot pool (S * slot bytes) and the work

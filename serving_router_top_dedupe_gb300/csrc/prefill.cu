@@ -490,12 +490,14 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   e = timed(5, [&]() -> cudaError_t {
     d.mt = p->I / 64;
     d.kb = p->H / 64;
-    cudaError_t r = launch_grouped_gemm(0, p->maps, x, T, d, p->n_sm, c.cs);
-    if (r != cudaSuccess) return r;
-    d.mt = p->H / 128;
-    d.kb = p->I / 64;
-    return launch_grouped_gemm(1, p->maps, x, T, d, p->n_sm, c.cs);
+    return launch_grouped_gemm(0, p->maps, x, T, d, p->n_sm, c.cs);
   });
+  if (e == cudaSuccess)
+    e = timed(8, [&]() -> cudaError_t {
+      d.mt = p->H / 128;
+      d.kb = p->I / 64;
+      return launch_grouped_gemm(1, p->maps, x, T, d, p->n_sm, c.cs);
+    });
   if (e != cudaSuccess) {
     if (err) *err = "grouped GEMM launch";
     return e;

@@ -23,8 +23,8 @@ FT_FILL_KERNEL, FT_FILL_MEMCPY = 0, 1
 FT_CPU = -1
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_STATE, FT_DEVERR_TIMEOUT, FT_DEVERR_CAPACITY = 1, 2, 4, 8
 
-PROFILE_KINDS = ("control", "fill", "gate_up", "down_combine", "prefill_route", "prefill_gemm",
-                 "prefill_combine", "prefill_copy")
+PROFILE_KINDS = ("control", "fill", "gate_up", "down_combine", "prefill_route", "prefill_gemm_gate_up",
+                 "prefill_combine", "prefill_copy", "prefill_gemm_down")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
@@ -67,7 +67,7 @@ class ft_step_trace(C.Structure):
 
 
 class ft_profile(C.Structure):
-    _fields_ = [("launches", C.c_uint64 * 8), ("total_ms", C.c_double * 8)]
+    _fields_ = [("launches", C.c_uint64 * 9), ("total_ms", C.c_double * 9)]
 
 
 _P = C.c_void_p
