@@ -252,9 +252,11 @@ ft_status alloc_work(ft_moe* h) {
   A(w.copy_slot, (size_t)kc);
   A(w.counts, (size_t)ft::C_NCOUNTS);
   A(w.g_w, nent);
+  A(w.g_fill, nent);
   A(w.g_off, nent + 1);
   A(w.g_pair, ngp);
   A(w.h, ngp * h->I);
+  A(w.ab, nent * 2 * h->I);
   A(w.rows, npair * h->H);
   A(w.shared_rows, (size_t)B * h->H);
   A(w.blk_count, (size_t)h->H / ft::kRowsPerItem2);
@@ -288,16 +290,18 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   cp.pool = h->pool;
   cp.slot_stride = h->lay.stride;
   cp.shared_w = h->cfg.has_shared ? h->shared_w + (size_t)layer * h->lay.stride : nullptr;
+  // In kernel-fill mode the whole layer is one chain of programmatic dependents on the
+  // compute stream; the memcpy mode hands the fill to the transfer stream and back.
+  const bool chain = h->cfg.fill_mode == FT_FILL_KERNEL;
+  cp.pdl = chain;
   cudaEvent_t pa;
   ft_status s;
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
   FT_CUDA(ft::launch_control(cp, cs));
   if ((s = prof_end(h, 0, cs, pa)) != FT_OK) return s;
 
-  // fill on the transfer stream (fork / join with events)
-  FT_CUDA(cudaEventRecord(h->ev_fork, cs));
-  FT_CUDA(cudaStreamWaitEvent(ts, h->ev_fork, 0));
-  if (h->cfg.fill_mode == FT_FILL_KERNEL) {
+  if (chain) {
+    // fill kernel right after the control kernel on the compute stream
     ft::FillParams fp{};
     fp.counts = h->w.counts;
     fp.copy_u = h->w.copy_u;
@@ -305,15 +309,19 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
     fp.pool = h->pool;
     fp.lay = h->lay;
     fp.n_banks = h->n_banks;
+    fp.pdl = true;
     for (int j = 0; j < h->n_banks; ++j) {
       fp.src[j] = h->bank[j].dev;
       fp.src_row[j] = h->bank[j].row;
     }
-    if ((s = prof_begin(h, ts, &pa)) != FT_OK) return s;
-    FT_CUDA(ft::launch_fill(fp, h->grid_fill, ts));
-    if ((s = prof_end(h, 1, ts, pa)) != FT_OK) return s;
+    if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
+    FT_CUDA(ft::launch_fill(fp, h->grid_fill, cs));
+    if ((s = prof_end(h, 1, cs, pa)) != FT_OK) return s;
   } else {
-    // host-driven cudaMemcpyAsync fills: read the copy list, then one copy per bank
+    // host-driven cudaMemcpyAsync fills on the transfer stream: read the copy list, then
+    // one copy per bank per filled expert
+    FT_CUDA(cudaEventRecord(h->ev_fork, cs));
+    FT_CUDA(cudaStreamWaitEvent(ts, h->ev_fork, 0));
     FT_CUDA(cudaMemcpyAsync(h->counts_host, h->w.counts, sizeof(int32_t) * ft::C_NCOUNTS,
                             cudaMemcpyDeviceToHost, ts));
     FT_CUDA(cudaMemcpyAsync(h->copy_host, h->w.copy_u, sizeof(int32_t) * h->kcap, cudaMemcpyDeviceToHost, ts));
@@ -331,19 +339,21 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
                                 cudaMemcpyHostToDevice, ts));
     }
     if ((s = prof_end(h, 1, ts, pa)) != FT_OK) return s;
+    FT_CUDA(cudaEventRecord(h->ev_join, ts));
+    FT_CUDA(cudaStreamWaitEvent(cs, h->ev_join, 0));
   }
-  FT_CUDA(cudaEventRecord(h->ev_join, ts));
-  FT_CUDA(cudaStreamWaitEvent(cs, h->ev_join, 0));
 
   ft::EvalParams ep{};
   ep.counts = h->w.counts;
   ep.g_w = h->w.g_w;
+  ep.g_fill = h->w.g_fill;
   ep.g_off = h->w.g_off;
   ep.g_pair = h->w.g_pair;
   ep.gates = h->w.gates;
   ep.slot_of_pair = h->w.slot_of_pair;
   ep.x = static_cast<const uint16_t*>(x);
   ep.h = h->w.h;
+  ep.ab = h->w.ab;
   ep.rows = rows_out ? rows_out : h->w.rows;
   ep.shared_rows = h->w.shared_rows;
   ep.c_partial = cpart;
@@ -356,6 +366,9 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   ep.k = h->K;
   ep.B = batch;
   ep.has_shared = h->cfg.has_shared;
+  ep.n_sm = h->n_sm;
+  ep.max_entries = h->kcap + 1;
+  ep.pdl = chain;
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
   FT_CUDA(ft::launch_gate_up(ep, h->cfg.wtype, h->grid_eval, cs));
   if ((s = prof_end(h, 2, cs, pa)) != FT_OK) return s;
@@ -520,6 +533,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   FT_CUDA(cudaHostAlloc((void**)&h->counts_host, sizeof(int32_t) * ft::C_NCOUNTS, cudaHostAllocDefault));
   FT_CUDA(cudaHostAlloc((void**)&h->copy_host, sizeof(int32_t) * 2 * h->kcap, cudaHostAllocDefault));
   FT_CUDA(ft::prepare_kernels(h->cfg.wtype, h->H, h->I));
+  FT_CUDA(ft::prepare_control());
   FT_CUDA(cudaDeviceSynchronize());
   return FT_OK;
 }

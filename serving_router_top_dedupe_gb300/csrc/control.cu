@@ -47,8 +47,13 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   __shared__ int s_miss[kMaxE];
   __shared__ int s_gidx[kMaxE];
   __shared__ int s_victims[kMaxE];
-  __shared__ unsigned long long s_vkeys[kMaxE];
-  __shared__ uint32_t s_hist[kBins];
+  __shared__ int s_res[kMaxE];                         // res[] of this layer's experts
+  __shared__ uint32_t s_hitbits[kRegJ * kCtrlThreads / 32];  // hit slots (register-stamp path)
+  __shared__ uint32_t s_wsum[32];
+  __shared__ uint8_t s_fflag[kMaxE];                   // expert of this layer filled in this step
+  extern __shared__ unsigned long long s_dyn[];
+  unsigned long long* s_vkeys = s_dyn;                 // [kMaxE]
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(s_dyn + kMaxE);  // [kBins]
   __shared__ int s_gcount[kMaxE + 1];
   __shared__ uint32_t s_err;
   __shared__ uint32_t s_clock;
@@ -61,8 +66,26 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   const int E = p.E, k = p.k, B = p.B, S = p.S;
   const int base_u = p.layer * E;
 
+  // State loads first, so their latency overlaps the routing: this layer's residency
+  // slice to shared memory, slot stamps to registers (S <= 16K slots).
+  const bool in_reg = S <= kRegJ * kCtrlThreads;
+  uint32_t rs[kRegJ];
+#pragma unroll
+  for (int j = 0; j < kRegJ; ++j) {
+    const int s = tid + j * kCtrlThreads;
+    rs[j] = (in_reg && s < S) ? p.stamp[s] : UINT_MAX;
+  }
+  for (int i = tid; i < E; i += blockDim.x) s_res[i] = p.res[base_u + i];
   for (int i = tid; i < kMaxE / 32; i += blockDim.x) s_bitmap[i] = 0;
-  for (int i = tid; i < E; i += blockDim.x) s_gidx[i] = -1;
+  for (int i = tid; i < kRegJ * kCtrlThreads / 32; i += blockDim.x) s_hitbits[i] = 0;
+  for (int i = tid; i < E; i += blockDim.x) {
+    s_gidx[i] = -1;
+    s_fflag[i] = 0;
+  }
+  // Everything above reads state the previous control kernel wrote (it has completed);
+  // logits and the work lists belong to the kernel right before this one: wait for it.
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     s_err = 0;
     s_clock = p.st->clock + 1u;
@@ -108,7 +131,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     for (int c = 0; c < nact; c += 32) {
       int i = c + lane;
       int u = i < nact ? s_active[i] : -1;
-      int slot = u >= 0 ? p.res[u] : -1;
+      int slot = u >= 0 ? s_res[u - base_u] : -1;
       if (slot >= S) {  // cannot happen with a consistent table
         atomicOr(&s_err, FT_DEVERR_BAD_STATE);
         slot = -1;
@@ -120,6 +143,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
       if (hit) {
         s_hit[nh + __popc(hb & lt)] = u;
         p.stamp[slot] = clock;  // hit refreshes recency
+        if (in_reg) atomicOr(&s_hitbits[slot >> 5], 1u << (slot & 31));
       } else if (valid) {
         s_miss[nm + __popc(mb & lt)] = u;
       }
@@ -140,20 +164,14 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
 
   // ---- 3. one-pass K-LRU victim scan over slots not hit in this step
   if (q > 0) {
-    // Stamps stay in registers for S <= 16K slots (read from global once).
-    uint32_t rs[kRegJ];
-    const bool in_reg = S <= kRegJ * kCtrlThreads;
-#pragma unroll
-    for (int j = 0; j < kRegJ; ++j) {
-      const int s = tid + j * kCtrlThreads;
-      rs[j] = (in_reg && s < S) ? p.stamp[s] : UINT_MAX;
-    }
+    // register stamps were read before this step's hits refreshed them: hits are excluded
+    // through s_hitbits instead
 #define FOR_CANDIDATES(...)                                          \
   if (in_reg) {                                                      \
     _Pragma("unroll") for (int j = 0; j < kRegJ; ++j) {              \
       const int s = tid + j * kCtrlThreads;                          \
       const uint32_t st = rs[j];                                     \
-      if (s < S && st < clock) { __VA_ARGS__ }                       \
+      if (s < S && st < clock && !((s_hitbits[s >> 5] >> (s & 31)) & 1u)) { __VA_ARGS__ } \
     }                                                                \
   } else {                                                           \
     for (int s = tid; s < S; s += kCtrlThreads) {                    \
@@ -200,30 +218,33 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
         FOR_CANDIDATES(const unsigned long long key = KEY_OF(s, st);
                        if ((key >> (shift + kDigit)) == pre) atomicAdd(&s_hist[(key >> shift) & (kBins - 1)], 1u);)
         __syncthreads();
-        if (warp == 0) {
-          constexpr int per = kBins / 32;
-          uint32_t sum = 0;
-          for (int b = 0; b < per; ++b) sum += s_hist[lane * per + ((b + lane) & (per - 1))];  // bank-skewed
-          uint32_t incl = sum;
+        {
+          // block-wide exclusive scan: thread t owns bins 2t and 2t+1
+          const uint32_t h0 = s_hist[2 * tid], h1 = s_hist[2 * tid + 1], v = h0 + h1;
+          uint32_t incl = v;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
           }
-          const uint32_t kk = (uint32_t)s_kk;
-          const uint32_t excl = incl - sum;
-          if (excl < kk && incl >= kk) {  // exactly one lane
-            uint32_t run = excl;
-            int d = per - 1;
-            for (int b = 0; b < per; ++b) {
-              const uint32_t hb = s_hist[lane * per + b];
-              if (run + hb >= kk) {
-                d = b;
-                break;
-              }
-              run += hb;
+          if (lane == 31) s_wsum[warp] = incl;
+          __syncthreads();
+          if (warp == 0) {
+            uint32_t ws = s_wsum[lane], wi = ws;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+              if (lane >= o) wi += y;
             }
-            s_prefix = (pre << kDigit) | (unsigned long long)(lane * per + d);
+            s_wsum[lane] = wi - ws;  // exclusive prefix of warp totals
+          }
+          __syncthreads();
+          const uint32_t kk = (uint32_t)s_kk;
+          const uint32_t excl = s_wsum[warp] + incl - v;
+          if (excl < kk && excl + v >= kk) {  // exactly one thread
+            const bool first = excl + h0 >= kk;
+            const uint32_t run = first ? excl : excl + h0;
+            s_prefix = (pre << kDigit) | (unsigned long long)(2 * tid + (first ? 0 : 1));
             s_kk = (int)(kk - run);
           }
         }
@@ -261,6 +282,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
       }
       p.owner[v] = u;
       p.res[u] = v;
+      s_res[u - base_u] = v;
+      s_fflag[u - base_u] = 1;
       p.stamp[v] = clock;
       p.w.copy_u[i] = u;
       p.w.copy_slot[i] = v;
@@ -275,13 +298,14 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     for (int c = 0; c < nact; c += 32) {
       int i = c + lane;
       int u = i < nact ? s_active[i] : -1;
-      int slot = u >= 0 ? p.res[u] : -1;
+      int slot = u >= 0 ? s_res[u - base_u] : -1;
       bool in = slot >= 0;
       uint32_t b = __ballot_sync(0xffffffffu, in);
       if (in) {
         int g = ng + __popc(b & ((1u << lane) - 1u));
         s_gidx[u - base_u] = g;
         p.w.g_w[g] = p.pool + (size_t)slot * p.slot_stride;
+        p.w.g_fill[g] = s_fflag[u - base_u];
       }
       ng += __popc(b);
     }
@@ -296,7 +320,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   for (int pi = tid; pi < npairs; pi += blockDim.x) {
     int e = s_sel[pi];
     int g = s_gidx[e];
-    p.w.slot_of_pair[pi] = g >= 0 ? p.res[base_u + e] : FT_CPU;
+    p.w.slot_of_pair[pi] = g >= 0 ? s_res[e] : FT_CPU;
     if (g >= 0) atomicAdd(&s_gcount[g], 1);
   }
   __syncthreads();
@@ -321,6 +345,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
       int ne = ng;
       if (p.has_shared) {
         p.w.g_w[ng] = p.shared_w;
+        p.w.g_fill[ng] = 0;
         p.w.g_off[ng + 1] = carry + B;
         ne = ng + 1;
       }
@@ -376,9 +401,14 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
 
 }  // namespace
 
+constexpr size_t kCtrlDynSmem = kMaxE * sizeof(unsigned long long) + kBins * sizeof(uint32_t);
+
 cudaError_t launch_control(const CtrlParams& p, cudaStream_t s) {
-  control_kernel<<<1, kCtrlThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(control_kernel, dim3(1), dim3(kCtrlThreads), kCtrlDynSmem, s, p.pdl, p);
+}
+
+cudaError_t prepare_control() {
+  return cudaFuncSetAttribute(control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtrlDynSmem);
 }
 
 }  // namespace ft

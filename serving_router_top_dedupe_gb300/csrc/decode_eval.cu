@@ -19,128 +19,15 @@
 // ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2, post-scaling).
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "ft_internal.cuh"
+#include "ft_dot.cuh"
 
 namespace ft {
 namespace {
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// Host-pool reads (mapped pinned memory over the host link): plain coherent loads with
-// evict-first L2 policy.  The read-only .nc path is far slower for host memory.
-__device__ __forceinline__ uint4 ld_host(const void* p) {
-  return __ldcs(reinterpret_cast<const uint4*>(p));
-}
-
-__device__ __forceinline__ float ld_cg_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
-// acc += w.lo*x.lo + w.hi*x.hi, BF16 operands, FP32 accumulation (exact products).
-__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
-  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
-      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(w), "r"(x));
-  return acc;
-}
-
-// acc += w.lo*x.lo + w.hi*x.hi, F16 operands, FP32 accumulation (exact products).
-__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float acc) {
-  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
-      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(w), "r"(x));
-  return acc;
-}
-
-// two E4M3 codes (low byte = element 0) -> f16x2 (element 0 in the low half)
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}" : "=r"(r) : "r"(two));
-  return r;
-}
-
-// 16 bytes of BF16 weights (8 elements) . 8 BF16 activations
-__device__ __forceinline__ float dot_bf16_bf16(uint4 w, uint4 x, float acc) {
-  acc = fma2_bf16(w.x, x.x, acc);
-  acc = fma2_bf16(w.y, x.y, acc);
-  acc = fma2_bf16(w.z, x.z, acc);
-  acc = fma2_bf16(w.w, x.w, acc);
-  return acc;
-}
-
-// 16 bytes of BF16 weights (8 elements) . 8 FP32 values
-__device__ __forceinline__ float dot_bf16_f32(uint4 w, const float* v, float acc) {
-  const float4 a = *reinterpret_cast<const float4*>(v);
-  const float4 b = *reinterpret_cast<const float4*>(v + 4);
-  acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
-  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
-  acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
-  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
-  acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
-  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
-  acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
-  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
-  return acc;
-}
-
-// one 32-bit word of E4M3 codes (4 elements) . 4 F16 values (as two f16x2 words)
-__device__ __forceinline__ float dot4_e4m3_f16(uint32_t w, uint32_t x01, uint32_t x23, float acc) {
-  acc = fma2_f16(e4m3x2_to_f16x2(w & 0xffffu), x01, acc);
-  acc = fma2_f16(e4m3x2_to_f16x2(w >> 16), x23, acc);
-  return acc;
-}
-
-// 16 bytes of E4M3 weights (16 elements) . 16 F16 values -> partial (not scaled)
-__device__ __forceinline__ float dot_e4m3_f16(uint4 w, uint4 xa, uint4 xb) {
-  float d = 0.f;
-  d = dot4_e4m3_f16(w.x, xa.x, xa.y, d);
-  d = dot4_e4m3_f16(w.y, xa.z, xa.w, d);
-  d = dot4_e4m3_f16(w.z, xb.x, xb.y, d);
-  d = dot4_e4m3_f16(w.w, xb.z, xb.w, d);
-  return d;
-}
-
-// 16 bytes of E4M3 weights . 16 FP32 values -> partial (not scaled)
-__device__ __forceinline__ float dot_e4m3_f32(uint4 w, const float* v) {
-  float d = 0.f;
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 xv = *reinterpret_cast<const float4*>(v + 4 * q);
-    uint32_t p01 = e4m3x2_to_f16x2(ws[q] & 0xffffu), p23 = e4m3x2_to_f16x2(ws[q] >> 16);
-    float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&p01));
-    float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&p23));
-    d = fmaf(f01.x, xv.x, d);
-    d = fmaf(f01.y, xv.y, d);
-    d = fmaf(f23.x, xv.z, d);
-    d = fmaf(f23.y, xv.w, d);
-  }
-  return d;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.0f + expf(-a)) * b; }
+using namespace dot;
 
 // ------------------------------------------------------------------------- fill
 // Work = q experts x n_banks contiguous segments.  CTA b copies a share of segment
@@ -167,6 +54,8 @@ __device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint
 }
 
 __global__ void __launch_bounds__(256) fill_kernel(FillParams p) {
+  pdl_wait();  // the copy list comes from the control kernel right before
+  pdl_trigger();
   const int q = p.counts[C_Q];
   if (q <= 0) return;
   const int nseg = q * p.n_banks;
@@ -200,6 +89,8 @@ __global__ void __launch_bounds__(256) fill_kernel(FillParams p) {
 template <int WT, int SEG, int TG>
 __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_wait();  // filled slots are written by the kernel right before
+  pdl_trigger();
   const int ne = p.counts[C_NENTRIES];
   const int I = p.I, H = p.H;
   const int rbs = I / 8;
@@ -299,6 +190,8 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
 template <int WT, int RPW, int TG>
 __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_last;
   const int ne = p.counts[C_NENTRIES];
   const int I = p.I, H = p.H, k = p.k, B = p.B;
@@ -407,14 +300,13 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
 
 template <int WT, int SEG, int TG>
 cudaError_t gate_up_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  gate_up_kernel<WT, SEG, TG><<<grid, kEvalThreads, (size_t)TG * p.H * 2, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(gate_up_kernel<WT, SEG, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.H * 2, s, p.pdl, p);
 }
 
 template <int WT, int TG>
 cudaError_t down_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  down_combine_kernel<WT, 4, TG><<<grid, kEvalThreads, (size_t)TG * p.I * 4, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(down_combine_kernel<WT, 4, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.I * 4, s, p.pdl,
+                  p);
 }
 
 template <typename F>
@@ -425,11 +317,12 @@ cudaError_t set_smem(F f, size_t bytes) {
 }  // namespace
 
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
-  fill_kernel<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(fill_kernel, dim3(grid), dim3(256), 0, s, p.pdl, p);
 }
 
 cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
+  if (p.B == 1 && stream_gemv_supported(wtype, p.H, p.I, p.max_entries, p.n_sm))
+    return launch_stream_gemv(0, p, wtype, p.n_sm, p.max_entries, s);
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) {
     return one ? gate_up_launch<FT_W_BF16, 8, 1>(p, grid, s) : gate_up_launch<FT_W_BF16, 8, 4>(p, grid, s);
@@ -440,6 +333,7 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
 
 cudaError_t prepare_kernels(int wtype, int H, int I) {
   cudaError_t e = cudaSuccess;
+  if ((e = prepare_stream_gemv()) != cudaSuccess) return e;
   const size_t gu1 = (size_t)H * 2, gu4 = 4 * gu1, dn1 = (size_t)I * 4, dn4 = 4 * dn1;
   if (wtype == FT_W_BF16) {
     if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 1>, gu1)) != cudaSuccess) return e;
@@ -456,6 +350,8 @@ cudaError_t prepare_kernels(int wtype, int H, int I) {
 }
 
 cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
+  if (p.B == 1 && stream_gemv_supported(wtype, p.H, p.I, p.max_entries, p.n_sm))
+    return launch_stream_gemv(1, p, wtype, p.n_sm, p.max_entries, s);
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) return one ? down_launch<FT_W_BF16, 1>(p, grid, s) : down_launch<FT_W_BF16, 4>(p, grid, s);
   return one ? down_launch<FT_W_FP8_E4M3_B128, 1>(p, grid, s) : down_launch<FT_W_FP8_E4M3_B128, 4>(p, grid, s);

@@ -1,0 +1,133 @@
+// Dot-product building blocks of the decode GEMV kernels.  Every (token, expert) dot is
+// formed the same way in every kernel that uses these: 16-byte chunks strided over the
+// lanes, accumulated in FP32 in chunk order, FP8 blocks scaled after their partial dot,
+// then an xor butterfly across the warp.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace ft {
+namespace dot {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Host-pool reads (mapped pinned memory over the host link): plain coherent loads with
+// evict-first L2 policy.  The read-only .nc path is far slower for host memory.
+__device__ __forceinline__ uint4 ld_host(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// acc += w.lo*x.lo + w.hi*x.hi, BF16 operands, FP32 accumulation (exact products).
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// acc += w.lo*x.lo + w.hi*x.hi, F16 operands, FP32 accumulation (exact products).
+__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
+// two E4M3 codes (low byte = element 0) -> f16x2 (element 0 in the low half)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 s;\n\tcvt.u16.u32 s, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, s;\n\t}" : "=r"(r) : "r"(two));
+  return r;
+}
+
+// 16 bytes of BF16 weights (8 elements) . 8 BF16 activations
+__device__ __forceinline__ float dot_bf16_bf16(uint4 w, uint4 x, float acc) {
+  acc = fma2_bf16(w.x, x.x, acc);
+  acc = fma2_bf16(w.y, x.y, acc);
+  acc = fma2_bf16(w.z, x.z, acc);
+  acc = fma2_bf16(w.w, x.w, acc);
+  return acc;
+}
+
+// 16 bytes of BF16 weights (8 elements) . 8 FP32 values
+__device__ __forceinline__ float dot_bf16_f32(uint4 w, const float* v, float acc) {
+  const float4 a = *reinterpret_cast<const float4*>(v);
+  const float4 b = *reinterpret_cast<const float4*>(v + 4);
+  acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
+  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
+  acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
+  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
+  acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
+  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
+  acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
+  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+  return acc;
+}
+
+// one 32-bit word of E4M3 codes (4 elements) . 4 F16 values (as two f16x2 words)
+__device__ __forceinline__ float dot4_e4m3_f16(uint32_t w, uint32_t x01, uint32_t x23, float acc) {
+  acc = fma2_f16(e4m3x2_to_f16x2(w & 0xffffu), x01, acc);
+  acc = fma2_f16(e4m3x2_to_f16x2(w >> 16), x23, acc);
+  return acc;
+}
+
+// 16 bytes of E4M3 weights (16 elements) . 16 F16 values -> partial (not scaled)
+__device__ __forceinline__ float dot_e4m3_f16(uint4 w, uint4 xa, uint4 xb) {
+  float d = 0.f;
+  d = dot4_e4m3_f16(w.x, xa.x, xa.y, d);
+  d = dot4_e4m3_f16(w.y, xa.z, xa.w, d);
+  d = dot4_e4m3_f16(w.z, xb.x, xb.y, d);
+  d = dot4_e4m3_f16(w.w, xb.z, xb.w, d);
+  return d;
+}
+
+// 16 bytes of E4M3 weights . 16 FP32 values -> partial (not scaled)
+__device__ __forceinline__ float dot_e4m3_f32(uint4 w, const float* v) {
+  float d = 0.f;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 xv = *reinterpret_cast<const float4*>(v + 4 * q);
+    uint32_t p01 = e4m3x2_to_f16x2(ws[q] & 0xffffu), p23 = e4m3x2_to_f16x2(ws[q] >> 16);
+    float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&p01));
+    float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&p23));
+    d = fmaf(f01.x, xv.x, d);
+    d = fmaf(f01.y, xv.y, d);
+    d = fmaf(f23.x, xv.z, d);
+    d = fmaf(f23.y, xv.w, d);
+  }
+  return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.0f + expf(-a)) * b; }
+
+}  // namespace dot
+}  // namespace ft

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "ft_moe.h"
 
@@ -50,9 +51,11 @@ struct DecodeWork {
   // Evaluation entries: 0..n_g-1 are G = H u F in ascending logical id; entry
   // n_g is the shared expert when the model has one.
   const uint8_t** g_w;     // [Kmax+1] base address of the entry's weights
+  int32_t* g_fill;         // [Kmax+1] 1 if the entry's slot is being filled in this step
   int32_t* g_off;          // [Kmax+2] prefix offsets into g_pair
   int32_t* g_pair;         // [maxB*k + maxB] routed: pair id t*k+r; shared: token t
   float* h;                // [(maxB*k + maxB) * I] intermediate, indexed like g_pair
+  float* ab;               // [(Kmax+1) * 2I] batch-1 path: raw gate (a) and up (b) dots per entry
   float* rows;             // [maxB*k*H] GPU pair rows when the caller gives no rows_out
   float* shared_rows;      // [maxB*H]
   uint32_t* blk_count;     // [H / kRowsPerItem2] combine arrival counters (self-resetting)
@@ -80,6 +83,7 @@ struct CtrlParams {
   const uint8_t* pool;
   size_t slot_stride;
   const uint8_t* shared_w;  // shared expert of this layer, or nullptr
+  bool pdl;                 // launched as a programmatic dependent
 };
 
 struct FillParams {
@@ -91,17 +95,20 @@ struct FillParams {
   const uint8_t* src[6];    // device-visible addresses of the host banks
   size_t src_row[6];        // bytes per logical id in each bank
   int n_banks;
+  bool pdl;
 };
 
 struct EvalParams {
   const int32_t* counts;
   const uint8_t* const* g_w;
+  const int32_t* g_fill;
   const int32_t* g_off;
   const int32_t* g_pair;
   const float* gates;
   const int32_t* slot_of_pair;
   const uint16_t* x;        // [B][H] bf16
   float* h;
+  float* ab;                // [entries][2I] (batch-1 path)
   float* rows;              // [B*k][H]
   float* shared_rows;       // [B][H]
   const float* c_partial;   // [B*k][H] or nullptr
@@ -110,14 +117,48 @@ struct EvalParams {
   uint32_t* error_word;
   SlotLayout lay;
   int H, I, k, B, has_shared;
+  int n_sm;                 // SMs of the device (one streaming CTA each)
+  int max_entries;          // capacity of the entry lists (kcap + 1)
+  bool pdl;                 // launched as programmatic dependents
 };
+
+// Programmatic dependent launch.  Kernels of the decode chain (control -> fill -> gate/up
+// -> down+combine -> next control) are launched with programmatic stream serialization.
+// Each kernel triggers its dependents only after its own wait, so when kernel n+1 starts,
+// kernel n-1 has completed: a prologue may read what kernels two or more back wrote, and
+// must wait before reading what the previous kernel wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` with the programmatic-serialization attribute when `pdl` is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel launchers (stream-ordered, no synchronisation).
 cudaError_t launch_control(const CtrlParams& p, cudaStream_t s);
+// Raise the control kernel's shared-memory limit (call once per device, before capture).
+cudaError_t prepare_control();
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s);
 cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s);
 // Set the dynamic shared-memory limits of every evaluation kernel (call once, before capture).
 cudaError_t prepare_kernels(int wtype, int H, int I);
+// Batch-1 decode GEMV streamed through shared memory (stream_gemv.cu).
+bool stream_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm);
+cudaError_t launch_stream_gemv(int phase, const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s);
+cudaError_t prepare_stream_gemv();
 
 }  // namespace ft

@@ -90,6 +90,7 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
       if (cudaGetSymbolAddress(&p, ft_noalloc_scratch) != cudaSuccess || !p) return FT_ERR_CUDA;
       if (cudaDeviceGetAttribute(&su->n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FT_ERR_CUDA;
       su->scratch = static_cast<unsigned char*>(p);
+      if (ft::prepare_control() != cudaSuccess) return FT_ERR_CUDA;
       su->done = true;
     }
     const int wi = wtype == FT_W_BF16 ? 0 : 1;
@@ -120,9 +121,11 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   w.copy_slot = cv.take<int32_t>(kcap);
   w.counts = cv.take<int32_t>(ft::C_NCOUNTS);
   w.g_w = cv.take<const uint8_t*>((size_t)kcap + 1);
+  w.g_fill = cv.take<int32_t>((size_t)kcap + 1);
   w.g_off = cv.take<int32_t>((size_t)kcap + 2);
   w.g_pair = cv.take<int32_t>(ngp);
   w.h = cv.take<float>(ngp * I);
+  w.ab = cv.take<float>(((size_t)kcap + 1) * 2 * I);
   w.rows = cv.take<float>(npair * H);
   w.shared_rows = cv.take<float>((size_t)B * H);
   w.blk_count = cv.take<uint32_t>((size_t)H / ft::kRowsPerItem2);
@@ -153,17 +156,20 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   cp.pool = static_cast<const uint8_t*>(experts_dev);
   cp.slot_stride = lay.stride;
   cp.shared_w = static_cast<const uint8_t*>(shared_dev);
+  cp.pdl = true;
   if (ft::launch_control(cp, s) != cudaSuccess) return FT_ERR_CUDA;
 
   ft::EvalParams ep{};
   ep.counts = w.counts;
   ep.g_w = w.g_w;
+  ep.g_fill = w.g_fill;
   ep.g_off = w.g_off;
   ep.g_pair = w.g_pair;
   ep.gates = w.gates;
   ep.slot_of_pair = w.slot_of_pair;
   ep.x = static_cast<const uint16_t*>(x_bf16);
   ep.h = w.h;
+  ep.ab = w.ab;
   ep.rows = rows_out ? rows_out : w.rows;
   ep.shared_rows = w.shared_rows;
   ep.c_partial = nullptr;
@@ -176,6 +182,9 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   ep.k = k;
   ep.B = B;
   ep.has_shared = has_shared;
+  ep.n_sm = su->n_sm;
+  ep.max_entries = kcap + 1;
+  ep.pdl = true;
   if (ft::launch_gate_up(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
   if (ft::launch_down_combine(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
   return FT_OK;
