@@ -256,7 +256,7 @@ ft_status alloc_work(ft_moe* h) {
   A(w.g_off, nent + 1);
   A(w.g_pair, ngp);
   A(w.h, ngp * h->I);
-  A(w.ab, nent * 2 * h->I);
+  A(w.ready, nent);
   A(w.rows, npair * h->H);
   A(w.shared_rows, (size_t)B * h->H);
   A(w.blk_count, (size_t)h->H / ft::kRowsPerItem2);
@@ -353,7 +353,7 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   ep.slot_of_pair = h->w.slot_of_pair;
   ep.x = static_cast<const uint16_t*>(x);
   ep.h = h->w.h;
-  ep.ab = h->w.ab;
+  ep.ready = h->w.ready;
   ep.rows = rows_out ? rows_out : h->w.rows;
   ep.shared_rows = h->w.shared_rows;
   ep.c_partial = cpart;
@@ -372,9 +372,11 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
   FT_CUDA(ft::launch_gate_up(ep, h->cfg.wtype, h->grid_eval, cs));
   if ((s = prof_end(h, 2, cs, pa)) != FT_OK) return s;
-  if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
-  FT_CUDA(ft::launch_down_combine(ep, h->cfg.wtype, h->grid_eval, cs));
-  if ((s = prof_end(h, 3, cs, pa)) != FT_OK) return s;
+  if (!ft::eval_fused(ep, h->cfg.wtype)) {
+    if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
+    FT_CUDA(ft::launch_down_combine(ep, h->cfg.wtype, h->grid_eval, cs));
+    if ((s = prof_end(h, 3, cs, pa)) != FT_OK) return s;
+  }
   return FT_OK;
 }
 

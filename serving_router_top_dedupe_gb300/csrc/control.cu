@@ -9,6 +9,12 @@
 //   slots or FT_CPU -> fixed-shape evaluation lists with device-resident counts.
 // Split rule: "FreeToken 完全拆解", section "q* 策略"; residual bandwidth
 // max(B_H-B_P, 0): "개인 장치에서 MoE 모델을 서빙하는 FreeToken", paragraph on the miss split.
+//
+// The kernel is latency-bound and its code is fetched cold on every launch (the weight
+// streams of the evaluation kernels pass through L2 in between), so it is kept compact:
+// one router width per instantiation, plain loops, slot stamps staged once in shared
+// memory, and a radix select that stops as soon as the selected bin holds exactly the
+// keys still wanted.
 #include <cfloat>
 #include <climits>
 
@@ -18,6 +24,13 @@
 namespace ft {
 namespace {
 
+constexpr int kThreads = kCtrlThreads;
+constexpr int kWarps = kThreads / 32;
+constexpr int kDigit = 9;  // radix-select digit: one histogram bin per thread
+constexpr int kBins = 1 << kDigit;
+static_assert(kBins == kThreads, "one histogram bin per thread");
+constexpr int kSmemSlots = 16384;  // slot stamps staged in shared memory up to this many slots
+constexpr size_t kDynSmemMax = kMaxE * sizeof(unsigned long long) + kSmemSlots * sizeof(uint32_t);
 
 // Fill count: q = clamp(floor(m*bp/bh + 1/2), 1, m) for m > 0; all misses when the
 // residual bandwidth B_H - B_P is not positive; never more than `evictable`.
@@ -35,11 +48,35 @@ __device__ __forceinline__ int split_q(int m, long long bp, long long bh, int ev
   return q < 0 ? 0 : (int)q;
 }
 
-constexpr int kRegJ = 16;      // stamps per thread held in registers (S <= 16K)
-constexpr int kDigit = 11;     // radix-select digit
-constexpr int kBins = 1 << kDigit;
+// Exclusive prefix sum of one value per thread over the block; *total gets the sum.
+__device__ __noinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t ws = lane < kWarps ? s_wsum[lane] : 0u;
+    uint32_t wi = ws;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kWarps) s_wsum[lane] = wi - ws;
+    if (lane == kWarps - 1) s_wsum[kWarps] = wi;
+  }
+  __syncthreads();
+  *total = s_wsum[kWarps];
+  const uint32_t r = s_wsum[warp] + incl - v;
+  __syncthreads();  // s_wsum may be reused right after
+  return r;
+}
 
-__global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) {
+template <int NPL>
+__global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ uint32_t s_bitmap[kMaxE / 32];
   __shared__ int s_sel[kMaxPairs];
   __shared__ int s_active[kMaxE];
@@ -47,45 +84,37 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   __shared__ int s_miss[kMaxE];
   __shared__ int s_gidx[kMaxE];
   __shared__ int s_victims[kMaxE];
-  __shared__ int s_res[kMaxE];                         // res[] of this layer's experts
-  __shared__ uint32_t s_hitbits[kRegJ * kCtrlThreads / 32];  // hit slots (register-stamp path)
-  __shared__ uint32_t s_wsum[32];
-  __shared__ uint8_t s_fflag[kMaxE];                   // expert of this layer filled in this step
-  extern __shared__ unsigned long long s_dyn[];
-  unsigned long long* s_vkeys = s_dyn;                 // [kMaxE]
-  uint32_t* s_hist = reinterpret_cast<uint32_t*>(s_dyn + kMaxE);  // [kBins]
-  __shared__ int s_gcount[kMaxE + 1];
-  __shared__ uint32_t s_err;
-  __shared__ uint32_t s_clock;
-  __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand;
+  __shared__ int s_res[kMaxE];                 // res[] of this layer's experts
+  __shared__ unsigned long long s_tok[kMaxE];  // tokens routed to each expert of this layer
+  __shared__ int s_goff[kMaxE + 1];
+  __shared__ uint8_t s_fflag[kMaxE];           // expert of this layer filled in this step
+  __shared__ uint32_t s_hist[kBins];
+  __shared__ uint32_t s_wsum[kWarps + 1];
+  __shared__ uint32_t s_err, s_clock, s_lo, s_hi;
+  __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand, s_kk, s_done;
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_kk;
-  __shared__ uint32_t s_lo, s_hi;
+  extern __shared__ unsigned long long s_dyn[];
+  unsigned long long* s_vkeys = s_dyn;                              // [kMaxE]
+  uint32_t* s_stamp = reinterpret_cast<uint32_t*>(s_dyn + kMaxE);  // [min(S, kSmemSlots)]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E, k = p.k, B = p.B, S = p.S;
   const int base_u = p.layer * E;
+  const bool in_smem = S <= kSmemSlots;
+  uint32_t* stv = in_smem ? s_stamp : p.stamp;  // stamps as the victim scan sees them
 
-  // State loads first, so their latency overlaps the routing: this layer's residency
-  // slice to shared memory, slot stamps to registers (S <= 16K slots).
-  const bool in_reg = S <= kRegJ * kCtrlThreads;
-  uint32_t rs[kRegJ];
-#pragma unroll
-  for (int j = 0; j < kRegJ; ++j) {
-    const int s = tid + j * kCtrlThreads;
-    rs[j] = (in_reg && s < S) ? p.stamp[s] : UINT_MAX;
-  }
-  for (int i = tid; i < E; i += blockDim.x) s_res[i] = p.res[base_u + i];
-  for (int i = tid; i < kMaxE / 32; i += blockDim.x) s_bitmap[i] = 0;
-  for (int i = tid; i < kRegJ * kCtrlThreads / 32; i += blockDim.x) s_hitbits[i] = 0;
-  for (int i = tid; i < E; i += blockDim.x) {
+  // State written by the previous control kernel (complete when this one starts, since
+  // every kernel of the chain triggers its dependents only after its own wait): this
+  // layer's residency slice and the slot stamps, staged while the previous kernel ends.
+  for (int i = tid; i < E; i += kThreads) {
+    s_res[i] = p.res[base_u + i];
     s_gidx[i] = -1;
     s_fflag[i] = 0;
+    s_tok[i] = 0ull;
   }
-  // Everything above reads state the previous control kernel wrote (it has completed);
-  // logits and the work lists belong to the kernel right before this one: wait for it.
-  pdl_wait();
-  pdl_trigger();
+  if (in_smem)
+    for (int s = tid; s < S; s += kThreads) s_stamp[s] = p.stamp[s];
+  for (int i = tid; i < kMaxE / 32; i += kThreads) s_bitmap[i] = 0;
   if (tid == 0) {
     s_err = 0;
     s_clock = p.st->clock + 1u;
@@ -94,56 +123,68 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     s_lo = UINT_MAX;
     s_hi = 0;
     s_ncand = 0;
+    s_done = 0;
   }
+  // logits and the work lists belong to the kernel right before this one
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const uint32_t clock = s_clock;
 
   // ---- 1. route: one warp per token
-  for (int t = warp; t < B; t += blockDim.x / 32) {
-    route_token_any(p.logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
+  for (int t = warp; t < B; t += kWarps) {
+    int e, rank;
+    float g;
+    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, lane, &s_err, e, g, rank);
+    if (rank >= 0) {
       const int idx = t * k + rank;
       p.w.sel[idx] = e;
       p.w.gates[idx] = g;
       s_sel[idx] = e;
       atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
-    });
+      atomicOr(&s_tok[e], 1ull << t);
+    }
   }
   __syncthreads();
 
-  // ---- 2. dedupe + classify (warp 0; A is at most min(B*k, E) ids)
+  // ---- 2. dedupe + classify (warp 0; A is at most min(B*k, E) ids, ascending)
   if (warp == 0) {
     const int nwords = (E + 31) / 32;
-    uint32_t word = lane < nwords ? s_bitmap[lane] : 0u;
-    int cnt = __popc(word), incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    int nact = 0, nh = 0, nm = 0;
+    for (int c = 0; c < nwords; c += 32) {
+      uint32_t word = c + lane < nwords ? s_bitmap[c + lane] : 0u;
+      const int cnt = __popc(word);
+      int incl = cnt;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int pos = nact + incl - cnt;
+      while (word) {
+        const int b = __ffs(word) - 1;
+        word &= word - 1;
+        s_active[pos++] = base_u + (c + lane) * 32 + b;
+      }
+      nact += __shfl_sync(0xffffffffu, incl, 31);
     }
-    int pos = incl - cnt;
-    while (word) {
-      int b = __ffs(word) - 1;
-      word &= word - 1;
-      s_active[pos++] = base_u + lane * 32 + b;
-    }
-    const int nact = __shfl_sync(0xffffffffu, incl, 31);
-    int nh = 0, nm = 0;
+    __syncwarp();
     for (int c = 0; c < nact; c += 32) {
-      int i = c + lane;
-      int u = i < nact ? s_active[i] : -1;
-      int slot = u >= 0 ? s_res[u - base_u] : -1;
+      const int i = c + lane;
+      const bool valid = i < nact;
+      const int u = valid ? s_active[i] : -1;
+      int slot = valid ? s_res[u - base_u] : -1;
       if (slot >= S) {  // cannot happen with a consistent table
         atomicOr(&s_err, FT_DEVERR_BAD_STATE);
         slot = -1;
       }
-      bool valid = i < nact, hit = valid && slot >= 0;
-      uint32_t hb = __ballot_sync(0xffffffffu, hit);
-      uint32_t mb = __ballot_sync(0xffffffffu, valid && !hit);
-      uint32_t lt = (1u << lane) - 1u;
+      const bool hit = valid && slot >= 0;
+      const uint32_t hb = __ballot_sync(0xffffffffu, hit);
+      const uint32_t mb = __ballot_sync(0xffffffffu, valid && !hit);
+      const uint32_t lt = (1u << lane) - 1u;
       if (hit) {
         s_hit[nh + __popc(hb & lt)] = u;
-        p.stamp[slot] = clock;  // hit refreshes recency
-        if (in_reg) atomicOr(&s_hitbits[slot >> 5], 1u << (slot & 31));
+        p.stamp[slot] = clock;  // a hit refreshes recency
+        stv[slot] = clock;
       } else if (valid) {
         s_miss[nm + __popc(mb & lt)] = u;
       }
@@ -161,28 +202,19 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
 
   const int q = s_q;
   const int kcap = p.kcap;
-
-  // ---- 3. one-pass K-LRU victim scan over slots not hit in this step
+  // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
   if (q > 0) {
-    // register stamps were read before this step's hits refreshed them: hits are excluded
-    // through s_hitbits instead
-#define FOR_CANDIDATES(...)                                          \
-  if (in_reg) {                                                      \
-    _Pragma("unroll") for (int j = 0; j < kRegJ; ++j) {              \
-      const int s = tid + j * kCtrlThreads;                          \
-      const uint32_t st = rs[j];                                     \
-      if (s < S && st < clock && !((s_hitbits[s >> 5] >> (s & 31)) & 1u)) { __VA_ARGS__ } \
-    }                                                                \
-  } else {                                                           \
-    for (int s = tid; s < S; s += kCtrlThreads) {                    \
-      const uint32_t st = p.stamp[s];                                \
-      if (st < clock) { __VA_ARGS__ }                                \
-    }                                                                \
-  }
-    // range of candidate stamps and their count
+    // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
     uint32_t lo = UINT_MAX, hi = 0;
     int nc = 0;
-    FOR_CANDIDATES(lo = min(lo, st); hi = max(hi, st); ++nc;)
+    for (int s = tid; s < S; s += kThreads) {
+      const uint32_t st = stv[s];
+      if (st < clock) {
+        lo = min(lo, st);
+        hi = max(hi, st);
+        ++nc;
+      }
+    }
     for (int o = 16; o > 0; o >>= 1) {
       lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
       hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
@@ -200,82 +232,70 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
     const uint32_t range = s_hi - st_lo;
     const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
-    // key = (stamp - lowest stamp, slot): unique, ordered like (stamp, slot)
-#define KEY_OF(s, st) ((((unsigned long long)((st) - st_lo)) << sbits) | (unsigned long long)(s))
+    // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
     unsigned long long thresh = ~0ull;
     if (want < ncand) {
       // radix select of the want-th smallest key, kDigit bits per pass, most significant first
-      const int passes = (width + kDigit - 1) / kDigit;
       if (tid == 0) {
         s_prefix = 0;
         s_kk = want;
       }
-      for (int ps = passes - 1; ps >= 0; --ps) {
+      for (int ps = (width + kDigit - 1) / kDigit - 1; ps >= 0; --ps) {
         const int shift = ps * kDigit;
-        for (int i = tid; i < kBins; i += kCtrlThreads) s_hist[i] = 0;
+        s_hist[tid] = 0;
         __syncthreads();
         const unsigned long long pre = s_prefix;
-        FOR_CANDIDATES(const unsigned long long key = KEY_OF(s, st);
-                       if ((key >> (shift + kDigit)) == pre) atomicAdd(&s_hist[(key >> shift) & (kBins - 1)], 1u);)
-        __syncthreads();
-        {
-          // block-wide exclusive scan: thread t owns bins 2t and 2t+1
-          const uint32_t h0 = s_hist[2 * tid], h1 = s_hist[2 * tid + 1], v = h0 + h1;
-          uint32_t incl = v;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          if (lane == 31) s_wsum[warp] = incl;
-          __syncthreads();
-          if (warp == 0) {
-            uint32_t ws = s_wsum[lane], wi = ws;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
-              if (lane >= o) wi += y;
-            }
-            s_wsum[lane] = wi - ws;  // exclusive prefix of warp totals
-          }
-          __syncthreads();
-          const uint32_t kk = (uint32_t)s_kk;
-          const uint32_t excl = s_wsum[warp] + incl - v;
-          if (excl < kk && excl + v >= kk) {  // exactly one thread
-            const bool first = excl + h0 >= kk;
-            const uint32_t run = first ? excl : excl + h0;
-            s_prefix = (pre << kDigit) | (unsigned long long)(2 * tid + (first ? 0 : 1));
-            s_kk = (int)(kk - run);
-          }
+        for (int s = tid; s < S; s += kThreads) {
+          const uint32_t st = stv[s];
+          if (st >= clock) continue;
+          const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+          if ((key >> (shift + kDigit)) == pre) atomicAdd(&s_hist[(key >> shift) & (kBins - 1)], 1u);
         }
         __syncthreads();
+        const uint32_t h = s_hist[tid];
+        const uint32_t kk = (uint32_t)s_kk;
+        uint32_t total;
+        const uint32_t excl = block_excl_scan(h, s_wsum, &total);
+        if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
+          s_prefix = (pre << kDigit) | (unsigned long long)tid;
+          s_kk = (int)(kk - excl);
+          s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
+        }
+        __syncthreads();
+        if (s_done) {
+          thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
+          break;
+        }
+        if (ps == 0) thresh = s_prefix;
       }
-      thresh = s_prefix;
     }
     // collect the `want` smallest keys (keys are unique), then order them
-    FOR_CANDIDATES(const unsigned long long key = KEY_OF(s, st); if (key <= thresh) {
-      const int i = atomicAdd(&s_nv, 1);
-      if (i < kMaxE) s_vkeys[i] = key;
-    })
-#undef FOR_CANDIDATES
-#undef KEY_OF
+    for (int s = tid; s < S; s += kThreads) {
+      const uint32_t st = stv[s];
+      if (st >= clock) continue;
+      const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+      if (key <= thresh) {
+        const int i = atomicAdd(&s_nv, 1);
+        if (i < kMaxE) s_vkeys[i] = key;
+      }
+    }
     __syncthreads();
     const int nv = min(s_nv, want);
     const unsigned long long smask = (1ull << sbits) - 1ull;
-    for (int i = tid; i < nv; i += kCtrlThreads) {
+    for (int i = tid; i < nv; i += kThreads) {
       const unsigned long long ki = s_vkeys[i];
       int rank = 0;
       for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
       s_victims[rank] = (int)(ki & smask);
     }
-    if (tid == 0) s_nv = nv;
     __syncthreads();
+    if (tid == 0) s_nv = nv;
 
     // ---- 4. install F = first q misses into the first q victims
-    for (int i = tid; i < q; i += blockDim.x) {
-      int v = s_victims[i];
-      int u = s_miss[i];
-      int old = p.owner[v];
+    for (int i = tid; i < q; i += kThreads) {
+      const int v = s_victims[i];
+      const int u = s_miss[i];
+      const int old = p.owner[v];
       if (old >= 0) {
         p.res[old] = -1;
         atomicAdd(&s_evict, 1);
@@ -291,57 +311,37 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
   }
   __syncthreads();
 
-  // ---- 5. G = resident part of A (ascending u): evaluation entries
+  // ---- 5. G = resident part of A (ascending u): evaluation entries and pair offsets
   if (warp == 0) {
     const int nact = s_nactive;
-    int ng = 0;
+    int ng = 0, carry = 0;
     for (int c = 0; c < nact; c += 32) {
-      int i = c + lane;
-      int u = i < nact ? s_active[i] : -1;
-      int slot = u >= 0 ? s_res[u - base_u] : -1;
-      bool in = slot >= 0;
-      uint32_t b = __ballot_sync(0xffffffffu, in);
-      if (in) {
-        int g = ng + __popc(b & ((1u << lane) - 1u));
-        s_gidx[u - base_u] = g;
-        p.w.g_w[g] = p.pool + (size_t)slot * p.slot_stride;
-        p.w.g_fill[g] = s_fflag[u - base_u];
-      }
-      ng += __popc(b);
-    }
-    if (lane == 0) s_ng = ng;
-  }
-  for (int i = tid; i <= kMaxE; i += blockDim.x) s_gcount[i] = 0;
-  __syncthreads();
-  const int ng = s_ng;
-
-  // rewrite pairs to slots / FT_CPU and count pairs per entry
-  const int npairs = B * k;
-  for (int pi = tid; pi < npairs; pi += blockDim.x) {
-    int e = s_sel[pi];
-    int g = s_gidx[e];
-    p.w.slot_of_pair[pi] = g >= 0 ? s_res[e] : FT_CPU;
-    if (g >= 0) atomicAdd(&s_gcount[g], 1);
-  }
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of per-entry pair counts -> g_off
-    int carry = 0;
-    for (int c = 0; c < ng; c += 32) {
-      int i = c + lane;
-      int v = i < ng ? s_gcount[i] : 0, incl = v;
+      const int i = c + lane;
+      const int e = i < nact ? s_active[i] - base_u : -1;
+      const int slot = e >= 0 ? s_res[e] : -1;
+      const bool in = slot >= 0;
+      const int cnt = in ? __popcll(s_tok[e]) : 0;
+      int incl = cnt;
       for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
       }
-      if (i < ng) {
-        p.w.g_off[i] = carry + incl - v;
-        s_gcount[i] = carry + incl - v;  // becomes the offset
+      const uint32_t b = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const int g = ng + __popc(b & ((1u << lane) - 1u));
+        s_gidx[e] = g;
+        s_goff[g] = carry + incl - cnt;
+        p.w.g_w[g] = p.pool + (size_t)slot * p.slot_stride;
+        p.w.g_fill[g] = s_fflag[e];
+        p.w.g_off[g] = carry + incl - cnt;
       }
+      ng += __popc(b);
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) {
+      s_ng = ng;
+      s_goff[ng] = carry;
       p.w.g_off[ng] = carry;
-      s_gcount[ng] = carry;
       int ne = ng;
       if (p.has_shared) {
         p.w.g_w[ng] = p.shared_w;
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
         ne = ng + 1;
       }
       int* cnt = p.w.counts;
-      cnt[C_NACTIVE] = s_nactive;
+      cnt[C_NACTIVE] = nact;
       cnt[C_NHIT] = s_nhit;
       cnt[C_NMISS] = s_nmiss;
       cnt[C_Q] = q;
@@ -365,25 +365,31 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     }
   }
   __syncthreads();
-  // place pairs: within an entry, ascending pair id
-  for (int pi = tid; pi < npairs; pi += blockDim.x) {
-    int e = s_sel[pi];
-    int g = s_gidx[e];
-    if (g < 0) continue;
-    int pos = 0;
-    for (int j = 0; j < pi; ++j) pos += (s_sel[j] == e);
-    p.w.g_pair[s_gcount[g] + pos] = pi;
+
+  // rewrite pairs to slots / FT_CPU and place them: within an entry, ascending pair id
+  // (= ascending token, since a token routes to an expert at most once)
+  const int npairs = B * k;
+  for (int pi = tid; pi < npairs; pi += kThreads) {
+    const int e = s_sel[pi];
+    const int g = s_gidx[e];
+    p.w.slot_of_pair[pi] = g >= 0 ? s_res[e] : FT_CPU;
+    if (g >= 0) {
+      const int t = pi / k;
+      const int pos = __popcll(s_tok[e] & ((1ull << t) - 1ull));
+      p.w.g_pair[s_goff[g] + pos] = pi;
+    }
   }
   if (p.has_shared) {
-    const int base = s_gcount[ng];
-    for (int t = tid; t < B; t += blockDim.x) p.w.g_pair[base + t] = t;
+    const int base = s_goff[s_ng];
+    for (int t = tid; t < B; t += kThreads) p.w.g_pair[base + t] = t;
   }
+  for (int i = tid; i <= kcap; i += kThreads) p.w.ready[i] = 0u;
   // lists for traces
-  for (int i = tid; i < s_nactive; i += blockDim.x) p.w.active[i] = s_active[i];
-  for (int i = tid; i < s_nhit; i += blockDim.x) p.w.hit[i] = s_hit[i];
-  for (int i = tid; i < s_nmiss; i += blockDim.x) p.w.miss[i] = s_miss[i];
+  for (int i = tid; i < s_nactive; i += kThreads) p.w.active[i] = s_active[i];
+  for (int i = tid; i < s_nhit; i += kThreads) p.w.hit[i] = s_hit[i];
+  for (int i = tid; i < s_nmiss; i += kThreads) p.w.miss[i] = s_miss[i];
   if (q > 0)
-    for (int i = tid; i < s_nv; i += blockDim.x) p.w.victims[i] = s_victims[i];
+    for (int i = tid; i < s_nv; i += kThreads) p.w.victims[i] = s_victims[i];
   if (tid == 0) {
     DevState* st = p.st;
     st->clock = clock;
@@ -394,21 +400,43 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) control_kernel(CtrlParams p) 
     st->evictions += (unsigned long long)s_evict;
     st->decode_steps += 1ull;
     st->eval_entries += (unsigned long long)(s_ng + (p.has_shared ? 1 : 0));
-    st->eval_pairs += (unsigned long long)(s_gcount[s_ng] + (p.has_shared ? B : 0));
+    st->eval_pairs += (unsigned long long)(s_goff[s_ng] + (p.has_shared ? B : 0));
     if (s_err) atomicOr(&st->error_word, s_err);
   }
 }
 
+template <int NPL>
+cudaError_t launch_npl(const CtrlParams& p, cudaStream_t s) {
+  const size_t smem = kMaxE * sizeof(unsigned long long) +
+                      (size_t)(p.S <= kSmemSlots ? p.S : 0) * sizeof(uint32_t);
+  return launch_k(control_kernel<NPL>, dim3(1), dim3(kThreads), smem, s, p.pdl, p);
+}
+
+template <int NPL>
+cudaError_t prepare_npl() {
+  return cudaFuncSetAttribute(control_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmemMax);
+}
+
 }  // namespace
 
-constexpr size_t kCtrlDynSmem = kMaxE * sizeof(unsigned long long) + kBins * sizeof(uint32_t);
-
+// One router width per instantiation: E <= 32 * NPL logits per lane.
 cudaError_t launch_control(const CtrlParams& p, cudaStream_t s) {
-  return launch_k(control_kernel, dim3(1), dim3(kCtrlThreads), kCtrlDynSmem, s, p.pdl, p);
+  if (p.E <= 32) return launch_npl<1>(p, s);
+  if (p.E <= 64) return launch_npl<2>(p, s);
+  if (p.E <= 128) return launch_npl<4>(p, s);
+  if (p.E <= 256) return launch_npl<8>(p, s);
+  if (p.E <= 512) return launch_npl<16>(p, s);
+  return launch_npl<32>(p, s);
 }
 
 cudaError_t prepare_control() {
-  return cudaFuncSetAttribute(control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtrlDynSmem);
+  cudaError_t e;
+  if ((e = prepare_npl<1>()) != cudaSuccess) return e;
+  if ((e = prepare_npl<2>()) != cudaSuccess) return e;
+  if ((e = prepare_npl<4>()) != cudaSuccess) return e;
+  if ((e = prepare_npl<8>()) != cudaSuccess) return e;
+  if ((e = prepare_npl<16>()) != cudaSuccess) return e;
+  return prepare_npl<32>();
 }
 
 }  // namespace ft

@@ -23,6 +23,7 @@
 
 #include "ft_internal.cuh"
 #include "ft_dot.cuh"
+#include "ft_ptx.cuh"
 
 namespace ft {
 namespace {
@@ -90,6 +91,7 @@ template <int WT, int SEG, int TG>
 __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_wait();  // filled slots are written by the kernel right before
+  const uint64_t pol = ptx::l2_evict_first();
   pdl_trigger();
   const int ne = p.counts[C_NENTRIES];
   const int I = p.I, H = p.H;
@@ -143,8 +145,8 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
         for (int s = 0; s < SEG; ++s) {
           const int c = c0 + s * 32 + lane;
           if (c < row_chunks) {
-            wa[s] = ld_stream(wg + (size_t)c * 16);
-            wb[s] = ld_stream(wu + (size_t)c * 16);
+            wa[s] = ld_stream(wg + (size_t)c * 16, pol);
+            wb[s] = ld_stream(wu + (size_t)c * 16, pol);
           }
         }
 #pragma unroll
@@ -191,6 +193,7 @@ template <int WT, int RPW, int TG>
 __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_wait();
+  const uint64_t pol = ptx::l2_evict_first();
   pdl_trigger();
   __shared__ int s_last;
   const int ne = p.counts[C_NENTRIES];
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
           for (int s = 0; s < SEG; ++s) {
             const int c = c0 + s * 32 + lane;
             if (c < row_chunks)
-              wv[r][s] = ld_stream(W + p.lay.down + ((size_t)(j0 + r) * I) * ESZ + (size_t)c * 16);
+              wv[r][s] = ld_stream(W + p.lay.down + ((size_t)(j0 + r) * I) * ESZ + (size_t)c * 16, pol);
           }
 #pragma unroll
         for (int s = 0; s < SEG; ++s) {
@@ -320,9 +323,12 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
   return launch_k(fill_kernel, dim3(grid), dim3(256), 0, s, p.pdl, p);
 }
 
+bool eval_fused(const EvalParams& p, int wtype) {
+  return p.B == 1 && fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
+}
+
 cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
-  if (p.B == 1 && stream_gemv_supported(wtype, p.H, p.I, p.max_entries, p.n_sm))
-    return launch_stream_gemv(0, p, wtype, p.n_sm, p.max_entries, s);
+  if (eval_fused(p, wtype)) return launch_fused_gemv(p, wtype, p.n_sm, batch1_entries(p), s);
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) {
     return one ? gate_up_launch<FT_W_BF16, 8, 1>(p, grid, s) : gate_up_launch<FT_W_BF16, 8, 4>(p, grid, s);
@@ -333,7 +339,7 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
 
 cudaError_t prepare_kernels(int wtype, int H, int I) {
   cudaError_t e = cudaSuccess;
-  if ((e = prepare_stream_gemv()) != cudaSuccess) return e;
+  if ((e = prepare_fused_gemv()) != cudaSuccess) return e;
   const size_t gu1 = (size_t)H * 2, gu4 = 4 * gu1, dn1 = (size_t)I * 4, dn4 = 4 * dn1;
   if (wtype == FT_W_BF16) {
     if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 1>, gu1)) != cudaSuccess) return e;
@@ -350,8 +356,7 @@ cudaError_t prepare_kernels(int wtype, int H, int I) {
 }
 
 cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
-  if (p.B == 1 && stream_gemv_supported(wtype, p.H, p.I, p.max_entries, p.n_sm))
-    return launch_stream_gemv(1, p, wtype, p.n_sm, p.max_entries, s);
+  if (eval_fused(p, wtype)) return cudaSuccess;  // the fused batch-1 kernel did the whole layer
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) return one ? down_launch<FT_W_BF16, 1>(p, grid, s) : down_launch<FT_W_BF16, 4>(p, grid, s);
   return one ? down_launch<FT_W_FP8_E4M3_B128, 1>(p, grid, s) : down_launch<FT_W_FP8_E4M3_B128, 4>(p, grid, s);

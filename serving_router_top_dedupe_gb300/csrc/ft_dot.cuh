@@ -19,6 +19,15 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// ld_stream with an L2 cache policy (see ft::ptx::l2_evict_first).
+__device__ __forceinline__ uint4 ld_stream(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 // Host-pool reads (mapped pinned memory over the host link): plain coherent loads with
 // evict-first L2 policy.  The read-only .nc path is far slower for host memory.
 __device__ __forceinline__ uint4 ld_host(const void* p) {

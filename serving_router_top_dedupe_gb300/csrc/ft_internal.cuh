@@ -14,7 +14,7 @@ constexpr int kMaxE = 1024;           // routed experts per layer
 constexpr int kMaxK = 16;             // top-k
 constexpr int kMaxBatch = 64;         // decode tokens per step
 constexpr int kMaxPairs = kMaxBatch * kMaxK;
-constexpr int kCtrlThreads = 1024;
+constexpr int kCtrlThreads = 512;     // decode control kernel (one CTA)
 constexpr int kEvalThreads = 256;     // GEMV CTAs: 8 warps
 constexpr int kRowsPerItem2 = 32;     // down-projection rows per work item (= combine block)
 constexpr uint32_t kSpinLimit = 1u << 22;
@@ -52,10 +52,10 @@ struct DecodeWork {
   // n_g is the shared expert when the model has one.
   const uint8_t** g_w;     // [Kmax+1] base address of the entry's weights
   int32_t* g_fill;         // [Kmax+1] 1 if the entry's slot is being filled in this step
+  uint32_t* ready;         // [Kmax+1] batch-1 fused kernel: h rows published per entry (zeroed by control)
   int32_t* g_off;          // [Kmax+2] prefix offsets into g_pair
   int32_t* g_pair;         // [maxB*k + maxB] routed: pair id t*k+r; shared: token t
   float* h;                // [(maxB*k + maxB) * I] intermediate, indexed like g_pair
-  float* ab;               // [(Kmax+1) * 2I] batch-1 path: raw gate (a) and up (b) dots per entry
   float* rows;             // [maxB*k*H] GPU pair rows when the caller gives no rows_out
   float* shared_rows;      // [maxB*H]
   uint32_t* blk_count;     // [H / kRowsPerItem2] combine arrival counters (self-resetting)
@@ -102,13 +102,13 @@ struct EvalParams {
   const int32_t* counts;
   const uint8_t* const* g_w;
   const int32_t* g_fill;
+  uint32_t* ready;          // [entries] h rows published per entry (batch-1 fused kernel)
   const int32_t* g_off;
   const int32_t* g_pair;
   const float* gates;
   const int32_t* slot_of_pair;
   const uint16_t* x;        // [B][H] bf16
   float* h;
-  float* ab;                // [entries][2I] (batch-1 path)
   float* rows;              // [B*k][H]
   float* shared_rows;       // [B][H]
   const float* c_partial;   // [B*k][H] or nullptr
@@ -156,9 +156,13 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
 cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaStream_t s);
 // Set the dynamic shared-memory limits of every evaluation kernel (call once, before capture).
 cudaError_t prepare_kernels(int wtype, int H, int I);
-// Batch-1 decode GEMV streamed through shared memory (stream_gemv.cu).
-bool stream_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm);
-cudaError_t launch_stream_gemv(int phase, const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s);
-cudaError_t prepare_stream_gemv();
+// Batch-1 decode evaluation in one persistent launch (decode_fused.cu).
+bool fused_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm);
+cudaError_t launch_fused_gemv(const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s);
+cudaError_t prepare_fused_gemv();
+// Entries of a batch-1 step: at most k routed experts plus the shared expert.
+inline int batch1_entries(const EvalParams& p) { return p.max_entries < p.k + 1 ? p.max_entries : p.k + 1; }
+// True when launch_gate_up runs the whole layer (launch_down_combine then launches nothing).
+bool eval_fused(const EvalParams& p, int wtype);
 
 }  // namespace ft

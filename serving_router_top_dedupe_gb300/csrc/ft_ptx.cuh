@@ -64,5 +64,54 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *counter >= target, for counters that other CTAs of the same grid
+// raise (every CTA of that grid is resident: one CTA per SM, grid <= SM count).  Gives up
+// after kFlagWaitNs (error word + abort flag) so that a lost signal cannot hang the GPU.
+constexpr uint64_t kFlagWaitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool wait_counter(const uint32_t* counter, uint32_t target, volatile int* abort_flag,
+                                             uint32_t* error_word) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (ld_acquire_gpu(counter) >= target) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kFlagWaitNs) break;
+    __nanosleep(64);
+  }
+  *abort_flag = 1;
+  atomicOr(error_word, FT_DEVERR_TIMEOUT);
+  return false;
+}
+
+// L2 policy for data read once per step (expert weights): evicted first, so that the
+// small per-step state, activations and kernel code stay resident in L2 across kernels.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 }  // namespace ptx
 }  // namespace ft

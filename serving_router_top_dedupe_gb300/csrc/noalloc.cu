@@ -125,7 +125,7 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   w.g_off = cv.take<int32_t>((size_t)kcap + 2);
   w.g_pair = cv.take<int32_t>(ngp);
   w.h = cv.take<float>(ngp * I);
-  w.ab = cv.take<float>(((size_t)kcap + 1) * 2 * I);
+  w.ready = cv.take<uint32_t>((size_t)kcap + 1);
   w.rows = cv.take<float>(npair * H);
   w.shared_rows = cv.take<float>((size_t)B * H);
   w.blk_count = cv.take<uint32_t>((size_t)H / ft::kRowsPerItem2);
@@ -169,7 +169,7 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   ep.slot_of_pair = w.slot_of_pair;
   ep.x = static_cast<const uint16_t*>(x_bf16);
   ep.h = w.h;
-  ep.ab = w.ab;
+  ep.ready = w.ready;
   ep.rows = rows_out ? rows_out : w.rows;
   ep.shared_rows = w.shared_rows;
   ep.c_partial = nullptr;
