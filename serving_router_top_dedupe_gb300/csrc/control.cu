@@ -133,17 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
 
   // ---- 1. route: one warp per token
   for (int t = warp; t < B; t += kWarps) {
-    int e, rank;
-    float g;
-    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, lane, &s_err, e, g, rank);
-    if (rank >= 0) {
+    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
       const int idx = t * k + rank;
       p.w.sel[idx] = e;
       p.w.gates[idx] = g;
       s_sel[idx] = e;
       atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
       atomicOr(&s_tok[e], 1ull << t);
-    }
+    });
   }
   __syncthreads();
 
@@ -235,13 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
     unsigned long long thresh = ~0ull;
     if (want < ncand) {
-      // radix select of the want-th smallest key, kDigit bits per pass, most significant first
+      // radix select of the want-th smallest key, most significant digit first.  Digits are
+      // taken from the top of the key's actual width, so the first pass spreads the keys
+      // over all kBins bins (few shared-memory atomics collide).
       if (tid == 0) {
         s_prefix = 0;
         s_kk = want;
       }
-      for (int ps = (width + kDigit - 1) / kDigit - 1; ps >= 0; --ps) {
-        const int shift = ps * kDigit;
+      for (int hi_bit = width; hi_bit > 0;) {
+        const int shift = hi_bit > kDigit ? hi_bit - kDigit : 0;
+        const int dbits = hi_bit - shift;
         s_hist[tid] = 0;
         __syncthreads();
         const unsigned long long pre = s_prefix;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
           const uint32_t st = stv[s];
           if (st >= clock) continue;
           const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
-          if ((key >> (shift + kDigit)) == pre) atomicAdd(&s_hist[(key >> shift) & (kBins - 1)], 1u);
+          if ((key >> hi_bit) == pre) atomicAdd(&s_hist[(key >> shift) & ((1u << dbits) - 1u)], 1u);
         }
         __syncthreads();
         const uint32_t h = s_hist[tid];
@@ -257,16 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
         uint32_t total;
         const uint32_t excl = block_excl_scan(h, s_wsum, &total);
         if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
-          s_prefix = (pre << kDigit) | (unsigned long long)tid;
+          s_prefix = (pre << dbits) | (unsigned long long)tid;
           s_kk = (int)(kk - excl);
           s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
         }
         __syncthreads();
-        if (s_done) {
+        if (s_done || shift == 0) {
           thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
           break;
         }
-        if (ps == 0) thresh = s_prefix;
+        hi_bit = shift;
       }
     }
     // collect the `want` smallest keys (keys are unique), then order them

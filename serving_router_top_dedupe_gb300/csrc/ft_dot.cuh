@@ -95,6 +95,19 @@ __device__ __forceinline__ float dot_bf16_f32(uint4 w, const float* v, float acc
   return acc;
 }
 
+// dot_bf16_f32 with the 8 FP32 values given as two float4 (same products, same order)
+__device__ __forceinline__ float dot_bf16_f32v(uint4 w, float4 a, float4 b, float acc) {
+  acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
+  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
+  acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
+  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
+  acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
+  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
+  acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
+  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+  return acc;
+}
+
 // one 32-bit word of E4M3 codes (4 elements) . 4 F16 values (as two f16x2 words)
 __device__ __forceinline__ float dot4_e4m3_f16(uint32_t w, uint32_t x01, uint32_t x23, float acc) {
   acc = fma2_f16(e4m3x2_to_f16x2(w & 0xffffu), x01, acc);
@@ -126,6 +139,23 @@ __device__ __forceinline__ float dot_e4m3_f32(uint4 w, const float* v) {
     d = fmaf(f01.y, xv.y, d);
     d = fmaf(f23.x, xv.z, d);
     d = fmaf(f23.y, xv.w, d);
+  }
+  return d;
+}
+
+// dot_e4m3_f32 with the 16 FP32 values given as four float4 (same products, same order)
+__device__ __forceinline__ float dot_e4m3_f32v(uint4 w, const float4 (&xv)[4]) {
+  float d = 0.f;
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t p01 = e4m3x2_to_f16x2(ws[q] & 0xffffu), p23 = e4m3x2_to_f16x2(ws[q] >> 16);
+    float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&p01));
+    float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&p23));
+    d = fmaf(f01.x, xv[q].x, d);
+    d = fmaf(f01.y, xv[q].y, d);
+    d = fmaf(f23.x, xv[q].z, d);
+    d = fmaf(f23.y, xv[q].w, d);
   }
   return d;
 }

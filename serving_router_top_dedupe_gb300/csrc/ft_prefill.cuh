@@ -33,6 +33,7 @@ struct GemmDesc {
   int kb;                    // K steps of 64: gate/up H/64, down I/64
   const int32_t* entry_off;  // [n_entries+1] first pair of each entry (pairs sorted by entry, token)
   const int32_t* tile_off;   // [n_entries+1] prefix of N tiles per entry
+  const int4* tiles;         // [N tiles] {entry, first pair, valid pairs, N (multiple of 16)}
   const int32_t* buf_slots;  // [E]
   const int32_t* pair_tok;   // [P] token of each pair
   const float* pair_gate;    // [P] gate of each pair (1 for the shared expert)
@@ -41,11 +42,11 @@ struct GemmDesc {
   uint32_t* error_word;
 };
 
-// Tensor maps and launch of the grouped GEMM.  mode 0: gate/up + SwiGLU from x (token
-// rows gathered); mode 1: down + gate weighting from h.
+// Tensor maps and launch of the grouped GEMM.  mode 0: gate/up + SwiGLU from the token
+// rows in pair order (xp); mode 1: down + gate weighting from h.
 struct GemmMaps;
 cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
-                             int I, const uint16_t* h_buf, int max_pairs);
+                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs);
 void gemm_maps_destroy(GemmMaps* m);
 cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, int T, const GemmDesc& d, int grid,
                                 cudaStream_t s);

@@ -3,6 +3,11 @@
 // precedes dedupe).  One warp routes one token: the k largest logits (equal logits:
 // lower expert id first) are chosen, listed in ascending expert id, and their gates
 // are a softmax over those k logits.  NaN logits rank as -inf and raise `err`.
+//
+// Lane l holds the logits of experts l, l+32, l+64, ... as order-preserving 32-bit
+// keys.  Each of the k rounds takes the warp-wide largest key with one redux.sync and
+// the lowest expert id holding it with a second one, so a round costs two warp
+// reductions instead of a shuffle butterfly over (value, id) pairs.
 #pragma once
 
 #include <climits>
@@ -11,87 +16,89 @@
 
 namespace ft {
 
-__device__ __forceinline__ bool route_better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
+// float -> uint32 with the same order; -0 is taken as +0 first, so equal logits give equal
+// keys (and then the lower expert id wins, as for any tie)
+__device__ __forceinline__ uint32_t route_key(float v) {
+  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// On return, lane r < k holds the token's rank-r choice: out_e (expert id, ascending in
-// r), out_g (gate), out_rank (= r); lanes >= k hold out_rank = -1.
-template <int NPL>  // logits held per lane: E <= 32*NPL
-__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int lane, uint32_t* err, int& out_e,
-                                                 float& out_g, int& out_rank) {
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Calls emit(e, gate, rank) once for each of the token's k choices, from the lane that
+// holds expert e; rank is e's position among the k choices in ascending expert id.
+template <int NPL, typename F>  // logits held per lane: E <= 32*NPL
+__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int lane, uint32_t* err, F&& emit) {
+  constexpr uint32_t kFull = 0xffffffffu;
   float v[NPL];
+  uint32_t key[NPL];
   uint32_t taken = 0;
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
     const int e = lane + 32 * j;
     float x = -INFINITY;
+    key[j] = 0u;  // not an expert: below every logit, never chosen (k <= E)
     if (e < E) {
       x = __ldg(z + e);
       if (x != x) {
         x = -INFINITY;
         atomicOr(err, FT_DEVERR_NAN_LOGIT);
       }
-    } else {
-      taken |= 1u << j;  // not an expert
+      key[j] = route_key(x);
     }
     v[j] = x;
   }
-  int my_e = INT_MAX;
-  float my_z = -INFINITY, zmax = -INFINITY;
+  uint32_t zmax_key = 0;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
+    // this lane's best untaken key; equal keys keep the lower j (= lower expert id)
+    uint32_t best = 0;
+    int bj = 0;
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
-      const int e = lane + 32 * j;
-      if (!(taken & (1u << j)) && route_better(v[j], e, bv, be)) {
-        bv = v[j];
-        be = e;
+      const bool free = !((taken >> j) & 1u);
+      if (free && key[j] > best) {
+        best = key[j];
+        bj = j;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (route_better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == r) {
-      my_e = be;
-      my_z = bv;
-    }
-    if (r == 0) zmax = bv;
+    const uint32_t kmax = __reduce_max_sync(kFull, best);
+    // lowest expert id holding kmax (a lane's best is its lowest untaken j with that key)
+    const uint32_t cand = (best == kmax && best != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const uint32_t emin = __reduce_min_sync(kFull, cand);
+    if ((int)(emin & 31u) == lane) taken |= 1u << (emin >> 5);
+    if (r == 0) zmax_key = kmax;
   }
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int oe = __shfl_sync(0xffffffffu, my_e, j);
-    if (lane < k && oe < my_e) ++rank;
-  }
-  const float ex = lane < k ? expf(my_z - zmax) : 0.f;
-  float sum = ex;
+  // ranks in ascending expert id: experts are ordered by (j, lane)
+  const float zmax = route_key_value(zmax_key);
+  uint32_t below = 0;  // chosen experts with a smaller j, then this j's lower lanes
+  float ex[NPL];
+  float sum = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  out_e = my_e;
-  out_g = ex / sum;
-  out_rank = lane < k ? rank : -1;
+  for (int j = 0; j < NPL; ++j) {
+    ex[j] = ((taken >> j) & 1u) ? expf(v[j] - zmax) : 0.f;
+    sum += ex[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const uint32_t b = __ballot_sync(kFull, (taken >> j) & 1u);
+    if ((taken >> j) & 1u) emit(lane + 32 * j, ex[j] / sum, (int)(below + __popc(b & ((1u << lane) - 1u))));
+    below += __popc(b);
+  }
 }
 
 // Dispatch on E (the number of logits each lane holds).
 template <typename F>
 __device__ __forceinline__ void route_token_any(const float* z, int E, int k, int lane, uint32_t* err, F&& emit) {
-  int e, rank;
-  float g;
-  if (E <= 32) route_token_warp<1>(z, E, k, lane, err, e, g, rank);
-  else if (E <= 64) route_token_warp<2>(z, E, k, lane, err, e, g, rank);
-  else if (E <= 128) route_token_warp<4>(z, E, k, lane, err, e, g, rank);
-  else if (E <= 256) route_token_warp<8>(z, E, k, lane, err, e, g, rank);
-  else if (E <= 512) route_token_warp<16>(z, E, k, lane, err, e, g, rank);
-  else route_token_warp<32>(z, E, k, lane, err, e, g, rank);
-  if (rank >= 0) emit(e, g, rank);
+  if (E <= 32) route_token_warp<1>(z, E, k, lane, err, emit);
+  else if (E <= 64) route_token_warp<2>(z, E, k, lane, err, emit);
+  else if (E <= 128) route_token_warp<4>(z, E, k, lane, err, emit);
+  else if (E <= 256) route_token_warp<8>(z, E, k, lane, err, emit);
+  else if (E <= 512) route_token_warp<16>(z, E, k, lane, err, emit);
+  else route_token_warp<32>(z, E, k, lane, err, emit);
 }
 
 }  // namespace ft

@@ -209,6 +209,35 @@ __global__ void prefill_place_kernel(const int32_t* sel, const float* gates, con
   }
 }
 
+// Token rows in pair order: xp[p] = x[pair_tok[p]] (BF16, one warp per row, 16-byte
+// vectors).  The gate/up GEMM then reads each N tile of tokens as one contiguous TMA box.
+__global__ void __launch_bounds__(256) prefill_permute_kernel(const uint16_t* x, const int32_t* pair_tok, int P,
+                                                             int H, uint16_t* xp) {
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < P; p += nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)__ldg(pair_tok + p) * H);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)p * H);
+    for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// N tiles of every entry: an entry with n_e pairs is split into ceil(n_e / kTileN) tiles
+// of equal size rounded up to 16.  tiles[q] = {entry, first pair, valid pairs, N}.
+__global__ void prefill_tiles_kernel(const int32_t* entry_off, const int32_t* tile_off, int n_entries, int4* tiles) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n_entries) return;
+  const int p0 = entry_off[e], ne = entry_off[e + 1] - p0;
+  const int t0 = tile_off[e], nt = tile_off[e + 1] - t0;
+  if (nt <= 0) return;
+  const int tsize = ((ne + nt - 1) / nt + 15) & ~15;
+  for (int j = 0; j < nt; ++j) {
+    const int n0 = j * tsize;
+    const int nvalid = min(tsize, ne - n0);
+    tiles[t0 + j] = make_int4(e, p0 + n0, nvalid, (nvalid + 15) & ~15);
+  }
+}
+
 // out[t] = shared row (if any) + the k pair rows in rank order (ascending expert id).
 __global__ void prefill_combine_kernel(const uint16_t* rows, const int32_t* pos_of, const int32_t* entry_off, int T,
                                        int k, int H, int E, int has_shared, float* out) {
@@ -244,7 +273,8 @@ struct PrefillState {
   int32_t *pair_tok = nullptr, *pos_of = nullptr, *buf_dev = nullptr, *pick_dev = nullptr, *pick_host = nullptr;
   float *gates = nullptr, *pair_gate = nullptr;
   uint32_t* masks = nullptr;
-  uint16_t *h = nullptr, *rows = nullptr;
+  uint16_t *h = nullptr, *rows = nullptr, *xp = nullptr;
+  int4* tiles = nullptr;
   GemmMaps* maps = nullptr;
   // chunk state (host)
   bool active = false;
@@ -342,6 +372,8 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   if (e == cudaSuccess) e = dev_alloc(&p->pair_gate, P);
   if (e == cudaSuccess) e = dev_alloc(&p->pos_of, T * k);
   if (e == cudaSuccess) e = dev_alloc(&p->h, P * c.I);
+  if (e == cudaSuccess) e = dev_alloc(&p->xp, P * c.H);
+  if (e == cudaSuccess) e = dev_alloc(&p->tiles, P / kTileN + (size_t)c.E + 2);
   if (e == cudaSuccess) e = dev_alloc(&p->rows, P * c.H);
   if (e == cudaSuccess) e = dev_alloc(&p->buf_dev, (size_t)2 * c.E);
   if (e == cudaSuccess) e = dev_alloc(&p->pick_dev, (size_t)2 * c.E);
@@ -354,7 +386,7 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pick_buffers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kPickMaxSlots * (int)sizeof(unsigned long long));
-  if (e == cudaSuccess) e = gemm_maps_create(&p->maps, c.pool, c.S, c.shared_w, c.L, c.H, c.I, p->h, (int)P);
+  if (e == cudaSuccess) e = gemm_maps_create(&p->maps, c.pool, c.S, c.shared_w, c.L, c.H, c.I, p->h, p->xp, (int)P);
   if (e != cudaSuccess) {
     prefill_destroy(p);
     return e;
@@ -369,7 +401,7 @@ void prefill_destroy(PrefillState* p) {
   if (p->cs) cudaStreamSynchronize(p->cs);
   if (p->ts) cudaStreamSynchronize(p->ts);
   void* bufs[] = {p->sel, p->gates, p->masks, p->wpre, p->entry_off, p->tile_off, p->pair_tok,
-                  p->pair_gate, p->pos_of, p->h, p->rows, p->buf_dev, p->pick_dev};
+                  p->pair_gate, p->pos_of, p->h, p->rows, p->xp, p->tiles, p->buf_dev, p->pick_dev};
   for (void* b : bufs)
     if (b) cudaFree(b);
   if (p->pick_host) cudaFreeHost(p->pick_host);
@@ -468,6 +500,9 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
     prefill_place_kernel<<<(n_pl + 255) / 256, 256, 0, c.cs>>>(p->sel, p->gates, p->masks, p->wpre, p->entry_off, T,
                                                                k, E, p->W, p->has_shared, p->pair_tok, p->pair_gate,
                                                                p->pos_of);
+    const int n_ent = E + (p->has_shared ? 1 : 0);
+    prefill_tiles_kernel<<<(n_ent + 255) / 256, 256, 0, c.cs>>>(p->entry_off, p->tile_off, n_ent, p->tiles);
+    prefill_permute_kernel<<<p->n_sm * 8, 256, 0, c.cs>>>(x, p->pair_tok, n_pl, p->H, p->xp);
     return cudaGetLastError();
   });
   if (e != cudaSuccess) return e;
@@ -481,6 +516,7 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   d.H = p->H;
   d.entry_off = p->entry_off;
   d.tile_off = p->tile_off;
+  d.tiles = p->tiles;
   d.buf_slots = p->buf_dev + (size_t)b * E;
   d.pair_tok = p->pair_tok;
   d.pair_gate = p->pair_gate;

@@ -7,14 +7,16 @@
 // to 256 of the expert's tokens (a multiple of 16), so ragged token counts pad only to 16.
 //
 //  mode 0 (gate/up + SwiGLU): one 128-row M tile holds 64 gate rows and the same 64 up
-//    rows of the expert (two TMA boxes), K = H.  The N operand gathers the expert's token
-//    rows of x with TMA tile::gather4.  Epilogue: h[p][i] = silu(g) * u as BF16.
+//    rows of the expert (two TMA boxes), K = H.  The N operand is the expert's token rows,
+//    copied into pair order beforehand so that a tile is one TMA box.  Epilogue:
+//    h[p][i] = silu(g) * u as BF16.
 //  mode 1 (down + gate weighting): M tile = 128 rows of W_down, K = I, the N operand is
 //    the expert's contiguous rows of h.  Epilogue: rows[p][j] = BF16(gate_p * y).
 //
 // One CTA per SM, persistent over tiles.  Warp 0 issues TMA into a 4-stage shared-memory
 // ring, warp 1 issues tcgen05.mma (one thread) into one of two TMEM accumulators, warps
-// 2-5 drain the other accumulator (tcgen05.ld) while the next tile accumulates.  Every
+// 2-9 drain the other accumulator (tcgen05.ld; two warps per TMEM lane quarter, taking
+// alternate 16-column steps) while the next tile accumulates.  Every
 // mbarrier wait is bounded: on timeout the kernel records FT_DEVERR_TIMEOUT, stops
 // issuing work, drains its outstanding copies (bounded) and frees TMEM before returning.
 #include <cuda.h>
@@ -31,7 +33,10 @@ constexpr int B_BYTES = BN_MAX * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_COLS = 16;               // TMEM columns drained per step
 constexpr int STG_PITCH = EPI_COLS + 1;    // staging row pitch (floats), bank-conflict free
-constexpr int GEMM_THREADS = 192;
+constexpr int SB_BYTES = EPI_COLS * BM * 2;  // BF16 output tile of one epilogue step
+constexpr int EPI_HALF_BYTES = BM * STG_PITCH * 4 + SB_BYTES;
+constexpr int EPI_WARPS = 8;              // two epilogue warps per TMEM lane quarter
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -75,22 +80,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// 2-D TMA tile load completing on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(pol)
       : "memory");
 }
 
-// Four rows (r0..r3) of `map`, each `box width` elements from column x, one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
-                                            int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+// L2 policies: weight tiles are read by the one or two N tiles of their expert at about the
+// same time, then never again in this layer (evict first); token tiles are re-read by every
+// M tile of the expert (evict last).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 // Shared-memory matrix descriptor: K-major tile, rows of 128 bytes with the 128-byte
@@ -148,27 +159,16 @@ struct TileInfo {
   int e, m, nvalid, N, pbase;
 };
 
-// Global tile g -> (entry, M tile, N range).  M tiles are innermost so consecutive tiles
-// of one CTA reuse the same token rows through L2.  An entry with n_e tokens is split
-// into ceil(n_e/256) N tiles of equal size rounded up to 16.
+// Global tile g -> (entry, M tile, N range).  M tiles are innermost, so the M tiles of one
+// N tile run on neighbouring CTAs at the same time and share its token rows through L2.
 __device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int g) {
   TileInfo t;
   t.m = g % d.mt;
-  const int q = g / d.mt;
-  int lo = 0, hi = d.n_entries;  // tile_off[lo] <= q < tile_off[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(d.tile_off + mid) <= q) lo = mid;
-    else hi = mid;
-  }
-  t.e = lo;
-  const int p0 = __ldg(d.entry_off + lo), ne = __ldg(d.entry_off + lo + 1) - p0;
-  const int t0 = __ldg(d.tile_off + lo), nt = __ldg(d.tile_off + lo + 1) - t0;
-  const int tsize = ((ne + nt - 1) / nt + 15) & ~15;
-  const int n0 = (q - t0) * tsize;
-  t.nvalid = min(tsize, ne - n0);
-  t.N = (t.nvalid + 15) & ~15;
-  t.pbase = p0 + n0;
+  const int4 q = __ldg(d.tiles + g / d.mt);
+  t.e = q.x;
+  t.pbase = q.y;
+  t.nvalid = q.z;
+  t.N = q.w;
   return t;
 }
 
@@ -178,8 +178,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmB, const GemmDesc d) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  float* stg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + BM * STG_PITCH * 4);
+  // per epilogue half: FP32 staging [BM][STG_PITCH], then a BF16 output tile [EPI_COLS][BM]
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * EPI_HALF_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
-      mbar_init(smem_u32(tempty + b), 128);
+      mbar_init(smem_u32(tempty + b), 32 * EPI_WARPS);
     }
     mbar_init(smem_u32(done), 1);
     *abort_flag = 0;
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     int last_par[STAGES];
@@ -235,19 +237,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       } else {
         arow0 = wbase * 3 * d.H + 2 * d.H + t.m * BM;  // down rows
       }
-      int rows[8];
-      const int ngroups = t.N / 4;
-      if (MODE == 0) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int gi = lane + 32 * j;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int n = min(4 * gi + r, t.nvalid - 1);
-            rows[4 * j + r] = gi < ngroups ? __ldg(d.pair_tok + t.pbase + n) : 0;
-          }
-        }
-      }
       bool ok = true;
       for (int kb = 0; kb < d.kb; ++kb) {
         int w_ok = lane == 0 ? (int)mbar_wait(smem_u32(empty + stage), phase ^ 1u, abort_flag, d.error_word) : 0;
@@ -259,25 +248,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t a_dst = smem_base + stage * STAGE_BYTES, b_dst = a_dst + A_BYTES;
         const uint32_t fb = smem_u32(full + stage);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, A_BYTES + (MODE == 0 ? t.N * 128 : B_BYTES));
+          // the token box is always BN_MAX rows (rows past the tile belong to the next entry
+          // or lie beyond the buffer and are zero-filled; the epilogue ignores them)
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           if (MODE == 0) {
-            tma_load_2d(a_dst, mA, kb * BK, arow0, fb);
-            tma_load_2d(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb);
+            tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
+            tma_load_2d_hint(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb, pol_w);
           } else {
-            tma_load_2d(a_dst, mA, kb * BK, arow0, fb);
-            tma_load_2d(b_dst, &tmB, kb * BK, t.pbase, fb);
+            tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
           }
+          tma_load_2d_hint(b_dst, &tmB, kb * BK, t.pbase, fb, pol_x);
         }
         __syncwarp();
-        if (MODE == 0) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int gi = lane + 32 * j;
-            if (gi < ngroups)
-              tma_gather4(b_dst + gi * 512, &tmB, kb * BK, rows[4 * j], rows[4 * j + 1], rows[4 * j + 2],
-                          rows[4 * j + 3], fb);
-          }
-        }
         last_par[stage] = (int)phase;
         if (++stage == STAGES) {
           stage = 0;
@@ -336,8 +318,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------------- epilogue
-    const int et = threadIdx.x - 64;       // 0..127
-    const int q4 = warp & 3;               // TMEM lane quarter this warp may access
+    const int half = (threadIdx.x - 64) >> 7;  // the two halves take alternate column steps
+    const int et = (threadIdx.x - 64) & 127;   // 0..127 within the half
+    const int q4 = warp & 3;                   // TMEM lane quarter this warp may access
+    float* stg = reinterpret_cast<float*>(epi + half * EPI_HALF_BYTES);
+    uint16_t* sb = reinterpret_cast<uint16_t*>(stg + BM * STG_PITCH);
+    const uint32_t bar_id = 1 + half;
     const int m = 32 * q4 + lane;          // accumulator row (TMEM lane)
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -347,33 +333,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, d.error_word)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * BN_MAX);
-      for (int c0 = 0; c0 < t.N; c0 += EPI_COLS) {
+      for (int c0 = half * EPI_COLS; c0 < t.N; c0 += 2 * EPI_COLS) {
         float v[EPI_COLS];
         tmem_ld16(tbase + c0, v);
+        // results go out as 16-byte row pieces through a BF16 tile in shared memory
         if (MODE == 0) {
 #pragma unroll
           for (int c = 0; c < EPI_COLS; ++c) stg[m * STG_PITCH + c] = v[c];
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
           const int i = et & 63, cb = (et >> 6) * (EPI_COLS / 2);
 #pragma unroll
-          for (int c = 0; c < EPI_COLS / 2; ++c) {
-            const int n = c0 + cb + c;
-            if (n < t.nvalid) {
-              const float gv = stg[i * STG_PITCH + cb + c], uv = stg[(64 + i) * STG_PITCH + cb + c];
-              const float hv = gv / (1.0f + expf(-gv)) * uv;
-              d.h[(size_t)(t.pbase + n) * d.I + t.m * 64 + i] = f2bf(hv);
-            }
+          for (int c = 0; c < EPI_COLS / 2; ++c) {  // h[n][i] for this thread's 8 tokens
+            const float gv = stg[i * STG_PITCH + cb + c], uv = stg[(64 + i) * STG_PITCH + cb + c];
+            sb[(cb + c) * 64 + i] = f2bf(gv / (1.0f + expf(-gv)) * uv);
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+          {  // 16 tokens x 64 h values: one 16-byte piece per thread
+            const int n = et >> 3, ch = et & 7;
+            if (c0 + n < t.nvalid)
+              *reinterpret_cast<uint4*>(d.h + (size_t)(t.pbase + c0 + n) * d.I + t.m * 64 + ch * 8) =
+                  *reinterpret_cast<const uint4*>(sb + n * 64 + ch * 8);
+          }
+          asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
         } else {
 #pragma unroll
           for (int c = 0; c < EPI_COLS; ++c) {
             const int n = c0 + c;
-            if (n < t.nvalid) {
-              const int p = t.pbase + n;
-              d.rows[(size_t)p * d.H + t.m * BM + m] = f2bf(__ldg(d.pair_gate + p) * v[c]);
-            }
+            const float gate = n < t.nvalid ? __ldg(d.pair_gate + t.pbase + n) : 0.f;
+            sb[c * BM + m] = f2bf(gate * v[c]);
           }
+          asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+#pragma unroll
+          for (int q = 0; q < EPI_COLS * BM / 8 / 128; ++q) {  // 16 tokens x 128 outputs
+            const int idx = et + 128 * q, n = idx >> 4, ch = idx & 15;
+            if (c0 + n < t.nvalid)
+              *reinterpret_cast<uint4*>(d.rows + (size_t)(t.pbase + c0 + n) * d.H + t.m * BM + ch * 8) =
+                  *reinterpret_cast<const uint4*>(sb + n * BM + ch * 8);
+          }
+          asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
         }
       }
       tc_fence_before();
@@ -424,7 +421,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + BM * STG_PITCH * 4 + 16 * 8 + 16; }
+size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + 2 * EPI_HALF_BYTES + 16 * 8 + 16; }
 
 }  // namespace
 
@@ -432,12 +429,13 @@ struct GemmMaps {
   CUtensorMap a_gu, a_gu_sh;    // weight rows of width H (gate, up): pool / shared experts
   CUtensorMap a_dn, a_dn_sh;    // weight rows of width I (down)
   CUtensorMap h_map;            // h [P][I]
+  CUtensorMap x_map;            // token rows in pair order [P][H]
   int H, I;
   bool attr_set = false;
 };
 
 cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
-                             int I, const uint16_t* h_buf, int max_pairs) {
+                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs) {
   GemmMaps* m = new GemmMaps();
   m->H = H;
   m->I = I;
@@ -449,6 +447,7 @@ cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const u
   if (e == cudaSuccess) e = make_map(&m->a_gu_sh, sh, H, sh_rows * 3 * I, (uint64_t)H * 2, BK, 64);
   if (e == cudaSuccess) e = make_map(&m->a_dn_sh, sh, I, sh_rows * 3 * H, (uint64_t)I * 2, BK, BM);
   if (e == cudaSuccess) e = make_map(&m->h_map, h_buf, I, (uint64_t)max_pairs, (uint64_t)I * 2, BK, BN_MAX);
+  if (e == cudaSuccess) e = make_map(&m->x_map, xp_buf, H, (uint64_t)max_pairs, (uint64_t)H * 2, BK, BN_MAX);
   if (e == cudaSuccess) {
     e = cudaFuncSetAttribute(grouped_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gemm_smem_bytes());
@@ -468,14 +467,10 @@ void gemm_maps_destroy(GemmMaps* m) { delete m; }
 
 cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, int T, const GemmDesc& d, int grid,
                                 cudaStream_t s) {
-  if (mode == 0) {
-    CUtensorMap xm;  // token rows of x, one row per gather4 row
-    cudaError_t e = make_map(&xm, x, m->H, (uint64_t)T, (uint64_t)m->H * 2, BK, 1);
-    if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<0><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_gu, m->a_gu_sh, xm, d);
-  } else {
-    grouped_gemm_kernel<1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_dn, m->a_dn_sh, m->h_map, d);
-  }
+  (void)x;
+  (void)T;
+  if (mode == 0) grouped_gemm_kernel<0><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_gu, m->a_gu_sh, m->x_map, d);
+  else grouped_gemm_kernel<1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_dn, m->a_dn_sh, m->h_map, d);
   return cudaGetLastError();
 }
 
