@@ -473,7 +473,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   h->lay = ft::make_layout(cfg->wtype, h->H, h->I);
   h->n_banks = fp8 ? 6 : 3;
   h->grid_eval = h->n_sm * 4;
-  h->grid_fill = h->n_sm * 2;
+  h->grid_fill = h->n_sm;
   if (cfg->compute_stream) {
     h->cs = (cudaStream_t)cfg->compute_stream;
   } else {

@@ -30,7 +30,9 @@ constexpr int kDigit = 9;  // radix-select digit: one histogram bin per thread
 constexpr int kBins = 1 << kDigit;
 static_assert(kBins == kThreads, "one histogram bin per thread");
 constexpr int kSmemSlots = 16384;  // slot stamps staged in shared memory up to this many slots
+constexpr int kSmemOwners = 8192;  // slot owners staged too up to this many slots
 constexpr size_t kDynSmemMax = kMaxE * sizeof(unsigned long long) + kSmemSlots * sizeof(uint32_t);
+static_assert(kSmemOwners * 2 <= kSmemSlots, "owners share the stamp area's budget");
 
 // Fill count: q = clamp(floor(m*bp/bh + 1/2), 1, m) for m > 0; all misses when the
 // residual bandwidth B_H - B_P is not positive; never more than `evictable`.
@@ -102,6 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   const int base_u = p.layer * E;
   const bool in_smem = S <= kSmemSlots;
   uint32_t* stv = in_smem ? s_stamp : p.stamp;  // stamps as the victim scan sees them
+  // slot owners, needed only by the install: staged with the stamps for small pools so that
+  // the install does not wait on global memory
+  const bool own_smem = S <= kSmemOwners;
+  int32_t* s_owner = reinterpret_cast<int32_t*>(s_stamp + S);
 
   // State written by the previous control kernel (complete when this one starts, since
   // every kernel of the chain triggers its dependents only after its own wait): this
@@ -114,6 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   }
   if (in_smem)
     for (int s = tid; s < S; s += kThreads) s_stamp[s] = p.stamp[s];
+  if (own_smem)
+    for (int s = tid; s < S; s += kThreads) s_owner[s] = p.owner[s];
   for (int i = tid; i < kMaxE / 32; i += kThreads) s_bitmap[i] = 0;
   if (tid == 0) {
     s_err = 0;
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
       p.w.gates[idx] = g;
       s_sel[idx] = e;
       atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
-      atomicOr(&s_tok[e], 1ull << t);
+      atomicOr(reinterpret_cast<uint32_t*>(&s_tok[e]) + (t >> 5), 1u << (t & 31));  // 32-bit half of the mask
     });
   }
   __syncthreads();
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     for (int i = tid; i < q; i += kThreads) {
       const int v = s_victims[i];
       const int u = s_miss[i];
-      const int old = p.owner[v];
+      const int old = own_smem ? s_owner[v] : p.owner[v];
       if (old >= 0) {
         p.res[old] = -1;
         atomicAdd(&s_evict, 1);
@@ -393,14 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   if (tid == 0) {
     DevState* st = p.st;
     st->clock = clock;
-    st->hits += (unsigned long long)s_nhit;
-    st->misses += (unsigned long long)s_nmiss;
-    st->fills += (unsigned long long)q;
-    st->cpu_execs += (unsigned long long)(s_nmiss - q);
-    st->evictions += (unsigned long long)s_evict;
-    st->decode_steps += 1ull;
-    st->eval_entries += (unsigned long long)(s_ng + (p.has_shared ? 1 : 0));
-    st->eval_pairs += (unsigned long long)(s_goff[s_ng] + (p.has_shared ? B : 0));
+    // counter updates without a read back (reductions): nothing on this path waits for them
+    atomicAdd(&st->hits, (unsigned long long)s_nhit);
+    atomicAdd(&st->misses, (unsigned long long)s_nmiss);
+    atomicAdd(&st->fills, (unsigned long long)q);
+    atomicAdd(&st->cpu_execs, (unsigned long long)(s_nmiss - q));
+    atomicAdd(&st->evictions, (unsigned long long)s_evict);
+    atomicAdd(&st->decode_steps, 1ull);
+    atomicAdd(&st->eval_entries, (unsigned long long)(s_ng + (p.has_shared ? 1 : 0)));
+    atomicAdd(&st->eval_pairs, (unsigned long long)(s_goff[s_ng] + (p.has_shared ? B : 0)));
     if (s_err) atomicOr(&st->error_word, s_err);
   }
 }
@@ -408,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
 template <int NPL>
 cudaError_t launch_npl(const CtrlParams& p, cudaStream_t s) {
   const size_t smem = kMaxE * sizeof(unsigned long long) +
-                      (size_t)(p.S <= kSmemSlots ? p.S : 0) * sizeof(uint32_t);
+                      (size_t)(p.S <= kSmemSlots ? p.S : 0) * sizeof(uint32_t) +
+                      (size_t)(p.S <= kSmemOwners ? p.S : 0) * sizeof(int32_t);
   return launch_k(control_kernel<NPL>, dim3(1), dim3(kThreads), smem, s, p.pdl, p);
 }
 

@@ -33,9 +33,11 @@ using namespace dot;
 // ------------------------------------------------------------------------- fill
 // Work = q experts x n_banks contiguous segments.  CTA b copies a share of segment
 // b mod nseg (addresses computed once per segment), issuing FILL_UNROLL 16-byte loads
-// from the mapped host pool before storing any, so the grid keeps several MB of host
-// reads in flight: one 6 MB expert then moves at the host link's rate.
-constexpr int FILL_UNROLL = 8;
+// from the mapped host pool before storing any, so the grid keeps MBs of host reads in
+// flight: one 6 MB expert then moves at the host link's rate.  The kernel stays small in
+// registers so that, while it waits for the control kernel, a CTA of the next kernel
+// (the batch-1 expert GEMV) fits beside it on the SM.
+constexpr int FILL_UNROLL = 4;
 
 __device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16,
                                              size_t first, size_t stride) {
