@@ -203,15 +203,19 @@ def _kernel_hash() -> str:
 
 
 def _traffic(kernel: str):
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    try:
-        t = json.load(open(path))
-    except (OSError, ValueError):
-        return None
-    e = t.get(kernel)
-    if not e or e.get("source_hash") != _kernel_hash():
-        return None
-    return e.get("dram_bytes_per_launch")
+    """DRAM bytes per launch of `kernel` from the ncu summaries under profiles/ (a line
+    `bench-traffic: <kernel> dram_bytes_per_launch=<n> source_hash=<h>`), or None when the
+    kernel sources changed since that capture."""
+    import glob
+
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(path, encoding="utf-8"):
+            if not line.startswith("bench-traffic:"):
+                continue
+            f = dict(kv.split("=", 1) for kv in line.split()[2:] if "=" in kv)
+            if line.split()[1] == kernel and f.get("source_hash") == _kernel_hash():
+                return int(f["dram_bytes_per_launch"])
+    return None
 
 
 def _peaks():
