@@ -90,27 +90,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// 2-D TMA tile load multicast to the CTAs of `mask` in this cluster (same shared-memory
-// offset and mbarrier offset in each), with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(pol)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // L2 policies: weight tiles are read by the one or two N tiles of their expert at about the
 // same time, then never again in this layer (evict first); token tiles are re-read by every
 // M tile of the expert (evict last).
@@ -154,14 +133,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// umma_commit arriving on the mbarrier at the same offset in every CTA of `mask`
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -188,16 +159,12 @@ struct TileInfo {
   int e, m, nvalid, N, pbase;
 };
 
-// Work item c of a cluster of CM CTAs -> (entry, M tile, N range) of the CTA with cluster
-// rank `rank`: the cluster's CTAs take CM consecutive M tiles of the same N tile (the
-// token operand is then loaded once per cluster and multicast).  M tiles are innermost, so
-// the M tiles of one N tile run at about the same time and share its rows through L2.
-template <int CM>
-__device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int c, int rank) {
+// Global tile g -> (entry, M tile, N range).  M tiles are innermost, so the M tiles of one
+// N tile run on neighbouring CTAs at the same time and share its token rows through L2.
+__device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int g) {
   TileInfo t;
-  const int groups = d.mt / CM;
-  t.m = (c % groups) * CM + rank;
-  const int4 q = __ldg(d.tiles + c / groups);
+  t.m = g % d.mt;
+  const int4 q = __ldg(d.tiles + g / d.mt);
   t.e = q.x;
   t.pbase = q.y;
   t.nvalid = q.z;
@@ -205,11 +172,10 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int c, int ra
   return t;
 }
 
-template <int MODE, int CM>
+template <int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
-                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB8,
-                        const GemmDesc d) {
+                        const __grid_constant__ CUtensorMap tmB, const GemmDesc d) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   // per epilogue half: FP32 staging [BM][STG_PITCH], then a BF16 output tile [EPI_COLS][BM]
@@ -227,7 +193,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), CM);  // released by the MMA of every CTA that writes into it
+      mbar_init(smem_u32(empty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
@@ -245,13 +211,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync();  // every CTA's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int rank = CM > 1 ? (int)cluster_rank() : 0;
-  const uint16_t cmask = (uint16_t)((1u << CM) - 1u);
-  const int c_first = blockIdx.x / CM, c_step = gridDim.x / CM;
-  const int total = (d.mt / CM) * __ldg(d.tile_off + d.n_entries);
+  const int total = d.mt * __ldg(d.tile_off + d.n_entries);
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
@@ -262,11 +224,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int last_par[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
-    for (int g = c_first; g < total; g += c_step) {
-      const TileInfo t = decode_tile<CM>(d, g, rank);
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const TileInfo t = decode_tile(d, g);
       if (t.nvalid <= 0) continue;
       const bool sh = t.e >= d.E;
-      const int npad = (t.N + 8 * CM - 1) / (8 * CM) * (8 * CM);  // token rows loaded (CM > 1)
       const CUtensorMap* mA = sh ? &tmAs : &tmA;
       const int wbase = sh ? d.layer : __ldg(d.buf_slots + t.e);
       int arow0, arow1 = 0;
@@ -286,24 +247,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         const uint32_t a_dst = smem_base + stage * STAGE_BYTES, b_dst = a_dst + A_BYTES;
         const uint32_t fb = smem_u32(full + stage);
-        // token rows past the tile belong to the next entry or lie beyond the buffer (zero
-        // filled); the epilogue ignores their columns
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, A_BYTES + (CM > 1 ? npad * 128 : B_BYTES));
+          // the token box is always BN_MAX rows (rows past the tile belong to the next entry
+          // or lie beyond the buffer and are zero-filled; the epilogue ignores them)
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
           if (MODE == 0) {
             tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
             tma_load_2d_hint(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb, pol_w);
           } else {
             tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
           }
-          if (CM == 1) tma_load_2d_hint(b_dst, &tmB, kb * BK, t.pbase, fb, pol_x);  // always BN_MAX rows
-        }
-        if (CM > 1) {  // this CTA's slice of the token tile, 8 rows per copy, to every CTA of the cluster
-          const int slice = npad / CM;
-          for (int bx = lane; bx < slice / 8; bx += 32) {
-            const int row = rank * slice + bx * 8;
-            tma_load_2d_mc(b_dst + (uint32_t)row * 128u, &tmB8, kb * BK, t.pbase + row, fb, cmask, pol_x);
-          }
+          tma_load_2d_hint(b_dst, &tmB, kb * BK, t.pbase, fb, pol_x);
         }
         __syncwarp();
         last_par[stage] = (int)phase;
@@ -326,13 +280,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int g = c_first; g < total && ok; g += c_step) {
-        const TileInfo t = decode_tile<CM>(d, g, rank);
+      for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+        const TileInfo t = decode_tile(d, g);
         if (t.nvalid <= 0) continue;
         if (!mbar_wait(smem_u32(tempty + acc), acc_phase ^ 1u, abort_flag, d.error_word)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
-        const uint32_t idesc = bf16_idesc(BM, CM > 1 ? (t.N + 8 * CM - 1) / (8 * CM) * (8 * CM) : t.N);
+        const uint32_t idesc = bf16_idesc(BM, t.N);
         for (int kb = 0; kb < d.kb; ++kb) {
           if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, d.error_word)) {
             ok = false;
@@ -343,8 +297,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), idesc, (kb | k) != 0);
-          if (CM > 1) umma_commit_mc(smem_u32(empty + stage), cmask);
-          else umma_commit(smem_u32(empty + stage));
+          umma_commit(smem_u32(empty + stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -374,8 +327,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int m = 32 * q4 + lane;          // accumulator row (TMEM lane)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int g = c_first; g < total; g += c_step) {
-      const TileInfo t = decode_tile<CM>(d, g, rank);
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const TileInfo t = decode_tile(d, g);
       if (t.nvalid <= 0) continue;
       if (!mbar_wait(smem_u32(tfull + acc), acc_phase, abort_flag, d.error_word)) break;
       tc_fence_after();
@@ -430,7 +383,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync();  // no CTA leaves while others may still write into it
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
@@ -476,68 +428,11 @@ size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + 2 * EPI_HALF_BYT
 struct GemmMaps {
   CUtensorMap a_gu, a_gu_sh;    // weight rows of width H (gate, up): pool / shared experts
   CUtensorMap a_dn, a_dn_sh;    // weight rows of width I (down)
-  CUtensorMap h_map, h_map8;    // h [P][I]: BN_MAX-row and 8-row boxes
-  CUtensorMap x_map, x_map8;    // token rows in pair order [P][H]: BN_MAX-row and 8-row boxes
+  CUtensorMap h_map;            // h [P][I]
+  CUtensorMap x_map;            // token rows in pair order [P][H]
   int H, I;
-  int cl_grid[2] = {0, 0};      // grid of the clustered kernel per mode (0: not available)
+  bool attr_set = false;
 };
-
-namespace {
-
-constexpr int kCluster = 4;  // CTAs sharing one token tile (multicast)
-
-template <int MODE, int CM>
-cudaError_t set_gemm_attr() {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<MODE, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)gemm_smem_bytes());
-}
-
-// Largest grid of resident clusters of kCluster CTAs (whole clusters only), or 0.
-template <int MODE>
-int cluster_grid(int n_sm) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(n_sm / kCluster * kCluster));
-  cfg.blockDim = dim3(GEMM_THREADS);
-  cfg.dynamicSmemBytes = gemm_smem_bytes();
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, kCluster>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  const int most = n_sm / kCluster;
-  return (n < most ? n : most) * kCluster;
-}
-
-template <int MODE>
-cudaError_t launch_mode(const GemmMaps* m, const CUtensorMap& a, const CUtensorMap& ash, const CUtensorMap& b,
-                        const CUtensorMap& b8, const GemmDesc& d, int grid, cudaStream_t s) {
-  if (m->cl_grid[MODE] > 0 && d.mt % kCluster == 0) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)m->cl_grid[MODE]);
-    cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = gemm_smem_bytes();
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, kCluster>, a, ash, b, b8, d);
-  }
-  grouped_gemm_kernel<MODE, 1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(a, ash, b, b8, d);
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
                              int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs) {
@@ -552,21 +447,13 @@ cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const u
   if (e == cudaSuccess) e = make_map(&m->a_gu_sh, sh, H, sh_rows * 3 * I, (uint64_t)H * 2, BK, 64);
   if (e == cudaSuccess) e = make_map(&m->a_dn_sh, sh, I, sh_rows * 3 * H, (uint64_t)I * 2, BK, BM);
   if (e == cudaSuccess) e = make_map(&m->h_map, h_buf, I, (uint64_t)max_pairs, (uint64_t)I * 2, BK, BN_MAX);
-  if (e == cudaSuccess) e = make_map(&m->h_map8, h_buf, I, (uint64_t)max_pairs, (uint64_t)I * 2, BK, 8);
   if (e == cudaSuccess) e = make_map(&m->x_map, xp_buf, H, (uint64_t)max_pairs, (uint64_t)H * 2, BK, BN_MAX);
-  if (e == cudaSuccess) e = make_map(&m->x_map8, xp_buf, H, (uint64_t)max_pairs, (uint64_t)H * 2, BK, 8);
-  if (e == cudaSuccess) e = set_gemm_attr<0, 1>();
-  if (e == cudaSuccess) e = set_gemm_attr<1, 1>();
-  if (e == cudaSuccess) e = set_gemm_attr<0, kCluster>();
-  if (e == cudaSuccess) e = set_gemm_attr<1, kCluster>();
   if (e == cudaSuccess) {
-    int dev = 0, n_sm = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) {
-      m->cl_grid[0] = cluster_grid<0>(n_sm);
-      m->cl_grid[1] = cluster_grid<1>(n_sm);
-    }
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)gemm_smem_bytes());
   }
   if (e != cudaSuccess) {
     delete m;
@@ -582,8 +469,9 @@ cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, 
                                 cudaStream_t s) {
   (void)x;
   (void)T;
-  if (mode == 0) return launch_mode<0>(m, m->a_gu, m->a_gu_sh, m->x_map, m->x_map8, d, grid, s);
-  return launch_mode<1>(m, m->a_dn, m->a_dn_sh, m->h_map, m->h_map8, d, grid, s);
+  if (mode == 0) grouped_gemm_kernel<0><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_gu, m->a_gu_sh, m->x_map, d);
+  else grouped_gemm_kernel<1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_dn, m->a_dn_sh, m->h_map, d);
+  return cudaGetLastError();
 }
 
 }  // namespace ft
