@@ -391,6 +391,12 @@ def run_ours(args, d: Dist) -> dict | None:
                 "algorithmic_bytes_per_launch": round(rl_bytes / max(1, rl_n)),
                 "traffic": tr}
     launches_per_layer = 3 if fused else 4
+    # the decode path as a whole: expert-weight bytes the evaluation reads per token over the
+    # timed time per token (control, fills and evaluation included)
+    wbytes_tok = cache["gpu_experts_per_token"] * 6 * H * w.inter
+    layer_rl = {"scope": "whole decode step (all kernels, fills included): expert weight bytes per token / time per token",
+                "bound": "hbm", "achieved": round(wbytes_tok / (tmax / args.steps) / 1e9, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(wbytes_tok / (tmax / args.steps) / 1e9 / peak, 4)}
 
     # end to end through the host-buffer C-ABI call (H2D inputs, D2H outputs, every step)
     n_e2e = min(args.e2e_steps, args.steps)
@@ -437,7 +443,7 @@ def run_ours(args, d: Dist) -> dict | None:
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see DESIGN.md)",
            "config": {**_config_desc(w), "parallelism": f"replicas x{d.world}" if d.world > 1 else "single GPU"},
            "hbm_gbs_expert_weights": hbm,
-           "roofline": roofline, "prefill": prefill, "e2e": e2e, "gpu_launches": args.steps * L * launches_per_layer, "clocks": clk,
+           "roofline": roofline, "decode_step_roofline": layer_rl, "prefill": prefill, "e2e": e2e, "gpu_launches": args.steps * L * launches_per_layer, "clocks": clk,
            "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1), "bp_after_timed_gbps": round(bp_after, 1),
            "fill_observed_gbs": round(fill_gbs, 1) if fill_gbs else None,
            "setup_s": round(setup_s, 1)}
