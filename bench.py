@@ -471,8 +471,9 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
     L, T, H, E, I, k = w.n_layers, w.prefill_tokens, w.hidden, w.n_experts, w.inter, w.top_k
     pool = synth.ExpertPool(w)
     banks = pool.routed_banks()
+    abl_sizes = () if args.no_prefill_ablation else (4096, 8192, 16384)
     cfg = F.make_config(L, H, I, E, k, False, F.FT_W_BF16, 1, w.cache_slots, w.bp_gbps, w.bh_gbps,
-                        max_prefill_tokens=T, device=d.local, compute_stream=stream.cuda_stream)
+                        max_prefill_tokens=max((T,) + abl_sizes), device=d.local, compute_stream=stream.cuda_stream)
     h = F.ft_moe_init(cfg, banks)
     # activations: two distinct layers' x, reused alternately (routing, which sets the work,
     # uses every layer's own logits)
@@ -500,6 +501,29 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
         chunk()
         prof = F.ft_moe_get_profile(h, reset=True)
         F.ft_moe_set_profiling(h, 0)
+        # ablation: second buffer off (each layer's copy at its own call, compute waits)
+        ablation = {}
+        if abl_sizes:
+            Tm = max(abl_sizes)
+            xa = torch.from_numpy(np.stack([synth.prefill_x(w, 1, l, Tm) for l in range(2)]).view(np.int16)).to(dev)
+            za = torch.stack([torch.from_numpy(synth.prefill_logits(w, 1, l, Tm)) for l in range(L)]).to(dev)
+            oa = torch.empty((Tm, H), dtype=torch.float32, device=dev)
+            for Ta in abl_sizes:
+                tps = {}
+                for ov in (True, False):
+                    F.ft_moe_set_prefill_overlap(h, ov)
+                    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a0.record(stream)
+                    for l in range(L):
+                        F.ft_moe_prefill_chunk(h, l, Ta, xa[l % 2, :Ta], za[l, :Ta], oa[:Ta])
+                    a1.record(stream)
+                    a1.synchronize()
+                    tps[ov] = Ta / (a0.elapsed_time(a1) * 1e-3)
+                ablation[str(Ta)] = {"tok_s_double_buffer": round(tps[True], 1),
+                                     "tok_s_single_buffer": round(tps[False], 1),
+                                     "loss_without_second_buffer": round(1.0 - tps[False] / tps[True], 4)}
+            F.ft_moe_set_prefill_overlap(h, True)
+            del xa, za, oa
     st = F.ft_moe_get_stats(h)
     F.ft_moe_destroy(h)
     del banks, pool
@@ -534,6 +558,7 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
             "chunk_bound_s": {kk: round(v, 4) for kk, v in bound_s.items()},
             "frac_of_chunk_bound": round(max(bound_s.values()) / chunk_s, 4),
             "kernels_ms_per_chunk": {kk: round(v[1], 3) for kk, v in prof.items() if v[0] and kk.startswith("prefill")},
+            "double_buffer_ablation": ablation,
             "error_word": st.error_word}
 
 
@@ -576,6 +601,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-chunks", type=int, default=2)
+    ap.add_argument("--no-prefill-ablation", action="store_true", help="skip the second-buffer-off chunks")
     ap.add_argument("--prefill-only", action="store_true", help="profiling: run only the prefill measurement")
     ap.add_argument("--prefill-layers", type=int, default=0, help="profiling only: fewer layers")
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling only: fewer tokens")

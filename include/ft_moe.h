@@ -213,6 +213,14 @@ ft_status ft_graph_destroy(ft_graph* g);
 ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x_bf16, const float* logits,
                                float* out);
 
+/* Ablation switch for the prefill double buffer ([FT] "全层双缓冲" measures the loss
+ * when the second buffer is off).  on = 1 (default): layer l+1 streams into the other
+ * buffer while layer l computes.  on = 0: each layer's weights are copied at the start
+ * of its own call and the computation waits for them; residency decisions and outputs
+ * are identical either way.  Takes effect at the next prefill call.
+ * Errors: FT_ERR_INVALID (null handle). */
+ft_status ft_moe_set_prefill_overlap(ft_moe* h, int on);
+
 /* Safe-point resize of the slot pool ([FT] "挑战三"; [FT2] paragraph on the memory
  * budget).  Growing adds empty slots.  Shrinking keeps the new_slots most recently
  * used experts (stamp desc, slot asc), drops the rest and moves kept experts from

@@ -73,6 +73,7 @@ struct ft_moe {
   int dev = 0, n_sm = 0;
   cudaStream_t cs = nullptr, ts = nullptr;
   bool own_cs = false, own_ts = false;
+  bool pf_overlap = true;  // prefill double buffer on
   ft::SlotLayout lay{};
   int S = 0, L = 0, E = 0, K = 0, H = 0, I = 0, kcap = 0;
   long long bp_mbs = 0, bh_mbs = 0;
@@ -850,6 +851,7 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
     c.bank_row[j] = h->bank[j].row;
   }
   c.prof = h->prof;
+  c.overlap = h->pf_overlap;
   if (!h->pf) {
     cudaError_t e = ft::prefill_create(&h->pf, c);
     if (e != cudaSuccess) return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA,
@@ -861,6 +863,12 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
                                     h->prof ? &ev : nullptr, &err);
   for (auto& r : ev) h->prof_live.push_back({r.first, r.second.first, r.second.second});
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill layer %d: %s %s", layer, cudaGetErrorString(e), err.c_str());
+  return FT_OK;
+}
+
+ft_status ft_moe_set_prefill_overlap(ft_moe* h, int on) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  h->pf_overlap = on != 0;
   return FT_OK;
 }
 

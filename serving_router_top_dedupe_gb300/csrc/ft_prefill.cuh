@@ -22,6 +22,7 @@ struct PrefillCtx {
   const uint8_t* bank_host[3];  // gate, up, down host banks (pinned)
   size_t bank_row[3];
   bool prof;
+  bool overlap;  // stream layer l+1 while layer l computes (the double buffer)
 };
 
 // Arguments of the grouped GEMM (prefill_gemm.cu).  Entries 0..E-1 are the layer's

@@ -483,7 +483,7 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // ---- stream the whole next layer into the other buffer while this one computes
-  if (layer + 1 < p->L) {
+  if (c.overlap && layer + 1 < p->L) {
     if ((e = load_buffer(p, layer + 1, b ^ 1, prof)) != cudaSuccess) return e;
     p->pending = layer + 1;
   }

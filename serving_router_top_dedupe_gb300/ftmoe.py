@@ -80,6 +80,7 @@ _SIGS = {
     "ft_graph_launch": [_P],
     "ft_graph_destroy": [_P],
     "ft_moe_prefill_chunk": [_P, C.c_int, C.c_int, _P, _P, _P],
+    "ft_moe_set_prefill_overlap": [_P, C.c_int],
     "ft_cache_resize": [_P, C.c_int],
     "ft_split_misses": [C.c_int, C.c_double, C.c_double, C.c_int, C.POINTER(C.c_int)],
     "ft_bench_bw": [C.c_size_t, C.c_int, C.POINTER(C.c_double)],
@@ -172,6 +173,10 @@ def ft_graph_destroy(g) -> None:
 
 def ft_moe_prefill_chunk(h, layer, n_tokens, x_bf16, logits, out) -> None:
     _check(_lib.ft_moe_prefill_chunk(h, layer, n_tokens, _ptr(x_bf16), _ptr(logits), _ptr(out)))
+
+
+def ft_moe_set_prefill_overlap(h, on: bool) -> None:
+    _check(_lib.ft_moe_set_prefill_overlap(h, 1 if on else 0))
 
 
 def ft_cache_resize(h, new_slots) -> None:

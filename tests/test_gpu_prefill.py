@@ -79,3 +79,20 @@ def test_prefill_rejects_small_pool():
         with pytest.raises(r.F.FtError) as e:
             r.F.ft_moe_prefill_chunk(r.h, 0, 8, x, z, o)
         assert e.value.status == r.F.FT_ERR_CAPACITY
+
+
+def test_prefill_double_buffer_off_same_results():
+    """The ablation switch (second buffer off: each layer loads at its own call) changes
+    timing only: residency after every layer and every output row equal the oracle, and
+    the outputs equal those of the double-buffered run bit for bit."""
+    w = synth.prefill().with_(n_layers=4, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=40,
+                              prefill_tokens=200)
+    outs = {}
+    for overlap in (True, False):
+        with Run(w, max_prefill_tokens=256) as r:
+            r.F.ft_moe_set_prefill_overlap(r.h, overlap)
+            for l in range(w.n_layers):
+                outs[overlap, l] = prefill_step(r, 0, l, 200)
+            r.compare_state()
+    for l in range(w.n_layers):
+        np.testing.assert_array_equal(outs[True, l], outs[False, l])
