@@ -508,6 +508,8 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
             xa = torch.from_numpy(np.stack([synth.prefill_x(w, 1, l, Tm) for l in range(2)]).view(np.int16)).to(dev)
             za = torch.stack([torch.from_numpy(synth.prefill_logits(w, 1, l, Tm)) for l in range(L)]).to(dev)
             oa = torch.empty((Tm, H), dtype=torch.float32, device=dev)
+            for l in range(L):  # warm-up chunk at the largest size
+                F.ft_moe_prefill_chunk(h, l, Tm, xa[l % 2], za[l], oa)
             for Ta in abl_sizes:
                 tps = {}
                 for ov in (True, False):

@@ -50,6 +50,15 @@ __device__ __forceinline__ int split_q(int m, long long bp, long long bh, int ev
   return q < 0 ? 0 : (int)q;
 }
 
+constexpr int kTour = 16;  // victim lists up to this length take the warp tournament
+
+// Warp-wide minimum of a 64-bit key: high halves first, then the low halves that tie.
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+  const uint32_t hi = __reduce_min_sync(0xffffffffu, (uint32_t)(v >> 32));
+  const uint32_t lo = __reduce_min_sync(0xffffffffu, (uint32_t)(v >> 32) == hi ? (uint32_t)v : 0xffffffffu);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
 // Exclusive prefix sum of one value per thread over the block; *total gets the sum.
 __device__ __noinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_wsum, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -92,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ uint8_t s_fflag[kMaxE];           // expert of this layer filled in this step
   __shared__ uint32_t s_hist[kBins];
   __shared__ uint32_t s_wsum[kWarps + 1];
+  __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_err, s_clock, s_lo, s_hi;
   __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand, s_kk, s_done;
   __shared__ unsigned long long s_prefix;
@@ -209,95 +219,144 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   const int kcap = p.kcap;
   // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
   if (q > 0) {
-    // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
-    uint32_t lo = UINT_MAX, hi = 0;
-    int nc = 0;
-    for (int s = tid; s < S; s += kThreads) {
-      const uint32_t st = stv[s];
-      if (st < clock) {
-        lo = min(lo, st);
-        hi = max(hi, st);
-        ++nc;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-      nc += __shfl_xor_sync(0xffffffffu, nc, o);
-    }
-    if (lane == 0) {
-      atomicMin(&s_lo, lo);
-      atomicMax(&s_hi, hi);
-      atomicAdd(&s_ncand, nc);
-    }
-    __syncthreads();
-    const uint32_t st_lo = s_lo;
-    const int ncand = s_ncand;
-    const int want = min(kcap, ncand);
     const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
-    const uint32_t range = s_hi - st_lo;
-    const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
-    // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
-    unsigned long long thresh = ~0ull;
-    if (want < ncand) {
-      // radix select of the want-th smallest key, most significant digit first.  Digits are
-      // taken from the top of the key's actual width, so the first pass spreads the keys
-      // over all kBins bins (few shared-memory atomics collide).
-      if (tid == 0) {
-        s_prefix = 0;
-        s_kk = want;
-      }
-      for (int hi_bit = width; hi_bit > 0;) {
-        const int shift = hi_bit > kDigit ? hi_bit - kDigit : 0;
-        const int dbits = hi_bit - shift;
-        s_hist[tid] = 0;
-        __syncthreads();
-        const unsigned long long pre = s_prefix;
-        for (int s = tid; s < S; s += kThreads) {
-          const uint32_t st = stv[s];
-          if (st >= clock) continue;
-          const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
-          if ((key >> hi_bit) == pre) atomicAdd(&s_hist[(key >> shift) & ((1u << dbits) - 1u)], 1u);
+    if (in_smem && kcap <= kTour) {
+      // Small K (batch 1-2): two-level tournament on keys (stamp, slot).  Each warp takes
+      // its K smallest keys in K rounds of a warp-wide minimum, then warp 0 takes the K
+      // smallest of those; the victims come out in ascending order.  Two block barriers.
+      const int nit = S > tid ? (S - tid + kThreads - 1) / kThreads : 0;  // slots tid + j*kThreads
+      uint32_t taken = 0;
+      int r = 0;
+      for (; r < kcap; ++r) {
+        unsigned long long mk = ~0ull;
+        int mj = 0;
+        for (int j = 0; j < nit; ++j) {
+          const int sl = tid + j * kThreads;
+          const uint32_t st = s_stamp[sl];
+          const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
+          if (!((taken >> j) & 1u) && st < clock && key < mk) {
+            mk = key;
+            mj = j;
+          }
         }
-        __syncthreads();
-        const uint32_t h = s_hist[tid];
-        const uint32_t kk = (uint32_t)s_kk;
-        uint32_t total;
-        const uint32_t excl = block_excl_scan(h, s_wsum, &total);
-        if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
-          s_prefix = (pre << dbits) | (unsigned long long)tid;
-          s_kk = (int)(kk - excl);
-          s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
-        }
-        __syncthreads();
-        if (s_done || shift == 0) {
-          thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
-          break;
-        }
-        hi_bit = shift;
+        const unsigned long long win = warp_min_u64(mk);
+        if (win == ~0ull) break;
+        if (mk == win) taken |= 1u << mj;
+        if (lane == 0) s_vkeys[warp * kTour + r] = win;
       }
-    }
-    // collect the `want` smallest keys (keys are unique), then order them
-    for (int s = tid; s < S; s += kThreads) {
-      const uint32_t st = stv[s];
-      if (st >= clock) continue;
-      const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
-      if (key <= thresh) {
-        const int i = atomicAdd(&s_nv, 1);
-        if (i < kMaxE) s_vkeys[i] = key;
+      if (lane == 0) s_wcnt[warp] = r;
+      __syncthreads();
+      if (warp == 0) {
+        taken = 0;
+        int nv = 0;
+        for (; nv < kcap; ++nv) {
+          unsigned long long mk = ~0ull;
+          int mj = 0;
+          for (int j = 0; j < kWarps * kTour / 32; ++j) {
+            const int it = lane + 32 * j, w = it / kTour, rr = it - w * kTour;
+            if (rr < s_wcnt[w] && !((taken >> j) & 1u) && s_vkeys[it] < mk) {
+              mk = s_vkeys[it];
+              mj = j;
+            }
+          }
+          const unsigned long long win = warp_min_u64(mk);
+          if (win == ~0ull) break;
+          if (mk == win) taken |= 1u << mj;
+          if (lane == 0) s_victims[nv] = (int)(win & ((1ull << sbits) - 1ull));
+        }
+        if (lane == 0) s_nv = nv;
       }
+      __syncthreads();
+    } else {
+      // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
+      uint32_t lo = UINT_MAX, hi = 0;
+      int nc = 0;
+      for (int s = tid; s < S; s += kThreads) {
+        const uint32_t st = stv[s];
+        if (st < clock) {
+          lo = min(lo, st);
+          hi = max(hi, st);
+          ++nc;
+        }
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        nc += __shfl_xor_sync(0xffffffffu, nc, o);
+      }
+      if (lane == 0) {
+        atomicMin(&s_lo, lo);
+        atomicMax(&s_hi, hi);
+        atomicAdd(&s_ncand, nc);
+      }
+      __syncthreads();
+      const uint32_t st_lo = s_lo;
+      const int ncand = s_ncand;
+      const int want = min(kcap, ncand);
+      const uint32_t range = s_hi - st_lo;
+      const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
+      // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
+      unsigned long long thresh = ~0ull;
+      if (want < ncand) {
+        // radix select of the want-th smallest key, most significant digit first.  Digits are
+        // taken from the top of the key's actual width, so the first pass spreads the keys
+        // over all kBins bins (few shared-memory atomics collide).
+        if (tid == 0) {
+          s_prefix = 0;
+          s_kk = want;
+        }
+        for (int hi_bit = width; hi_bit > 0;) {
+          const int shift = hi_bit > kDigit ? hi_bit - kDigit : 0;
+          const int dbits = hi_bit - shift;
+          s_hist[tid] = 0;
+          __syncthreads();
+          const unsigned long long pre = s_prefix;
+          for (int s = tid; s < S; s += kThreads) {
+            const uint32_t st = stv[s];
+            if (st >= clock) continue;
+            const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+            if ((key >> hi_bit) == pre) atomicAdd(&s_hist[(key >> shift) & ((1u << dbits) - 1u)], 1u);
+          }
+          __syncthreads();
+          const uint32_t h = s_hist[tid];
+          const uint32_t kk = (uint32_t)s_kk;
+          uint32_t total;
+          const uint32_t excl = block_excl_scan(h, s_wsum, &total);
+          if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
+            s_prefix = (pre << dbits) | (unsigned long long)tid;
+            s_kk = (int)(kk - excl);
+            s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
+          }
+          __syncthreads();
+          if (s_done || shift == 0) {
+            thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
+            break;
+          }
+          hi_bit = shift;
+        }
+      }
+      // collect the `want` smallest keys (keys are unique), then order them
+      for (int s = tid; s < S; s += kThreads) {
+        const uint32_t st = stv[s];
+        if (st >= clock) continue;
+        const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+        if (key <= thresh) {
+          const int i = atomicAdd(&s_nv, 1);
+          if (i < kMaxE) s_vkeys[i] = key;
+        }
+      }
+      __syncthreads();
+      const int nv = min(s_nv, want);
+      const unsigned long long smask = (1ull << sbits) - 1ull;
+      for (int i = tid; i < nv; i += kThreads) {
+        const unsigned long long ki = s_vkeys[i];
+        int rank = 0;
+        for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
+        s_victims[rank] = (int)(ki & smask);
+      }
+      __syncthreads();
+      if (tid == 0) s_nv = nv;
     }
-    __syncthreads();
-    const int nv = min(s_nv, want);
-    const unsigned long long smask = (1ull << sbits) - 1ull;
-    for (int i = tid; i < nv; i += kThreads) {
-      const unsigned long long ki = s_vkeys[i];
-      int rank = 0;
-      for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
-      s_victims[rank] = (int)(ki & smask);
-    }
-    __syncthreads();
-    if (tid == 0) s_nv = nv;
 
     // ---- 4. install F = first q misses into the first q victims
     for (int i = tid; i < q; i += kThreads) {
