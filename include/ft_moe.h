@@ -163,6 +163,23 @@ typedef struct {
 ft_status ft_moe_init(const ft_moe_config* cfg, const ft_banks* host_pool, const ft_banks* shared,
                       ft_moe** out);
 
+/* In-step host evaluation of the C set ([FT] "Device-side 缓存控制": the host branch of a
+ * layer-step runs inside the step, and only its result joins the GPU's).  When a hook is
+ * set, every decode layer-step enqueues after its control kernel: a copy of the step's
+ * routing (sel, gates and slot_of_pair, where FT_CPU marks the C pairs) into pinned host
+ * memory, a call of the hook in stream order (cudaLaunchHostFunc, on a driver thread;
+ * graph-capturable as a host node), and a copy of the rows the hook wrote back to the
+ * device, which then serve as the step's c_partial (the c_partial argument is ignored and
+ * may be NULL).  The hook must write rows[(t*top_k + r)*H .. +H) = gate-weighted expert
+ * output for every pair with slot_of_pair[t*top_k + r] == FT_CPU, may leave other rows
+ * unwritten, and must not call CUDA.  Arrays are [batch*top_k] and [batch*top_k*H],
+ * row-major; they stay valid only during the call.  The library itself executes no expert
+ * arithmetic on the host.  fn = NULL removes the hook.  Errors: FT_ERR_INVALID (null
+ * handle), FT_ERR_STATE (called while a graph of this handle is being captured). */
+typedef void (*ft_host_hook)(void* user, int layer, int batch, const int32_t* sel, const float* gates,
+                             const int32_t* slot_of_pair, float* rows);
+ft_status ft_moe_set_host_hook(ft_moe* h, ft_host_hook fn, void* user);
+
 /* One decode layer-step ([FT] "执行顺序与工程细节", "Device-side 缓存控制").
  *   layer     0 <= layer < L
  *   batch     1 <= batch <= max_batch tokens

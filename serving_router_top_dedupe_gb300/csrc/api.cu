@@ -74,6 +74,12 @@ struct ft_moe {
   cudaStream_t cs = nullptr, ts = nullptr;
   bool own_cs = false, own_ts = false;
   bool pf_overlap = true;  // prefill double buffer on
+  // in-step host hook for the C set: pinned staging of routing and rows, device rows
+  ft_host_hook hook = nullptr;
+  void* hook_user = nullptr;
+  int32_t *hk_sel = nullptr, *hk_slot = nullptr;
+  float *hk_gates = nullptr, *hk_rows = nullptr, *hk_rows_dev = nullptr;
+  std::vector<std::pair<ft_moe*, std::pair<int, int>>> hook_ctx;  // (handle, (layer, batch)), stable
   ft::SlotLayout lay{};
   int S = 0, L = 0, E = 0, K = 0, H = 0, I = 0, kcap = 0;
   long long bp_mbs = 0, bh_mbs = 0;
@@ -269,6 +275,12 @@ ft_status alloc_work(ft_moe* h) {
 }
 
 // Enqueue one decode layer-step (control -> fill -> gate/up -> down+combine).
+void CUDART_CB host_hook_call(void* arg) {
+  auto* c = static_cast<std::pair<ft_moe*, std::pair<int, int>>*>(arg);
+  ft_moe* h = c->first;
+  if (h->hook) h->hook(h->hook_user, c->second.first, c->second.second, h->hk_sel, h->hk_gates, h->hk_slot, h->hk_rows);
+}
+
 ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const float* logits,
                         const float* cpart, float* out, float* rows_out) {
   cudaStream_t cs = h->cs, ts = h->ts;
@@ -301,6 +313,18 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   FT_CUDA(ft::launch_control(cp, cs));
   if ((s = prof_end(h, 0, cs, pa)) != FT_OK) return s;
 
+  // in-step host branch for the C set: routing out, hook, rows back (stream order)
+  const bool hooked = h->hook != nullptr;
+  if (hooked) {
+    const size_t np = (size_t)batch * h->K;
+    FT_CUDA(cudaMemcpyAsync(h->hk_sel, h->w.sel, np * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    FT_CUDA(cudaMemcpyAsync(h->hk_gates, h->w.gates, np * sizeof(float), cudaMemcpyDeviceToHost, cs));
+    FT_CUDA(cudaMemcpyAsync(h->hk_slot, h->w.slot_of_pair, np * sizeof(int32_t), cudaMemcpyDeviceToHost, cs));
+    FT_CUDA(cudaLaunchHostFunc(cs, host_hook_call, &h->hook_ctx[(size_t)layer * (h->cfg.max_batch + 1) + batch]));
+    FT_CUDA(cudaMemcpyAsync(h->hk_rows_dev, h->hk_rows, np * h->H * sizeof(float), cudaMemcpyHostToDevice, cs));
+    cpart = h->hk_rows_dev;
+  }
+
   if (chain) {
     // fill kernel right after the control kernel on the compute stream
     ft::FillParams fp{};
@@ -310,7 +334,7 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
     fp.pool = h->pool;
     fp.lay = h->lay;
     fp.n_banks = h->n_banks;
-    fp.pdl = true;
+    fp.pdl = !hooked;  // after the host branch's copies the fill follows a plain dependency
     for (int j = 0; j < h->n_banks; ++j) {
       fp.src[j] = h->bank[j].dev;
       fp.src_row[j] = h->bank[j].row;
@@ -387,7 +411,7 @@ ft_status check_step(ft_moe* h, int layer, int batch, const void* x, const float
   if (layer < 0 || layer >= h->L) return fail(FT_ERR_INVALID, "layer %d out of range", layer);
   if (batch < 1 || batch > h->cfg.max_batch) return fail(FT_ERR_INVALID, "batch %d out of range", batch);
   if (!x || !logits || !out) return fail(FT_ERR_INVALID, "null x/logits/out");
-  if (!cpart && h->bh_mbs > h->bp_mbs)
+  if (!cpart && !h->hook && h->bh_mbs > h->bp_mbs)
     return fail(FT_ERR_INVALID, "c_partial may be NULL only when B_H <= B_P (every miss filled)");
   if (h->pf) ft::prefill_interrupt(h->pf);
   return FT_OK;
@@ -866,6 +890,29 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   return FT_OK;
 }
 
+ft_status ft_moe_set_host_hook(ft_moe* h, ft_host_hook fn, void* user) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "cannot change the host hook during capture");
+  FT_CUDA(cudaSetDevice(h->dev));
+  if (fn && !h->hk_sel) {
+    const size_t np = (size_t)h->cfg.max_batch * h->K;
+    FT_CUDA(cudaMallocHost(&h->hk_sel, np * sizeof(int32_t)));
+    FT_CUDA(cudaMallocHost(&h->hk_slot, np * sizeof(int32_t)));
+    FT_CUDA(cudaMallocHost(&h->hk_gates, np * sizeof(float)));
+    FT_CUDA(cudaMallocHost(&h->hk_rows, np * h->H * sizeof(float)));
+    FT_CUDA(cudaMalloc(&h->hk_rows_dev, np * h->H * sizeof(float)));
+    h->hook_ctx.resize((size_t)h->L * (h->cfg.max_batch + 1));
+    for (int l = 0; l < h->L; ++l)
+      for (int b = 0; b <= h->cfg.max_batch; ++b)
+        h->hook_ctx[(size_t)l * (h->cfg.max_batch + 1) + b] = {h, {l, b}};
+  }
+  const ft_status st = ft_moe_synchronize(h);  // no step of the old hook is in flight
+  if (st != FT_OK) return st;
+  h->hook = fn;
+  h->hook_user = user;
+  return FT_OK;
+}
+
 ft_status ft_moe_set_prefill_overlap(ft_moe* h, int on) {
   if (!h) return fail(FT_ERR_INVALID, "null handle");
   h->pf_overlap = on != 0;
@@ -976,6 +1023,11 @@ ft_status ft_moe_destroy(ft_moe* h) {
   if (h->shared_w) cudaFree(h->shared_w);
   if (h->counts_host) cudaFreeHost(h->counts_host);
   if (h->copy_host) cudaFreeHost(h->copy_host);
+  if (h->hk_sel) cudaFreeHost(h->hk_sel);
+  if (h->hk_slot) cudaFreeHost(h->hk_slot);
+  if (h->hk_gates) cudaFreeHost(h->hk_gates);
+  if (h->hk_rows) cudaFreeHost(h->hk_rows);
+  if (h->hk_rows_dev) cudaFree(h->hk_rows_dev);
   if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   if (h->ev_join) cudaEventDestroy(h->ev_join);
   if (h->ev_ctrl) cudaEventDestroy(h->ev_ctrl);

@@ -81,6 +81,7 @@ _SIGS = {
     "ft_graph_destroy": [_P],
     "ft_moe_prefill_chunk": [_P, C.c_int, C.c_int, _P, _P, _P],
     "ft_moe_set_prefill_overlap": [_P, C.c_int],
+    "ft_moe_set_host_hook": [_P, _P, _P],
     "ft_cache_resize": [_P, C.c_int],
     "ft_split_misses": [C.c_int, C.c_double, C.c_double, C.c_int, C.POINTER(C.c_int)],
     "ft_bench_bw": [C.c_size_t, C.c_int, C.POINTER(C.c_double)],
@@ -136,6 +137,7 @@ def ft_moe_init(cfg: ft_moe_config, host_pool: dict, shared: dict | None = None)
     h = C.c_void_p()
     hp, sh = _banks(host_pool), _banks(shared)
     _check(_lib.ft_moe_init(C.byref(cfg), C.byref(hp), C.byref(sh) if sh is not None else None, C.byref(h)))
+    _hook_k[h.value], _hook_h[h.value] = cfg.top_k, cfg.hidden
     return h.value
 
 
@@ -173,6 +175,34 @@ def ft_graph_destroy(g) -> None:
 
 def ft_moe_prefill_chunk(h, layer, n_tokens, x_bf16, logits, out) -> None:
     _check(_lib.ft_moe_prefill_chunk(h, layer, n_tokens, _ptr(x_bf16), _ptr(logits), _ptr(out)))
+
+
+HOST_HOOK = C.CFUNCTYPE(None, C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_int32), C.POINTER(C.c_float),
+                        C.POINTER(C.c_int32), C.POINTER(C.c_float))
+_hooks = {}  # handle -> callback object, kept alive while registered
+
+
+def ft_moe_set_host_hook(h, fn) -> None:
+    """fn(layer, batch, sel[B*k], gates[B*k], slot_of_pair[B*k], rows[B*k*H]) with numpy views;
+    it must fill the rows of the pairs whose slot is FT_CPU.  None removes the hook.  The
+    hook runs on a CUDA driver thread: callers that wait for the stream must release the
+    interpreter lock while they wait (ft_moe_synchronize and the other calls here do)."""
+    if fn is None:
+        _check(_lib.ft_moe_set_host_hook(h, None, None))
+        _hooks.pop(h, None)
+        return
+
+    def tramp(_user, layer, batch, sel, gates, slot, rows):
+        n = batch * _hook_k[h]
+        fn(layer, batch, np.ctypeslib.as_array(sel, (n,)), np.ctypeslib.as_array(gates, (n,)),
+           np.ctypeslib.as_array(slot, (n,)), np.ctypeslib.as_array(rows, (n, _hook_h[h])))
+
+    cb = HOST_HOOK(tramp)
+    _check(_lib.ft_moe_set_host_hook(h, C.cast(cb, C.c_void_p), None))
+    _hooks[h] = cb
+
+
+_hook_k, _hook_h = {}, {}
 
 
 def ft_moe_set_prefill_overlap(h, on: bool) -> None:

@@ -189,3 +189,87 @@ def test_resize_shrink_and_grow_match_oracle():
                 for l in range(w.n_layers):
                     r.step(s, l, tr, check_out=True)
             r.compare_state()
+
+
+def test_host_hook_evaluates_the_c_set_in_step():
+    """The in-step host branch: the hook sees the step's routing, computes the C pairs'
+    rows (here with the float64 oracle) and the library folds them in.  Decisions match the
+    oracle, outputs match the oracle, and they equal bit for bit a run that passes the same
+    rows through c_partial; the same holds for a graph replay with the hook as a host node."""
+    import oracle as O
+
+    w = synth.decode_bf16().with_(n_layers=2, n_experts=64, steps=6, cache_slots=12)
+    tr = synth.routing_trace(w, steps=w.steps + 3)  # 3 more tokens for the graph replays
+    pool = synth.ExpertPool(w)
+    banks, shared = pool.routed_banks(), pool.shared_banks()
+    seen = []
+
+    def rows_for(layer, xb, sel, gates, slot):
+        cp = np.zeros((w.batch, w.top_k, w.hidden), dtype=np.float32)
+        for t in range(w.batch):
+            for r in range(w.top_k):
+                if slot[t, r] < 0:
+                    cp[t, r] = O.pair_row(pool.expert(layer * w.n_experts + int(sel[t, r])),
+                                          O.bf16_to_f64(xb[t]), gates[t, r], False).astype(np.float32)
+        return cp
+
+    with Run(w, banks, shared) as hooked, Run(w, banks, shared) as plain:
+        F = hooked.F
+        xcur, hook_rows = {}, {}
+
+        def hook(layer, batch, sel, gates, slot, rows):
+            k = w.top_k
+            cp = rows_for(layer, xcur[layer], sel.reshape(batch, k), gates.reshape(batch, k), slot.reshape(batch, k))
+            rows.reshape(batch, k, w.hidden)[:] = cp
+            hook_rows[layer] = cp
+            seen.append((layer, int((slot < 0).sum())))
+
+        F.ft_moe_set_host_hook(hooked.h, hook)
+        dev = torch.device("cuda:0")
+        for s in range(w.steps):
+            for l in range(w.n_layers):
+                xb, z = hooked.inputs(s, l, tr)
+                xcur[l] = xb
+                sel, gates = O.route(z, w.top_k)
+                rec = hooked.sim.decode_step(l, w.n_experts, sel, hooked.bp, hooked.bh)
+                x_d = torch.from_numpy(xb.view(np.int16)).to(dev)
+                z_d = torch.from_numpy(z).to(dev)
+                out_d = torch.empty((w.batch, w.hidden), dtype=torch.float32, device=dev)
+                F.ft_moe_decode_step(hooked.h, l, w.batch, x_d, z_d, None, out_d)
+                F.ft_moe_synchronize(hooked.h)  # the hook runs while this call waits
+                gt = F.ft_moe_get_step_trace(hooked.h, w.batch, w.top_k, hooked.kcap)
+                hooked.compare(rec, sel, gates, gt)
+                cp = rows_for(l, xb, sel, gates, rec.slot_of_pair)
+                ref = O.decode_layer_outputs(rec, sel, gates, xb, cp, hooked.expert, shared=hooked.shared_expert(l),
+                                             n_experts=w.n_experts)
+                out = out_d.cpu().numpy()
+                assert O.rel_err_rows(out, ref) <= 1e-2
+                # the hook computed its rows from the device's gates: pass exactly those rows
+                _, _, out_p, _ = plain.step(s, l, tr, cpart=hook_rows[l])
+                np.testing.assert_array_equal(out, out_p)
+        hooked.compare_state()
+        assert any(n > 0 for _, n in seen)
+
+        # a graph with the hook as a host node, replayed for the next steps
+        L, B, H, E, k = w.n_layers, w.batch, w.hidden, w.n_experts, w.top_k
+        x = torch.empty((L, B, H), dtype=torch.int16, device=dev)
+        z = torch.empty((L, B, E), dtype=torch.float32, device=dev)
+        outg = torch.empty((L, B, H), dtype=torch.float32, device=dev)
+        g = F.ft_moe_graph_capture_decode(hooked.h, 0, L, B, x, z, None, outg)
+        for s in range(w.steps, w.steps + 3):
+            for l in range(L):
+                xb, zz = hooked.inputs(s, l, tr)
+                xcur[l] = xb
+                x[l].copy_(torch.from_numpy(xb.view(np.int16)))
+                z[l].copy_(torch.from_numpy(zz))
+            F.ft_graph_launch(g)
+            F.ft_moe_synchronize(hooked.h)
+            for l in range(L):
+                xb, zz = hooked.inputs(s, l, tr)
+                sel, gates = O.route(zz, k)
+                rec = hooked.sim.decode_step(l, E, sel, hooked.bp, hooked.bh)
+                _, _, out_p, _ = plain.step(s, l, tr, cpart=hook_rows[l])
+                np.testing.assert_array_equal(outg[l].cpu().numpy(), out_p)
+        hooked.compare_state()
+        F.ft_graph_destroy(g)
+        F.ft_moe_set_host_hook(hooked.h, None)

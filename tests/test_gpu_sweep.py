@@ -42,7 +42,7 @@ def test_sweep_points_identical_outputs(sweep_pool, batch):
     base = synth.sweep_point(batch, 1.0, synth.SWEEP_RATIOS[0]).with_(n_layers=LAYERS, steps=steps)
     tr = synth.routing_trace(base)
     # reference: everything resident and every miss filled (B_P > B_H), so no host pairs
-    ref = base.with_(cache_slots=base.n_logical, bp_gbps=80.0, bh_gbps=50.0)
+    ref = base.with_(cache_slots=base.n_logical, bp_gbps=80.0, bh_gbps=50.0)  # 100% of the 2-layer pool
     rows, outs = {}, {}
     with Run(ref, banks, shared) as r:
         for s in range(steps):
@@ -54,7 +54,8 @@ def test_sweep_points_identical_outputs(sweep_pool, batch):
     table = []
     for cap in synth.SWEEP_CAPACITIES:
         for ratio in synth.SWEEP_RATIOS:
-            w = synth.sweep_point(batch, cap, ratio).with_(n_layers=LAYERS, steps=steps)
+            w = synth.sweep_point(batch, cap, ratio).with_(
+                n_layers=LAYERS, steps=steps, cache_slots=synth.capacity_slots(cap, LAYERS, base.n_experts))
             with Run(w, banks, shared) as r:
                 for s in range(steps):
                     for l in range(LAYERS):
