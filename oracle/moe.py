@@ -21,6 +21,8 @@ design notes with its reason):
   * One global clock ticks once per layer-step; LRU ties break by slot index.
   * The C set leaves residency and recency untouched.
   * Router gates are a softmax over the k selected logits; ties pick the lower id.
+    Two other gate functions (softmax over all E, normalised sigmoid) are
+    written out for routers that use them.
   * FP8 blocks are 1x128 along the reduction dimension of each output row.
   * The output sums, per token, the shared expert first and then the k pair
     rows in ascending expert id.
@@ -68,13 +70,27 @@ def split_misses(m: int, bp_mbs: int, bh_mbs: int, evictable: int) -> int:
 
 
 # ===================================================================== router
-def route(logits: np.ndarray, k: int):
-    """Top-k router with softmax gates.
+GATE_SOFTMAX_TOPK = 0   # softmax over the k chosen logits
+GATE_SOFTMAX_ALL = 1    # softmax over all E logits; the k chosen probabilities as they are
+GATE_SIGMOID_TOPK = 2   # sigmoid of each chosen logit, normalised to sum 1 over the k
+
+
+def route(logits: np.ndarray, k: int, gate_mode: int = GATE_SOFTMAX_TOPK):
+    """Top-k router.
 
     For each token the k experts with the largest logits are chosen (equal
-    logits: the lower expert id first), listed in ascending expert id; the
-    gates are a softmax over those k logits, computed in float64 and stored
-    as float32.  [FT, "Device-side 缓存控制"] (routing precedes dedupe).
+    logits: the lower expert id first), listed in ascending expert id.
+    [FT, "Device-side 缓存控制"] (routing precedes dedupe).  The gate function
+    is the router's own, which the pages do not print for the models they name
+    (Qwen3.6-35B-A3B, DeepSeek-V4-Flash [FT2, opening paragraph]); three
+    textbook forms are written out, each in float64 and stored as float32:
+
+      GATE_SOFTMAX_TOPK:  g_r = exp(z_r) / sum_{j chosen} exp(z_j)
+      GATE_SOFTMAX_ALL:   g_r = exp(z_r) / sum_{j < E} exp(z_j)
+      GATE_SIGMOID_TOPK:  g_r = s(z_r) / sum_{j chosen} s(z_j),  s(z) = 1 / (1 + exp(-z))
+
+    The softmax exponentials are shifted by the largest logit (an exact identity).
+    All three gate functions are increasing in z, so the choice is the same.
     """
     B, E = logits.shape
     sel = np.empty((B, k), dtype=np.int64)
@@ -85,10 +101,29 @@ def route(logits: np.ndarray, k: int):
         order = np.lexsort((ids, -z))          # primary: logit desc; secondary: id asc
         chosen = np.sort(order[:k])
         zs = z[chosen]
-        w = np.exp(zs - zs.max())
+        if gate_mode == GATE_SOFTMAX_TOPK:
+            w = np.exp(zs - zs.max())
+            g = w / w.sum()
+        elif gate_mode == GATE_SOFTMAX_ALL:
+            w = np.exp(z - z.max())
+            g = w[chosen] / w.sum()
+        elif gate_mode == GATE_SIGMOID_TOPK:
+            s = 1.0 / (1.0 + np.exp(-zs))
+            g = s / s.sum()
+        else:
+            raise ValueError(f"unknown gate mode {gate_mode}")
         sel[t] = chosen
-        gates[t] = (w / w.sum()).astype(np.float32)
+        gates[t] = g.astype(np.float32)
     return sel, gates
+
+
+def router_logits(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """Router logits z[t, e] = sum_h x[t, h] * W_router[e, h], float64 over the
+    decoded BF16 values.  x_bits: uint16 [B, H]; w_bits: uint16 [E, H].  The
+    router is the layer's gate projection, run on the GPU with the rest of the
+    control path ([FT2], decode paragraph: the GPU router dedupes the active
+    experts; [P3] §3.3: gate and sort run locally on each GPU)."""
+    return bf16_to_f64(x_bits) @ bf16_to_f64(w_bits).T
 
 
 def dedupe(sel: np.ndarray, layer: int, n_experts: int) -> list[int]:

@@ -110,6 +110,80 @@ def test_router_ties_pick_lower_id_brute_force():
         assert np.allclose(gates[0], np.array(w) / sum(w), rtol=1e-6)
 
 
+def test_router_gate_functions_match_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    for B, E, k in [(1, 16, 2), (8, 256, 8), (5, 40, 7)]:
+        z = (rng.standard_normal((B, E)) * 3).astype(np.float32)
+        tz = torch.from_numpy(z).double()
+        sel0, _ = O.route(z, k)
+        idx = torch.from_numpy(sel0)
+        sel1, g1 = O.route(z, k, O.GATE_SOFTMAX_ALL)
+        sel2, g2 = O.route(z, k, O.GATE_SIGMOID_TOPK)
+        assert np.array_equal(sel1, sel0) and np.array_equal(sel2, sel0)
+        ref1 = torch.gather(torch.softmax(tz, dim=1), 1, idx)
+        s = torch.gather(torch.sigmoid(tz), 1, idx)
+        ref2 = s / s.sum(dim=1, keepdim=True)
+        np.testing.assert_allclose(g1, ref1.float().numpy(), rtol=1e-6, atol=0)
+        np.testing.assert_allclose(g2, ref2.float().numpy(), rtol=1e-6, atol=0)
+
+
+def test_router_gate_functions_brute_force_and_closed_forms():
+    rng = random.Random(13)
+    for _ in range(100):
+        E = rng.randint(2, 20)
+        k = rng.randint(1, E)
+        z = np.array([rng.uniform(-6, 6) for _ in range(E)], dtype=np.float32)
+        ranked = sorted(range(E), key=lambda e: (-float(z[e]), e))
+        chosen = sorted(ranked[:k])
+        ex = [math.exp(float(v)) for v in z]
+        sg = [1.0 / (1.0 + math.exp(-float(v))) for v in z]
+        _, g1 = O.route(z[None, :], k, O.GATE_SOFTMAX_ALL)
+        _, g2 = O.route(z[None, :], k, O.GATE_SIGMOID_TOPK)
+        assert np.allclose(g1[0], [ex[e] / sum(ex) for e in chosen], rtol=1e-6)
+        assert np.allclose(g2[0], [sg[e] / sum(sg[j] for j in chosen) for e in chosen], rtol=1e-6)
+        # softmax over all E is the top-k softmax scaled by the chosen experts' share of the mass
+        _, g0 = O.route(z[None, :], k)
+        share = sum(ex[e] for e in chosen) / sum(ex)
+        assert np.allclose(g1[0], g0[0] * share, rtol=1e-6)
+    # two experts with opposite logits: s(a) + s(-a) = 1, so the normalised sigmoid gate is s(a)
+    for a in (0.25, 1.0, 3.0):
+        _, g = O.route(np.array([[a, -a]], dtype=np.float32), 2, O.GATE_SIGMOID_TOPK)
+        assert abs(float(g[0, 0]) - 1.0 / (1.0 + math.exp(-a))) < 1e-7
+    # k = E: softmax over all E and over the k chosen coincide
+    z = np.array([[0.5, -1.0, 2.0, 0.0]], dtype=np.float32)
+    assert np.array_equal(O.route(z, 4, O.GATE_SOFTMAX_ALL)[1], O.route(z, 4)[1])
+
+
+def _bf16_bits(v: np.ndarray) -> np.ndarray:
+    """float32 values that are exact in BF16 -> their BF16 bit patterns"""
+    b = np.asarray(v, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0)
+    return (b >> 16).astype(np.uint16)
+
+
+def test_router_logits_brute_force_and_closed_forms():
+    rng = np.random.default_rng(17)
+    B, E, H = 3, 5, 24
+    # small integers and halves are exact in BF16
+    x = rng.integers(-8, 9, size=(B, H)).astype(np.float32) / 2
+    w = rng.integers(-8, 9, size=(E, H)).astype(np.float32) / 4
+    z = O.router_logits(_bf16_bits(x), _bf16_bits(w))
+    assert z.shape == (B, E)
+    for t in range(B):
+        for e in range(E):
+            assert z[t, e] == sum(float(x[t, h]) * float(w[e, h]) for h in range(H))
+    # one-hot router rows pick single hidden coordinates
+    eye = np.zeros((E, H), dtype=np.float32)
+    for e in range(E):
+        eye[e, 3 * e + 1] = 1.0
+    ze = O.router_logits(_bf16_bits(x), _bf16_bits(eye))
+    assert np.array_equal(ze, x[:, [3 * e + 1 for e in range(E)]].astype(np.float64))
+    # a router row equal to the token gives its squared norm
+    zs = O.router_logits(_bf16_bits(x[:1]), _bf16_bits(x))
+    assert zs[0, 0] == float(np.dot(x[0].astype(np.float64), x[0].astype(np.float64)))
+
+
 def test_dedupe_is_sorted_union():
     sel = np.array([[3, 5], [1, 5], [3, 9]])
     assert O.dedupe(sel, 2, 16) == [33, 35, 37, 41]
