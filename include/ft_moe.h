@@ -10,7 +10,7 @@
  *  - A slot pool in HBM holds whole experts; one global LRU over all MoE layers,
  *    addressed by the logical id u = layer*E + expert ([FT] "语义感知专家缓存",
  *    [FT] "FTW 权重格式与平台适配").
- *  - Per decode layer-step, one control kernel routes (top-k softmax), dedupes the
+ *  - Per decode layer-step, one control kernel routes (top-k and gates), dedupes the
  *    batch's experts, classifies hits/misses against the residency table, computes
  *    the fill count q, finds the K least recently used victims in one pass and
  *    rewrites routed ids to slots or FT_CPU ([FT] "Device-side 缓存控制").
@@ -134,7 +134,7 @@ typedef struct {
   int layer, batch, q, n_active, n_hit, n_miss, n_victims, n_cpu;
   uint32_t clock;
   int32_t* sel;          /* [batch*top_k] expert ids, ascending per token */
-  float* gates;          /* [batch*top_k] softmax over the token's k logits */
+  float* gates;          /* [batch*top_k] gates (ft_gate of ft_moe_set_router) */
   int32_t* slot_of_pair; /* [batch*top_k] slot id, or FT_CPU */
   int32_t* active;       /* [K] A: sorted unique logical ids */
   int32_t* hit;          /* [K] H, ascending */
@@ -144,11 +144,11 @@ typedef struct {
 
 /* Per-kernel CUDA-event timing collected while profiling is on. */
 typedef struct {
-  uint64_t launches[9];  /* 0 control, 1 fill, 2 gemv phase 1 (gate/up), 3 gemv phase 2 (down)
+  uint64_t launches[10]; /* 0 control, 1 fill, 2 gemv phase 1 (gate/up), 3 gemv phase 2 (down)
                             + combine, 4 prefill routing (route, scan, place), 5 prefill grouped
                             GEMM gate/up + SwiGLU, 6 prefill combine, 7 prefill layer copy,
-                            8 prefill grouped GEMM down + gate weighting */
-  double total_ms[9];
+                            8 prefill grouped GEMM down + gate weighting, 9 router logits */
+  double total_ms[10];
 } ft_profile;
 
 /* Create the library state: allocates the slot pool (S * slot bytes) and the work
@@ -237,6 +237,49 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
  * are identical either way.  Takes effect at the next prefill call.
  * Errors: FT_ERR_INVALID (null handle). */
 ft_status ft_moe_set_prefill_overlap(ft_moe* h, int on);
+
+/* Gate functions of the router: how the k chosen logits of a token become its gates.
+ * The choice itself is always the k largest logits (equal logits: lower expert id).
+ *   FT_GATE_SOFTMAX_TOPK  g_r = exp(z_r) / sum over the k chosen of exp(z_j)  (default)
+ *   FT_GATE_SOFTMAX_ALL   g_r = exp(z_r) / sum over all E experts of exp(z_j)  (not renormalised)
+ *   FT_GATE_SIGMOID_TOPK  g_r = s(z_r) / sum over the k chosen of s(z_j),  s = logistic sigmoid */
+typedef enum { FT_GATE_SOFTMAX_TOPK = 0, FT_GATE_SOFTMAX_ALL = 1, FT_GATE_SIGMOID_TOPK = 2 } ft_gate;
+
+/* Router of the layers, for the calls that take hidden states instead of logits ([FT2]
+ * decode paragraph: the GPU router dedupes the layer's active experts; [P3] §3.3: gate and
+ * sort run on the GPU).
+ *   w_router_bf16  host [L][E][H] BF16: row e of layer l gives logit e (z = x . row); copied
+ *                  into device memory owned by the library.  NULL keeps the weights
+ *                  already set (none at init).
+ *   gate           ft_gate; applies to every later decode and prefill call, with logits
+ *                  given or computed.
+ * Synchronises.  Errors: FT_ERR_INVALID (null handle, unknown gate), FT_ERR_STATE (called
+ * during a graph capture), FT_ERR_NOMEM, FT_ERR_CUDA. */
+ft_status ft_moe_set_router(ft_moe* h, const void* w_router_bf16, int gate);
+
+/* Router logits z[t][e] = sum_h x[t][h] * W_router[layer][e][h]: BF16 products accumulated
+ * in FP32 in a fixed order, so the same inputs give the same bits in every call, inside a
+ * decode step or not.
+ *   n_tokens    1 <= n <= max(max_batch, max_prefill_tokens)
+ *   x_bf16      dev [n][H] BF16, 16-byte aligned
+ *   logits_out  dev [n][E] FP32
+ * Enqueues on the compute stream.  Errors: FT_ERR_INVALID (arguments), FT_ERR_STATE (no
+ * router weights set). */
+ft_status ft_moe_router_logits(ft_moe* h, int layer, int n_tokens, const void* x_bf16, float* logits_out);
+
+/* ft_moe_decode_step with the router inside the step: a router kernel computes the
+ * logits from x (as ft_moe_router_logits) and the step continues on them, in the same
+ * chain of kernels and graph-capturable in the same way.
+ *   logits_out  optional dev [batch][E] FP32: receives the step's logits; NULL uses a
+ *               library buffer.
+ * Other arguments and errors as ft_moe_decode_step, plus FT_ERR_STATE (no router weights). */
+ft_status ft_moe_decode_step_hidden(ft_moe* h, int layer, int batch, const void* x_bf16, const float* c_partial,
+                                    float* out, float* rows_out, float* logits_out);
+
+/* ft_moe_prefill_chunk with the router inside the call: the chunk's logits are computed
+ * from x into a library buffer, then the layer proceeds as ft_moe_prefill_chunk.
+ * Errors as ft_moe_prefill_chunk, plus FT_ERR_STATE (no router weights). */
+ft_status ft_moe_prefill_chunk_hidden(ft_moe* h, int layer, int n_tokens, const void* x_bf16, float* out);
 
 /* Safe-point resize of the slot pool ([FT] "挑战三"; [FT2] paragraph on the memory
  * budget).  Growing adds empty slots.  Shrinking keeps the new_slots most recently

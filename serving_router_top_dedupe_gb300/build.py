@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "lib", "libftmoe.so")
-SOURCES = ["control.cu", "decode_eval.cu", "prefill.cu", "prefill_gemm.cu", "api.cu", "noalloc.cu", "decode_fused.cu"]
+SOURCES = ["control.cu", "decode_eval.cu", "prefill.cu", "prefill_gemm.cu", "api.cu", "noalloc.cu", "decode_fused.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr"]

@@ -74,6 +74,10 @@ struct ft_moe {
   cudaStream_t cs = nullptr, ts = nullptr;
   bool own_cs = false, own_ts = false;
   bool pf_overlap = true;  // prefill double buffer on
+  // router (hidden-state entry points): device weights [L][E][H], logits buffer
+  int gate = FT_GATE_SOFTMAX_TOPK;
+  uint16_t* router_w = nullptr;
+  float* router_z = nullptr;  // [max(max_batch, max_prefill_tokens)][E]
   // in-step host hook for the C set: pinned staging of routing and rows, device rows
   ft_host_hook hook = nullptr;
   void* hook_user = nullptr;
@@ -293,6 +297,7 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   cp.S = h->S;
   cp.kcap = std::min(batch * h->K, h->E);
   cp.has_shared = h->cfg.has_shared;
+  cp.gate = h->gate;
   cp.bp_mbs = h->bp_mbs;
   cp.bh_mbs = h->bh_mbs;
   cp.res = h->res;
@@ -402,6 +407,35 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
     FT_CUDA(ft::launch_down_combine(ep, h->cfg.wtype, h->grid_eval, cs));
     if ((s = prof_end(h, 3, cs, pa)) != FT_OK) return s;
   }
+  return FT_OK;
+}
+
+// Router kernel for n tokens of `layer` into z, on the compute stream.
+ft_status enqueue_router(ft_moe* h, int layer, int n, const void* x, float* z, bool pdl) {
+  ft::RouterParams rp{};
+  rp.x = static_cast<const uint16_t*>(x);
+  rp.w = h->router_w + (size_t)layer * h->E * h->H;
+  rp.z = z;
+  rp.T = n;
+  rp.E = h->E;
+  rp.H = h->H;
+  ft::router_shape(n, h->E, h->H, &rp.tok_tile, &rp.e_per_warp);
+  rp.pdl = pdl;
+  cudaEvent_t pa;
+  ft_status s;
+  if ((s = prof_begin(h, h->cs, &pa)) != FT_OK) return s;
+  FT_CUDA(ft::launch_router(rp, h->cs));
+  return prof_end(h, 9, h->cs, pa);
+}
+
+ft_status check_router(ft_moe* h, int layer, int n, const void* x) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (!h->router_w) return fail(FT_ERR_STATE, "no router weights: call ft_moe_set_router first");
+  if (layer < 0 || layer >= h->L) return fail(FT_ERR_INVALID, "layer %d out of range", layer);
+  const int nmax = std::max(h->cfg.max_batch, h->cfg.max_prefill_tokens);
+  if (n < 1 || n > nmax) return fail(FT_ERR_INVALID, "n_tokens %d outside [1, %d]", n, nmax);
+  if (!x) return fail(FT_ERR_INVALID, "null x");
+  if (reinterpret_cast<uintptr_t>(x) % 16) return fail(FT_ERR_INVALID, "x must be 16-byte aligned");
   return FT_OK;
 }
 
@@ -561,6 +595,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   FT_CUDA(cudaHostAlloc((void**)&h->copy_host, sizeof(int32_t) * 2 * h->kcap, cudaHostAllocDefault));
   FT_CUDA(ft::prepare_kernels(h->cfg.wtype, h->H, h->I));
   FT_CUDA(ft::prepare_control());
+  FT_CUDA(ft::prepare_router());
   FT_CUDA(cudaDeviceSynchronize());
   return FT_OK;
 }
@@ -597,6 +632,60 @@ ft_status ft_moe_decode_step(ft_moe* h, int layer, int batch, const void* x_bf16
     return fail(FT_ERR_STATE, "FT_FILL_MEMCPY steps cannot be captured into a graph");
   FT_CUDA(cudaSetDevice(h->dev));
   return enqueue_layer(h, layer, batch, x_bf16, logits, c_partial, out, rows_out);
+}
+
+ft_status ft_moe_set_router(ft_moe* h, const void* w_router_bf16, int gate) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (gate != FT_GATE_SOFTMAX_TOPK && gate != FT_GATE_SOFTMAX_ALL && gate != FT_GATE_SIGMOID_TOPK)
+    return fail(FT_ERR_INVALID, "unknown gate function %d", gate);
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "cannot change the router during capture");
+  FT_CUDA(cudaSetDevice(h->dev));
+  FT_CUDA(cudaStreamSynchronize(h->cs));
+  if (w_router_bf16) {
+    const size_t bytes = (size_t)h->L * h->E * h->H * sizeof(uint16_t);
+    if (!h->router_w) {
+      cudaError_t e = cudaMalloc(&h->router_w, bytes);
+      if (e != cudaSuccess) {
+        h->router_w = nullptr;
+        return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA, "router weights: %s",
+                    cudaGetErrorString(e));
+      }
+      const size_t zb = (size_t)std::max(h->cfg.max_batch, h->cfg.max_prefill_tokens) * h->E * sizeof(float);
+      e = cudaMalloc(&h->router_z, zb);
+      if (e != cudaSuccess) {
+        cudaFree(h->router_w);
+        h->router_w = nullptr;
+        h->router_z = nullptr;
+        return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA, "router logits: %s",
+                    cudaGetErrorString(e));
+      }
+    }
+    FT_CUDA(cudaMemcpy(h->router_w, w_router_bf16, bytes, cudaMemcpyHostToDevice));
+  }
+  h->gate = gate;
+  return FT_OK;
+}
+
+ft_status ft_moe_router_logits(ft_moe* h, int layer, int n_tokens, const void* x_bf16, float* logits_out) {
+  ft_status s = check_router(h, layer, n_tokens, x_bf16);
+  if (s != FT_OK) return s;
+  if (!logits_out) return fail(FT_ERR_INVALID, "null logits_out");
+  FT_CUDA(cudaSetDevice(h->dev));
+  return enqueue_router(h, layer, n_tokens, x_bf16, logits_out, false);
+}
+
+ft_status ft_moe_decode_step_hidden(ft_moe* h, int layer, int batch, const void* x_bf16, const float* c_partial,
+                                    float* out, float* rows_out, float* logits_out) {
+  ft_status s = check_router(h, layer, batch, x_bf16);
+  if (s != FT_OK) return s;
+  float* z = logits_out ? logits_out : h->router_z;
+  if ((s = check_step(h, layer, batch, x_bf16, z, c_partial, out)) != FT_OK) return s;
+  if (h->cfg.fill_mode == FT_FILL_MEMCPY && capturing(h->cs))
+    return fail(FT_ERR_STATE, "FT_FILL_MEMCPY steps cannot be captured into a graph");
+  FT_CUDA(cudaSetDevice(h->dev));
+  // the router joins the step's chain of programmatic dependents (kernel-fill mode)
+  if ((s = enqueue_router(h, layer, batch, x_bf16, z, h->cfg.fill_mode == FT_FILL_KERNEL)) != FT_OK) return s;
+  return enqueue_layer(h, layer, batch, x_bf16, z, c_partial, out, rows_out);
 }
 
 ft_status ft_moe_decode_layers(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_bf16,
@@ -876,6 +965,7 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   }
   c.prof = h->prof;
   c.overlap = h->pf_overlap;
+  c.gate = h->gate;
   if (!h->pf) {
     cudaError_t e = ft::prefill_create(&h->pf, c);
     if (e != cudaSuccess) return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA,
@@ -888,6 +978,22 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   for (auto& r : ev) h->prof_live.push_back({r.first, r.second.first, r.second.second});
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill layer %d: %s %s", layer, cudaGetErrorString(e), err.c_str());
   return FT_OK;
+}
+
+ft_status ft_moe_prefill_chunk_hidden(ft_moe* h, int layer, int n_tokens, const void* x_bf16, float* out) {
+  ft_status s = check_router(h, layer, n_tokens, x_bf16);
+  if (s != FT_OK) return s;
+  if (n_tokens > h->cfg.max_prefill_tokens)
+    return fail(FT_ERR_INVALID, "n_tokens %d above max_prefill_tokens=%d", n_tokens, h->cfg.max_prefill_tokens);
+  if (!out) return fail(FT_ERR_INVALID, "null out");
+  // the checks of ft_moe_prefill_chunk that do not depend on the logits, before any work
+  if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
+  if (h->S < 2 * h->E)
+    return fail(FT_ERR_CAPACITY, "prefill double buffering needs >= 2E = %d slots (have %d)", 2 * h->E, h->S);
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
+  FT_CUDA(cudaSetDevice(h->dev));
+  if ((s = enqueue_router(h, layer, n_tokens, x_bf16, h->router_z, false)) != FT_OK) return s;
+  return ft_moe_prefill_chunk(h, layer, n_tokens, x_bf16, h->router_z, out);
 }
 
 ft_status ft_moe_set_host_hook(ft_moe* h, ft_host_hook fn, void* user) {
@@ -1021,6 +1127,8 @@ ft_status ft_moe_destroy(ft_moe* h) {
   for (void* p : h->allocs) cudaFree(p);
   if (h->pool) cudaFree(h->pool);
   if (h->shared_w) cudaFree(h->shared_w);
+  if (h->router_w) cudaFree(h->router_w);
+  if (h->router_z) cudaFree(h->router_z);
   if (h->counts_host) cudaFreeHost(h->counts_host);
   if (h->copy_host) cudaFreeHost(h->copy_host);
   if (h->hk_sel) cudaFreeHost(h->hk_sel);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
 
   // ---- 1. route: one warp per token
   for (int t = warp; t < B; t += kWarps) {
-    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
+    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, p.gate, lane, &s_err, [&](int e, float g, int rank) {
       const int idx = t * k + rank;
       p.w.sel[idx] = e;
       p.w.gates[idx] = g;
@@ -220,54 +220,79 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
   if (q > 0) {
     const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
+    bool picked = false;
     if (in_smem && kcap <= kTour) {
-      // Small K (batch 1-2): two-level tournament on keys (stamp, slot).  Each warp takes
-      // its K smallest keys in K rounds of a warp-wide minimum, then warp 0 takes the K
-      // smallest of those; the victims come out in ascending order.  Two block barriers.
+      // Small K (batch 1-2).  Each thread's smallest key (stamp, slot) is found in one scan;
+      // the K-th smallest of those per-thread minima bounds the K-th smallest key overall,
+      // since they are K distinct keys.  A warp tournament over the minima finds that bound
+      // T, a second scan gathers every key <= T, and rank counting orders them.  A rare
+      // gather larger than the key buffer falls through to the radix select.
       const int nit = S > tid ? (S - tid + kThreads - 1) / kThreads : 0;  // slots tid + j*kThreads
-      uint32_t taken = 0;
+      unsigned long long mk = ~0ull;
+      for (int j = 0; j < nit; ++j) {
+        const int sl = tid + j * kThreads;
+        const uint32_t st = s_stamp[sl];
+        const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
+        if (st < clock && key < mk) mk = key;
+      }
       int r = 0;
-      for (; r < kcap; ++r) {
-        unsigned long long mk = ~0ull;
-        int mj = 0;
-        for (int j = 0; j < nit; ++j) {
-          const int sl = tid + j * kThreads;
-          const uint32_t st = s_stamp[sl];
-          const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
-          if (!((taken >> j) & 1u) && st < clock && key < mk) {
-            mk = key;
-            mj = j;
-          }
-        }
+      for (; r < kcap; ++r) {  // this warp's K smallest minima, ascending
         const unsigned long long win = warp_min_u64(mk);
         if (win == ~0ull) break;
-        if (mk == win) taken |= 1u << mj;
+        if (mk == win) mk = ~0ull;
         if (lane == 0) s_vkeys[warp * kTour + r] = win;
       }
       if (lane == 0) s_wcnt[warp] = r;
+      if (tid == 0) s_nv = 0;
       __syncthreads();
       if (warp == 0) {
-        taken = 0;
-        int nv = 0;
-        for (; nv < kcap; ++nv) {
-          unsigned long long mk = ~0ull;
+        uint32_t taken = 0;
+        unsigned long long kth = ~0ull - 1ull;  // fewer than K minima: every key qualifies
+        for (int n = 0; n < kcap; ++n) {
+          unsigned long long m2 = ~0ull;
           int mj = 0;
           for (int j = 0; j < kWarps * kTour / 32; ++j) {
             const int it = lane + 32 * j, w = it / kTour, rr = it - w * kTour;
-            if (rr < s_wcnt[w] && !((taken >> j) & 1u) && s_vkeys[it] < mk) {
-              mk = s_vkeys[it];
+            if (rr < s_wcnt[w] && !((taken >> j) & 1u) && s_vkeys[it] < m2) {
+              m2 = s_vkeys[it];
               mj = j;
             }
           }
-          const unsigned long long win = warp_min_u64(mk);
+          const unsigned long long win = warp_min_u64(m2);
           if (win == ~0ull) break;
-          if (mk == win) taken |= 1u << mj;
-          if (lane == 0) s_victims[nv] = (int)(win & ((1ull << sbits) - 1ull));
+          if (m2 == win) taken |= 1u << mj;
+          if (n == kcap - 1) kth = win;
         }
-        if (lane == 0) s_nv = nv;
+        if (lane == 0) s_prefix = kth;
       }
       __syncthreads();
-    } else {
+      const unsigned long long bound = s_prefix;
+      for (int j = 0; j < nit; ++j) {
+        const int sl = tid + j * kThreads;
+        const uint32_t st = s_stamp[sl];
+        const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
+        if (st < clock && key <= bound) {
+          const int i = atomicAdd(&s_nv, 1);
+          if (i < kMaxE) s_vkeys[i] = key;
+        }
+      }
+      __syncthreads();
+      const int nc = s_nv;
+      if (nc <= kMaxE) {
+        const unsigned long long smask = (1ull << sbits) - 1ull;
+        for (int i = tid; i < nc; i += kThreads) {
+          const unsigned long long ki = s_vkeys[i];
+          int rank = 0;
+          for (int j = 0; j < nc; ++j) rank += s_vkeys[j] < ki;
+          if (rank < kcap) s_victims[rank] = (int)(ki & smask);
+        }
+        picked = true;
+      }
+      __syncthreads();
+      if (tid == 0) s_nv = picked ? min(nc, kcap) : 0;
+      __syncthreads();
+    }
+    if (!picked) {
       // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
       uint32_t lo = UINT_MAX, hi = 0;
       int nc = 0;

@@ -74,6 +74,7 @@ SlotLayout make_layout(int wtype, int H, int I);
 struct CtrlParams {
   const float* logits;
   int B, E, k, layer, S, kcap, has_shared;
+  int gate;  // FT_GATE_*
   long long bp_mbs, bh_mbs;
   int32_t* res;
   int32_t* owner;
@@ -147,8 +148,23 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+struct RouterParams {
+  const uint16_t* x;  // [T][H] BF16 hidden states
+  const uint16_t* w;  // [E][H] BF16 router projection of the layer
+  float* z;           // [T][E] FP32 logits
+  int T, E, H;
+  int tok_tile;       // token rows staged per CTA
+  int e_per_warp;     // router rows per warp
+  bool pdl;
+};
+
 // Kernel launchers (stream-ordered, no synchronisation).
 cudaError_t launch_control(const CtrlParams& p, cudaStream_t s);
+// Router logits (router.cu): launch shape for T tokens, then the launch.
+void router_shape(int T, int E, int H, int* tok_tile, int* e_per_warp);
+size_t router_smem_bytes(int tok_tile, int H);
+cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
+cudaError_t prepare_router();
 // Raise the control kernel's shared-memory limit (call once per device, before capture).
 cudaError_t prepare_control();
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s);

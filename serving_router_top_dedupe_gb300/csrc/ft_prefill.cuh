@@ -23,6 +23,7 @@ struct PrefillCtx {
   size_t bank_row[3];
   bool prof;
   bool overlap;  // stream layer l+1 while layer l computes (the double buffer)
+  int gate;      // FT_GATE_*
 };
 
 // Arguments of the grouped GEMM (prefill_gemm.cu).  Entries 0..E-1 are the layer's

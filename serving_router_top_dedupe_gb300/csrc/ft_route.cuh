@@ -1,8 +1,11 @@
-// Per-token top-k softmax routing, shared by the decode control kernel and the
-// prefill router ("FreeToken 完全拆解", section "Device-side 缓存控制": routing
-// precedes dedupe).  One warp routes one token: the k largest logits (equal logits:
-// lower expert id first) are chosen, listed in ascending expert id, and their gates
-// are a softmax over those k logits.  NaN logits rank as -inf and raise `err`.
+// Per-token top-k routing, shared by the decode control kernel and the prefill router
+// ("FreeToken 完全拆解", section "Device-side 缓存控制": routing precedes dedupe).  One
+// warp routes one token: the k largest logits (equal logits: lower expert id first) are
+// chosen and listed in ascending expert id.  Their gates follow the router's gate
+// function (FT_GATE_*): a softmax over the k chosen logits, a softmax over all E logits
+// (not renormalised), or the chosen logits' sigmoids normalised to sum 1.  All three
+// increase with the logit, so the choice does not depend on the gate function.  NaN
+// logits rank as -inf and raise `err`.
 //
 // Lane l holds the logits of experts l, l+32, l+64, ... as order-preserving 32-bit
 // keys.  Each of the k rounds takes the warp-wide largest key with one redux.sync and
@@ -30,7 +33,8 @@ __device__ __forceinline__ float route_key_value(uint32_t key) {
 // Calls emit(e, gate, rank) once for each of the token's k choices, from the lane that
 // holds expert e; rank is e's position among the k choices in ascending expert id.
 template <int NPL, typename F>  // logits held per lane: E <= 32*NPL
-__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int lane, uint32_t* err, F&& emit) {
+__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int gate, int lane, uint32_t* err,
+                                                 F&& emit) {
   constexpr uint32_t kFull = 0xffffffffu;
   float v[NPL];
   uint32_t key[NPL];
@@ -71,14 +75,31 @@ __device__ __forceinline__ void route_token_warp(const float* z, int E, int k, i
     if (r == 0) zmax_key = kmax;
   }
   // ranks in ascending expert id: experts are ordered by (j, lane)
-  const float zmax = route_key_value(zmax_key);
+  const float zmax = route_key_value(zmax_key);  // the largest chosen logit
   uint32_t below = 0;  // chosen experts with a smaller j, then this j's lower lanes
   float ex[NPL];
   float sum = 0.f;
+  if (gate == FT_GATE_SIGMOID_TOPK) {
+    // s(z_j) / s(zmax), an exact rewrite of the sigmoid ratio in which no exponential
+    // overflows: (1 + e^-zmax) / (1 + e^-z) above zero, e^(z - zmax) (1 + e^zmax) / (1 + e^z)
+    // at or below it
 #pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    ex[j] = ((taken >> j) & 1u) ? expf(v[j] - zmax) : 0.f;
-    sum += ex[j];
+    for (int j = 0; j < NPL; ++j) {
+      float w = 0.f;
+      if ((taken >> j) & 1u)
+        w = zmax > 0.f ? (1.f + expf(-zmax)) / (1.f + expf(-v[j]))
+                       : expf(v[j] - zmax) * (1.f + expf(zmax)) / (1.f + expf(v[j]));
+      ex[j] = w;
+      sum += w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const bool in = gate == FT_GATE_SOFTMAX_ALL ? lane + 32 * j < E : ((taken >> j) & 1u) != 0u;
+      const float e = in ? expf(v[j] - zmax) : 0.f;
+      ex[j] = e;
+      sum += e;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
@@ -92,13 +113,14 @@ __device__ __forceinline__ void route_token_warp(const float* z, int E, int k, i
 
 // Dispatch on E (the number of logits each lane holds).
 template <typename F>
-__device__ __forceinline__ void route_token_any(const float* z, int E, int k, int lane, uint32_t* err, F&& emit) {
-  if (E <= 32) route_token_warp<1>(z, E, k, lane, err, emit);
-  else if (E <= 64) route_token_warp<2>(z, E, k, lane, err, emit);
-  else if (E <= 128) route_token_warp<4>(z, E, k, lane, err, emit);
-  else if (E <= 256) route_token_warp<8>(z, E, k, lane, err, emit);
-  else if (E <= 512) route_token_warp<16>(z, E, k, lane, err, emit);
-  else route_token_warp<32>(z, E, k, lane, err, emit);
+__device__ __forceinline__ void route_token_any(const float* z, int E, int k, int gate, int lane, uint32_t* err,
+                                                F&& emit) {
+  if (E <= 32) route_token_warp<1>(z, E, k, gate, lane, err, emit);
+  else if (E <= 64) route_token_warp<2>(z, E, k, gate, lane, err, emit);
+  else if (E <= 128) route_token_warp<4>(z, E, k, gate, lane, err, emit);
+  else if (E <= 256) route_token_warp<8>(z, E, k, gate, lane, err, emit);
+  else if (E <= 512) route_token_warp<16>(z, E, k, gate, lane, err, emit);
+  else route_token_warp<32>(z, E, k, gate, lane, err, emit);
 }
 
 }  // namespace ft

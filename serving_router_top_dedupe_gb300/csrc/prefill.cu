@@ -105,8 +105,9 @@ __global__ void __launch_bounds__(1024) install_layer_kernel(int layer, int E, c
   }
 }
 
-// One warp per token: top-k softmax, then the token's bit in each chosen expert's mask.
-__global__ void __launch_bounds__(256) prefill_route_kernel(const float* logits, int T, int E, int k, int W,
+// One warp per token: top-k routing and gates, then the token's bit in each chosen
+// expert's mask.
+__global__ void __launch_bounds__(256) prefill_route_kernel(const float* logits, int T, int E, int k, int gate, int W,
                                                            int32_t* sel, float* gates, uint32_t* masks,
                                                            uint32_t* error_word) {
   __shared__ uint32_t s_err;
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const float* logits,
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (t < T) {
-    route_token_any(logits + (size_t)t * E, E, k, lane, &s_err, [&](int e, float g, int rank) {
+    route_token_any(logits + (size_t)t * E, E, k, gate, lane, &s_err, [&](int e, float g, int rank) {
       sel[(size_t)t * k + rank] = e;
       gates[(size_t)t * k + rank] = g;
       atomicOr(masks + (size_t)e * W + (t >> 5), 1u << (t & 31));
@@ -492,7 +493,7 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   e = timed(4, [&]() -> cudaError_t {
     cudaError_t r = cudaMemsetAsync(p->masks, 0, sizeof(uint32_t) * (size_t)E * p->W, c.cs);
     if (r != cudaSuccess) return r;
-    prefill_route_kernel<<<(T + 7) / 8, 256, 0, c.cs>>>(logits, T, E, k, p->W, p->sel, p->gates, p->masks,
+    prefill_route_kernel<<<(T + 7) / 8, 256, 0, c.cs>>>(logits, T, E, k, c.gate, p->W, p->sel, p->gates, p->masks,
                                                         &c.st->error_word);
     prefill_scan_kernel<<<1, 1024, 0, c.cs>>>(p->masks, p->W, E, T, p->has_shared, p->wpre, p->entry_off,
                                               p->tile_off);

@@ -20,11 +20,12 @@ FT_OK, FT_ERR_INVALID, FT_ERR_CUDA, FT_ERR_NOMEM, FT_ERR_PIN = 0, 1, 2, 3, 4
 FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, FT_ERR_DEVICE = 5, 6, 7, 8
 FT_W_BF16, FT_W_FP8_E4M3_B128 = 0, 1
 FT_FILL_KERNEL, FT_FILL_MEMCPY = 0, 1
+FT_GATE_SOFTMAX_TOPK, FT_GATE_SOFTMAX_ALL, FT_GATE_SIGMOID_TOPK = 0, 1, 2
 FT_CPU = -1
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_STATE, FT_DEVERR_TIMEOUT, FT_DEVERR_CAPACITY = 1, 2, 4, 8
 
 PROFILE_KINDS = ("control", "fill", "gate_up", "down_combine", "prefill_route", "prefill_gemm_gate_up",
-                 "prefill_combine", "prefill_copy", "prefill_gemm_down")
+                 "prefill_combine", "prefill_copy", "prefill_gemm_down", "router")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
@@ -67,7 +68,7 @@ class ft_step_trace(C.Structure):
 
 
 class ft_profile(C.Structure):
-    _fields_ = [("launches", C.c_uint64 * 9), ("total_ms", C.c_double * 9)]
+    _fields_ = [("launches", C.c_uint64 * 10), ("total_ms", C.c_double * 10)]
 
 
 _P = C.c_void_p
@@ -82,6 +83,10 @@ _SIGS = {
     "ft_moe_prefill_chunk": [_P, C.c_int, C.c_int, _P, _P, _P],
     "ft_moe_set_prefill_overlap": [_P, C.c_int],
     "ft_moe_set_host_hook": [_P, _P, _P],
+    "ft_moe_set_router": [_P, _P, C.c_int],
+    "ft_moe_router_logits": [_P, C.c_int, C.c_int, _P, _P],
+    "ft_moe_decode_step_hidden": [_P, C.c_int, C.c_int, _P, _P, _P, _P, _P],
+    "ft_moe_prefill_chunk_hidden": [_P, C.c_int, C.c_int, _P, _P],
     "ft_cache_resize": [_P, C.c_int],
     "ft_split_misses": [C.c_int, C.c_double, C.c_double, C.c_int, C.POINTER(C.c_int)],
     "ft_bench_bw": [C.c_size_t, C.c_int, C.POINTER(C.c_double)],
@@ -175,6 +180,26 @@ def ft_graph_destroy(g) -> None:
 
 def ft_moe_prefill_chunk(h, layer, n_tokens, x_bf16, logits, out) -> None:
     _check(_lib.ft_moe_prefill_chunk(h, layer, n_tokens, _ptr(x_bf16), _ptr(logits), _ptr(out)))
+
+
+def ft_moe_set_router(h, w_router_bf16, gate=FT_GATE_SOFTMAX_TOPK) -> None:
+    """w_router_bf16: host uint16 array [L][E][H] (BF16 bits), or None to keep the weights."""
+    if w_router_bf16 is not None:
+        w_router_bf16 = np.ascontiguousarray(w_router_bf16, dtype=np.uint16)
+    _check(_lib.ft_moe_set_router(h, _ptr(w_router_bf16), int(gate)))
+
+
+def ft_moe_router_logits(h, layer, n_tokens, x_bf16, logits_out) -> None:
+    _check(_lib.ft_moe_router_logits(h, layer, n_tokens, _ptr(x_bf16), _ptr(logits_out)))
+
+
+def ft_moe_decode_step_hidden(h, layer, batch, x_bf16, c_partial, out, rows_out=None, logits_out=None) -> None:
+    _check(_lib.ft_moe_decode_step_hidden(h, layer, batch, _ptr(x_bf16), _ptr(c_partial), _ptr(out),
+                                          _ptr(rows_out), _ptr(logits_out)))
+
+
+def ft_moe_prefill_chunk_hidden(h, layer, n_tokens, x_bf16, out) -> None:
+    _check(_lib.ft_moe_prefill_chunk_hidden(h, layer, n_tokens, _ptr(x_bf16), _ptr(out)))
 
 
 HOST_HOOK = C.CFUNCTYPE(None, C.c_void_p, C.c_int, C.c_int, C.POINTER(C.c_int32), C.POINTER(C.c_float),

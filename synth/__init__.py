@@ -36,6 +36,7 @@ TAG_OFFSET = 7
 TAG_X, TAG_LOGIT = 10, 11
 TAG_PERM, TAG_TRACE = 12, 13
 TAG_PREFILL_X, TAG_PREFILL_Z = 30, 31
+TAG_ROUTER = 40
 
 W_BF16 = 0
 W_FP8_E4M3_B128 = 1
@@ -338,6 +339,14 @@ def prefill_logits(w: Workload, chunk: int, layer: int, n_tokens: int) -> np.nda
     """Prefill router logits ~ U(-1, 1): nearly every expert is active in a chunk."""
     u = uniform(derive_key(w.seed, TAG_PREFILL_Z, chunk, layer), n_tokens * w.n_experts)
     return (2.0 * u - 1.0).astype(np.float32).reshape(n_tokens, w.n_experts)
+
+
+def router_weights(w: Workload) -> np.ndarray:
+    """Router projection of every layer: bf16 bits [L, E, H], N(0, (2/sqrt(H))^2), so that
+    the logits of x ~ N(0, 1) have a spread of about 2."""
+    z = normal(derive_key(w.seed, TAG_ROUTER), w.n_layers * w.n_experts * w.hidden)
+    z = z * (2.0 / np.sqrt(w.hidden))
+    return f32_to_bf16_bits(z.astype(np.float32)).reshape(w.n_layers, w.n_experts, w.hidden)
 
 
 # ------------------------------------------------------------------ routing trace

@@ -17,6 +17,16 @@ OUT_TOL = 1e-2
 GATE_RTOL = 2e-6
 
 
+def router_tol(xb, wr):
+    """Per-logit error bound of the GPU router against the float64 oracle.  BF16 x BF16
+    products are exact in FP32; each lane adds H/32 of them in sequence and five xor
+    butterfly levels follow, so to first order |z - z_ref| <= (H/32 + 5) u sum_h |x_h w_h|
+    with u = 2^-24 (one rounding per addition)."""
+    H = xb.shape[1]
+    mag = np.abs(O.bf16_to_f64(xb)) @ np.abs(O.bf16_to_f64(wr)).T
+    return (H / 32 + 5) * 2.0 ** -24 * mag * 1.01 + 1e-30
+
+
 def _F():
     from serving_router_top_dedupe_gb300 import ftmoe
 
@@ -27,7 +37,7 @@ class Run:
     """One library handle plus its oracle twin."""
 
     def __init__(self, w: synth.Workload, banks=None, shared=None, fill_mode=None, max_batch=None,
-                 max_prefill_tokens=0, cache_slots=None):
+                 max_prefill_tokens=0, cache_slots=None, gate=0, router=None):
         F = _F()
         self.F = F
         self.w = w
@@ -48,6 +58,9 @@ class Run:
         self.kcap = min(self.B * w.top_k, w.n_experts)
         self.dev = torch.device("cuda:0")
         self.max_err = 0.0
+        self.gate, self.router = gate, router
+        if router is not None or gate != 0:
+            F.ft_moe_set_router(self.h, router, gate)
 
     def close(self):
         if self.h:
@@ -76,6 +89,23 @@ class Run:
                                   gates[t, r], self.fp8).astype(np.float32)
         return cp
 
+    def gpu_logits(self, layer, xb):
+        """Router logits of the GPU (ft_moe_router_logits), checked against the oracle's
+        float64 logits within router_tol; the decisions are then taken on these values on
+        both sides."""
+        T = xb.shape[0]
+        x_d = torch.from_numpy(xb.view(np.int16)).to(self.dev)
+        z_d = torch.empty((T, self.w.n_experts), dtype=torch.float32, device=self.dev)
+        torch.cuda.synchronize()  # the library runs on its own stream
+        self.F.ft_moe_router_logits(self.h, layer, T, x_d, z_d)
+        self.F.ft_moe_synchronize(self.h)
+        z = z_d.cpu().numpy()
+        ref = O.router_logits(xb, self.router[layer])
+        err = np.abs(z.astype(np.float64) - ref)
+        tol = router_tol(xb, self.router[layer])
+        assert np.all(err <= tol), f"layer {layer}: router logit error {err.max():.3e} above its bound"
+        return z
+
     # ------------------------------------------------------------- one step
     def inputs(self, step, layer, trace=None, batch=None):
         w = self.w if batch is None else self.w.with_(batch=batch)
@@ -85,12 +115,16 @@ class Run:
         return xb, z
 
     def step(self, step, layer, trace=None, check_out=False, cpart=None, rows_out=False, batch=None,
-             xz=None):
-        """Run one decode layer-step on both sides and compare.  Returns (rec, gpu_trace, out, rows)."""
+             xz=None, hidden=False):
+        """Run one decode layer-step on both sides and compare.  Returns (rec, gpu_trace, out, rows).
+        hidden: the step takes hidden states (ft_moe_decode_step_hidden); the oracle routes on
+        the GPU router's logits, which gpu_logits has checked against its own."""
         F = self.F
         xb, z = self.inputs(step, layer, trace, batch) if xz is None else xz
         B = xb.shape[0]
-        sel, gates = O.route(z, self.w.top_k)
+        if hidden:
+            z = self.gpu_logits(layer, xb)
+        sel, gates = O.route(z, self.w.top_k, self.gate)
         rec = self.sim.decode_step(layer, self.w.n_experts, sel, self.bp, self.bh)
         if cpart is None:
             cpairs = [(t, r) for t in range(B) for r in range(self.w.top_k) if rec.slot_of_pair[t, r] < 0]
@@ -101,7 +135,12 @@ class Run:
         out_d = torch.empty((B, self.w.hidden), dtype=torch.float32, device=self.dev)
         rows_d = torch.zeros((B, self.w.top_k, self.w.hidden), dtype=torch.float32, device=self.dev) \
             if rows_out else None
-        F.ft_moe_decode_step(self.h, layer, B, x_d, z_d, c_d, out_d, rows_d)
+        if hidden:
+            lg_d = torch.empty((B, self.w.n_experts), dtype=torch.float32, device=self.dev)
+            F.ft_moe_decode_step_hidden(self.h, layer, B, x_d, c_d, out_d, rows_d, lg_d)
+            assert np.array_equal(lg_d.cpu().numpy(), z), "router logits inside the step differ"
+        else:
+            F.ft_moe_decode_step(self.h, layer, B, x_d, z_d, c_d, out_d, rows_d)
         gt = F.ft_moe_get_step_trace(self.h, self.B, self.w.top_k, self.kcap)
         self.compare(rec, sel, gates, gt)
         out = out_d.cpu().numpy()
@@ -138,17 +177,22 @@ class Run:
         return s
 
 
-def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None):
+def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None, hidden=False):
     """One prefill layer on both sides; compares residency state, and outputs of
-    `check_tokens` (all when None) against the float64 oracle."""
+    `check_tokens` (all when None) against the float64 oracle.  hidden: the call takes
+    hidden states (ft_moe_prefill_chunk_hidden) and both sides route on the GPU router's
+    logits, checked first against the oracle's."""
     F, w = r.F, r.w
     xb = synth.prefill_x(w, chunk, layer, T)
-    z = synth.prefill_logits(w, chunk, layer, T)
+    z = r.gpu_logits(layer, xb) if hidden else synth.prefill_logits(w, chunk, layer, T)
     r.sim.prefill_layer(layer, w.n_experts, w.n_layers)
     x_d = torch.from_numpy(xb.view(np.int16)).to(r.dev)
     z_d = torch.from_numpy(z).to(r.dev)
     out_d = torch.empty((T, w.hidden), dtype=torch.float32, device=r.dev)
-    F.ft_moe_prefill_chunk(r.h, layer, T, x_d, z_d, out_d)
+    if hidden:
+        F.ft_moe_prefill_chunk_hidden(r.h, layer, T, x_d, out_d)
+    else:
+        F.ft_moe_prefill_chunk(r.h, layer, T, x_d, z_d, out_d)
     st = F.ft_moe_get_state(r.h, w.n_logical, r.sim.S)
     assert st["clock"] == r.sim.clock
     assert np.array_equal(st["res"], r.sim.res), f"prefill layer {layer}: residency table"
@@ -156,7 +200,7 @@ def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None):
     assert np.array_equal(st["stamp"].astype(np.int64), r.sim.stamp), f"prefill layer {layer}: stamps"
     out = out_d.cpu().numpy()
     tokens = range(T) if check_tokens is None else check_tokens
-    sel, gates = O.route(z, w.top_k)
+    sel, gates = O.route(z, w.top_k, r.gate)
     ref = O.prefill_outputs(layer, sel, gates, xb, r.expert, w.n_experts, tokens=list(tokens),
                             shared=r.shared_expert(layer))
     err = O.rel_err_rows(out[list(tokens)], ref)
