@@ -396,7 +396,7 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   ep.k = h->K;
   ep.B = batch;
   ep.has_shared = h->cfg.has_shared;
-  ep.n_sm = h->n_sm;
+  ep.n_sm = chain ? h->n_sm - h->grid_fill : h->n_sm;  // the fill kernel's SMs are left to it
   ep.max_entries = h->kcap + 1;
   ep.pdl = chain;
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
@@ -532,7 +532,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   h->lay = ft::make_layout(cfg->wtype, h->H, h->I);
   h->n_banks = fp8 ? 6 : 3;
   h->grid_eval = h->n_sm * 4;
-  h->grid_fill = h->n_sm;
+  h->grid_fill = std::max(1, std::min(ft::kFillSms, h->n_sm / 4));
   if (cfg->compute_stream) {
     h->cs = (cudaStream_t)cfg->compute_stream;
   } else {

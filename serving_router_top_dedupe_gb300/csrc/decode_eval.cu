@@ -33,10 +33,15 @@ using namespace dot;
 // ------------------------------------------------------------------------- fill
 // Work = q experts x n_banks contiguous segments.  CTA b copies a share of segment
 // b mod nseg (addresses computed once per segment), issuing FILL_UNROLL 16-byte loads
-// from the mapped host pool before storing any, so the grid keeps MBs of host reads in
-// flight: one 6 MB expert then moves at the host link's rate.  The kernel stays small in
-// registers so that, while it waits for the control kernel, a CTA of the next kernel
-// (the batch-1 expert GEMV) fits beside it on the SM.
+// from the mapped host pool before storing any, so the grid keeps ~0.5 MB of host reads
+// in flight: one 6 MB expert then moves at the host link's rate.
+//
+// The grid is a few CTAs on SMs of their own.  A streaming CTA that shares an SM with a
+// fill CTA stalls behind the fill's host loads until the fill ends (measured on GB300:
+// such SMs finished their share of the resident experts ~33 us late, at the fill's end,
+// while the other SMs took ~11 us), so each fill CTA reserves enough shared memory that
+// no batch-1 GEMV CTA is placed beside it, and the GEMV runs on the remaining SMs.  The
+// next layer's control CTA still fits beside a fill CTA.
 constexpr int FILL_UNROLL = 4;
 
 __device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n16,
@@ -56,7 +61,7 @@ __device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint
   }
 }
 
-__global__ void __launch_bounds__(256) fill_kernel(FillParams p) {
+__global__ void __launch_bounds__(kFillThreads) fill_kernel(FillParams p) {
   pdl_wait();  // the copy list comes from the control kernel right before
   pdl_trigger();
   const int q = p.counts[C_Q];
@@ -322,7 +327,7 @@ cudaError_t set_smem(F f, size_t bytes) {
 }  // namespace
 
 cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
-  return launch_k(fill_kernel, dim3(grid), dim3(256), 0, s, p.pdl, p);
+  return launch_k(fill_kernel, dim3(grid), dim3(kFillThreads), kFillSmemReserve, s, p.pdl, p);
 }
 
 bool eval_fused(const EvalParams& p, int wtype) {
@@ -342,6 +347,7 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
 cudaError_t prepare_kernels(int wtype, int H, int I) {
   cudaError_t e = cudaSuccess;
   if ((e = prepare_fused_gemv()) != cudaSuccess) return e;
+  if ((e = set_smem(fill_kernel, kFillSmemReserve)) != cudaSuccess) return e;
   const size_t gu1 = (size_t)H * 2, gu4 = 4 * gu1, dn1 = (size_t)I * 4, dn4 = 4 * dn1;
   if (wtype == FT_W_BF16) {
     if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 1>, gu1)) != cudaSuccess) return e;

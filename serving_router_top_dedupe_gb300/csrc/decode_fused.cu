@@ -7,15 +7,20 @@
 // rows in flight in a ring of shared-memory stages filled by cp.async.bulk, and the same
 // ring carries both halves of the layer:
 //
-//  phase 0 (gate/up): units g*I + i over all entries, split evenly over the CTAs; a stage
-//                     holds gate rows i0.. and the same up rows of one entry; a consumer
-//                     warp forms a = W_g[i].x, b = W_u[i].x and writes h[g][i] = silu(a)*b.
+//  phase 0 (gate/up): units (entry, row i), split evenly over the CTAs; a stage holds gate
+//                     rows i0.. and the same up rows of one entry; a consumer warp forms
+//                     a = W_g[i].x, b = W_u[i].x and writes h[g][i] = silu(a)*b.
 //  phase 1 (down):    each CTA owns output rows j0..j0+nj-1 and streams W_down[g][j] of
 //                     every entry g for them.  These rows do not depend on h, so the
 //                     producer streams them right behind its phase-0 rows; only the
 //                     consumers wait, until every CTA has published its h rows.
 //  combine:           out[j] = shared + the k pair rows in ascending expert id (GPU row
 //                     gate_r * y, or the caller's c_partial row for a host-evaluated pair).
+//
+// Both phases run twice: first for the experts resident before the step, then, once the
+// fill kernel of the step has completed, for the experts it filled.  While a fill crosses
+// the host link, the resident experts' whole layer (both phases) is evaluated; after it,
+// only the filled experts' rows remain, spread over every CTA.
 //
 // The hand-off between the phases is a per-entry counter that each CTA raises by the h rows
 // it wrote (release), and that consumers wait on (acquire, bounded).  It needs every CTA to
@@ -104,13 +109,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
   const size_t rh = (size_t)H * ESZ, ri = (size_t)I * ESZ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // phase-0 units u0 .. u0+n0-1 (unit g*I + i); phase-1 local rows t = g*nj + jl, output row j0 + jl
-  const long long R0 = (long long)ne * I;
-  const int u0 = (int)(R0 * blockIdx.x / gridDim.x);
-  const int n0 = (int)(R0 * (blockIdx.x + 1) / gridDim.x) - u0;
+  // Entries split into two passes: those resident before this step (pass 0) and those the
+  // fill kernel right before writes (pass 1).  Within a pass, phase-0 units v (entry
+  // pe[v / I], row v % I) are split evenly over the CTAs; phase-1 rows t (entry pe[t / nj],
+  // output row j0 + t % nj) are this CTA's output rows of every entry of the pass.
+  __shared__ int s_pe[2][kMaxK + 2];
+  __shared__ int s_np[2];
   const int j0 = (int)((long long)H * blockIdx.x / gridDim.x);
   const int nj = (int)((long long)H * (blockIdx.x + 1) / gridDim.x) - j0;
-  const int n1 = nj * ne;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < pl.nst; ++s) {
@@ -119,6 +125,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
     }
     *abort_flag = 0;
     mbar_fence_init();
+    int n[2] = {0, 0};
+    for (int g = 0; g < ne && g < kMaxK + 2; ++g) {
+      const int ps = p.g_fill[g] != 0 ? 1 : 0;
+      s_pe[ps][n[ps]++] = g;
+    }
+    s_np[0] = n[0];
+    s_np[1] = n[1];
   }
   __syncthreads();
 
@@ -127,54 +140,54 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
     if (lane == 0) {
       const uint64_t pol = l2_evict_first();
       int c = 0;
-      // Phase 0 streams the experts that were resident before this step first (the fill
-      // kernel right before does not write their slots), joins the dependency chain, then
-      // streams the filled experts.  Phase 1 follows without waiting for anything.
+      // Pass 0 streams the experts that were resident before this step (the fill kernel
+      // right before does not write their slots): their gate/up rows, then their down rows.
+      // Pass 1 joins the dependency chain and streams the filled experts the same way.
       for (int pass = 0; pass < 2 && !*abort_flag; ++pass) {
-        if (pass == 1) {
-          pdl_wait();
-          pdl_trigger();
-        }
-        int t = 0;
-        while (t < n0) {
-          const int u = u0 + t, g = u / I, i = u - g * I;
-          const int last = min(n0, (g + 1) * I - u0);
-          if ((p.g_fill[g] != 0) != (pass == 1)) {
-            t = last;
-            continue;
-          }
+        if (pass == 1) pdl_wait();
+        const int npe = s_np[pass];
+        const int* pe = s_pe[pass];
+        const long long R0 = (long long)npe * I;
+        const int v1 = (int)(R0 * (blockIdx.x + 1) / gridDim.x);
+        for (int v = (int)(R0 * blockIdx.x / gridDim.x); v < v1 && !*abort_flag;) {
+          const int gi = v / I, i = v - gi * I, g = pe[gi];
+          const int nr = min(pl.pairs, min(v1, (gi + 1) * I) - v);
           const int s = c % pl.nst, use = c / pl.nst;
           if (!mbar_wait(smem_u32(empty + s), (uint32_t)(use & 1) ^ 1u, abort_flag, p.error_word)) break;
-          const int nr = min(pl.pairs, last - t);
-          meta[s] = make_int4(0, t, nr, 0);
+          meta[s] = make_int4(0, v, nr, pass);
           const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
           const uint8_t* src = p.g_w[g] + p.lay.gate + (size_t)i * rh;
           mbar_arrive_expect_tx(fb, (uint32_t)(2 * nr * rh));
           bulk_g2s_hint(dst, src, (uint32_t)(nr * rh), fb, pol);
           bulk_g2s_hint(dst + (uint32_t)(nr * rh), src + (size_t)I * rh, (uint32_t)(nr * rh), fb, pol);
+          v += nr;
+          ++c;
+        }
+        // The next layer's control kernel may start once the pre-fill gate/up rows are on
+        // their way: its prologue reads only state that earlier control kernels wrote, and
+        // it waits for this grid to complete before anything else.
+        if (pass == 0) pdl_trigger();
+        const int n1 = npe * nj;
+        for (int t = 0; t < n1 && !*abort_flag;) {
+          const int s = c % pl.nst, use = c / pl.nst;
+          if (!mbar_wait(smem_u32(empty + s), (uint32_t)(use & 1) ^ 1u, abort_flag, p.error_word)) break;
+          const int nr = min(pl.drows, n1 - t);
+          meta[s] = make_int4(1, t, nr, pass);
+          const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
+          mbar_arrive_expect_tx(fb, (uint32_t)(nr * ri));
+          // a stage may span entries: one bulk copy per entry segment (its rows are contiguous)
+          uint32_t off = 0;
+          for (int tt = t; tt < t + nr;) {
+            const int gi = tt / nj, jl = tt - gi * nj;
+            const int seg = min(t + nr, (gi + 1) * nj) - tt;
+            bulk_g2s_hint(dst + off, p.g_w[pe[gi]] + p.lay.down + (size_t)(j0 + jl) * ri, (uint32_t)(seg * ri), fb,
+                          pol);
+            off += (uint32_t)(seg * ri);
+            tt += seg;
+          }
           t += nr;
           ++c;
         }
-      }
-      int t = 0;
-      while (t < n1 && !*abort_flag) {
-        const int s = c % pl.nst, use = c / pl.nst;
-        if (!mbar_wait(smem_u32(empty + s), (uint32_t)(use & 1) ^ 1u, abort_flag, p.error_word)) break;
-        const int nr = min(pl.drows, n1 - t);
-        meta[s] = make_int4(1, t, nr, 0);
-        const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
-        mbar_arrive_expect_tx(fb, (uint32_t)(nr * ri));
-        // a stage may span entries: one bulk copy per entry segment (its rows are contiguous)
-        uint32_t off = 0;
-        for (int tt = t; tt < t + nr;) {
-          const int g = tt / nj, jl = tt - g * nj;
-          const int seg = min(t + nr, (g + 1) * nj) - tt;
-          bulk_g2s_hint(dst + off, p.g_w[g] + p.lay.down + (size_t)(j0 + jl) * ri, (uint32_t)(seg * ri), fb, pol);
-          off += (uint32_t)(seg * ri);
-          tt += seg;
-        }
-        t += nr;
-        ++c;
       }
       if (*abort_flag)  // let copies already issued land before the CTA exits
         for (int cc = (c > pl.nst ? c - pl.nst : 0); cc < c; ++cc)
@@ -201,128 +214,151 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
       }
       *reinterpret_cast<uint4*>(xs + (size_t)idx * 8) = v;
     }
-    if (WT == FT_W_FP8_E4M3_B128) pdl_wait();  // block scales of filled slots are read directly
     asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
 
-    int c = 0;
-    // ---- phase 0: h = silu(W_g x) * (W_u x)
-    for (int done = 0; done < n0;) {
-      const int s = c % pl.nst, use = c / pl.nst;
-      if (!mbar_wait(smem_u32(full + s), (uint32_t)(use & 1), abort_flag, p.error_word)) break;
-      const int4 m = meta[s];
-      const uint8_t* st = stages + (size_t)s * pl.stage;
-      // items rotate over the warps from stage to stage, so small stages keep all warps busy
-      for (int q = ((cw - done) % kConsumers + kConsumers) % kConsumers; q < m.z; q += kConsumers) {
-        const int u = u0 + m.y + q, g = u / I, i = u - g * I;
-        const uint8_t* rg = st + (size_t)q * rh;          // gate row
-        const uint8_t* ru = st + ((size_t)m.z + q) * rh;  // the same up row
-        float a = 0.f, b = 0.f;                           // two independent chains
-        if (WT == FT_W_BF16) {
-          for (int c16 = lane; c16 < H / EPC; c16 += 32) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
-            a = dot_bf16_bf16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), xv, a);
-            b = dot_bf16_bf16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), xv, b);
-          }
-        } else {
-          const float* sg = reinterpret_cast<const float*>(p.g_w[g] + p.lay.gs) + (size_t)i * (H / 128);
-          const float* su = reinterpret_cast<const float*>(p.g_w[g] + p.lay.us) + (size_t)i * (H / 128);
-          for (int c16 = lane; c16 < H / EPC; c16 += 32) {
-            const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)c16 * 16);
-            const uint4 x0 = xp[0], x1 = xp[1];
-            a = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), x0, x1), __ldg(sg + c16 / 8), a);
-            b = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), x0, x1), __ldg(su + c16 / 8), b);
-          }
-        }
-        const float ab2[2] = {warp_sum(a), warp_sum(b)};
-        if (lane == 0) p.h[(size_t)g * I + i] = silu_mul(ab2[0], ab2[1]);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + s));
-      done += m.z;
-      ++c;
-    }
-
-    // combine inputs that do not depend on h, fetched while the other CTAs finish phase 0:
-    // lane r < k holds pair r; the caller's rows of host-evaluated pairs go to shared memory
+    // combine inputs that do not depend on h: lane r < k holds pair r
     const bool res_r = lane < k && p.slot_of_pair[lane] >= 0;
     const uint32_t res_mask = __ballot_sync(0xffffffffu, res_r);
     const int gi_r = __popc(res_mask & ((1u << lane) - 1u));
     const float gate_r = lane < k ? p.gates[lane] : 0.f;
-    for (int idx = ct; idx < nj * k; idx += 32 * kConsumers) {
-      const int jl = idx / k, r = idx - jl * k;
-      float v = 0.f;
-      if (p.slot_of_pair[r] < 0) {
-        if (p.c_partial) v = p.c_partial[(size_t)r * H + j0 + jl];
-        else atomicOr(p.error_word, FT_DEVERR_CAPACITY);
-      }
-      cb[idx] = v;
-    }
 
-    // ---- hand-off: publish this CTA's h rows, wait for every entry's rows, stage h
-    asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
-    if (ct == 0) {
-      __threadfence();
-      for (int u = u0; u < u0 + n0;) {
-        const int g = u / I;
-        const int end = min(u0 + n0, (g + 1) * I);
-        atomicAdd(p.ready + g, (uint32_t)(end - u));
-        u = end;
-      }
-      for (int g = 0; g < ne; ++g)
-        if (!wait_counter(p.ready + g, (uint32_t)I, abort_flag, p.error_word)) break;
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
-    {
-      const float4* hg = reinterpret_cast<const float4*>(p.h);
-      float4* h4 = reinterpret_cast<float4*>(hs);
-      for (int i4 = ct; i4 < ne * I / 4; i4 += 32 * kConsumers) h4[i4] = __ldcg(hg + i4);
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
-
-    // ---- phase 1: y[g][j] = W_d[g][j] . h[g]
-    for (int done = 0; done < n1;) {
-      const int s = c % pl.nst, use = c / pl.nst;
-      if (!mbar_wait(smem_u32(full + s), (uint32_t)(use & 1), abort_flag, p.error_word)) break;
-      const int4 m = meta[s];
-      const uint8_t* st = stages + (size_t)s * pl.stage;
-      // up to kRowsILP rows per warp at once: independent chains, each row in the usual order
-      for (int q = ((cw - done) % kConsumers + kConsumers) % kConsumers; q < m.z; q += kRowsILP * kConsumers) {
-        float acc[kRowsILP];
-        const float* hv[kRowsILP];
-        const float* sc[kRowsILP];
-        int tr[kRowsILP];
-        bool ok[kRowsILP];
-#pragma unroll
-        for (int r = 0; r < kRowsILP; ++r) {
-          const int qq = q + r * kConsumers;
-          ok[r] = qq < m.z;
-          const int t = m.y + (ok[r] ? qq : q), g = t / nj, jl = t - g * nj;
-          tr[r] = t;
-          hv[r] = hs + (size_t)g * I;
-          sc[r] = WT == FT_W_BF16 ? nullptr
-                                  : reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128);
-          acc[r] = 0.f;
+    // the caller's rows of host-evaluated pairs, [jl][r]
+    auto fetch_cb = [&]() {
+      for (int idx = ct; idx < nj * k; idx += 32 * kConsumers) {
+        const int jl = idx / k, r = idx - jl * k;
+        float val = 0.f;
+        if (p.slot_of_pair[r] < 0) {
+          if (p.c_partial) val = p.c_partial[(size_t)r * H + j0 + jl];
+          else atomicOr(p.error_word, FT_DEVERR_CAPACITY);
         }
-        for (int c16 = lane; c16 < I / EPC; c16 += 32) {
+        cb[idx] = val;
+      }
+    };
+    bool cb_done = false;
+
+    int c = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int npe = s_np[pass];
+      if (npe == 0) continue;
+      const int* pe = s_pe[pass];
+      if (WT == FT_W_FP8_E4M3_B128 && pass == 1) pdl_wait();  // block scales of filled slots are read directly
+      const long long R0 = (long long)npe * I;
+      const int v0 = (int)(R0 * blockIdx.x / gridDim.x);
+      const int n0 = (int)(R0 * (blockIdx.x + 1) / gridDim.x) - v0;
+
+      // ---- phase 0: h = silu(W_g x) * (W_u x)
+      for (int done = 0; done < n0;) {
+        const int s = c % pl.nst, use = c / pl.nst;
+        if (!mbar_wait(smem_u32(full + s), (uint32_t)(use & 1), abort_flag, p.error_word)) break;
+        const int4 m = meta[s];
+        const uint8_t* st = stages + (size_t)s * pl.stage;
+        // items rotate over the warps from stage to stage, so small stages keep all warps busy
+        for (int q = ((cw - done) % kConsumers + kConsumers) % kConsumers; q < m.z; q += kConsumers) {
+          const int v = m.y + q, gi = v / I, i = v - gi * I, g = pe[gi];
+          const uint8_t* rg = st + (size_t)q * rh;          // gate row
+          const uint8_t* ru = st + ((size_t)m.z + q) * rh;  // the same up row
+          float a = 0.f, b = 0.f;                           // two independent chains
+          if (WT == FT_W_BF16) {
+            for (int c16 = lane; c16 < H / EPC; c16 += 32) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
+              a = dot_bf16_bf16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), xv, a);
+              b = dot_bf16_bf16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), xv, b);
+            }
+          } else {
+            const float* sg = reinterpret_cast<const float*>(p.g_w[g] + p.lay.gs) + (size_t)i * (H / 128);
+            const float* su = reinterpret_cast<const float*>(p.g_w[g] + p.lay.us) + (size_t)i * (H / 128);
+            for (int c16 = lane; c16 < H / EPC; c16 += 32) {
+              const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)c16 * 16);
+              const uint4 x0 = xp[0], x1 = xp[1];
+              a = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), x0, x1), __ldg(sg + c16 / 8),
+                       a);
+              b = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), x0, x1), __ldg(su + c16 / 8),
+                       b);
+            }
+          }
+          const float ab2[2] = {warp_sum(a), warp_sum(b)};
+          if (lane == 0) p.h[(size_t)g * I + i] = silu_mul(ab2[0], ab2[1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        done += m.z;
+        ++c;
+      }
+
+      if (!cb_done) {
+        fetch_cb();  // while the other CTAs finish phase 0
+        cb_done = true;
+      }
+
+      // ---- hand-off: publish this CTA's h rows of the pass, wait for the pass's entries,
+      // stage their h
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
+      if (ct == 0) {
+        __threadfence();
+        for (int v = v0; v < v0 + n0;) {
+          const int gi = v / I;
+          const int end = min(v0 + n0, (gi + 1) * I);
+          atomicAdd(p.ready + pe[gi], (uint32_t)(end - v));
+          v = end;
+        }
+        for (int gi = 0; gi < npe; ++gi)
+          if (!wait_counter(p.ready + pe[gi], (uint32_t)I, abort_flag, p.error_word)) break;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
+      for (int gi = 0; gi < npe; ++gi) {
+        const float4* hg = reinterpret_cast<const float4*>(p.h + (size_t)pe[gi] * I);
+        float4* h4 = reinterpret_cast<float4*>(hs + (size_t)pe[gi] * I);
+        for (int i4 = ct; i4 < I / 4; i4 += 32 * kConsumers) h4[i4] = __ldcg(hg + i4);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
+
+      // ---- phase 1: y[g][j] = W_d[g][j] . h[g]
+      const int n1 = npe * nj;
+      for (int done = 0; done < n1;) {
+        const int s = c % pl.nst, use = c / pl.nst;
+        if (!mbar_wait(smem_u32(full + s), (uint32_t)(use & 1), abort_flag, p.error_word)) break;
+        const int4 m = meta[s];
+        const uint8_t* st = stages + (size_t)s * pl.stage;
+        // up to kRowsILP rows per warp at once: independent chains, each row in the usual order
+        for (int q = ((cw - done) % kConsumers + kConsumers) % kConsumers; q < m.z; q += kRowsILP * kConsumers) {
+          float acc[kRowsILP];
+          const float* hv[kRowsILP];
+          const float* sc[kRowsILP];
+          int yi[kRowsILP];
+          bool ok[kRowsILP];
 #pragma unroll
           for (int r = 0; r < kRowsILP; ++r) {
-            if (!ok[r]) continue;
-            const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16);
-            if (WT == FT_W_BF16) acc[r] = dot_bf16_f32(wv, hv[r] + c16 * EPC, acc[r]);
-            else acc[r] = fmaf(dot_e4m3_f32(wv, hv[r] + c16 * EPC), __ldg(sc[r] + c16 / 8), acc[r]);
+            const int qq = q + r * kConsumers;
+            ok[r] = qq < m.z;
+            const int t = m.y + (ok[r] ? qq : q), gi = t / nj, jl = t - gi * nj, g = pe[gi];
+            yi[r] = g * nj + jl;
+            hv[r] = hs + (size_t)g * I;
+            sc[r] = WT == FT_W_BF16 ? nullptr
+                                    : reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128);
+            acc[r] = 0.f;
+          }
+          for (int c16 = lane; c16 < I / EPC; c16 += 32) {
+#pragma unroll
+            for (int r = 0; r < kRowsILP; ++r) {
+              if (!ok[r]) continue;
+              const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16);
+              if (WT == FT_W_BF16) acc[r] = dot_bf16_f32(wv, hv[r] + c16 * EPC, acc[r]);
+              else acc[r] = fmaf(dot_e4m3_f32(wv, hv[r] + c16 * EPC), __ldg(sc[r] + c16 / 8), acc[r]);
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < kRowsILP; ++r) {
+            const float v = warp_sum(acc[r]);
+            if (ok[r] && lane == 0) ybuf[yi[r]] = v;  // [entry][jl]
           }
         }
-#pragma unroll
-        for (int r = 0; r < kRowsILP; ++r) {
-          const float v = warp_sum(acc[r]);
-          if (ok[r] && lane == 0) ybuf[tr[r]] = v;  // [entry][jl]
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(empty + s));
+        done += m.z;
+        ++c;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + s));
-      done += m.z;
-      ++c;
     }
+    if (!cb_done) fetch_cb();  // no GPU entry at all: every pair is host-evaluated
     asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
 
     // ---- combine: one warp per output row; lane r < k holds pair r (ascending expert id)

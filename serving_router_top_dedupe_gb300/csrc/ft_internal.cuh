@@ -118,7 +118,7 @@ struct EvalParams {
   uint32_t* error_word;
   SlotLayout lay;
   int H, I, k, B, has_shared;
-  int n_sm;                 // SMs of the device (one streaming CTA each)
+  int n_sm;                 // CTAs of the batch-1 GEMV (one per SM it may use)
   int max_entries;          // capacity of the entry lists (kcap + 1)
   bool pdl;                 // launched as programmatic dependents
 };
@@ -157,6 +157,12 @@ struct RouterParams {
   int e_per_warp;     // router rows per warp
   bool pdl;
 };
+
+// Fill kernel shape: CTAs (SMs) that carry the host-link copy, threads per CTA, and the
+// shared memory each reserves so that no batch-1 GEMV CTA (~150 KB) shares its SM.
+constexpr int kFillSms = 16;
+constexpr int kFillThreads = 512;
+constexpr size_t kFillSmemReserve = 120 * 1024;
 
 // Kernel launchers (stream-ordered, no synchronisation).
 cudaError_t launch_control(const CtrlParams& p, cudaStream_t s);
