@@ -47,7 +47,6 @@ constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxStages = 8;
 constexpr size_t kStageTarget = 32 * 1024;
 constexpr size_t kSmemBudget = 220 * 1024;  // largest ring
-constexpr size_t kSmemShared = 150 * 1024;  // ring that still leaves room for a CTA of the next kernel
 constexpr int kRowsILP = 4;                 // phase-1 rows a consumer warp forms at once
 
 __host__ __device__ inline size_t round128(size_t b) { return (b + 127) / 128 * 128; }
@@ -75,10 +74,9 @@ __host__ __device__ inline FusedPlan make_fused_plan(int wtype, int H, int I, in
   pl.ybuf = round128((size_t)jpc * max_entries * 4);
   pl.cb = round128((size_t)jpc * kMaxK * 4);
   const size_t fixed = pl.xs + pl.hs + pl.ybuf + pl.cb + 1024;
-  // Prefer a ring that leaves room on the SM for a CTA of the next kernel; take the large
-  // ring when that would leave fewer than three stages.
-  int nst = fixed >= kSmemShared ? 0 : (int)((kSmemShared - fixed) / pl.stage);
-  if (nst < 3) nst = fixed >= kSmemBudget ? 0 : (int)((kSmemBudget - fixed) / pl.stage);
+  // The deepest ring that fits: bytes in flight per SM set the streaming rate.  (No CTA of
+  // another kernel shares the SM: the next layer's control kernel runs beside a fill CTA.)
+  const int nst = fixed >= kSmemBudget ? 0 : (int)((kSmemBudget - fixed) / pl.stage);
   pl.nst = nst > kMaxStages ? kMaxStages : nst;
   return pl;
 }
@@ -88,10 +86,15 @@ inline size_t fused_smem_bytes(const FusedPlan& pl) {
          128;
 }
 
-template <int WT>
+// HC, IC: 16-byte chunks per lane of an H row and of an I row when the shape is known at
+// compile time (0: taken from the parameters).  With them the dot loops are straight-line
+// code; with runtime bounds the guarded loops measured ~2.7x slower per row on GB300.
+template <int WT, int HC, int IC>
 __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, FusedPlan pl) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  // rounded up by pointer arithmetic on the shared array, so that the compiler still knows
+  // every derived pointer is in shared memory (shared loads, not generic ones)
+  uint8_t* smem = smem_raw + ((128u - (ptx::smem_u32(smem_raw) & 127u)) & 127u);
   uint8_t* stages = smem;
   uint16_t* xs = reinterpret_cast<uint16_t*>(stages + (size_t)pl.nst * pl.stage);
   float* hs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + pl.xs);
@@ -105,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
   constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
   constexpr int EPC = 16 / ESZ;  // weights per 16-byte chunk
   const int ne = p.counts[C_NENTRIES];
-  const int H = p.H, I = p.I, k = p.k;
+  // compile-time shapes make the unit and row index arithmetic constant as well
+  const int H = HC > 0 ? HC * 32 * EPC : p.H, I = IC > 0 ? IC * 32 * EPC : p.I, k = p.k;
   const size_t rh = (size_t)H * ESZ, ri = (size_t)I * ESZ;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -168,10 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
         // it waits for this grid to complete before anything else.
         if (pass == 0) pdl_trigger();
         const int n1 = npe * nj;
+        // phase-1 stages hold whole entries when an entry's rows fit in a stage
+        const int p1_rows = nj > 0 && nj <= pl.drows ? pl.drows / nj * nj : pl.drows;
         for (int t = 0; t < n1 && !*abort_flag;) {
           const int s = c % pl.nst, use = c / pl.nst;
           if (!mbar_wait(smem_u32(empty + s), (uint32_t)(use & 1) ^ 1u, abort_flag, p.error_word)) break;
-          const int nr = min(pl.drows, n1 - t);
+          const int nr = min(p1_rows, n1 - t);
           meta[s] = make_int4(1, t, nr, pass);
           const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
           mbar_arrive_expect_tx(fb, (uint32_t)(nr * ri));
@@ -258,7 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           const uint8_t* rg = st + (size_t)q * rh;          // gate row
           const uint8_t* ru = st + ((size_t)m.z + q) * rh;  // the same up row
           float a = 0.f, b = 0.f;                           // two independent chains
-          if (WT == FT_W_BF16) {
+          if (WT == FT_W_BF16 && HC > 0) {
+#pragma unroll
+            for (int cc = 0; cc < HC; ++cc) {
+              const int c16 = lane + 32 * cc;
+              const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
+              a = dot_bf16_bf16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), xv, a);
+              b = dot_bf16_bf16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), xv, b);
+            }
+          } else if (WT == FT_W_BF16) {
             for (int c16 = lane; c16 < H / EPC; c16 += 32) {
               const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
               a = dot_bf16_bf16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), xv, a);
@@ -267,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           } else {
             const float* sg = reinterpret_cast<const float*>(p.g_w[g] + p.lay.gs) + (size_t)i * (H / 128);
             const float* su = reinterpret_cast<const float*>(p.g_w[g] + p.lay.us) + (size_t)i * (H / 128);
+#pragma unroll 4
             for (int c16 = lane; c16 < H / EPC; c16 += 32) {
               const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)c16 * 16);
               const uint4 x0 = xp[0], x1 = xp[1];
@@ -305,10 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           if (!wait_counter(p.ready + pe[gi], (uint32_t)I, abort_flag, p.error_word)) break;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
-      for (int gi = 0; gi < npe; ++gi) {
-        const float4* hg = reinterpret_cast<const float4*>(p.h + (size_t)pe[gi] * I);
-        float4* h4 = reinterpret_cast<float4*>(hs + (size_t)pe[gi] * I);
-        for (int i4 = ct; i4 < I / 4; i4 += 32 * kConsumers) h4[i4] = __ldcg(hg + i4);
+      // one flat loop, so that every thread's loads of all the pass's entries are in flight
+      // together
+      for (int idx = ct; idx < npe * (I / 4); idx += 32 * kConsumers) {
+        const int gi = idx / (I / 4), i4 = idx - gi * (I / 4);
+        const size_t off = (size_t)pe[gi] * (I / 4) + i4;
+        reinterpret_cast<float4*>(hs)[off] = __ldcg(reinterpret_cast<const float4*>(p.h) + off);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
 
@@ -319,8 +336,57 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
         if (!mbar_wait(smem_u32(full + s), (uint32_t)(use & 1), abort_flag, p.error_word)) break;
         const int4 m = meta[s];
         const uint8_t* st = stages + (size_t)s * pl.stage;
+        const int rot = ((cw - done) % kConsumers + kConsumers) % kConsumers;
+        if (WT == FT_W_BF16 && IC > 0) {
+          // Work items are blocks of kRowsILP consecutive rows of one entry, so a warp loads
+          // that entry's h chunks once into registers for all the rows of the block.
+          // Products and their order per row are those of the per-row form below.
+          // items: entry-runs of the stage split into blocks of kRowsILP rows; a block past a
+          // run's end computes clamped duplicate rows and stores only its own
+          const int gfirst = m.y / nj, glast = (m.y + m.z - 1) / nj;
+          const int nb = (nj + kRowsILP - 1) / kRowsILP;  // blocks per run, at most
+          for (int item = rot; item < (glast - gfirst + 1) * nb; item += kConsumers) {
+            const int gi = gfirst + item / nb;
+            const int ra = max(m.y, gi * nj), rb = min(m.y + m.z, (gi + 1) * nj);
+            const int r0 = ra + (item % nb) * kRowsILP;
+            if (r0 >= rb) continue;
+            const int g = pe[gi];
+            const float* hv = hs + (size_t)g * I;
+            float4 h0[IC > 0 ? IC : 1], h1[IC > 0 ? IC : 1];
+#pragma unroll
+            for (int cc = 0; cc < IC; ++cc) {
+              const int c16 = lane + 32 * cc;
+              h0[cc] = *reinterpret_cast<const float4*>(hv + c16 * EPC);
+              h1[cc] = *reinterpret_cast<const float4*>(hv + c16 * EPC + 4);
+            }
+            const uint8_t* wrow[kRowsILP];
+#pragma unroll
+            for (int r = 0; r < kRowsILP; ++r) wrow[r] = st + (size_t)(min(r0 + r, rb - 1) - m.y) * ri;
+            float acc[kRowsILP];
+#pragma unroll
+            for (int r = 0; r < kRowsILP; ++r) acc[r] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < IC; ++cc) {
+              const int c16 = lane + 32 * cc;
+#pragma unroll
+              for (int r = 0; r < kRowsILP; ++r)
+                acc[r] = dot_bf16_f32v(*reinterpret_cast<const uint4*>(wrow[r] + (size_t)c16 * 16), h0[cc], h1[cc],
+                                       acc[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < kRowsILP; ++r) {
+              const float v = warp_sum(acc[r]);
+              if (r0 + r < rb && lane == 0) ybuf[(size_t)g * nj + (r0 + r - gi * nj)] = v;  // [entry][jl]
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(empty + s));
+          done += m.z;
+          ++c;
+          continue;
+        }
         // up to kRowsILP rows per warp at once: independent chains, each row in the usual order
-        for (int q = ((cw - done) % kConsumers + kConsumers) % kConsumers; q < m.z; q += kRowsILP * kConsumers) {
+        for (int q = rot; q < m.z; q += kRowsILP * kConsumers) {
           float acc[kRowsILP];
           const float* hv[kRowsILP];
           const float* sc[kRowsILP];
@@ -337,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
                                     : reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128);
             acc[r] = 0.f;
           }
+#pragma unroll 4
           for (int c16 = lane; c16 < I / EPC; c16 += 32) {
 #pragma unroll
             for (int r = 0; r < kRowsILP; ++r) {
@@ -381,10 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
   __syncthreads();
 }
 
-template <int WT>
+template <int WT, int HC, int IC>
 cudaError_t launch_fused_t(const EvalParams& p, int n_sm, int max_entries, cudaStream_t s) {
   const FusedPlan pl = make_fused_plan(WT, p.H, p.I, max_entries, n_sm);
-  return launch_k(fused_gemv_kernel<WT>, dim3(n_sm), dim3(kThreads), fused_smem_bytes(pl), s, p.pdl, p, pl);
+  return launch_k(fused_gemv_kernel<WT, HC, IC>, dim3(n_sm), dim3(kThreads), fused_smem_bytes(pl), s, p.pdl, p, pl);
+}
+
+// Shapes compiled with fixed chunk counts: the 35B-A3B expert shape (H 2048, I 512, BF16).
+template <int WT, int HC, int IC>
+constexpr bool fixed_shape_matches(int H, int I) {
+  return H == HC * 32 * (WT == FT_W_BF16 ? 8 : 16) && I == IC * 32 * (WT == FT_W_BF16 ? 8 : 16);
 }
 
 }  // namespace
@@ -395,15 +468,21 @@ bool fused_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm) {
 }
 
 cudaError_t launch_fused_gemv(const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s) {
-  return wtype == FT_W_BF16 ? launch_fused_t<FT_W_BF16>(p, n_sm, max_entries, s)
-                            : launch_fused_t<FT_W_FP8_E4M3_B128>(p, n_sm, max_entries, s);
+  if (wtype == FT_W_BF16 && fixed_shape_matches<FT_W_BF16, 8, 2>(p.H, p.I))
+    return launch_fused_t<FT_W_BF16, 8, 2>(p, n_sm, max_entries, s);
+  return wtype == FT_W_BF16 ? launch_fused_t<FT_W_BF16, 0, 0>(p, n_sm, max_entries, s)
+                            : launch_fused_t<FT_W_FP8_E4M3_B128, 0, 0>(p, n_sm, max_entries, s);
 }
 
 cudaError_t prepare_fused_gemv() {
   const int lim = (int)(kSmemBudget + 4096);
-  cudaError_t e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  cudaError_t e =
+      cudaFuncSetAttribute(fused_gemv_kernel<FT_W_BF16, 8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_FP8_E4M3_B128>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_BF16, 0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             lim);
   return e;
 }
 

@@ -44,18 +44,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of parity `parity`.  On timeout: error word + abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* error_word) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-  }
-  *abort_flag = 1;
-  atomicOr(error_word, FT_DEVERR_TIMEOUT);
-  return false;
-}
-
 // Bulk async copy global -> shared (16-byte aligned, size a multiple of 16), completing
 // `bytes` of transaction count on `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -89,6 +77,38 @@ __device__ __forceinline__ bool wait_counter(const uint32_t* counter, uint32_t t
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kFlagWaitNs) break;
     __nanosleep(64);
+  }
+  *abort_flag = 1;
+  atomicOr(error_word, FT_DEVERR_TIMEOUT);
+  return false;
+}
+
+// try_wait that lets the thread be suspended for up to `ns` while the phase is incomplete
+// (it resumes as soon as the phase completes), instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity`.  A waiting thread is suspended rather than
+// polling, so warps that wait take no issue slots from the warps of the same SM that work.
+// Gives up after kFlagWaitNs (error word + abort flag).
+constexpr uint32_t kSuspendHintNs = 2000;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* error_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kFlagWaitNs) break;
   }
   *abort_flag = 1;
   atomicOr(error_word, FT_DEVERR_TIMEOUT);
