@@ -282,6 +282,45 @@ class SlotCache:
         self.prefill_next_layer = layer + 1 if layer + 1 < n_layers else None
         return list(buf)
 
+    def prefill_layer_on_demand(self, layer: int, n_experts: int, active) -> list[list[int]]:
+        """Residency effect of one prefill layer when the pool cannot hold two
+        full layers (S < 2E).
+
+        [FT, "全层双缓冲"] and [FT2, paragraph on the double buffer]: without
+        room for the two full-layer buffers, prefill loads experts on demand
+        instead of oversubscribing memory.  Reading used here: the layer's
+        routing is known first; its active experts (sorted unique ids routed by
+        the chunk) that are resident are hits and are stamped with this step's
+        clock; the others are loaded into the least recently used slots that do
+        not hold a hit, ascending (stamp, slot), and stamped too.  When there
+        are fewer such slots (W) than misses, the misses are taken in ascending
+        id, W at a time, each wave into the same W slots, so the layer ends
+        with its hits and its last wave resident.  Prefill is not counted as
+        hits, misses or fills.  Returns the waves (lists of logical ids).
+        """
+        E = n_experts
+        self.buffers = None
+        self.prefill_next_layer = None
+        A = [layer * E + int(e) for e in sorted(set(int(e) for e in active))]
+        hits = [u for u in A if self.res[u] >= 0]
+        misses = [u for u in A if self.res[u] < 0]
+        self.clock += 1
+        for u in hits:
+            self.stamp[self.res[u]] = self.clock
+        free = int(np.count_nonzero(self.stamp < self.clock))
+        if misses and free == 0:
+            raise ValueError("no slot outside this layer's hits")
+        victims = self.lru_candidates(min(free, len(misses)))
+        waves = [misses[i:i + len(victims)] for i in range(0, len(misses), max(1, len(victims)))]
+        for wave in waves:
+            for u, v in zip(wave, victims):
+                if self.owner[v] >= 0:
+                    self.res[self.owner[v]] = -1
+                self.owner[v] = u
+                self.res[u] = v
+                self.stamp[v] = self.clock
+        return waves
+
     # -------------------------------------------------------------- resize
     def resize(self, new_slots: int) -> list[tuple[int, int]]:
         """Safe-point resize of the expert cache.

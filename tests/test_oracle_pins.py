@@ -184,6 +184,64 @@ def test_router_logits_brute_force_and_closed_forms():
     assert zs[0, 0] == float(np.dot(x[0].astype(np.float64), x[0].astype(np.float64)))
 
 
+def _naive_on_demand(slots, layer, E, active, clock):
+    """Independent model of an on-demand prefill layer: `slots` is a list of
+    [stamp, owner] per slot; returns the new clock.  Hits are refreshed; the misses
+    go, W at a time in ascending id, into the W least recently used slots that hold
+    no hit, ordered by (stamp, slot index)."""
+    clock += 1
+    want = sorted({layer * E + e for e in active})
+    where = {o: i for i, (st, o) in enumerate(slots) if o >= 0}
+    hit_slots = {where[u] for u in want if u in where}
+    for i in hit_slots:
+        slots[i][0] = clock
+    missing = [u for u in want if u not in where]
+    free = sorted((st, i) for i, (st, o) in enumerate(slots) if i not in hit_slots)
+    if missing:
+        assert free, "capacity"
+    width = len(free)
+    for start in range(0, len(missing), max(1, width)):
+        for (st, i), u in zip(free, missing[start:start + width]):
+            slots[i] = [clock, u]
+    return clock
+
+
+def test_on_demand_prefill_matches_naive_model_and_invariants():
+    rng = random.Random(23)
+    for _ in range(300):
+        E = rng.randint(2, 12)
+        L = rng.randint(1, 3)
+        S = rng.randint(1, 2 * E - 1)
+        cache = O.SlotCache(S, L * E)
+        slots = [[0, -1] for _ in range(S)]
+        clock = 0
+        for _step in range(rng.randint(1, 6)):
+            layer = rng.randrange(L)
+            active = rng.sample(range(E), rng.randint(1, E))
+            hits_before = sum(1 for e in set(active) if cache.res[layer * E + e] >= 0)
+            if hits_before == S and len(set(active)) > S:
+                continue  # no slot outside the hits: the capacity error case
+            waves = cache.prefill_layer_on_demand(layer, E, active)
+            clock = _naive_on_demand(slots, layer, E, active, clock)
+            assert cache.clock == clock
+            assert [int(v) for v in cache.stamp] == [st for st, _ in slots]
+            assert [int(v) for v in cache.owner] == [o for _, o in slots]
+            # residency is a bijection on occupied slots
+            for v in range(S):
+                if cache.owner[v] >= 0:
+                    assert cache.res[cache.owner[v]] == v
+            assert int(np.count_nonzero(cache.res >= 0)) == int(np.count_nonzero(cache.owner >= 0))
+            # the last wave and every hit of the layer are resident and stamped now
+            for u in (waves[-1] if waves else []):
+                assert cache.res[u] >= 0 and cache.stamp[cache.res[u]] == cache.clock
+            assert sum(len(w) for w in waves) == len(set(active)) - hits_before
+    # no slot outside the hits and a miss left: the reading has no answer
+    cache = O.SlotCache(1, 4)
+    cache.prefill_layer_on_demand(0, 4, [0])
+    with pytest.raises(ValueError):
+        cache.prefill_layer_on_demand(0, 4, [0, 1])
+
+
 def test_dedupe_is_sorted_union():
     sel = np.array([[3, 5], [1, 5], [3, 9]])
     assert O.dedupe(sel, 2, 16) == [33, 35, 37, 41]
