@@ -224,9 +224,14 @@ ft_status ft_graph_destroy(ft_graph* g);
  * in buffer (l - first) mod 2; the whole of layer l+1 is copied into the other
  * buffer with cudaMemcpyAsync on the transfer stream while layer l's routing and
  * grouped GEMM run on the compute stream.  All pairs run on the GPU.
+ * When the pool cannot hold two full layers (S < 2E), experts are loaded on demand
+ * instead, after the layer's routing: the chunk's resident experts are hits, the
+ * others go (ascending id) into the least recently used slots outside the hits, in
+ * waves when they outnumber those slots; this path synchronises with the host.
  *   n_tokens  1 <= T <= max_prefill_tokens
  *   x_bf16    dev [T][H] BF16;  logits dev [T][E] FP32;  out dev [T][H] FP32
- * Errors: FT_ERR_CAPACITY when S < 2E (the on-demand path is not built). */
+ * Errors: FT_ERR_CAPACITY when every slot holds an expert of the layer that the chunk
+ * uses and a miss remains (on-demand path only). */
 ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x_bf16, const float* logits,
                                float* out);
 

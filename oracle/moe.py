@@ -304,12 +304,12 @@ class SlotCache:
         A = [layer * E + int(e) for e in sorted(set(int(e) for e in active))]
         hits = [u for u in A if self.res[u] >= 0]
         misses = [u for u in A if self.res[u] < 0]
+        free = self.S - len(hits)  # slots that hold no hit of this layer
+        if misses and free == 0:
+            raise ValueError("no slot outside this layer's hits")  # nothing changed
         self.clock += 1
         for u in hits:
             self.stamp[self.res[u]] = self.clock
-        free = int(np.count_nonzero(self.stamp < self.clock))
-        if misses and free == 0:
-            raise ValueError("no slot outside this layer's hits")
         victims = self.lru_candidates(min(free, len(misses)))
         waves = [misses[i:i + len(victims)] for i in range(0, len(misses), max(1, len(victims)))]
         for wave in waves:

@@ -936,8 +936,6 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
     return fail(FT_ERR_INVALID, "n_tokens %d outside [1, max_prefill_tokens=%d]", n_tokens, h->cfg.max_prefill_tokens);
   if (!x_bf16 || !logits || !out) return fail(FT_ERR_INVALID, "null x/logits/out");
   if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
-  if (h->S < 2 * h->E)
-    return fail(FT_ERR_CAPACITY, "prefill double buffering needs >= 2E = %d slots (have %d)", 2 * h->E, h->S);
   if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
   FT_CUDA(cudaSetDevice(h->dev));
   ft::PrefillCtx c{};
@@ -973,9 +971,16 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   }
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev;
   std::string err;
-  cudaError_t e = ft::prefill_layer(h->pf, c, layer, n_tokens, static_cast<const uint16_t*>(x_bf16), logits, out,
-                                    h->prof ? &ev : nullptr, &err);
+  // two full-layer buffers when the pool holds them, else experts on demand
+  const bool streamed = h->S >= 2 * h->E;
+  cudaError_t e =
+      streamed ? ft::prefill_layer(h->pf, c, layer, n_tokens, static_cast<const uint16_t*>(x_bf16), logits, out,
+                                   h->prof ? &ev : nullptr, &err)
+               : ft::prefill_layer_on_demand(h->pf, c, layer, n_tokens, static_cast<const uint16_t*>(x_bf16), logits,
+                                             out, h->prof ? &ev : nullptr, &err);
   for (auto& r : ev) h->prof_live.push_back({r.first, r.second.first, r.second.second});
+  if (e == cudaErrorNotSupported && err.rfind("capacity", 0) == 0)
+    return fail(FT_ERR_CAPACITY, "prefill layer %d: %s", layer, err.c_str());
   if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill layer %d: %s %s", layer, cudaGetErrorString(e), err.c_str());
   return FT_OK;
 }
@@ -988,8 +993,6 @@ ft_status ft_moe_prefill_chunk_hidden(ft_moe* h, int layer, int n_tokens, const 
   if (!out) return fail(FT_ERR_INVALID, "null out");
   // the checks of ft_moe_prefill_chunk that do not depend on the logits, before any work
   if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
-  if (h->S < 2 * h->E)
-    return fail(FT_ERR_CAPACITY, "prefill double buffering needs >= 2E = %d slots (have %d)", 2 * h->E, h->S);
   if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
   FT_CUDA(cudaSetDevice(h->dev));
   if ((s = enqueue_router(h, layer, n_tokens, x_bf16, h->router_z, false)) != FT_OK) return s;

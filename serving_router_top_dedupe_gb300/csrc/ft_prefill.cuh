@@ -65,5 +65,10 @@ void prefill_destroy(PrefillState* p);
 void prefill_interrupt(PrefillState* p);
 cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T, const uint16_t* x,
                           const float* logits, float* out, ProfEvents* prof, std::string* err);
+// One prefill layer with experts loaded on demand, for pools smaller than two full layers
+// (S < 2E).  Host-synchronising.  Returns cudaErrorNotSupported with *err naming the
+// capacity when a miss has no slot outside the layer's hits.
+cudaError_t prefill_layer_on_demand(PrefillState* p, const PrefillCtx& c, int layer, int T, const uint16_t* x,
+                                    const float* logits, float* out, ProfEvents* prof, std::string* err);
 
 }  // namespace ft

@@ -339,6 +339,25 @@ cudaError_t dev_alloc(T** ptr, size_t n) {
   return cudaMalloc(reinterpret_cast<void**>(ptr), (n ? n : 1) * sizeof(T));
 }
 
+// Route a chunk and sort its pairs by entry: per-expert token masks, pair offsets and N
+// tiles per entry, the pair lists, the tile table and the token rows in pair order.
+cudaError_t route_chunk(PrefillState* p, const PrefillCtx& c, int T, const uint16_t* x, const float* logits) {
+  const int E = p->E, k = p->K;
+  cudaError_t r = cudaMemsetAsync(p->masks, 0, sizeof(uint32_t) * (size_t)E * p->W, c.cs);
+  if (r != cudaSuccess) return r;
+  prefill_route_kernel<<<(T + 7) / 8, 256, 0, c.cs>>>(logits, T, E, k, c.gate, p->W, p->sel, p->gates, p->masks,
+                                                      &c.st->error_word);
+  prefill_scan_kernel<<<1, 1024, 0, c.cs>>>(p->masks, p->W, E, T, p->has_shared, p->wpre, p->entry_off, p->tile_off);
+  const int n_pl = T * k + (p->has_shared ? T : 0);
+  prefill_place_kernel<<<(n_pl + 255) / 256, 256, 0, c.cs>>>(p->sel, p->gates, p->masks, p->wpre, p->entry_off, T, k,
+                                                             E, p->W, p->has_shared, p->pair_tok, p->pair_gate,
+                                                             p->pos_of);
+  const int n_ent = E + (p->has_shared ? 1 : 0);
+  prefill_tiles_kernel<<<(n_ent + 255) / 256, 256, 0, c.cs>>>(p->entry_off, p->tile_off, n_ent, p->tiles);
+  prefill_permute_kernel<<<p->n_sm * 8, 256, 0, c.cs>>>(x, p->pair_tok, n_pl, p->H, p->xp);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
@@ -490,22 +509,7 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   }
 
   // ---- route the chunk and sort its pairs by expert
-  e = timed(4, [&]() -> cudaError_t {
-    cudaError_t r = cudaMemsetAsync(p->masks, 0, sizeof(uint32_t) * (size_t)E * p->W, c.cs);
-    if (r != cudaSuccess) return r;
-    prefill_route_kernel<<<(T + 7) / 8, 256, 0, c.cs>>>(logits, T, E, k, c.gate, p->W, p->sel, p->gates, p->masks,
-                                                        &c.st->error_word);
-    prefill_scan_kernel<<<1, 1024, 0, c.cs>>>(p->masks, p->W, E, T, p->has_shared, p->wpre, p->entry_off,
-                                              p->tile_off);
-    const int n_pl = T * k + (p->has_shared ? T : 0);
-    prefill_place_kernel<<<(n_pl + 255) / 256, 256, 0, c.cs>>>(p->sel, p->gates, p->masks, p->wpre, p->entry_off, T,
-                                                               k, E, p->W, p->has_shared, p->pair_tok, p->pair_gate,
-                                                               p->pos_of);
-    const int n_ent = E + (p->has_shared ? 1 : 0);
-    prefill_tiles_kernel<<<(n_ent + 255) / 256, 256, 0, c.cs>>>(p->entry_off, p->tile_off, n_ent, p->tiles);
-    prefill_permute_kernel<<<p->n_sm * 8, 256, 0, c.cs>>>(x, p->pair_tok, n_pl, p->H, p->xp);
-    return cudaGetLastError();
-  });
+  e = timed(4, [&]() -> cudaError_t { return route_chunk(p, c, T, x, logits); });
   if (e != cudaSuccess) return e;
 
   // ---- grouped GEMMs on the tensor cores
@@ -554,6 +558,176 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
     p->active = false;
     p->next_layer = -1;
   }
+  return cudaSuccess;
+}
+
+}  // namespace ft
+
+namespace ft {
+namespace {
+
+__global__ void count_prefill_layer_kernel(DevState* st) { st->prefill_layers += 1ull; }
+
+}  // namespace
+
+// One prefill layer when the pool cannot hold two full-layer buffers (S < 2E): the
+// experts are loaded on demand instead ("FreeToken 完全拆解", section "全层双缓冲": without
+// room for the two buffers, prefill falls back to on-demand loading rather than
+// oversubscribing memory).  The chunk is routed first.  Its active experts that are
+// resident are hits and are stamped with the step's clock; the others go, in ascending
+// id, into the least recently used slots that hold no hit, W at a time when there are
+// more misses than such slots, each wave into the same W slots.  Every wave copies its
+// experts from the host pool and runs the two grouped GEMMs over its entries (the first
+// wave also over the hits and the shared expert); one combine follows.  The decisions are
+// taken on the host, between host synchronisations: this path serves pools too small for
+// the streamed one, where the host link is the bound anyway.
+cudaError_t prefill_layer_on_demand(PrefillState* p, const PrefillCtx& c, int layer, int T, const uint16_t* x,
+                                    const float* logits, float* out, ProfEvents* prof, std::string* err) {
+  cudaError_t e;
+  if (p->active) prefill_interrupt(p);  // a streamed chunk cannot continue here
+  p->cs = c.cs;
+  p->ts = c.ts;
+  const int E = p->E, L = p->L, S = c.S;
+  const bool sh = p->has_shared != 0;
+  const int n_ent = E + (sh ? 1 : 0);
+  auto timed = [&](int kind, auto&& body) -> cudaError_t {
+    cudaEvent_t a = nullptr, z = nullptr;
+    if (prof) {
+      cudaEventCreate(&a);
+      cudaEventCreate(&z);
+      cudaEventRecord(a, c.cs);
+    }
+    cudaError_t r = body();
+    if (prof) {
+      cudaEventRecord(z, c.cs);
+      prof->push_back({kind, {a, z}});
+    }
+    return r;
+  };
+
+  // ---- route the chunk, then read its per-expert pair offsets and the residency state
+  if ((e = timed(4, [&]() -> cudaError_t { return route_chunk(p, c, T, x, logits); })) != cudaSuccess) return e;
+  std::vector<int32_t> eoff(n_ent + 1), res((size_t)L * E), owner(S);
+  std::vector<uint32_t> stamp(S);
+  uint32_t clock = 0;
+  if ((e = cudaMemcpyAsync(eoff.data(), p->entry_off, sizeof(int32_t) * (n_ent + 1), cudaMemcpyDeviceToHost, c.cs)) ||
+      (e = cudaMemcpyAsync(res.data(), c.res, sizeof(int32_t) * res.size(), cudaMemcpyDeviceToHost, c.cs)) ||
+      (e = cudaMemcpyAsync(owner.data(), c.owner, sizeof(int32_t) * S, cudaMemcpyDeviceToHost, c.cs)) ||
+      (e = cudaMemcpyAsync(stamp.data(), c.stamp, sizeof(uint32_t) * S, cudaMemcpyDeviceToHost, c.cs)) ||
+      (e = cudaMemcpyAsync(&clock, &c.st->clock, sizeof(uint32_t), cudaMemcpyDeviceToHost, c.cs)) ||
+      (e = cudaStreamSynchronize(c.cs)))
+    return e;
+
+  // ---- decisions: hits, misses (ascending id), LRU slots outside the hits
+  const int base = layer * E;
+  std::vector<int> hits, misses;
+  for (int x_e = 0; x_e < E; ++x_e) {
+    if (eoff[x_e + 1] <= eoff[x_e]) continue;
+    (res[base + x_e] >= 0 ? hits : misses).push_back(base + x_e);
+  }
+  std::vector<char> hit_slot(S, 0);
+  for (int u : hits) hit_slot[res[u]] = 1;
+  std::vector<int> cand;
+  for (int v = 0; v < S; ++v)
+    if (!hit_slot[v]) cand.push_back(v);
+  if (!misses.empty() && cand.empty()) {
+    if (err) *err = "capacity: every slot holds an expert of this layer that the chunk uses";
+    return cudaErrorNotSupported;
+  }
+  std::sort(cand.begin(), cand.end(), [&](int a, int b) { return stamp[a] != stamp[b] ? stamp[a] < stamp[b] : a < b; });
+  const int width = std::min((int)cand.size(), (int)misses.size());
+  const uint32_t now = clock + 1;
+  std::vector<int32_t> slot_of(E, 0);  // slot the GEMM reads for each expert of the layer (idle ones: 0)
+  for (int u : hits) {
+    stamp[res[u]] = now;
+    slot_of[u - base] = res[u];
+  }
+
+  // ---- waves
+  const size_t seg[3] = {p->lay.gate, p->lay.up, p->lay.down};
+  const int n_waves = misses.empty() ? 1 : ((int)misses.size() + width - 1) / width;
+  std::vector<int32_t> toff(n_ent + 1);
+  for (int w = 0; w < n_waves; ++w) {
+    std::vector<char> in_wave(n_ent, 0);
+    if (w == 0) {
+      for (int u : hits) in_wave[u - base] = 1;
+      if (sh) in_wave[E] = 1;
+    }
+    const int m0 = w * width, m1 = std::min((int)misses.size(), m0 + width);
+    for (int i = m0; i < m1; ++i) {
+      const int u = misses[i], v = cand[i - m0];
+      if (owner[v] >= 0) res[owner[v]] = -1;
+      owner[v] = u;
+      res[u] = v;
+      stamp[v] = now;
+      in_wave[u - base] = 1;
+      slot_of[u - base] = v;
+      // after the previous wave's GEMMs (same stream), which read this slot
+      for (int j = 0; j < 3; ++j)
+        if ((e = cudaMemcpyAsync(p->pool + (size_t)v * p->lay.stride + seg[j], p->bank_host[j] + (size_t)u * p->bank_row[j],
+                                 p->bank_row[j], cudaMemcpyHostToDevice, c.cs)) != cudaSuccess)
+          return e;
+    }
+    toff[0] = 0;
+    for (int i = 0; i < n_ent; ++i)
+      toff[i + 1] = toff[i] + (in_wave[i] ? (eoff[i + 1] - eoff[i] + kTileN - 1) / kTileN : 0);
+    if ((e = cudaMemcpyAsync(p->tile_off, toff.data(), sizeof(int32_t) * (n_ent + 1), cudaMemcpyHostToDevice, c.cs)) ||
+        (e = cudaMemcpyAsync(p->buf_dev, slot_of.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice, c.cs)))
+      return e;
+    prefill_tiles_kernel<<<(n_ent + 255) / 256, 256, 0, c.cs>>>(p->entry_off, p->tile_off, n_ent, p->tiles);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    GemmDesc d{};
+    d.n_entries = n_ent;
+    d.E = E;
+    d.layer = layer;
+    d.I = p->I;
+    d.H = p->H;
+    d.entry_off = p->entry_off;
+    d.tile_off = p->tile_off;
+    d.tiles = p->tiles;
+    d.buf_slots = p->buf_dev;
+    d.pair_tok = p->pair_tok;
+    d.pair_gate = p->pair_gate;
+    d.h = p->h;
+    d.rows = p->rows;
+    d.error_word = &c.st->error_word;
+    e = timed(5, [&]() -> cudaError_t {
+      d.mt = p->I / 64;
+      d.kb = p->H / 64;
+      return launch_grouped_gemm(0, p->maps, x, T, d, p->n_sm, c.cs);
+    });
+    if (e == cudaSuccess)
+      e = timed(8, [&]() -> cudaError_t {
+        d.mt = p->H / 128;
+        d.kb = p->I / 64;
+        return launch_grouped_gemm(1, p->maps, x, T, d, p->n_sm, c.cs);
+      });
+    if (e != cudaSuccess) {
+      if (err) *err = "grouped GEMM launch";
+      return e;
+    }
+    // the host arrays above are rewritten by the next wave: let this wave's copies finish
+    if ((e = cudaStreamSynchronize(c.cs)) != cudaSuccess) return e;
+  }
+
+  // ---- residency state back, then the fixed-order combine
+  if ((e = cudaMemcpyAsync(c.res, res.data(), sizeof(int32_t) * res.size(), cudaMemcpyHostToDevice, c.cs)) ||
+      (e = cudaMemcpyAsync(c.owner, owner.data(), sizeof(int32_t) * S, cudaMemcpyHostToDevice, c.cs)) ||
+      (e = cudaMemcpyAsync(c.stamp, stamp.data(), sizeof(uint32_t) * S, cudaMemcpyHostToDevice, c.cs)) ||
+      (e = cudaMemcpyAsync(&c.st->clock, &now, sizeof(uint32_t), cudaMemcpyHostToDevice, c.cs)))
+    return e;
+  count_prefill_layer_kernel<<<1, 1, 0, c.cs>>>(c.st);
+  e = timed(6, [&]() -> cudaError_t {
+    const size_t n = (size_t)T * (p->H / 8);
+    prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, c.cs>>>(p->rows, p->pos_of, p->entry_off, T, p->K,
+                                                                          p->H, E, p->has_shared, out);
+    return cudaGetLastError();
+  });
+  if (e != cudaSuccess) return e;
+  // the host copies of the state are locals: they must be read before returning
+  if ((e = cudaStreamSynchronize(c.cs)) != cudaSuccess) return e;
+  p->active = false;
+  p->next_layer = -1;
   return cudaSuccess;
 }
 

@@ -185,7 +185,11 @@ def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None, hidd
     F, w = r.F, r.w
     xb = synth.prefill_x(w, chunk, layer, T)
     z = r.gpu_logits(layer, xb) if hidden else synth.prefill_logits(w, chunk, layer, T)
-    r.sim.prefill_layer(layer, w.n_experts, w.n_layers)
+    if r.S >= 2 * w.n_experts:
+        r.sim.prefill_layer(layer, w.n_experts, w.n_layers)
+    else:  # the pool cannot hold two full layers: experts on demand
+        sel_z, _ = O.route(z, w.top_k, r.gate)
+        r.sim.prefill_layer_on_demand(layer, w.n_experts, np.unique(sel_z))
     x_d = torch.from_numpy(xb.view(np.int16)).to(r.dev)
     z_d = torch.from_numpy(z).to(r.dev)
     out_d = torch.empty((T, w.hidden), dtype=torch.float32, device=r.dev)

@@ -68,17 +68,50 @@ def test_prefill_with_shared_expert():
             prefill_step(r, 0, l, 300, check_tokens=list(range(0, 300, 7)))
 
 
-def test_prefill_rejects_small_pool():
-    w = synth.prefill().with_(n_layers=2, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=31)
+@pytest.mark.parametrize("slots", [31, 6])
+def test_prefill_on_demand_small_pool_then_decode(slots):
+    """Pools smaller than two full layers (16 experts, top-2): 31 slots load each layer's
+    misses in one wave, 6 slots in waves of at most 6.  Residency after every layer and
+    every output row are compared with the oracle; decode steps follow on what is left."""
+    w = synth.prefill().with_(n_layers=4, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=slots,
+                              prefill_tokens=200)
+    with Run(w, max_prefill_tokens=256) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 200)
+        for l in range(w.n_layers):  # a second chunk: some experts are now hits
+            prefill_step(r, 1, l, 120)
+        r.compare_state()
+        r.w = w.with_(logits="normal")
+        for s in range(3):
+            for l in range(w.n_layers):
+                r.step(s, l, check_out=True)
+        r.compare_state()
+        print(f"slots {slots}: max rel err {r.max_err:.2e}")
+
+
+def test_prefill_on_demand_capacity_error_changes_nothing():
+    """One slot: after a layer, its last expert is resident; a chunk that uses it and
+    another expert has no slot for the miss, so the call fails and no state changes."""
+    w = synth.prefill().with_(n_layers=2, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=1,
+                              prefill_tokens=64)
     with Run(w, max_prefill_tokens=64) as r:
         import torch
 
+        prefill_step(r, 0, 0, 64)
+        r.compare_state()
+        u = int(r.sim.owner[0])  # the one slot holds the layer's last loaded expert
+        assert u >= 0
+        e_res = u % w.n_experts
+        z = torch.full((8, 16), -4.0, dtype=torch.float32, device="cuda")
+        z[:, e_res] = 5.0
+        z[:, (e_res + 1) % 16] = 4.0  # every token: the resident expert and one more
         x = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
-        z = torch.zeros((8, 16), dtype=torch.float32, device="cuda")
         o = torch.empty((8, 256), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
         with pytest.raises(r.F.FtError) as e:
             r.F.ft_moe_prefill_chunk(r.h, 0, 8, x, z, o)
         assert e.value.status == r.F.FT_ERR_CAPACITY
+        r.compare_state()  # unchanged: the oracle was not stepped
 
 
 def test_prefill_double_buffer_off_same_results():

@@ -238,8 +238,11 @@ def test_on_demand_prefill_matches_naive_model_and_invariants():
     # no slot outside the hits and a miss left: the reading has no answer
     cache = O.SlotCache(1, 4)
     cache.prefill_layer_on_demand(0, 4, [0])
+    before = (cache.clock, cache.res.copy(), cache.owner.copy(), cache.stamp.copy())
     with pytest.raises(ValueError):
         cache.prefill_layer_on_demand(0, 4, [0, 1])
+    assert cache.clock == before[0] and np.array_equal(cache.res, before[1])
+    assert np.array_equal(cache.owner, before[2]) and np.array_equal(cache.stamp, before[3])
 
 
 def test_dedupe_is_sorted_union():
