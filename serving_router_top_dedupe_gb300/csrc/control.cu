@@ -143,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     s_ncand = 0;
     s_done = 0;
   }
+  // The logits may be written by the kernel right before this one, so they are read only
+  // after the wait; an L2 prefetch of their lines now is safe (the L2 is coherent and a
+  // prefetch returns no data) and takes the DRAM latency off the routing step.
+  for (int i = tid * 32; i < B * E; i += kThreads * 32)
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.logits + i));
   // logits and the work lists belong to the kernel right before this one
   pdl_wait();
   pdl_trigger();

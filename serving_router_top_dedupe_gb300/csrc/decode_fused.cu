@@ -316,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           atomicAdd(p.ready + pe[gi], (uint32_t)(end - v));
           v = end;
         }
-        for (int gi = 0; gi < npe; ++gi)
-          if (!wait_counter(p.ready + pe[gi], (uint32_t)I, abort_flag, p.error_word)) break;
       }
+      // every warp waits on its own entries' counters, so the polls run side by side
+      if (lane == 0)
+        for (int gi = cw; gi < npe; gi += kConsumers)
+          if (!wait_counter(p.ready + pe[gi], (uint32_t)I, abort_flag, p.error_word)) break;
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
       // one flat loop, so that every thread's loads of all the pass's entries are in flight
       // together
