@@ -392,6 +392,46 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
+NVFP4_BLOCK = 16   # elements per block scale along the reduction dimension
+
+
+def _e2m1_value(code: int) -> float:
+    """One E2M1 (FP4) code: 1 sign, 2 exponent (bias 1), 1 mantissa bit; exponent 0 is
+    subnormal (m/2).  The block-scaled 4-bit formats that [FT, 主结果] names for its models
+    (MXFP4, NVFP4) use these elements."""
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m * 0.5
+    return s * 2.0 ** (e - 1) * (1.0 + m / 2.0)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_unpack_to_f64(packed: np.ndarray) -> np.ndarray:
+    """Packed FP4 rows [R][K/2] (byte j: element 2j in the low nibble, 2j+1 in the high
+    nibble) -> float64 [R][K]."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.float64)
+    out[..., 0::2] = E2M1_TABLE[b & 0xF]
+    out[..., 1::2] = E2M1_TABLE[b >> 4]
+    return out
+
+
+def matvec_nvfp4(packed: np.ndarray, block_scales: np.ndarray, tensor_scale: float, x: np.ndarray) -> np.ndarray:
+    """NVFP4 rows times x: E2M1 elements, one E4M3 scale per 1x16 block along the
+    reduction dimension applied after the block's dot product, then the bank's FP32
+    tensor scale.  (The post-scaling order of [P3, §4.2], with NVFP4's block size.)"""
+    w = e2m1_unpack_to_f64(packed)
+    R, K = w.shape
+    nb = K // NVFP4_BLOCK
+    block_dots = np.einsum("rbk,bk->rb", w.reshape(R, nb, NVFP4_BLOCK),
+                           np.asarray(x, dtype=np.float64).reshape(nb, NVFP4_BLOCK))
+    return float(tensor_scale) * (block_dots * e4m3_to_f64(block_scales)).sum(axis=1)
+
+
 def silu(a: np.ndarray) -> np.ndarray:
     return a / (1.0 + np.exp(-a))
 
@@ -415,8 +455,17 @@ def swiglu_expert(expert: dict, x: np.ndarray, fp8: bool) -> np.ndarray:
 
     Bank layout (per expert, row-major): gate [I][H], up [I][H], down [H][I];
     FP8 scales gate_scale/up_scale [I][H/128], down_scale [H][I/128].
+    `fp8` is the weight type: 0/False BF16, 1/True FP8 E4M3, 2 NVFP4 (packed E2M1
+    [rows][K/2], E4M3 block scales [rows][K/16], tensor_scale [4] FP32: gate, up,
+    down, unused).
     [FT2, paragraph on the double buffer] / [P3, §4.3] (gate, up, down projections).
     """
+    if fp8 == 2:  # NVFP4: tensor_scale holds the gate, up and down banks' scales
+        ts = expert["tensor_scale"].astype(np.float64)
+        a = matvec_nvfp4(expert["gate"], expert["gate_bscale"], ts[0], x)
+        b = matvec_nvfp4(expert["up"], expert["up_bscale"], ts[1], x)
+        h = silu(a) * b
+        return matvec_nvfp4(expert["down"], expert["down_bscale"], ts[2], h)
     if fp8:
         a = matvec_post_scaled(expert["gate"], expert["gate_scale"], x)
         b = matvec_post_scaled(expert["up"], expert["up_scale"], x)

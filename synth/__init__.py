@@ -32,6 +32,7 @@ _GAMMA = 0x9E3779B97F4A7C15
 # Stream tags (arbitrary distinct integers).
 TAG_GATE, TAG_UP, TAG_DOWN = 1, 2, 3
 TAG_GATE_SCALE, TAG_UP_SCALE, TAG_DOWN_SCALE = 4, 5, 6
+TAG_TENSOR_SCALE = 8
 TAG_OFFSET = 7
 TAG_X, TAG_LOGIT = 10, 11
 TAG_PERM, TAG_TRACE = 12, 13
@@ -40,6 +41,7 @@ TAG_ROUTER = 40
 
 W_BF16 = 0
 W_FP8_E4M3_B128 = 1
+W_NVFP4 = 2
 
 FP8_BLOCK = 128
 
@@ -222,6 +224,10 @@ def bank_shapes(w: Workload) -> dict:
     if w.wtype == W_FP8_E4M3_B128:
         s.update({"gate_scale": (I, H // FP8_BLOCK), "up_scale": (I, H // FP8_BLOCK),
                   "down_scale": (H, I // FP8_BLOCK)})
+    if w.wtype == W_NVFP4:  # packed E2M1 (two per byte), E4M3 scales per 16, FP32 tensor scales
+        s = {"gate": (I, H // 2), "up": (I, H // 2), "down": (H, I // 2),
+             "gate_bscale": (I, H // 16), "up_bscale": (I, H // 16), "down_bscale": (H, I // 16),
+             "tensor_scale": (4,)}
     return s
 
 
@@ -230,11 +236,16 @@ def bank_dtypes(w: Workload) -> dict:
     d = {"gate": wd, "up": wd, "down": wd}
     if w.wtype == W_FP8_E4M3_B128:
         d.update({"gate_scale": np.float32, "up_scale": np.float32, "down_scale": np.float32})
+    if w.wtype == W_NVFP4:
+        d.update({"gate_bscale": np.uint8, "up_bscale": np.uint8, "down_bscale": np.uint8,
+                  "tensor_scale": np.float32})
     return d
 
 
 _TAGS = {"gate": TAG_GATE, "up": TAG_UP, "down": TAG_DOWN,
-         "gate_scale": TAG_GATE_SCALE, "up_scale": TAG_UP_SCALE, "down_scale": TAG_DOWN_SCALE}
+         "gate_scale": TAG_GATE_SCALE, "up_scale": TAG_UP_SCALE, "down_scale": TAG_DOWN_SCALE,
+         "gate_bscale": TAG_GATE_SCALE, "up_bscale": TAG_UP_SCALE, "down_bscale": TAG_DOWN_SCALE,
+         "tensor_scale": TAG_TENSOR_SCALE}
 
 
 class ExpertPool:
@@ -247,7 +258,10 @@ class ExpertPool:
     BF16 banks: N(0, weight_std) rounded to bfloat16.  FP8 banks: E4M3 codes
     from N(0, weight_std * 448) (saturating RNE), with one FP32 scale per
     128-element block along the reduction dimension drawn from U(0.5, 2)/448,
-    so that dequantised weights have roughly the BF16 banks' spread.
+    so that dequantised weights have roughly the BF16 banks' spread.  NVFP4
+    banks: uniform E2M1 codes, E4M3 block scales in [0.5, 2) per 16 elements
+    and per-expert FP32 tensor scales in U(0.004, 0.008) (dequantised weights
+    of about 0.02 rms).
     """
 
     def __init__(self, w: Workload):
@@ -259,8 +273,14 @@ class ExpertPool:
             n = int(np.prod(shp))
             period = _prime_at_least(max(1 << 22, 2 * n + 1))
             key = derive_key(w.seed, _TAGS[kind])
-            if kind.endswith("_scale"):
+            if kind == "tensor_scale":
+                vals = (0.004 + 0.004 * uniform(key, period)).astype(np.float32)
+            elif kind.endswith("_bscale"):  # E4M3 codes 0x30..0x3F: 0.5 .. 1.875
+                vals = (0x30 + (raw_u64(key, period) & np.uint64(0xF))).astype(np.uint8)
+            elif kind.endswith("_scale"):
                 vals = ((0.5 + 1.5 * uniform(key, period)) / 448.0).astype(np.float32)
+            elif w.wtype == W_NVFP4:  # two uniform E2M1 codes per byte
+                vals = (raw_u64(key, period) & np.uint64(0xFF)).astype(np.uint8)
             elif w.wtype == W_BF16:
                 vals = f32_to_bf16_bits((normal(key, period) * w.weight_std).astype(np.float32))
             else:

@@ -245,6 +245,45 @@ def test_on_demand_prefill_matches_naive_model_and_invariants():
     assert np.array_equal(cache.owner, before[2]) and np.array_equal(cache.stamp, before[3])
 
 
+def test_e2m1_values_from_float32_bit_patterns():
+    """Every FP4 (E2M1) code against the float32 with the same sign, exponent and
+    mantissa fields (exponent rebiased from 1 to 127; exponent 0 is subnormal)."""
+    import struct
+
+    for code in range(16):
+        sign, exp, man = code >> 3, (code >> 1) & 3, code & 1
+        if exp == 0:
+            ref = (-1.0 if sign else 1.0) * man * 0.5
+        else:
+            bits = (sign << 31) | ((exp - 1 + 127) << 23) | (man << 22)
+            ref = struct.unpack("<f", struct.pack("<I", bits))[0]
+        assert O.E2M1_TABLE[code] == ref, code
+    # byte 0x21: element 0 is the low nibble (code 1 = 0.5), element 1 the high one (code 2 = 1)
+    assert O.e2m1_unpack_to_f64(np.array([[0x21, 0xF7]], dtype=np.uint8)).tolist() == [[0.5, 1.0, 6.0, -6.0]]
+
+
+def test_nvfp4_matvec_post_scaled_equals_dequantise_first_and_brute_force():
+    rng = np.random.default_rng(29)
+    R, K = 5, 64
+    packed = rng.integers(0, 256, size=(R, K // 2), dtype=np.uint8)
+    bscale = rng.integers(0x28, 0x48, size=(R, K // O.NVFP4_BLOCK), dtype=np.uint8)
+    ts = 0.0073
+    x = rng.standard_normal(K)
+    y = O.matvec_nvfp4(packed, bscale, ts, x)
+    w = O.e2m1_unpack_to_f64(packed) * np.repeat(O.e4m3_to_f64(bscale), O.NVFP4_BLOCK, axis=1) * ts
+    np.testing.assert_allclose(y, w @ x, rtol=1e-12, atol=1e-15)
+    for r in range(R):  # scalar loop: nibbles, blocks, scales written out
+        tot = 0.0
+        for b in range(K // 16):
+            part = 0.0
+            for j in range(16):
+                k = 16 * b + j
+                code = (int(packed[r, k // 2]) >> (4 * (k % 2))) & 0xF
+                part += O.E2M1_TABLE[code] * x[k]
+            tot += part * O.e4m3_to_f64(np.array([bscale[r, b]]))[0]
+        assert abs(ts * tot - y[r]) <= 1e-12 * max(1.0, abs(y[r]))
+
+
 def test_dedupe_is_sorted_union():
     sel = np.array([[3, 5], [1, 5], [3, 9]])
     assert O.dedupe(sel, 2, 16) == [33, 35, 37, 41]
