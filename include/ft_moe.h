@@ -58,7 +58,16 @@ typedef enum {
   FT_ERR_DEVICE = 8     /* the device error word is non-zero */
 } ft_status;
 
-typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1 } ft_wtype;
+/* Expert weight formats.
+ *   FT_W_BF16           BF16 weights.
+ *   FT_W_FP8_E4M3_B128  E4M3 weights, one FP32 scale per 1x128 block along the reduction
+ *                       dimension, applied after the block's dot product ([P3] §4.2).
+ *   FT_W_NVFP4          E2M1 (FP4) weights packed two per byte (element 2j in the low
+ *                       nibble), one E4M3 scale per 1x16 block along the reduction
+ *                       dimension applied after the block's dot product, then one FP32
+ *                       tensor scale per bank of each expert ([FT] 主结果 names NVFP4
+ *                       experts).  Decode only; prefill is BF16. */
+typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1, FT_W_NVFP4 = 2 } ft_wtype;
 
 /* How a decode step moves F-set experts from the host pool into their slots.
  * FT_FILL_KERNEL: one fixed-shape copy kernel on the transfer stream reads the
@@ -80,7 +89,7 @@ typedef enum { FT_FILL_KERNEL = 0, FT_FILL_MEMCPY = 1 } ft_fill_mode;
 
 typedef struct {
   int n_layers;           /* L: MoE layers */
-  int hidden;             /* H: model width (multiple of 256; FP8: of 128) */
+  int hidden;             /* H: model width (multiple of 256; FP8: of 512) */
   int inter;              /* I: expert intermediate width (multiple of 128) */
   int n_experts;          /* E: routed experts per layer (<= 1024) */
   int top_k;              /* k (<= 16, <= E) */
@@ -99,10 +108,14 @@ typedef struct {
 
 /* Host expert banks ([FT] "FTW 权重格式与平台适配": first dimension of every bank is
  * the logical id; rows with the same id form one expert).  Row-major:
- *   gate, up   [L*E][I][H]        BF16 bits (uint16) or E4M3 codes (uint8)
- *   down       [L*E][H][I]
- *   gate_scale, up_scale [L*E][I][H/128] FP32 (FP8 only; NULL for BF16)
+ *   gate, up   [L*E][I][H]        BF16 bits (uint16), E4M3 codes (uint8), or NVFP4:
+ *                                 [L*E][I][H/2] packed E2M1 codes
+ *   down       [L*E][H][I]        (NVFP4: [L*E][H][I/2])
+ *   gate_scale, up_scale [L*E][I][H/128] FP32 (FP8 only; NULL otherwise)
  *   down_scale [L*E][H][I/128]           FP32 (FP8 only)
+ *   gate_bscale, up_bscale [L*E][I][H/16] E4M3 codes (NVFP4 only; NULL otherwise)
+ *   down_bscale [L*E][H][I/16]            E4M3 codes (NVFP4 only)
+ *   tensor_scale [L*E][4] FP32: gate, up, down, unused (NVFP4 only)
  * For the shared-expert banks the first dimension is L (one per layer). */
 typedef struct {
   const void* gate;
@@ -111,6 +124,10 @@ typedef struct {
   const float* gate_scale;
   const float* up_scale;
   const float* down_scale;
+  const uint8_t* gate_bscale;
+  const uint8_t* up_bscale;
+  const uint8_t* down_bscale;
+  const float* tensor_scale;
 } ft_banks;
 
 typedef struct ft_moe ft_moe;

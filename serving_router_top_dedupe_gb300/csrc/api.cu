@@ -88,7 +88,7 @@ struct ft_moe {
   int S = 0, L = 0, E = 0, K = 0, H = 0, I = 0, kcap = 0;
   long long bp_mbs = 0, bh_mbs = 0;
   double bp_gbps = 0, bh_gbps = 0;
-  HostBank bank[6];
+  HostBank bank[7];
   int n_banks = 3;
   uint8_t* pool = nullptr;
   uint8_t* shared_w = nullptr;
@@ -120,9 +120,10 @@ namespace ft {
 
 SlotLayout make_layout(int wtype, int H, int I) {
   SlotLayout l{};
-  const size_t esz = wtype == FT_W_BF16 ? 2 : 1;
-  l.gate_b = (size_t)I * H * esz;
-  l.down_b = (size_t)H * I * esz;
+  // weight bytes per element times 2: BF16 4, FP8 2, FP4 1
+  const size_t e2 = wtype == FT_W_BF16 ? 4 : (wtype == FT_W_FP8_E4M3_B128 ? 2 : 1);
+  l.gate_b = (size_t)I * H * e2 / 2;
+  l.down_b = (size_t)H * I * e2 / 2;
   l.gate = 0;
   l.up = l.gate_b;
   l.down = 2 * l.gate_b;
@@ -130,12 +131,18 @@ SlotLayout make_layout(int wtype, int H, int I) {
   if (wtype == FT_W_FP8_E4M3_B128) {
     l.gs_b = (size_t)I * (H / 128) * 4;
     l.ds_b = (size_t)H * (I / 128) * 4;
-    l.gs = end;
-    l.us = l.gs + l.gs_b;
-    l.ds = l.us + l.gs_b;
-    end = l.ds + l.ds_b;
-  } else {
-    l.gs = l.us = l.ds = end;
+  } else if (wtype == FT_W_NVFP4) {
+    l.gs_b = (size_t)I * (H / 16);
+    l.ds_b = (size_t)H * (I / 16);
+  }
+  l.gs = end;
+  l.us = l.gs + l.gs_b;
+  l.ds = l.us + l.gs_b;
+  end = l.ds + l.ds_b;
+  l.ts = end;
+  if (wtype == FT_W_NVFP4) {
+    l.ts_b = 16;
+    end += l.ts_b;
   }
   l.used = end;
   l.stride = (end + 255) / 256 * 256;
@@ -230,8 +237,9 @@ ft_status check_cfg(const ft_moe_config* c) {
     return fail(FT_ERR_INVALID, "n_layers >= 1 and 1 <= n_experts <= %d required", ft::kMaxE);
   if (c->top_k < 1 || c->top_k > ft::kMaxK || c->top_k > c->n_experts)
     return fail(FT_ERR_INVALID, "1 <= top_k <= min(%d, n_experts) required", ft::kMaxK);
-  if (c->wtype != FT_W_BF16 && c->wtype != FT_W_FP8_E4M3_B128) return fail(FT_ERR_INVALID, "unknown wtype");
-  const int hmul = c->wtype == FT_W_BF16 ? 256 : 512;
+  if (c->wtype != FT_W_BF16 && c->wtype != FT_W_FP8_E4M3_B128 && c->wtype != FT_W_NVFP4)
+    return fail(FT_ERR_INVALID, "unknown wtype");
+  const int hmul = c->wtype == FT_W_FP8_E4M3_B128 ? 512 : 256;
   if (c->hidden < hmul || c->hidden % hmul) return fail(FT_ERR_INVALID, "hidden must be a multiple of %d", hmul);
   if (c->inter < 128 || c->inter % 128) return fail(FT_ERR_INVALID, "inter must be a multiple of 128");
   if (c->max_batch < 1 || c->max_batch > ft::kMaxBatch)
@@ -359,7 +367,7 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
                             cudaMemcpyDeviceToHost, ts));
     FT_CUDA(cudaStreamSynchronize(ts));
     const int q = h->counts_host[ft::C_Q];
-    const size_t seg[6] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds};
+    const size_t seg[7] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds, h->lay.ts};
     if ((s = prof_begin(h, ts, &pa)) != FT_OK) return s;
     for (int i = 0; i < q; ++i) {
       const int u = h->copy_host[i], slot = h->copy_host[h->kcap + i];
@@ -530,7 +538,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   h->S = cfg->cache_slots;
   h->kcap = std::min(cfg->max_batch * cfg->top_k, cfg->n_experts);
   h->lay = ft::make_layout(cfg->wtype, h->H, h->I);
-  h->n_banks = fp8 ? 6 : 3;
+  h->n_banks = fp8 ? 6 : (cfg->wtype == FT_W_NVFP4 ? 7 : 3);
   h->grid_eval = h->n_sm * 4;
   h->grid_fill = std::max(1, std::min(ft::kFillSms, h->n_sm / 4));
   if (cfg->compute_stream) {
@@ -558,9 +566,16 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
 
   // host pool: pin + map every bank
   const size_t nlog = (size_t)h->L * h->E;
-  const void* bp[6] = {host_pool->gate, host_pool->up, host_pool->down,
-                       host_pool->gate_scale, host_pool->up_scale, host_pool->down_scale};
-  const size_t rows[6] = {h->lay.gate_b, h->lay.gate_b, h->lay.down_b, h->lay.gs_b, h->lay.gs_b, h->lay.ds_b};
+  const bool fp4 = cfg->wtype == FT_W_NVFP4;
+  const void* bp[7] = {host_pool->gate,
+                       host_pool->up,
+                       host_pool->down,
+                       fp4 ? (const void*)host_pool->gate_bscale : host_pool->gate_scale,
+                       fp4 ? (const void*)host_pool->up_bscale : host_pool->up_scale,
+                       fp4 ? (const void*)host_pool->down_bscale : host_pool->down_scale,
+                       host_pool->tensor_scale};
+  const size_t rows[7] = {h->lay.gate_b, h->lay.gate_b, h->lay.down_b, h->lay.gs_b,
+                          h->lay.gs_b,   h->lay.ds_b,   h->lay.ts_b};
   for (int j = 0; j < h->n_banks; ++j) {
     if (rows[j] % 16) return fail(FT_ERR_INVALID, "bank row bytes not a multiple of 16");
     if ((s = register_bank(h->bank[j], bp[j], rows[j], nlog)) != FT_OK) return s;
@@ -574,9 +589,14 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   }
   if (cfg->has_shared) {
     FT_CUDA(cudaMalloc(&h->shared_w, (size_t)h->L * h->lay.stride));
-    const void* sp[6] = {shared->gate, shared->up, shared->down, shared->gate_scale, shared->up_scale,
-                         shared->down_scale};
-    const size_t seg[6] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds};
+    const void* sp[7] = {shared->gate,
+                         shared->up,
+                         shared->down,
+                         fp4 ? (const void*)shared->gate_bscale : shared->gate_scale,
+                         fp4 ? (const void*)shared->up_bscale : shared->up_scale,
+                         fp4 ? (const void*)shared->down_bscale : shared->down_scale,
+                         shared->tensor_scale};
+    const size_t seg[7] = {h->lay.gate, h->lay.up, h->lay.down, h->lay.gs, h->lay.us, h->lay.ds, h->lay.ts};
     for (int l = 0; l < h->L; ++l)
       for (int j = 0; j < h->n_banks; ++j)
         FT_CUDA(cudaMemcpy(h->shared_w + (size_t)l * h->lay.stride + seg[j],
@@ -605,11 +625,14 @@ ft_status ft_moe_init(const ft_moe_config* cfg, const ft_banks* host_pool, const
   if (s != FT_OK) return s;
   if (!out || !host_pool || !host_pool->gate || !host_pool->up || !host_pool->down)
     return fail(FT_ERR_INVALID, "null host pool / out");
-  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128;
-  if (fp8 && (!host_pool->gate_scale || !host_pool->up_scale || !host_pool->down_scale))
-    return fail(FT_ERR_INVALID, "FP8 banks need scale arrays");
-  if (cfg->has_shared && (!shared || !shared->gate || !shared->up || !shared->down ||
-                          (fp8 && (!shared->gate_scale || !shared->up_scale || !shared->down_scale))))
+  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128, fp4 = cfg->wtype == FT_W_NVFP4;
+  auto scales_ok = [&](const ft_banks* b) {
+    if (fp8) return b->gate_scale && b->up_scale && b->down_scale;
+    if (fp4) return b->gate_bscale && b->up_bscale && b->down_bscale && b->tensor_scale;
+    return true;
+  };
+  if (!scales_ok(host_pool)) return fail(FT_ERR_INVALID, "FP8 / NVFP4 banks need their scale arrays");
+  if (cfg->has_shared && (!shared || !shared->gate || !shared->up || !shared->down || !scales_ok(shared)))
     return fail(FT_ERR_INVALID, "has_shared set but shared banks missing");
   *out = nullptr;
   ft_moe* h = new ft_moe();

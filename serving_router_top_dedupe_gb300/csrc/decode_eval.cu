@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kFillThreads) fill_kernel(FillParams p) {
       case 2: nbytes = p.src_row[2]; doff = p.lay.down; sb = p.src[2]; break;
       case 3: nbytes = p.src_row[3]; doff = p.lay.gs; sb = p.src[3]; break;
       case 4: nbytes = p.src_row[4]; doff = p.lay.us; sb = p.src[4]; break;
-      default: nbytes = p.src_row[5]; doff = p.lay.ds; sb = p.src[5]; break;
+      case 5: nbytes = p.src_row[5]; doff = p.lay.ds; sb = p.src[5]; break;
+      default: nbytes = p.src_row[6]; doff = p.lay.ts; sb = p.src[6]; break;
     }
     const int uid = p.copy_u[i];
     const uint4* src = reinterpret_cast<const uint4*>(sb + (size_t)uid * nbytes);
@@ -105,20 +106,22 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
   const int rbs = I / 8;
   const int n_items = ne * rbs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
-  constexpr int EPC = 16 / ESZ;  // elements per 16-byte chunk
+  constexpr int EPC = WT == FT_W_BF16 ? 8 : (WT == FT_W_FP8_E4M3_B128 ? 16 : 32);  // elements per 16-byte chunk
   const int row_chunks = H / EPC;
-  // x tile: BF16 path keeps raw bf16 (2 B); FP8 path keeps f16 (2 B) -> H*2 bytes per token
+  // x tile: BF16 path keeps raw bf16 (2 B); FP8 and FP4 paths keep f16 (2 B) -> H*2 bytes per token
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int g = item / rbs, rb = item - g * rbs;
     const int i = rb * 8 + warp;
     const uint8_t* W = p.g_w[g];
-    const uint8_t* wg = W + p.lay.gate + (size_t)i * H * ESZ;
-    const uint8_t* wu = W + p.lay.up + (size_t)i * H * ESZ;
+    const uint8_t* wg = W + p.lay.gate + (size_t)i * row_chunks * 16;
+    const uint8_t* wu = W + p.lay.up + (size_t)i * row_chunks * 16;
     const float* sg = reinterpret_cast<const float*>(W + p.lay.gs) + (size_t)i * (H / 128);
     const float* su = reinterpret_cast<const float*>(W + p.lay.us) + (size_t)i * (H / 128);
+    // NVFP4: two E4M3 block scales per 16-byte chunk, read as one 16-bit word
+    const uint16_t* bg = reinterpret_cast<const uint16_t*>(W + p.lay.gs) + (size_t)i * (H / 32);
+    const uint16_t* bu = reinterpret_cast<const uint16_t*>(W + p.lay.us) + (size_t)i * (H / 32);
     const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
     const bool shared_entry = p.has_shared && g == ne - 1;
     for (int t0 = 0; t0 < np; t0 += TG) {
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
         const int pr = p.g_pair[p0 + t0 + tt];
         const int tok = shared_entry ? pr : pr / p.k;
         uint4 v = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + c8 * 8);
-        if (WT == FT_W_FP8_E4M3_B128) {  // bf16 -> f16 (exact for the f16 normal range)
+        if (WT != FT_W_BF16) {  // bf16 -> f16 (exact for the f16 normal range)
           const uint32_t in[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[4];
 #pragma unroll
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
                   acc_b[tt] = dot_bf16_bf16(wb[s], xv, acc_b[tt]);
                 }
               }
-            } else {
+            } else if (WT == FT_W_FP8_E4M3_B128) {
               const float scg = __ldg(sg + c / 8), scu = __ldg(su + c / 8);
 #pragma unroll
               for (int tt = 0; tt < TG; ++tt) {
@@ -180,15 +183,32 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
                   acc_b[tt] = fmaf(dot_e4m3_f16(wb[s], xa, xb), scu, acc_b[tt]);
                 }
               }
+            } else {
+              const float2 sg2 = e4m3x2_to_float2(__ldg(bg + c)), su2 = e4m3x2_to_float2(__ldg(bu + c));
+#pragma unroll
+              for (int tt = 0; tt < TG; ++tt) {
+                if (tt < nt) {
+                  const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)tt * H + c * 32);
+                  const uint4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
+                  acc_a[tt] = fmaf(dot16_e2m1_f16(wa[s].x, wa[s].y, x0, x1), sg2.x, acc_a[tt]);
+                  acc_a[tt] = fmaf(dot16_e2m1_f16(wa[s].z, wa[s].w, x2, x3), sg2.y, acc_a[tt]);
+                  acc_b[tt] = fmaf(dot16_e2m1_f16(wb[s].x, wb[s].y, x0, x1), su2.x, acc_b[tt]);
+                  acc_b[tt] = fmaf(dot16_e2m1_f16(wb[s].z, wb[s].w, x2, x3), su2.y, acc_b[tt]);
+                }
+              }
             }
           }
         }
       }
+      // NVFP4: the banks' tensor scales multiply the finished sums
+      const float tsa = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(W + p.lay.ts)) : 1.f;
+      const float tsb = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(W + p.lay.ts) + 1) : 1.f;
 #pragma unroll
       for (int tt = 0; tt < TG; ++tt) {
         const float a = warp_sum(acc_a[tt]);
         const float b = warp_sum(acc_b[tt]);
-        if (lane == 0 && tt < nt) p.h[(size_t)(p0 + t0 + tt) * I + i] = silu_mul(a, b);
+        if (lane == 0 && tt < nt)
+          p.h[(size_t)(p0 + t0 + tt) * I + i] = WT == FT_W_NVFP4 ? silu_mul(a * tsa, b * tsb) : silu_mul(a, b);
       }
     }
   }
@@ -210,8 +230,7 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
   const int nrb = H / R2;
   const int n_items = ne * nrb;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
-  constexpr int EPC = 16 / ESZ;
+  constexpr int EPC = WT == FT_W_BF16 ? 8 : (WT == FT_W_FP8_E4M3_B128 ? 16 : 32);  // elements per 16-byte chunk
   const int row_chunks = I / EPC;
   float* hs = reinterpret_cast<float*>(smem);  // [TG][I]
 
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int tt = 0; tt < TG; ++tt) acc[r][tt] = 0.f;
-      constexpr int SEG = ESZ == 2 ? 2 : 4;
+      constexpr int SEG = WT == FT_W_BF16 ? 2 : 4;
       for (int c0 = 0; c0 < row_chunks; c0 += 32 * SEG) {
         uint4 wv[RPW][SEG];
 #pragma unroll
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
           for (int s = 0; s < SEG; ++s) {
             const int c = c0 + s * 32 + lane;
             if (c < row_chunks)
-              wv[r][s] = ld_stream(W + p.lay.down + ((size_t)(j0 + r) * I) * ESZ + (size_t)c * 16, pol);
+              wv[r][s] = ld_stream(W + p.lay.down + (size_t)(j0 + r) * row_chunks * 16 + (size_t)c * 16, pol);
           }
 #pragma unroll
         for (int s = 0; s < SEG; ++s) {
@@ -256,21 +275,32 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
 #pragma unroll
                 for (int tt = 0; tt < TG; ++tt)
                   if (tt < nt) acc[r][tt] = dot_bf16_f32(wv[r][s], hs + (size_t)tt * I + c * 8, acc[r][tt]);
-              } else {
+              } else if (WT == FT_W_FP8_E4M3_B128) {
                 const float sc = __ldg(reinterpret_cast<const float*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 128) + c / 8);
 #pragma unroll
                 for (int tt = 0; tt < TG; ++tt)
                   if (tt < nt) acc[r][tt] = fmaf(dot_e4m3_f32(wv[r][s], hs + (size_t)tt * I + c * 16), sc, acc[r][tt]);
+              } else {
+                const float2 sd = e4m3x2_to_float2(
+                    __ldg(reinterpret_cast<const uint16_t*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 32) + c));
+#pragma unroll
+                for (int tt = 0; tt < TG; ++tt)
+                  if (tt < nt) {
+                    const float* hv = hs + (size_t)tt * I + c * 32;
+                    acc[r][tt] = fmaf(dot16_e2m1_f32(wv[r][s].x, wv[r][s].y, hv), sd.x, acc[r][tt]);
+                    acc[r][tt] = fmaf(dot16_e2m1_f32(wv[r][s].z, wv[r][s].w, hv + 16), sd.y, acc[r][tt]);
+                  }
               }
             }
           }
         }
       }
+      const float tsd = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(W + p.lay.ts) + 2) : 1.f;
 #pragma unroll
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int tt = 0; tt < TG; ++tt) {
-          const float y = warp_sum(acc[r][tt]);
+          const float y = WT == FT_W_NVFP4 ? warp_sum(acc[r][tt]) * tsd : warp_sum(acc[r][tt]);
           if (lane == 0 && tt < nt) {
             const int pr = p.g_pair[p0 + t0 + tt];
             if (shared_entry) p.shared_rows[(size_t)pr * H + j0 + r] = y;
@@ -331,7 +361,8 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
 }
 
 bool eval_fused(const EvalParams& p, int wtype) {
-  return p.B == 1 && fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
+  // the persistent batch-1 kernel is built for BF16 and FP8; NVFP4 runs the batched kernels
+  return p.B == 1 && wtype != FT_W_NVFP4 && fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
 }
 
 cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
@@ -340,6 +371,8 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
   if (wtype == FT_W_BF16) {
     return one ? gate_up_launch<FT_W_BF16, 8, 1>(p, grid, s) : gate_up_launch<FT_W_BF16, 8, 4>(p, grid, s);
   }
+  if (wtype == FT_W_NVFP4)
+    return one ? gate_up_launch<FT_W_NVFP4, 4, 1>(p, grid, s) : gate_up_launch<FT_W_NVFP4, 4, 4>(p, grid, s);
   return one ? gate_up_launch<FT_W_FP8_E4M3_B128, 7, 1>(p, grid, s)
              : gate_up_launch<FT_W_FP8_E4M3_B128, 7, 4>(p, grid, s);
 }
@@ -354,6 +387,11 @@ cudaError_t prepare_kernels(int wtype, int H, int I) {
     if ((e = set_smem(gate_up_kernel<FT_W_BF16, 8, 4>, gu4)) != cudaSuccess) return e;
     if ((e = set_smem(down_combine_kernel<FT_W_BF16, 4, 1>, dn1)) != cudaSuccess) return e;
     e = set_smem(down_combine_kernel<FT_W_BF16, 4, 4>, dn4);
+  } else if (wtype == FT_W_NVFP4) {
+    if ((e = set_smem(gate_up_kernel<FT_W_NVFP4, 4, 1>, gu1)) != cudaSuccess) return e;
+    if ((e = set_smem(gate_up_kernel<FT_W_NVFP4, 4, 4>, gu4)) != cudaSuccess) return e;
+    if ((e = set_smem(down_combine_kernel<FT_W_NVFP4, 4, 1>, dn1)) != cudaSuccess) return e;
+    e = set_smem(down_combine_kernel<FT_W_NVFP4, 4, 4>, dn4);
   } else {
     if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 1>, gu1)) != cudaSuccess) return e;
     if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 4>, gu4)) != cudaSuccess) return e;
@@ -367,6 +405,7 @@ cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaSt
   if (eval_fused(p, wtype)) return cudaSuccess;  // the fused batch-1 kernel did the whole layer
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) return one ? down_launch<FT_W_BF16, 1>(p, grid, s) : down_launch<FT_W_BF16, 4>(p, grid, s);
+  if (wtype == FT_W_NVFP4) return one ? down_launch<FT_W_NVFP4, 1>(p, grid, s) : down_launch<FT_W_NVFP4, 4>(p, grid, s);
   return one ? down_launch<FT_W_FP8_E4M3_B128, 1>(p, grid, s) : down_launch<FT_W_FP8_E4M3_B128, 4>(p, grid, s);
 }
 

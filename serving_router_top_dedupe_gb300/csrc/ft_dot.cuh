@@ -71,6 +71,52 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return r;
 }
 
+// two E4M3 codes in a 16-bit word (low byte first) -> two floats (low byte in .x)
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  const uint32_t h2 = e4m3x2_to_f16x2(two);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// two E2M1 (FP4) codes in one byte (low nibble = element 0) -> f16x2 (element 0 in the
+// low half)
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 s;\n\tcvt.u8.u32 s, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, s;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// one 16-element NVFP4 block: E2M1 codes in two 32-bit words (w0: elements 0..7, low byte
+// first) . 16 F16 values (xa: 0..7, xb: 8..15) -> the block's partial dot (not scaled)
+__device__ __forceinline__ float dot16_e2m1_f16(uint32_t w0, uint32_t w1, uint4 xa, uint4 xb) {
+  float d = 0.f;
+  d = fma2_f16(e2m1x2_to_f16x2(w0 & 0xffu), xa.x, d);
+  d = fma2_f16(e2m1x2_to_f16x2((w0 >> 8) & 0xffu), xa.y, d);
+  d = fma2_f16(e2m1x2_to_f16x2((w0 >> 16) & 0xffu), xa.z, d);
+  d = fma2_f16(e2m1x2_to_f16x2(w0 >> 24), xa.w, d);
+  d = fma2_f16(e2m1x2_to_f16x2(w1 & 0xffu), xb.x, d);
+  d = fma2_f16(e2m1x2_to_f16x2((w1 >> 8) & 0xffu), xb.y, d);
+  d = fma2_f16(e2m1x2_to_f16x2((w1 >> 16) & 0xffu), xb.z, d);
+  d = fma2_f16(e2m1x2_to_f16x2(w1 >> 24), xb.w, d);
+  return d;
+}
+
+// one 16-element NVFP4 block . 16 FP32 values -> the block's partial dot (not scaled)
+__device__ __forceinline__ float dot16_e2m1_f32(uint32_t w0, uint32_t w1, const float* v) {
+  float d = 0.f;
+  const uint32_t ws[2] = {w0, w1};
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t h2 = e2m1x2_to_f16x2((ws[q] >> (8 * b)) & 0xffu);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      d = fmaf(f.x, v[8 * q + 2 * b], d);
+      d = fmaf(f.y, v[8 * q + 2 * b + 1], d);
+    }
+  }
+  return d;
+}
+
 // 16 bytes of BF16 weights (8 elements) . 8 BF16 activations
 __device__ __forceinline__ float dot_bf16_bf16(uint4 w, uint4 x, float acc) {
   acc = fma2_bf16(w.x, x.x, acc);

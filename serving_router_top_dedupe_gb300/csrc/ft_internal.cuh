@@ -66,6 +66,7 @@ struct DecodeWork {
 struct SlotLayout {
   size_t gate, up, down, gs, us, ds;  // byte offsets
   size_t gate_b, down_b, gs_b, ds_b;  // byte sizes (up == gate, us == gs)
+  size_t ts, ts_b;                    // NVFP4 tensor scales (4 FP32), else ts_b == 0
   size_t used, stride;                // bytes used, slot stride (256-aligned)
 };
 
@@ -93,8 +94,8 @@ struct FillParams {
   const int32_t* copy_slot;
   uint8_t* pool;
   SlotLayout lay;
-  const uint8_t* src[6];    // device-visible addresses of the host banks
-  size_t src_row[6];        // bytes per logical id in each bank
+  const uint8_t* src[7];    // device-visible addresses of the host banks
+  size_t src_row[7];        // bytes per logical id in each bank
   int n_banks;
   bool pdl;
 };

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libftmoe.so")
 
 FT_OK, FT_ERR_INVALID, FT_ERR_CUDA, FT_ERR_NOMEM, FT_ERR_PIN = 0, 1, 2, 3, 4
 FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, FT_ERR_DEVICE = 5, 6, 7, 8
-FT_W_BF16, FT_W_FP8_E4M3_B128 = 0, 1
+FT_W_BF16, FT_W_FP8_E4M3_B128, FT_W_NVFP4 = 0, 1, 2
 FT_FILL_KERNEL, FT_FILL_MEMCPY = 0, 1
 FT_GATE_SOFTMAX_TOPK, FT_GATE_SOFTMAX_ALL, FT_GATE_SIGMOID_TOPK = 0, 1, 2
 FT_CPU = -1
@@ -46,9 +46,12 @@ class ft_moe_config(C.Structure):
                 ("compute_stream", C.c_void_p), ("transfer_stream", C.c_void_p)]
 
 
+_BANK_KEYS = ("gate", "up", "down", "gate_scale", "up_scale", "down_scale", "gate_bscale", "up_bscale",
+              "down_bscale", "tensor_scale")
+
+
 class ft_banks(C.Structure):
-    _fields_ = [("gate", C.c_void_p), ("up", C.c_void_p), ("down", C.c_void_p),
-                ("gate_scale", C.c_void_p), ("up_scale", C.c_void_p), ("down_scale", C.c_void_p)]
+    _fields_ = [(k, C.c_void_p) for k in _BANK_KEYS]
 
 
 class ft_stats(C.Structure):
@@ -134,7 +137,7 @@ def _ptr(t) -> int | None:
 def _banks(d: dict | None) -> ft_banks | None:
     if d is None:
         return None
-    return ft_banks(*[_ptr(d.get(k)) for k in ("gate", "up", "down", "gate_scale", "up_scale", "down_scale")])
+    return ft_banks(*[_ptr(d.get(k)) for k in _BANK_KEYS])
 
 
 # ----------------------------------------------------------- same-named calls

@@ -46,7 +46,7 @@ class Run:
             banks = pool.routed_banks()
             shared = pool.shared_banks()
         self.banks, self.shared = banks, shared
-        self.fp8 = w.wtype == synth.W_FP8_E4M3_B128
+        self.fp8 = int(w.wtype)  # weight type for the oracle: 0 BF16, 1 FP8, 2 NVFP4
         self.S = w.cache_slots if cache_slots is None else cache_slots
         self.B = w.batch if max_batch is None else max_batch
         cfg = F.make_config(w.n_layers, w.hidden, w.inter, w.n_experts, w.top_k, w.has_shared, w.wtype, self.B,
