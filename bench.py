@@ -440,7 +440,7 @@ def run_ours(args, d: Dist) -> dict | None:
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see DESIGN.md)",
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded: locality trace, N(0,1) BF16 activations, generated expert banks)",
            "config": {**_config_desc(w), "parallelism": f"replicas x{d.world}" if d.world > 1 else "single GPU"},
            "hbm_gbs_expert_weights": hbm,
            "roofline": roofline, "decode_step_roofline": layer_rl, "prefill": prefill, "e2e": e2e, "gpu_launches": args.steps * L * launches_per_layer, "clocks": clk,
