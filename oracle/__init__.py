@@ -8,4 +8,4 @@ from .moe import (FT_CPU, Counters, SlotCache, StepRecord, all_pair_rows, bf16_t
                   decode_layer_outputs, dedupe, e4m3_to_f64, matvec_post_scaled, mbps, pair_row,
                   prefill_outputs, rel_err_rows, route, router_logits, silu, split_misses, swiglu_expert,
                   GATE_SOFTMAX_TOPK, GATE_SOFTMAX_ALL, GATE_SIGMOID_TOPK, E2M1_TABLE, e2m1_unpack_to_f64,
-                  matvec_nvfp4, NVFP4_BLOCK)
+                  matvec_nvfp4, NVFP4_BLOCK, e8m0_to_f64, matvec_mxfp4, MXFP4_BLOCK)

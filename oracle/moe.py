@@ -432,6 +432,27 @@ def matvec_nvfp4(packed: np.ndarray, block_scales: np.ndarray, tensor_scale: flo
     return float(tensor_scale) * (block_dots * e4m3_to_f64(block_scales)).sum(axis=1)
 
 
+MXFP4_BLOCK = 32   # elements per E8M0 block scale along the reduction dimension
+
+
+def e8m0_to_f64(codes: np.ndarray) -> np.ndarray:
+    """E8M0 scale codes (OCP MX): 2^(code - 127); code 255 is NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))
+
+
+def matvec_mxfp4(packed: np.ndarray, scale_codes: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """MXFP4 rows times x: E2M1 elements (packed as for NVFP4), one E8M0 scale per 1x32
+    block along the reduction dimension applied after the block's dot product (the
+    post-scaling order of [P3, §4.2], with MXFP4's block)."""
+    w = e2m1_unpack_to_f64(packed)
+    R, K = w.shape
+    nb = K // MXFP4_BLOCK
+    block_dots = np.einsum("rbk,bk->rb", w.reshape(R, nb, MXFP4_BLOCK),
+                           np.asarray(x, dtype=np.float64).reshape(nb, MXFP4_BLOCK))
+    return (block_dots * e8m0_to_f64(scale_codes)).sum(axis=1)
+
+
 def silu(a: np.ndarray) -> np.ndarray:
     return a / (1.0 + np.exp(-a))
 
@@ -457,9 +478,14 @@ def swiglu_expert(expert: dict, x: np.ndarray, fp8: bool) -> np.ndarray:
     FP8 scales gate_scale/up_scale [I][H/128], down_scale [H][I/128].
     `fp8` is the weight type: 0/False BF16, 1/True FP8 E4M3, 2 NVFP4 (packed E2M1
     [rows][K/2], E4M3 block scales [rows][K/16], tensor_scale [4] FP32: gate, up,
-    down, unused).
+    down, unused), 3 MXFP4 (packed E2M1, E8M0 block scales [rows][K/32]).
     [FT2, paragraph on the double buffer] / [P3, §4.3] (gate, up, down projections).
     """
+    if fp8 == 3:  # MXFP4
+        a = matvec_mxfp4(expert["gate"], expert["gate_bscale"], x)
+        b = matvec_mxfp4(expert["up"], expert["up_bscale"], x)
+        h = silu(a) * b
+        return matvec_mxfp4(expert["down"], expert["down_bscale"], h)
     if fp8 == 2:  # NVFP4: tensor_scale holds the gate, up and down banks' scales
         ts = expert["tensor_scale"].astype(np.float64)
         a = matvec_nvfp4(expert["gate"], expert["gate_bscale"], ts[0], x)

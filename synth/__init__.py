@@ -42,6 +42,7 @@ TAG_ROUTER = 40
 W_BF16 = 0
 W_FP8_E4M3_B128 = 1
 W_NVFP4 = 2
+W_MXFP4 = 3
 
 FP8_BLOCK = 128
 
@@ -228,6 +229,9 @@ def bank_shapes(w: Workload) -> dict:
         s = {"gate": (I, H // 2), "up": (I, H // 2), "down": (H, I // 2),
              "gate_bscale": (I, H // 16), "up_bscale": (I, H // 16), "down_bscale": (H, I // 16),
              "tensor_scale": (4,)}
+    if w.wtype == W_MXFP4:  # packed E2M1, E8M0 scales per 32
+        s = {"gate": (I, H // 2), "up": (I, H // 2), "down": (H, I // 2),
+             "gate_bscale": (I, H // 32), "up_bscale": (I, H // 32), "down_bscale": (H, I // 32)}
     return s
 
 
@@ -239,6 +243,8 @@ def bank_dtypes(w: Workload) -> dict:
     if w.wtype == W_NVFP4:
         d.update({"gate_bscale": np.uint8, "up_bscale": np.uint8, "down_bscale": np.uint8,
                   "tensor_scale": np.float32})
+    if w.wtype == W_MXFP4:
+        d.update({"gate_bscale": np.uint8, "up_bscale": np.uint8, "down_bscale": np.uint8})
     return d
 
 
@@ -261,7 +267,8 @@ class ExpertPool:
     so that dequantised weights have roughly the BF16 banks' spread.  NVFP4
     banks: uniform E2M1 codes, E4M3 block scales in [0.5, 2) per 16 elements
     and per-expert FP32 tensor scales in U(0.004, 0.008) (dequantised weights
-    of about 0.02 rms).
+    of about 0.02 rms).  MXFP4 banks: uniform E2M1 codes and E8M0 block scales
+    2^-8 .. 2^-6 per 32 elements.
     """
 
     def __init__(self, w: Workload):
@@ -275,11 +282,13 @@ class ExpertPool:
             key = derive_key(w.seed, _TAGS[kind])
             if kind == "tensor_scale":
                 vals = (0.004 + 0.004 * uniform(key, period)).astype(np.float32)
+            elif kind.endswith("_bscale") and w.wtype == W_MXFP4:  # E8M0 codes 119..121: 2^-8 .. 2^-6
+                vals = (119 + (raw_u64(key, period) % np.uint64(3))).astype(np.uint8)
             elif kind.endswith("_bscale"):  # E4M3 codes 0x30..0x3F: 0.5 .. 1.875
                 vals = (0x30 + (raw_u64(key, period) & np.uint64(0xF))).astype(np.uint8)
             elif kind.endswith("_scale"):
                 vals = ((0.5 + 1.5 * uniform(key, period)) / 448.0).astype(np.float32)
-            elif w.wtype == W_NVFP4:  # two uniform E2M1 codes per byte
+            elif w.wtype in (W_NVFP4, W_MXFP4):  # two uniform E2M1 codes per byte
                 vals = (raw_u64(key, period) & np.uint64(0xFF)).astype(np.uint8)
             elif w.wtype == W_BF16:
                 vals = f32_to_bf16_bits((normal(key, period) * w.weight_std).astype(np.float32))

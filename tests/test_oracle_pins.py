@@ -284,6 +284,29 @@ def test_nvfp4_matvec_post_scaled_equals_dequantise_first_and_brute_force():
         assert abs(ts * tot - y[r]) <= 1e-12 * max(1.0, abs(y[r]))
 
 
+def test_e8m0_and_mxfp4_matvec():
+    """E8M0 codes against ldexp; the MXFP4 post-scaled product against dequantise-first and
+    a scalar loop over nibbles and 32-element blocks."""
+    codes = np.arange(255)
+    assert all(O.e8m0_to_f64(codes)[c] == math.ldexp(1.0, int(c) - 127) for c in codes)
+    assert np.isnan(O.e8m0_to_f64(np.array([255]))[0])
+    rng = np.random.default_rng(31)
+    R, K = 4, 96
+    packed = rng.integers(0, 256, size=(R, K // 2), dtype=np.uint8)
+    sc = rng.integers(118, 124, size=(R, K // O.MXFP4_BLOCK), dtype=np.uint8)
+    x = rng.standard_normal(K)
+    y = O.matvec_mxfp4(packed, sc, x)
+    w = O.e2m1_unpack_to_f64(packed) * np.repeat(O.e8m0_to_f64(sc), O.MXFP4_BLOCK, axis=1)
+    np.testing.assert_allclose(y, w @ x, rtol=1e-12, atol=1e-15)
+    for r in range(R):
+        tot = 0.0
+        for b in range(K // 32):
+            part = sum(O.E2M1_TABLE[(int(packed[r, k // 2]) >> (4 * (k % 2))) & 0xF] * x[k]
+                       for k in range(32 * b, 32 * b + 32))
+            tot += part * 2.0 ** (int(sc[r, b]) - 127)
+        assert abs(tot - y[r]) <= 1e-12 * max(1.0, abs(y[r]))
+
+
 def test_dedupe_is_sorted_union():
     sel = np.array([[3, 5], [1, 5], [3, 9]])
     assert O.dedupe(sel, 2, 16) == [33, 35, 37, 41]
