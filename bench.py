@@ -195,8 +195,9 @@ def _pool_banks(w, d: Dist):
 
 
 def _kernel_hash() -> str:
+    """Hash of the batch-1 GEMV's sources: its translation unit and the headers it includes."""
     h = hashlib.sha256()
-    for f in ("decode_fused.cu", "decode_eval.cu", "ft_dot.cuh", "ft_ptx.cuh", "ft_internal.cuh"):
+    for f in ("decode_fused.cu", "ft_dot.cuh", "ft_ptx.cuh", "ft_internal.cuh"):
         with open(os.path.join(ROOT, "serving_router_top_dedupe_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -66,8 +66,12 @@ typedef enum {
  *                       nibble), one E4M3 scale per 1x16 block along the reduction
  *                       dimension applied after the block's dot product, then one FP32
  *                       tensor scale per bank of each expert ([FT] 主结果 names NVFP4
- *                       experts).  Decode only; prefill is BF16. */
-typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1, FT_W_NVFP4 = 2 } ft_wtype;
+ *                       experts).  Decode only; prefill is BF16.
+ *   FT_W_MXFP4          E2M1 weights packed as for NVFP4, one E8M0 scale (2^(code-127))
+ *                       per 1x32 block along the reduction dimension, applied after the
+ *                       block's dot product; no tensor scale ([FT] 主结果: MXFP4 checkpoints).
+ *                       Decode only. */
+typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1, FT_W_NVFP4 = 2, FT_W_MXFP4 = 3 } ft_wtype;
 
 /* How a decode step moves F-set experts from the host pool into their slots.
  * FT_FILL_KERNEL: one fixed-shape copy kernel on the transfer stream reads the
@@ -113,8 +117,9 @@ typedef struct {
  *   down       [L*E][H][I]        (NVFP4: [L*E][H][I/2])
  *   gate_scale, up_scale [L*E][I][H/128] FP32 (FP8 only; NULL otherwise)
  *   down_scale [L*E][H][I/128]           FP32 (FP8 only)
- *   gate_bscale, up_bscale [L*E][I][H/16] E4M3 codes (NVFP4 only; NULL otherwise)
- *   down_bscale [L*E][H][I/16]            E4M3 codes (NVFP4 only)
+ *   gate_bscale, up_bscale [L*E][I][H/16] E4M3 codes (NVFP4), [L*E][I][H/32] E8M0 codes
+ *                                          (MXFP4); NULL otherwise
+ *   down_bscale [L*E][H][I/16] (NVFP4) or [L*E][H][I/32] (MXFP4)
  *   tensor_scale [L*E][4] FP32: gate, up, down, unused (NVFP4 only)
  * For the shared-expert banks the first dimension is L (one per layer). */
 typedef struct {

@@ -121,7 +121,7 @@ namespace ft {
 SlotLayout make_layout(int wtype, int H, int I) {
   SlotLayout l{};
   // weight bytes per element times 2: BF16 4, FP8 2, FP4 1
-  const size_t e2 = wtype == FT_W_BF16 ? 4 : (wtype == FT_W_FP8_E4M3_B128 ? 2 : 1);
+  const size_t e2 = wtype == FT_W_BF16 ? 4 : (wtype == FT_W_FP8_E4M3_B128 ? 2 : 1);  // FP4 formats: 1
   l.gate_b = (size_t)I * H * e2 / 2;
   l.down_b = (size_t)H * I * e2 / 2;
   l.gate = 0;
@@ -134,6 +134,9 @@ SlotLayout make_layout(int wtype, int H, int I) {
   } else if (wtype == FT_W_NVFP4) {
     l.gs_b = (size_t)I * (H / 16);
     l.ds_b = (size_t)H * (I / 16);
+  } else if (wtype == FT_W_MXFP4) {
+    l.gs_b = (size_t)I * (H / 32);
+    l.ds_b = (size_t)H * (I / 32);
   }
   l.gs = end;
   l.us = l.gs + l.gs_b;
@@ -237,7 +240,8 @@ ft_status check_cfg(const ft_moe_config* c) {
     return fail(FT_ERR_INVALID, "n_layers >= 1 and 1 <= n_experts <= %d required", ft::kMaxE);
   if (c->top_k < 1 || c->top_k > ft::kMaxK || c->top_k > c->n_experts)
     return fail(FT_ERR_INVALID, "1 <= top_k <= min(%d, n_experts) required", ft::kMaxK);
-  if (c->wtype != FT_W_BF16 && c->wtype != FT_W_FP8_E4M3_B128 && c->wtype != FT_W_NVFP4)
+  if (c->wtype != FT_W_BF16 && c->wtype != FT_W_FP8_E4M3_B128 && c->wtype != FT_W_NVFP4 &&
+      c->wtype != FT_W_MXFP4)
     return fail(FT_ERR_INVALID, "unknown wtype");
   const int hmul = c->wtype == FT_W_FP8_E4M3_B128 ? 512 : 256;
   if (c->hidden < hmul || c->hidden % hmul) return fail(FT_ERR_INVALID, "hidden must be a multiple of %d", hmul);
@@ -538,7 +542,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   h->S = cfg->cache_slots;
   h->kcap = std::min(cfg->max_batch * cfg->top_k, cfg->n_experts);
   h->lay = ft::make_layout(cfg->wtype, h->H, h->I);
-  h->n_banks = fp8 ? 6 : (cfg->wtype == FT_W_NVFP4 ? 7 : 3);
+  h->n_banks = cfg->wtype == FT_W_NVFP4 ? 7 : (fp8 || cfg->wtype == FT_W_MXFP4 ? 6 : 3);
   h->grid_eval = h->n_sm * 4;
   h->grid_fill = std::max(1, std::min(ft::kFillSms, h->n_sm / 4));
   if (cfg->compute_stream) {
@@ -566,7 +570,7 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
 
   // host pool: pin + map every bank
   const size_t nlog = (size_t)h->L * h->E;
-  const bool fp4 = cfg->wtype == FT_W_NVFP4;
+  const bool fp4 = cfg->wtype == FT_W_NVFP4 || cfg->wtype == FT_W_MXFP4;
   const void* bp[7] = {host_pool->gate,
                        host_pool->up,
                        host_pool->down,
@@ -625,10 +629,11 @@ ft_status ft_moe_init(const ft_moe_config* cfg, const ft_banks* host_pool, const
   if (s != FT_OK) return s;
   if (!out || !host_pool || !host_pool->gate || !host_pool->up || !host_pool->down)
     return fail(FT_ERR_INVALID, "null host pool / out");
-  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128, fp4 = cfg->wtype == FT_W_NVFP4;
+  const bool fp8 = cfg->wtype == FT_W_FP8_E4M3_B128, nv4 = cfg->wtype == FT_W_NVFP4, mx4 = cfg->wtype == FT_W_MXFP4;
   auto scales_ok = [&](const ft_banks* b) {
     if (fp8) return b->gate_scale && b->up_scale && b->down_scale;
-    if (fp4) return b->gate_bscale && b->up_bscale && b->down_bscale && b->tensor_scale;
+    if (nv4) return b->gate_bscale && b->up_bscale && b->down_bscale && b->tensor_scale;
+    if (mx4) return b->gate_bscale && b->up_bscale && b->down_bscale;
     return true;
   };
   if (!scales_ok(host_pool)) return fail(FT_ERR_INVALID, "FP8 / NVFP4 banks need their scale arrays");

@@ -30,6 +30,12 @@ namespace {
 
 using namespace dot;
 
+// E8M0 scale code -> float: 2^(code - 127), built from the float's exponent field
+// (code 0 is the subnormal 2^-127; code 255, NaN in the format, is never written).
+__device__ __forceinline__ float e8m0_to_float(uint32_t code) {
+  return __uint_as_float(code ? code << 23 : 0x00400000u);
+}
+
 // ------------------------------------------------------------------------- fill
 // Work = q experts x n_banks contiguous segments.  CTA b copies a share of segment
 // b mod nseg (addresses computed once per segment), issuing FILL_UNROLL 16-byte loads
@@ -119,9 +125,12 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
     const uint8_t* wu = W + p.lay.up + (size_t)i * row_chunks * 16;
     const float* sg = reinterpret_cast<const float*>(W + p.lay.gs) + (size_t)i * (H / 128);
     const float* su = reinterpret_cast<const float*>(W + p.lay.us) + (size_t)i * (H / 128);
-    // NVFP4: two E4M3 block scales per 16-byte chunk, read as one 16-bit word
+    // NVFP4: two E4M3 block scales per 16-byte chunk, read as one 16-bit word;
+    // MXFP4: one E8M0 block scale per 16-byte chunk
     const uint16_t* bg = reinterpret_cast<const uint16_t*>(W + p.lay.gs) + (size_t)i * (H / 32);
     const uint16_t* bu = reinterpret_cast<const uint16_t*>(W + p.lay.us) + (size_t)i * (H / 32);
+    const uint8_t* mg = W + p.lay.gs + (size_t)i * (H / 32);
+    const uint8_t* mu = W + p.lay.us + (size_t)i * (H / 32);
     const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
     const bool shared_entry = p.has_shared && g == ne - 1;
     for (int t0 = 0; t0 < np; t0 += TG) {
@@ -181,6 +190,19 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
                   const uint4 xa = xp[0], xb = xp[1];
                   acc_a[tt] = fmaf(dot_e4m3_f16(wa[s], xa, xb), scg, acc_a[tt]);
                   acc_b[tt] = fmaf(dot_e4m3_f16(wb[s], xa, xb), scu, acc_b[tt]);
+                }
+              }
+            } else if (WT == FT_W_MXFP4) {
+              const float scg = e8m0_to_float(__ldg(mg + c)), scu = e8m0_to_float(__ldg(mu + c));
+#pragma unroll
+              for (int tt = 0; tt < TG; ++tt) {
+                if (tt < nt) {
+                  const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)tt * H + c * 32);
+                  const uint4 x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
+                  const float da = dot16_e2m1_f16(wa[s].x, wa[s].y, x0, x1) + dot16_e2m1_f16(wa[s].z, wa[s].w, x2, x3);
+                  const float db = dot16_e2m1_f16(wb[s].x, wb[s].y, x0, x1) + dot16_e2m1_f16(wb[s].z, wb[s].w, x2, x3);
+                  acc_a[tt] = fmaf(da, scg, acc_a[tt]);
+                  acc_b[tt] = fmaf(db, scu, acc_b[tt]);
                 }
               }
             } else {
@@ -280,6 +302,15 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
 #pragma unroll
                 for (int tt = 0; tt < TG; ++tt)
                   if (tt < nt) acc[r][tt] = fmaf(dot_e4m3_f32(wv[r][s], hs + (size_t)tt * I + c * 16), sc, acc[r][tt]);
+              } else if (WT == FT_W_MXFP4) {
+                const float sd = e8m0_to_float(__ldg(W + p.lay.ds + (size_t)(j0 + r) * (I / 32) + c));
+#pragma unroll
+                for (int tt = 0; tt < TG; ++tt)
+                  if (tt < nt) {
+                    const float* hv = hs + (size_t)tt * I + c * 32;
+                    const float d = dot16_e2m1_f32(wv[r][s].x, wv[r][s].y, hv) + dot16_e2m1_f32(wv[r][s].z, wv[r][s].w, hv + 16);
+                    acc[r][tt] = fmaf(d, sd, acc[r][tt]);
+                  }
               } else {
                 const float2 sd = e4m3x2_to_float2(
                     __ldg(reinterpret_cast<const uint16_t*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 32) + c));
@@ -361,8 +392,9 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
 }
 
 bool eval_fused(const EvalParams& p, int wtype) {
-  // the persistent batch-1 kernel is built for BF16 and FP8; NVFP4 runs the batched kernels
-  return p.B == 1 && wtype != FT_W_NVFP4 && fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
+  // the persistent batch-1 kernel is built for BF16 and FP8; the FP4 formats run the batched kernels
+  return p.B == 1 && (wtype == FT_W_BF16 || wtype == FT_W_FP8_E4M3_B128) &&
+         fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
 }
 
 cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_t s) {
@@ -373,6 +405,8 @@ cudaError_t launch_gate_up(const EvalParams& p, int wtype, int grid, cudaStream_
   }
   if (wtype == FT_W_NVFP4)
     return one ? gate_up_launch<FT_W_NVFP4, 4, 1>(p, grid, s) : gate_up_launch<FT_W_NVFP4, 4, 4>(p, grid, s);
+  if (wtype == FT_W_MXFP4)
+    return one ? gate_up_launch<FT_W_MXFP4, 4, 1>(p, grid, s) : gate_up_launch<FT_W_MXFP4, 4, 4>(p, grid, s);
   return one ? gate_up_launch<FT_W_FP8_E4M3_B128, 7, 1>(p, grid, s)
              : gate_up_launch<FT_W_FP8_E4M3_B128, 7, 4>(p, grid, s);
 }
@@ -392,6 +426,11 @@ cudaError_t prepare_kernels(int wtype, int H, int I) {
     if ((e = set_smem(gate_up_kernel<FT_W_NVFP4, 4, 4>, gu4)) != cudaSuccess) return e;
     if ((e = set_smem(down_combine_kernel<FT_W_NVFP4, 4, 1>, dn1)) != cudaSuccess) return e;
     e = set_smem(down_combine_kernel<FT_W_NVFP4, 4, 4>, dn4);
+  } else if (wtype == FT_W_MXFP4) {
+    if ((e = set_smem(gate_up_kernel<FT_W_MXFP4, 4, 1>, gu1)) != cudaSuccess) return e;
+    if ((e = set_smem(gate_up_kernel<FT_W_MXFP4, 4, 4>, gu4)) != cudaSuccess) return e;
+    if ((e = set_smem(down_combine_kernel<FT_W_MXFP4, 4, 1>, dn1)) != cudaSuccess) return e;
+    e = set_smem(down_combine_kernel<FT_W_MXFP4, 4, 4>, dn4);
   } else {
     if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 1>, gu1)) != cudaSuccess) return e;
     if ((e = set_smem(gate_up_kernel<FT_W_FP8_E4M3_B128, 7, 4>, gu4)) != cudaSuccess) return e;
@@ -406,6 +445,7 @@ cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaSt
   const bool one = p.B == 1;
   if (wtype == FT_W_BF16) return one ? down_launch<FT_W_BF16, 1>(p, grid, s) : down_launch<FT_W_BF16, 4>(p, grid, s);
   if (wtype == FT_W_NVFP4) return one ? down_launch<FT_W_NVFP4, 1>(p, grid, s) : down_launch<FT_W_NVFP4, 4>(p, grid, s);
+  if (wtype == FT_W_MXFP4) return one ? down_launch<FT_W_MXFP4, 1>(p, grid, s) : down_launch<FT_W_MXFP4, 4>(p, grid, s);
   return one ? down_launch<FT_W_FP8_E4M3_B128, 1>(p, grid, s) : down_launch<FT_W_FP8_E4M3_B128, 4>(p, grid, s);
 }
 

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libftmoe.so")
 
 FT_OK, FT_ERR_INVALID, FT_ERR_CUDA, FT_ERR_NOMEM, FT_ERR_PIN = 0, 1, 2, 3, 4
 FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, FT_ERR_DEVICE = 5, 6, 7, 8
-FT_W_BF16, FT_W_FP8_E4M3_B128, FT_W_NVFP4 = 0, 1, 2
+FT_W_BF16, FT_W_FP8_E4M3_B128, FT_W_NVFP4, FT_W_MXFP4 = 0, 1, 2, 3
 FT_FILL_KERNEL, FT_FILL_MEMCPY = 0, 1
 FT_GATE_SOFTMAX_TOPK, FT_GATE_SOFTMAX_ALL, FT_GATE_SIGMOID_TOPK = 0, 1, 2
 FT_CPU = -1

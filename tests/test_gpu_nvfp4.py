@@ -1,7 +1,8 @@
-"""GPU parity of NVFP4 experts on the decode path: E2M1 weights packed two per byte, one
-E4M3 scale per 1x16 block applied after the block's dot product and one FP32 tensor
-scale per bank, against the float64 oracle; fills move every bank, tensor scales
-included, by the copy kernel and by cudaMemcpyAsync."""
+"""GPU parity of block-FP4 experts on the decode path against the float64 oracle: NVFP4
+(E2M1 weights packed two per byte, one E4M3 scale per 1x16 block applied after the
+block's dot product, one FP32 tensor scale per bank) and MXFP4 (the same elements, one
+E8M0 scale per 1x32 block); fills move every bank by the copy kernel and by
+cudaMemcpyAsync."""
 import numpy as np
 import pytest
 
@@ -18,10 +19,14 @@ def _lib():
     g.build()
 
 
+FP4 = [synth.W_NVFP4, synth.W_MXFP4]
+
+
+@pytest.mark.parametrize("wtype", FP4)
 @pytest.mark.parametrize("batch", [1, 4])
-def test_nvfp4_tiny_every_step(batch):
+def test_fp4_tiny_every_step(batch, wtype):
     """16 experts top-2, 8 slots, 11.8:47.5: fills, evictions and host pairs."""
-    w = synth.tiny().with_(wtype=synth.W_NVFP4, batch=batch, steps=10)
+    w = synth.tiny().with_(wtype=wtype, batch=batch, steps=10)
     with Run(w) as r:
         for s in range(w.steps):
             for l in range(w.n_layers):
@@ -31,10 +36,10 @@ def test_nvfp4_tiny_every_step(batch):
         assert r.sim.cnt.fills > 0 and r.sim.cnt.cpu_execs > 0
 
 
-@pytest.mark.parametrize("batch", [1, 4])
-def test_nvfp4_35b_expert_shape(batch):
+@pytest.mark.parametrize("wtype,batch", [(synth.W_NVFP4, 1), (synth.W_NVFP4, 4), (synth.W_MXFP4, 1)])
+def test_fp4_35b_expert_shape(wtype, batch):
     """H 2048, I 512, 256 experts top-8 + shared expert, 2 layers, 25% of the pool."""
-    w = synth.decode_bf16(batch=batch).with_(wtype=synth.W_NVFP4, n_layers=2, steps=8,
+    w = synth.decode_bf16(batch=batch).with_(wtype=wtype, n_layers=2, steps=8,
                                              cache_slots=synth.capacity_slots(0.25, 2, 256))
     tr = synth.routing_trace(w)
     with Run(w) as r:
@@ -45,8 +50,9 @@ def test_nvfp4_35b_expert_shape(batch):
         print(f"batch {batch}: max rel err {r.max_err:.2e}")
 
 
-def test_nvfp4_memcpy_fill_matches_kernel_fill():
-    w = synth.tiny().with_(wtype=synth.W_NVFP4, steps=8)
+@pytest.mark.parametrize("wtype", FP4)
+def test_fp4_memcpy_fill_matches_kernel_fill(wtype):
+    w = synth.tiny().with_(wtype=wtype, steps=8)
     pool = synth.ExpertPool(w)
     banks = pool.routed_banks()
     with Run(w, banks, None) as a, Run(w, banks, None, fill_mode=1) as b:
