@@ -77,6 +77,26 @@ def test_init_rejects_bad_config_without_touching_the_gpu(F):
     with pytest.raises(F.FtError) as e:  # FP8 without scale banks
         F.ft_moe_init(F.make_config(**{**base, "wtype": F.FT_W_FP8_E4M3_B128, "hidden": 512}), banks)
     assert e.value.status == F.FT_ERR_INVALID
+    u8 = np.zeros(16, np.uint8)
+    for wt in (F.FT_W_NVFP4, F.FT_W_MXFP4):  # block-FP4 without their scale banks
+        with pytest.raises(F.FtError) as e:
+            F.ft_moe_init(F.make_config(**{**base, "wtype": wt}), {"gate": u8, "up": u8, "down": u8})
+        assert e.value.status == F.FT_ERR_INVALID
+    with pytest.raises(F.FtError) as e:  # NVFP4 needs the tensor scales too
+        F.ft_moe_init(F.make_config(**{**base, "wtype": F.FT_W_NVFP4}),
+                      {"gate": u8, "up": u8, "down": u8, "gate_bscale": u8, "up_bscale": u8, "down_bscale": u8})
+    assert e.value.status == F.FT_ERR_INVALID
+
+
+def test_router_and_prefill_calls_reject_a_null_handle(F):
+    for call in (lambda: F.ft_moe_set_router(None, None, 0), lambda: F.ft_moe_router_logits(None, 0, 1, 1, 1),
+                 lambda: F.ft_moe_decode_step_hidden(None, 0, 1, 1, 1, 1),
+                 lambda: F.ft_moe_prefill_chunk_hidden(None, 0, 1, 1, 1),
+                 lambda: F.ft_moe_prefill_chunk(None, 0, 1, 1, 1, 1),
+                 lambda: F.ft_moe_set_host_hook(None, None), lambda: F.ft_moe_set_prefill_overlap(None, True)):
+        with pytest.raises(F.FtError) as e:
+            call()
+        assert e.value.status == F.FT_ERR_INVALID
 
 
 def test_null_handle_calls_fail_cleanly(F):
