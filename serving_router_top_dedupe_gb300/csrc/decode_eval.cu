@@ -16,7 +16,11 @@
 // butterfly), independent of slot, batch composition or split, so outputs are identical
 // across cache capacities.  FP8 E4M3 rows are decoded with the hardware e4m3x2->f16x2
 // conversion; each 128-element block's partial dot is multiplied by its FP32 scale once
-// ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2, post-scaling).
+// ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2, post-scaling).  The block-FP4 formats named in
+// "FreeToken 完全拆解" (section 主结果) take the same order: E2M1 pairs are decoded with the
+// hardware e2m1x2->f16x2 conversion, each block's partial dot (16 elements for NVFP4, 32 for
+// MXFP4) is multiplied by its scale (E4M3, or E8M0 = 2^(code-127)), and NVFP4's per-bank FP32
+// tensor scale multiplies the finished row sum.
 #include <cuda_fp16.h>
 
 #include <algorithm>
