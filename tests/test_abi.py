@@ -42,6 +42,21 @@ def test_library_exports_every_declared_symbol(F):
     assert declared == set(F.EXPORTED)
 
 
+def test_binding_argument_counts_match_the_header(F):
+    """Every declared entry point takes as many arguments in the binding's ctypes
+    signature as in the C declaration."""
+    arity = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        for m in re.finditer(r"^\s*(?:ft_status|const char\*)\s+(ft_\w+)\s*\(([^)]*)\)\s*;", text, re.M):
+            args = m.group(2).strip()
+            arity[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    assert len(arity) >= 20
+    for name, n in arity.items():
+        if name in F._SIGS:
+            assert len(F._SIGS[name]) == n, name
+
+
 def test_split_host_mirror_matches_oracle(F):
     rng = random.Random(3)
     for _ in range(2000):
