@@ -91,6 +91,8 @@ def route(logits: np.ndarray, k: int, gate_mode: int = GATE_SOFTMAX_TOPK):
 
     The softmax exponentials are shifted by the largest logit (an exact identity).
     All three gate functions are increasing in z, so the choice is the same.
+    A NaN logit ranks as -inf (it then ties with any -inf logit, lower id first);
+    -0 and +0 are equal logits.
     """
     B, E = logits.shape
     sel = np.empty((B, k), dtype=np.int64)
@@ -98,6 +100,7 @@ def route(logits: np.ndarray, k: int, gate_mode: int = GATE_SOFTMAX_TOPK):
     ids = np.arange(E)
     for t in range(B):
         z = logits[t].astype(np.float64)
+        z = np.where(np.isnan(z), -np.inf, z)
         order = np.lexsort((ids, -z))          # primary: logit desc; secondary: id asc
         chosen = np.sort(order[:k])
         zs = z[chosen]

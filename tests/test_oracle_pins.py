@@ -110,6 +110,42 @@ def test_router_ties_pick_lower_id_brute_force():
         assert np.allclose(gates[0], np.array(w) / sum(w), rtol=1e-6)
 
 
+def test_router_nan_ranks_as_minus_inf_and_signed_zeros_tie():
+    """Brute force over small rows with NaN, -inf, -0 and +0: NaN takes the place of -inf,
+    -0 equals +0, and equal keys go to the lower id.  Gates of the softmax over the chosen:
+    a -inf logit among them gets exactly 0."""
+    rng = random.Random(17)
+    vals = [0.0, -0.0, 1.0, -1.0, float("-inf"), float("nan"), 2.5]
+    for _ in range(300):
+        E = rng.randint(2, 20)
+        k = rng.randint(1, E)
+        z = np.array([rng.choice(vals) for _ in range(E)], dtype=np.float32)
+        z[rng.randrange(E)] = 3.0                      # at least one finite logit on top
+        key = [float("-inf") if math.isnan(float(v)) else float(v) for v in z]
+        ranked = sorted(range(E), key=lambda e: (-key[e], e))
+        chosen = sorted(ranked[:k])
+        sel, gates = O.route(z[None, :], k)
+        assert list(sel[0]) == chosen
+        top = max(key[e] for e in chosen)
+        ex = [0.0 if key[e] == float("-inf") else math.exp(key[e] - top) for e in chosen]
+        np.testing.assert_allclose(gates[0], np.array(ex) / sum(ex), rtol=1e-6, atol=0)
+        assert all(g == 0.0 for g, e in zip(gates[0], chosen) if key[e] == float("-inf"))
+
+
+def test_rel_err_rows_hand_computed():
+    """The output metric, per row max|y - ref| / max|ref|, then the largest row.  The case
+    is built so that each plausible slip gives another value: |y| as the denominator gives
+    0.142857, one global max over all rows 0.1, an element-wise ratio 1.0, a mean over the
+    rows 0.1125."""
+    y = np.array([[1.0, -2.0, 3.5], [90.0, 0.0, 0.0]])
+    ref = np.array([[0.5, -2.0, 4.0], [100.0, 0.0, 0.0]])
+    assert O.rel_err_rows(y, ref) == pytest.approx(0.125, abs=1e-15)
+    assert O.rel_err_rows(ref, y) == pytest.approx(max(0.5 / 3.5, 10.0 / 90.0), abs=1e-15)
+    assert O.rel_err_rows(np.array([1.0, 2.0]), np.array([2.0, 2.0])) == pytest.approx(0.5)  # one row
+    assert O.rel_err_rows(np.zeros((2, 3)), np.zeros((2, 3))) == 0.0
+    assert O.rel_err_rows(ref, ref) == 0.0
+
+
 def test_router_gate_functions_match_torch():
     torch = pytest.importorskip("torch")
     rng = np.random.default_rng(5)
@@ -635,3 +671,29 @@ def test_resize_keeps_most_recent_and_output_unchanged():
     _check_state_bijection(c)
     c.resize(30)
     assert c.S == 30 and all(c.owner[10:] == -1) and all(c.stamp[10:] == 0)
+
+
+def test_resize_pairs_movers_and_free_slots_in_ascending_order():
+    """Hand-worked shrink: keep the new_slots most recent (stamp desc, slot asc), then move
+    the kept entries at slots >= new_slots into the free slots below, both ascending."""
+    c = O.SlotCache(8, 20)
+    c.owner[:] = [10, 11, -1, 13, 14, 15, 16, 17]
+    c.stamp[:] = [1, 9, 0, 3, 8, 7, 2, 6]
+    for s, u in enumerate(c.owner):
+        if u >= 0:
+            c.res[u] = s
+    c.clock = 9
+    moves = c.resize(4)
+    assert moves == [(4, 0), (5, 2), (7, 3)]
+    assert list(c.owner) == [14, 11, 15, 17] and list(c.stamp) == [8, 9, 7, 6]
+    assert [int(c.res[u]) for u in (10, 11, 13, 14, 15, 16, 17)] == [-1, 1, -1, 0, 2, -1, 3]
+    # equal stamps at the cut: the lower slot is kept
+    c = O.SlotCache(6, 6)
+    c.owner[:] = [0, 1, 2, 3, 4, 5]
+    c.res[:] = [0, 1, 2, 3, 4, 5]
+    c.stamp[:] = [1, 5, 2, 5, 5, 5]
+    c.clock = 5
+    moves = c.resize(3)
+    assert moves == [(3, 0), (4, 2)]
+    assert list(c.owner) == [3, 1, 4] and list(c.stamp) == [5, 5, 5]
+    assert [int(v) for v in c.res] == [-1, 1, -1, 0, 2, -1]
