@@ -370,6 +370,9 @@ ft_status ft_moe_destroy(ft_moe* h);
  *   shared_dev   dev, one slot in the same layout, or NULL (no shared expert)
  *   x_bf16 [batch][H] BF16, logits [batch][E] FP32, out [batch][H] FP32 (dev);
  *   rows_out     optional dev [batch][top_k][H] FP32 gate-weighted pair rows
+ *   error_word_out optional dev uint32: receives this call's FT_DEVERR_* bits (for example
+ *                FT_DEVERR_NAN_LOGIT for a NaN logit, ranked as -inf), written in stream
+ *                order after the output; NULL skips it
  *   stream       cudaStream_t to enqueue on (NULL: legacy default stream)
  * It calls no cudaMalloc, cudaFree or other allocating routine.  All intermediates live
  * in one file-scope device array of 8 MiB that every GPU loading the library holds until
@@ -385,7 +388,7 @@ ft_status ft_moe_destroy(ft_moe* h);
 ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, int hidden, int inter, int wtype,
                                          const void* experts_dev, const void* shared_dev, int batch,
                                          const void* x_bf16, const float* logits, float* out,
-                                         float* rows_out, void* stream);
+                                         float* rows_out, uint32_t* error_word_out, void* stream);
 
 /* Thread-local message describing the last error of this thread ("" if none). */
 const char* ft_last_error(void);

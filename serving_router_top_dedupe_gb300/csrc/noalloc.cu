@@ -48,6 +48,12 @@ __global__ void noalloc_reset(int32_t* res, int32_t* owner, uint32_t* stamp, ft:
   if (blockIdx.x == 0 && threadIdx.x == 0) *st = ft::DevState{};
 }
 
+// Copies this call's device error word (cleared by noalloc_reset at the start of the call)
+// to the caller's word.
+__global__ void noalloc_export_error(const ft::DevState* st, uint32_t* out) {
+  if (threadIdx.x == 0) *out = *reinterpret_cast<const volatile uint32_t*>(&st->error_word);
+}
+
 // Bump allocator over the scratch array (offsets only; nothing is allocated).
 struct Carve {
   unsigned char* base;
@@ -66,7 +72,7 @@ struct Carve {
 extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, int hidden, int inter, int wtype,
                                                     const void* experts_dev, const void* shared_dev, int batch,
                                                     const void* x_bf16, const float* logits, float* out,
-                                                    float* rows_out, void* stream) {
+                                                    float* rows_out, uint32_t* error_word_out, void* stream) {
   if (n_experts < 1 || n_experts > ft::kMaxE || top_k < 1 || top_k > ft::kMaxK || top_k > n_experts)
     return FT_ERR_INVALID;
   if (wtype != FT_W_BF16 && wtype != FT_W_FP8_E4M3_B128) return FT_ERR_INVALID;
@@ -156,7 +162,11 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   cp.pool = static_cast<const uint8_t*>(experts_dev);
   cp.slot_stride = lay.stride;
   cp.shared_w = static_cast<const uint8_t*>(shared_dev);
-  cp.pdl = true;
+  // Plain stream order, no programmatic dependent launch: the control kernel's prologue
+  // reads the table that noalloc_reset writes, and at batch 1 the evaluation kernel's
+  // prologue reads the lists the control kernel writes (in ft_moe_decode_step a fill
+  // kernel sits between the two; here nothing does).
+  cp.pdl = false;
   if (ft::launch_control(cp, s) != cudaSuccess) return FT_ERR_CUDA;
 
   ft::EvalParams ep{};
@@ -184,8 +194,12 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   ep.has_shared = has_shared;
   ep.n_sm = su->n_sm;
   ep.max_entries = kcap + 1;
-  ep.pdl = true;
+  ep.pdl = false;
   if (ft::launch_gate_up(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
   if (ft::launch_down_combine(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
+  if (error_word_out) {
+    noalloc_export_error<<<1, 32, 0, s>>>(st, error_word_out);
+    if (cudaGetLastError() != cudaSuccess) return FT_ERR_CUDA;
+  }
   return FT_OK;
 }

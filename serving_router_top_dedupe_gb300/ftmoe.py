@@ -102,7 +102,7 @@ _SIGS = {
     "ft_moe_synchronize": [_P],
     "ft_moe_destroy": [_P],
     "ft_moe_decode_resident_noalloc": [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, _P, C.c_int, _P, _P, _P, _P,
-                                       _P],
+                                       _P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -308,12 +308,13 @@ def ft_moe_destroy(h) -> None:
 
 
 def ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, experts_dev, shared_dev, batch, x_bf16,
-                                   logits, out, rows_out=None, stream=None) -> None:
+                                   logits, out, rows_out=None, error_word_out=None, stream=None) -> None:
     """Allocation-free layer evaluation (see include/ft_moe.h): every intermediate lives in
-    the library's fixed 8 MiB device scratch array; nothing is allocated by the call."""
+    the library's fixed 8 MiB device scratch array; nothing is allocated by the call.
+    error_word_out: optional device uint32 that receives the call's device error bits."""
     st = _lib.ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, _ptr(experts_dev),
                                              _ptr(shared_dev), batch, _ptr(x_bf16), _ptr(logits), _ptr(out),
-                                             _ptr(rows_out), stream)
+                                             _ptr(rows_out), _ptr(error_word_out), stream)
     if st != FT_OK:
         raise FtError(st, "ft_moe_decode_resident_noalloc failed")
 
