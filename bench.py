@@ -1,13 +1,19 @@
 #!/usr/bin/env python3
 """Benchmark of the MoE-layer expert-cache hot path on one GB300 (or N replicas).
 
-Workload (decode): 40 MoE layers of the 35B-A3B expert shape (H 2048, I 512,
+Headline workload (decode): 40 MoE layers of the 35B-A3B expert shape (H 2048, I 512,
 256 routed experts top-8 + one shared expert, BF16), batch 1, a routing trace with
-temporal locality (p = 0.7 reuse, Zipf(1.1) redraws), slot cache = 37% of the
-routed pool (3788 slots), B_P:B_H = 52.7:77.3.  One step = one token through all
-40 layers (control -> fill -> gate/up GEMV -> down GEMV + combine per layer),
-replayed as one CUDA graph.  Inputs are synthetic and seeded; the expert weights
-read per token (2.27 GB) exceed L2, so no flush is needed between steps.
+temporal locality (p = 0.7 reuse, Zipf(1.1) redraws), slot cache = 37% of the routed
+pool (3788 slots), B_P:B_H = 52.7:77.3.  One step = one token through all 40 layers
+(control -> fill -> expert GEMV + combine per layer), replayed as one CUDA graph.  Each
+handle first runs an untimed prefix of the trace so that the timed steps start from a
+steady cache.  Inputs are synthetic and seeded; the expert weights read per token
+(2.27 GB) exceed L2, so no flush is needed between steps.
+
+Beside it, on the same line: the same workload with B_P measured on this machine, the FP8
+large-expert decode workload (8 layers, H 7168, I 2048, E4M3 with 1x128 block scales, 11%
+cache) at batch 1 and 8, and the 8192-token prefill chunk.  `--sweep` times the
+batch x capacity x split grid instead.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
 """
@@ -112,27 +118,20 @@ class Dist:
         if self.pg:
             self.pg.barrier()
 
-    def max(self, v: float) -> float:
-        if not self.pg:
-            return v
+    def _reduce(self, v: float, op) -> float:
         import torch
 
         dev = torch.device("cuda", self.local) if torch.cuda.is_available() and \
             self.pg.get_backend() == "nccl" else torch.device("cpu")
         t = torch.tensor([v], dtype=torch.float64, device=dev)
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        self.pg.all_reduce(t, op=op)
         return float(t.item())
+
+    def max(self, v: float) -> float:
+        return v if not self.pg else self._reduce(v, self.pg.ReduceOp.MAX)
 
     def sum(self, v: float) -> float:
-        if not self.pg:
-            return v
-        import torch
-
-        dev = torch.device("cuda", self.local) if torch.cuda.is_available() and \
-            self.pg.get_backend() == "nccl" else torch.device("cpu")
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
-        return float(t.item())
+        return v if not self.pg else self._reduce(v, self.pg.ReduceOp.SUM)
 
     def close(self):
         if self.pg:
@@ -144,6 +143,36 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, d: Dist) -> tuple[
     total = d.sum(units_per_rank)
     tmax = d.max(seconds_per_rank)
     return total / tmax, tmax
+
+
+# ------------------------------------------------------------- host memory
+def _pinned_empty(shape, dtype):
+    """Page-locked, device-mapped host array from the library's host allocator
+    (ft_host_alloc: exact size, released by _release_host).  ft_moe_init uses such memory
+    as it is and registers nothing."""
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
+    a = F.host_array(shape, dtype)
+    _PINNED.add(id(a))
+    return a
+
+
+_PINNED: set = set()
+
+
+def _release_host(banks):
+    """Free the bank arrays that _pinned_empty made (after every handle using them is gone)."""
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
+    if banks:
+        for a in banks.values():
+            if id(a) in _PINNED:
+                _PINNED.discard(id(a))
+                F.free_host_array(a)
+
+
+def _host_empty(args):
+    return _pinned_empty if args.host_alloc == "pinned" else (lambda shape, dtype: np.empty(shape, dtype))
 
 
 # ------------------------------------------------------------------ inputs
@@ -161,24 +190,46 @@ def _workload():
     return w
 
 
-def _config_desc(w) -> dict:
-    name = "decode_bf16_35B-A3B-shape" if not (_OVERRIDE.get("layers") or _OVERRIDE.get("slots")) \
-        else "decode_bf16_35B-A3B-shape (reduced, profiling only)"
-    return {"workload": name, "n_layers": w.n_layers, "hidden": w.hidden,
-            "expert_inter": w.inter, "n_experts": w.n_experts, "top_k": w.top_k, "shared_expert": w.has_shared,
-            "weights": "bf16", "global_batch": w.batch, "cache_slots": w.cache_slots,
-            "cache_fraction": round(w.cache_slots / w.n_logical, 4), "bp_bh_gbps": [w.bp_gbps, w.bh_gbps],
-            "trace": "p=0.7 reuse, Zipf(1.1) redraw, 512-step cycle",
-            "l2": "inputs larger than L2 (2.27 GB of expert weights per token), no flush"}
+def _expert_bytes(w) -> int:
+    import synth
+
+    H, I = w.hidden, w.inter
+    if w.wtype == synth.W_BF16:
+        return 6 * H * I
+    return 3 * H * I + 4 * (2 * I * (H // 128) + H * (I // 128))
 
 
-def _pool_banks(w, d: Dist):
+def _config_desc(w, args=None, warm=None) -> dict:
+    import synth
+
+    reduced = _OVERRIDE.get("layers") or _OVERRIDE.get("slots")
+    if w.wtype == synth.W_BF16:
+        name = "decode_bf16_35B-A3B-shape" + (" (reduced, profiling only)" if reduced else "")
+    else:
+        name = "decode_fp8_large-expert"
+    d = {"workload": name, "n_layers": w.n_layers, "hidden": w.hidden,
+         "expert_inter": w.inter, "n_experts": w.n_experts, "top_k": w.top_k, "shared_expert": w.has_shared,
+         "weights": "bf16" if w.wtype == synth.W_BF16 else "fp8_e4m3 + fp32 scale per 1x128 block",
+         "global_batch": w.batch, "cache_slots": w.cache_slots,
+         "cache_fraction": round(w.cache_slots / w.n_logical, 4), "bp_bh_gbps": [w.bp_gbps, w.bh_gbps],
+         "trace": "p=0.7 reuse, Zipf(1.1) redraw",
+         "l2": f"inputs larger than L2 ({_expert_bytes(w) * w.top_k * w.n_layers / 1e9:.2f} GB of expert weights "
+               f"per token), no flush"}
+    if warm is not None:
+        d["cache_warm_prefix_tokens"] = warm
+    if args is not None:
+        d["host_pool"] = "cudaHostAlloc (page-locked, mapped)" if args.host_alloc == "pinned" \
+            else "malloc + cudaHostRegister"
+    return d
+
+
+def _pool_banks(w, d: Dist, args):
     """Host expert pool.  Replicas on one node share one copy in /dev/shm."""
     import synth
 
     pool = synth.ExpertPool(w)
     if d.world == 1:
-        return pool, pool.routed_banks(), pool.shared_banks()
+        return pool, pool.routed_banks(empty=_host_empty(args)), pool.shared_banks()
     tag = f"/dev/shm/ftmoe_pool_{w.seed}"
     banks = {}
     if d.rank == 0:
@@ -227,8 +278,19 @@ def _peaks():
         return FALLBACK_HBM, "fallback"
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 # ------------------------------------------------------------ CPU oracle
-def oracle_decode_tokens(w, banks, shared, trace, n_tokens, time_budget_s):
+def oracle_decode_tokens(w, pool, trace, n_tokens, time_budget_s):
     """Time the CPU oracle on a bounded sample: whole tokens (all layers) of the same
     trace, cache simulation included.  Returns (tokens, seconds, cpu_seconds)."""
     import oracle as O
@@ -236,7 +298,6 @@ def oracle_decode_tokens(w, banks, shared, trace, n_tokens, time_budget_s):
 
     sim = O.SlotCache(w.cache_slots, w.n_logical)
     bp, bh = O.mbps(w.bp_gbps), O.mbps(w.bh_gbps)
-    expert = lambda u: {k: v[u] for k, v in banks.items()}
     c0, t0 = time.process_time(), time.perf_counter()
     done = 0
     for s in range(n_tokens):
@@ -246,16 +307,261 @@ def oracle_decode_tokens(w, banks, shared, trace, n_tokens, time_budget_s):
             sel, gates = O.route(z, w.top_k)
             rec = sim.decode_step(l, w.n_experts, sel, bp, bh)
             cp = np.zeros((w.batch, w.top_k, w.hidden), dtype=np.float32)
-            sh = {k: v[l] for k, v in shared.items()} if shared is not None else None
-            O.decode_layer_outputs(rec, sel, gates, xb, cp, expert, shared=sh, n_experts=w.n_experts)
+            sh = pool.shared(l) if w.has_shared else None
+            O.decode_layer_outputs(rec, sel, gates, xb, cp, pool.expert, shared=sh, n_experts=w.n_experts)
         done += 1
         if time.perf_counter() - t0 > time_budget_s:
             break
     return done, time.perf_counter() - t0, time.process_time() - c0
 
 
-# ------------------------------------------------------------------- ours
+def _oracle_child(args) -> None:
+    """--oracle-child: time the oracle in this process (started with its thread count set in
+    the environment) and print one JSON object."""
+    import synth
+
+    w = _workload()
+    pool = synth.ExpertPool(w)
+    trace = synth.routing_trace(w)
+    oracle_decode_tokens(w, pool, trace, 1, 1e9)          # untimed warm-up token
+    n, sec, cpu = oracle_decode_tokens(w, pool, trace, args.cpu_tokens, args.cpu_budget)
+    print(json.dumps({"tokens": n, "seconds": sec, "cpu_seconds": cpu}), flush=True)
+
+
+def cpu_baselines(args) -> dict:
+    """The oracle as it stands, on the host cores: one thread, then every core, each in a
+    fresh process whose math-library thread count is fixed before numpy loads."""
+    res = {}
+    ncores = os.cpu_count() or 1
+    for label, thr in (("single_thread", 1), ("all_cores", ncores)):
+        env = dict(os.environ)
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k] = str(thr)
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child",
+                            "--cpu-tokens", str(args.cpu_tokens), "--cpu-budget", str(args.cpu_budget)],
+                           capture_output=True, text=True, env=env, timeout=600)
+        line = [l for l in r.stdout.splitlines() if l.startswith("{")]
+        if r.returncode != 0 or not line:
+            res[label] = {"error": (r.stderr or r.stdout)[-300:]}
+            continue
+        o = json.loads(line[-1])
+        res[label] = {"value": round(o["tokens"] / o["seconds"], 4), "threads": thr,
+                      "cpu_util": round(o["cpu_seconds"] / o["seconds"], 2), "tokens": o["tokens"],
+                      "seconds": round(o["seconds"], 1)}
+    return res
+
+
+# ------------------------------------------------------------------- decode
+def run_decode(args, d: Dist, dev, stream, w, banks, shared, label, warm_tokens, steps, warmup, n_prof,
+               e2e_steps=0, want_clocks=False, existing=None):
+    """One decode workload through a CUDA graph of all its layers.  Returns a result dict
+    (and the handle when the caller wants to keep it)."""
+    import torch
+
+    import synth
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
+    L, Bt, H, E, k = w.n_layers, w.batch, w.hidden, w.n_experts, w.top_k
+    ebytes = _expert_bytes(w)
+    n_total = warm_tokens + warmup + steps + n_prof + e2e_steps
+    t_setup = time.perf_counter()
+    trace = synth.routing_trace(w, steps=n_total)
+    # logits follow the trace at every token (they set the work); activations and host rows
+    # come from a ring of distinct tokens (their values do not change the work)
+    n_ring = min(64, n_total)
+    zs = np.empty((n_total, L, Bt, E), dtype=np.float32)
+    for s in range(n_total):
+        for l in range(L):
+            zs[s, l] = synth.decode_logits(w, s, l, trace)
+    xs = np.empty((n_ring, L, Bt, H), dtype=np.uint16)
+    for s in range(n_ring):
+        for l in range(L):
+            xs[s, l] = synth.decode_x(w, s, l)
+    cfg = F.make_config(L, H, w.inter, E, k, w.has_shared, w.wtype, Bt, w.cache_slots, w.bp_gbps, w.bh_gbps,
+                        device=d.local, compute_stream=stream.cuda_stream)
+    h = F.ft_moe_init(cfg, banks, shared)
+    z_all = torch.from_numpy(zs).to(dev)
+    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    # host-side partial rows of C pairs: synthetic stand-ins (their content does not change the work)
+    cp_all = (torch.randn((n_ring, L, Bt, k, H), device=dev, generator=gen) * 0.01).float()
+    x_s = torch.empty((L, Bt, H), dtype=torch.int16, device=dev)
+    z_s = torch.empty((L, Bt, E), dtype=torch.float32, device=dev)
+    c_s = torch.empty((L, Bt, k, H), dtype=torch.float32, device=dev)
+    o_s = torch.empty((L, Bt, H), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+    g = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
+    setup_s = time.perf_counter() - t_setup
+
+    def load(i):
+        x_s.copy_(x_all[i % n_ring])
+        z_s.copy_(z_all[i])
+        c_s.copy_(cp_all[i % n_ring])
+
+    res = {"config": _config_desc(w, args, warm_tokens), "steps": steps, "warmup": warmup}
+    with torch.cuda.stream(stream):
+        for i in range(warm_tokens + warmup):      # untimed: cache warm prefix, then warm-up steps
+            load(i)
+            F.ft_graph_launch(g)
+        stream.synchronize()
+        st0 = F.ft_moe_get_stats(h)
+        clocks = ClockSampler(d.local) if want_clocks else None
+        d.barrier()
+        torch.cuda.synchronize(dev)
+        if clocks:
+            clocks.start()
+            time.sleep(0.3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(warm_tokens + warmup, warm_tokens + warmup + steps):
+            load(i)
+            F.ft_graph_launch(g)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize(dev)
+        d.barrier()
+        res["clocks"] = clocks.stop() if clocks else None
+        ms = e0.elapsed_time(e1)
+        st1 = F.ft_moe_get_stats(h)
+    value, tmax = aggregate(steps * Bt, ms * 1e-3, d)
+    miss = st1.misses - st0.misses
+    acts = (st1.hits - st0.hits) + miss
+    res["value"], res["unit"], res["ms_per_step"] = round(value, 2), "tok/s", round(tmax * 1e3 / steps, 5)
+    res["cache"] = {"miss_rate": round(miss / max(1, acts), 4),
+                    "fills_per_token": round((st1.fills - st0.fills) / (steps * Bt), 3),
+                    "host_pairs_per_token": round((st1.cpu_execs - st0.cpu_execs) / (steps * Bt), 3),
+                    "gpu_experts_per_step": round((st1.eval_entries - st0.eval_entries) / steps, 2),
+                    "fill_gb_per_token": round((st1.fills - st0.fills) / (steps * Bt) * ebytes / 1e9, 4),
+                    "error_word": st1.error_word}
+
+    # Kernel profile: replays of a graph captured with timing events as nodes, on each
+    # kernel's own stream.  Each profiled token is replayed twice: the first replay is the
+    # token as it comes (fills included); the second finds every expert it needs resident
+    # (the token's own experts are the most recent), so its GEMV time is the pure weight
+    # stream, with no wait on a fill.
+    F.ft_moe_set_profiling(h, 1)
+    gp = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
+    F.ft_moe_get_profile(h, reset=True)
+    tot = {"mixed": {}, "resident": {}}
+    sdelta = {"mixed": [0, 0, 0, 0], "resident": [0, 0, 0, 0]}   # entries, pairs, fills, steps
+    base = warm_tokens + warmup + steps
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            load(base + i)
+            for kind in ("mixed", "resident"):
+                s0 = F.ft_moe_get_stats(h)
+                F.ft_graph_launch(gp)
+                pr = F.ft_moe_get_profile(h, reset=True)
+                s1 = F.ft_moe_get_stats(h)
+                for kk, (n, msum) in pr.items():
+                    a = tot[kind].setdefault(kk, [0, 0.0])
+                    a[0] += n
+                    a[1] += msum
+                dd = sdelta[kind]
+                dd[0] += s1.eval_entries - s0.eval_entries
+                dd[1] += s1.eval_pairs - s0.eval_pairs
+                dd[2] += s1.fills - s0.fills
+                dd[3] += 1
+    F.ft_graph_destroy(gp)
+    F.ft_moe_set_profiling(h, 0)
+    peak, peak_kind = _peaks()
+    esz_x = 2
+    I = w.inter
+
+    def gemv_bytes(ent, prs, nsteps):
+        gu = ent * (2 * ebytes // 3) + prs * (H * esz_x + I * 4)
+        dn = ent * (ebytes // 3) + prs * (I * 4 + H * 4) + nsteps * L * Bt * H * 4 * (k + 2)
+        return gu, dn
+
+    kern = {}
+    for kind in ("mixed", "resident"):
+        pr = tot[kind]
+        ent, prs, fills, nst = sdelta[kind]
+        gu_b, dn_b = gemv_bytes(ent, prs, nst)
+        tot_ms = sum(v[1] for v in pr.values()) or 1.0
+        kk = {}
+        for name, (n, msum) in pr.items():
+            if n:
+                kk[name] = {"launches": n, "avg_us": round(1e3 * msum / n, 3), "share": round(msum / tot_ms, 4)}
+        gu_n, gu_ms = pr.get("gate_up", [0, 0.0])
+        dn_n, dn_ms = pr.get("down_combine", [0, 0.0])
+        fused = dn_n == 0
+        if fused and gu_n:
+            kk["expert_gemv_fused"] = kk.pop("gate_up")
+            kk["expert_gemv_fused"]["achieved_gbs"] = round((gu_b + dn_b) / (gu_ms * 1e-3) / 1e9, 1)
+            kk["expert_gemv_fused"]["bytes_per_launch"] = round((gu_b + dn_b) / gu_n)
+        else:
+            if gu_n:
+                kk["gate_up"]["achieved_gbs"] = round(gu_b / (gu_ms * 1e-3) / 1e9, 1)
+                kk["gate_up"]["bytes_per_launch"] = round(gu_b / gu_n)
+            if dn_n:
+                kk["down_combine"]["achieved_gbs"] = round(dn_b / (dn_ms * 1e-3) / 1e9, 1)
+                kk["down_combine"]["bytes_per_launch"] = round(dn_b / dn_n)
+        if pr.get("fill", [0, 0])[1]:
+            kk.setdefault("fill", {})["observed_gbs"] = round(fills * ebytes / (pr["fill"][1] * 1e-3) / 1e9, 1) \
+                if fills else None
+        kern[kind] = kk
+    res["kernels"] = kern
+    # roofline of the dominant kernel: the expert GEMV, timed on the replays whose experts
+    # were all resident (no fill to wait for) when there were such replays
+    src = "resident" if sdelta["resident"][2] == 0 else "mixed"
+    kk = kern[src]
+    name = "expert_gemv_fused" if "expert_gemv_fused" in kk else "gate_up"
+    if name in kk and "achieved_gbs" in kk[name]:
+        ach = kk[name]["achieved_gbs"]
+        res["roofline"] = {
+            "kernel": ("expert GEMV, batch 1, one launch: gate/up + SwiGLU + down + combine" if name ==
+                       "expert_gemv_fused" else "gate_up (expert GEMV: gate+up rows, SwiGLU)"),
+            "timed_on": ("replays whose experts were all resident (no fill wait)" if src == "resident" else
+                         "replays as they come (fills included)"),
+            "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": kk[name]["bytes_per_launch"],
+            "avg_us": kk[name]["avg_us"]}
+    # the decode path as a whole: expert-weight bytes evaluated per step over the timed step time
+    wbytes = (st1.eval_entries - st0.eval_entries) / steps * ebytes
+    res["decode_step_roofline"] = {
+        "scope": "whole decode step (all kernels, fills included): expert weight bytes evaluated per step / "
+                 "time per step", "bound": "hbm", "achieved": round(wbytes / (tmax / steps) / 1e9, 1),
+        "peak": peak, "unit": "GB/s", "frac": round(wbytes / (tmax / steps) / 1e9 / peak, 4)}
+    res["hbm_gbs_expert_weights"] = {kn: v.get("achieved_gbs") for kn, v in kern[src].items()
+                                     if "achieved_gbs" in v}
+    res["setup_s"] = round(setup_s, 1)
+
+    if e2e_steps:
+        # end to end through the host-buffer C-ABI call (H2D inputs, D2H outputs, every step)
+        xh = torch.empty((L, Bt, H), dtype=torch.int16).pin_memory()
+        zh = torch.empty((L, Bt, E), dtype=torch.float32).pin_memory()
+        ch = torch.empty((L, Bt, k, H), dtype=torch.float32).pin_memory()
+        oh = torch.empty((L, Bt, H), dtype=torch.float32).pin_memory()
+        cp_host = cp_all.cpu()
+        F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)   # capture the cached graph
+        t_e2e = 0.0
+        for i in range(e2e_steps):
+            s = base + n_prof + i
+            xh.copy_(torch.from_numpy(xs[s % n_ring].view(np.int16)))
+            zh.copy_(torch.from_numpy(zs[s]))
+            ch.copy_(cp_host[s % n_ring])
+            t0 = time.perf_counter()
+            F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)
+            t_e2e += time.perf_counter() - t0
+        e2e_v, _ = aggregate(e2e_steps * Bt, t_e2e, d)
+        res["e2e"] = {"value": round(e2e_v, 2), "unit": "tok/s",
+                      "h2d_bytes_per_step": L * Bt * (H * 2 + E * 4 + k * H * 4),
+                      "d2h_bytes_per_step": L * Bt * H * 4, "steps": e2e_steps,
+                      "api": "ft_moe_decode_layers_host (pinned host buffers, cached graph)"}
+    F.ft_graph_destroy(g)
+    F.ft_moe_destroy(h)
+    del x_all, z_all, cp_all
+    torch.cuda.empty_cache()
+    res["launches_per_layer"] = 3 if "expert_gemv_fused" in kern["mixed"] else 4
+    res["label"] = label
+    return res
+
+
 def run_ours(args, d: Dist) -> dict | None:
+    import gc
+
     import torch
 
     import synth
@@ -266,188 +572,64 @@ def run_ours(args, d: Dist) -> dict | None:
 
     torch.cuda.set_device(d.local)
     dev = torch.device("cuda", d.local)
-    w = _workload()
-    L, Bt, H, E, k = w.n_layers, w.batch, w.hidden, w.n_experts, w.top_k
-    t_setup = time.perf_counter()
-    pool, banks, shared = _pool_banks(w, d)
-    trace = synth.routing_trace(w)
-    n_tr = w.steps
-    xs = np.empty((n_tr, L, Bt, H), dtype=np.uint16)
-    zs = np.empty((n_tr, L, Bt, E), dtype=np.float32)
-    for s in range(n_tr):
-        for l in range(L):
-            xs[s, l] = synth.decode_x(w, s, l)
-            zs[s, l] = synth.decode_logits(w, s, l, trace)
     stream = torch.cuda.Stream(device=dev)
-    cfg = F.make_config(L, H, w.inter, E, k, w.has_shared, F.FT_W_BF16, Bt, w.cache_slots, w.bp_gbps, w.bh_gbps,
-                        device=d.local, compute_stream=stream.cuda_stream)
-    h = F.ft_moe_init(cfg, banks, shared)
+    w = _workload()
+    pool, banks, shared = _pool_banks(w, d, args)
     bp_measured = F.ft_bench_bw(256 << 20, 8)
-    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
-    z_all = torch.from_numpy(zs).to(dev)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(w.seed)
-    # host-side partial rows of C pairs: synthetic stand-ins (content does not change the work)
-    cp_all = (torch.randn((n_tr, L, Bt, k, H), device=dev, generator=gen) * 0.01).float()
-    x_s = torch.empty((L, Bt, H), dtype=torch.int16, device=dev)
-    z_s = torch.empty((L, Bt, E), dtype=torch.float32, device=dev)
-    c_s = torch.empty((L, Bt, k, H), dtype=torch.float32, device=dev)
-    o_s = torch.empty((L, Bt, H), dtype=torch.float32, device=dev)
-    torch.cuda.synchronize(dev)
-    g = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
-    setup_s = time.perf_counter() - t_setup
-
-    def load(i):
-        s = i % n_tr
-        x_s.copy_(x_all[s])
-        z_s.copy_(z_all[s])
-        c_s.copy_(cp_all[s])
-
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            load(i)
-            F.ft_graph_launch(g)
-        stream.synchronize()
-        st0 = F.ft_moe_get_stats(h)
-        clocks = ClockSampler(d.local)
-        d.barrier()
-        torch.cuda.synchronize(dev)
-        clocks.start()
-        time.sleep(0.3)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.warmup, args.warmup + args.steps):
-            load(i)
-            F.ft_graph_launch(g)
-        e1.record(stream)
-        e1.synchronize()
-        torch.cuda.synchronize(dev)
-        d.barrier()
-        clk = clocks.stop()
-        ms = e0.elapsed_time(e1)
-        st1 = F.ft_moe_get_stats(h)
-    bp_after = F.ft_bench_bw(256 << 20, 8)
-    value, tmax = aggregate(args.steps * Bt, ms * 1e-3, d)
-    layer_steps = (st1.decode_steps - st0.decode_steps)
-    miss = st1.misses - st0.misses
-    acts = (st1.hits - st0.hits) + miss
-    cache = {"miss_rate": miss / max(1, acts), "fills_per_token": (st1.fills - st0.fills) / args.steps,
-             "host_pairs_per_token": (st1.cpu_execs - st0.cpu_execs) / args.steps,
-             "gpu_experts_per_token": (st1.eval_entries - st0.eval_entries) / args.steps,
-             "fill_gb_per_token": (st1.fills - st0.fills) / args.steps * 6 * H * w.inter / 1e9,
-             "error_word": st1.error_word}
-
-    # kernel profile: replays of a graph captured with timing events as nodes (events on
-    # each kernel's own stream), read after every replay; same trace, continuing state
-    n_prof = min(args.profile_steps, n_tr)
-    F.ft_moe_set_profiling(h, 1)
-    gp = F.ft_moe_graph_capture_decode(h, 0, L, Bt, x_s, z_s, c_s, o_s)
-    F.ft_moe_get_profile(h, reset=True)
-    sp0 = F.ft_moe_get_stats(h)
-    with torch.cuda.stream(stream):
-        for i in range(n_prof):
-            load(args.warmup + args.steps + i)
-            F.ft_graph_launch(gp)
-            F.ft_moe_get_profile(h, reset=False)
-    prof = F.ft_moe_get_profile(h, reset=True)
-    sp1 = F.ft_moe_get_stats(h)
-    F.ft_graph_destroy(gp)
-    F.ft_moe_set_profiling(h, 0)
-    fill_bytes_prof = (sp1.fills - sp0.fills) * 6 * H * w.inter
-    fill_gbs = fill_bytes_prof / (prof["fill"][1] * 1e-3) / 1e9 if prof["fill"][1] else None
-    ent = sp1.eval_entries - sp0.eval_entries
-    prs = sp1.eval_pairs - sp0.eval_pairs
-    esz = 2
-    gate_up_bytes = ent * 2 * w.inter * H * esz + prs * (H * 2 + w.inter * 4)
-    down_bytes = ent * H * w.inter * esz + prs * (w.inter * 4 + H * 4) + n_prof * L * Bt * H * 4 * (k + 2)
-    tot_ms = sum(v[1] for v in prof.values())
-    kernels = {}
-    for name, (n, msum) in prof.items():
-        if n:
-            kernels[name] = {"launches": n, "avg_us": round(1e3 * msum / n, 3), "share": round(msum / tot_ms, 4)}
-    peak, peak_kind = _peaks()
-    gu_n, gu_ms = prof["gate_up"]
-    dn_n, dn_ms = prof["down_combine"]
-    fused = dn_n == 0  # batch 1: one persistent kernel evaluates the whole layer
-    if fused:
-        gv_bytes = gate_up_bytes + down_bytes
-        ach = gv_bytes / (gu_ms * 1e-3) / 1e9 if gu_ms else None
-        if "gate_up" in kernels:
-            kernels["expert_gemv_fused"] = kernels.pop("gate_up")
-            kernels["expert_gemv_fused"]["achieved_gbs"] = round(ach, 1) if ach else None
-        hbm = {"expert_gemv_fused": round(ach, 1) if ach else None}
-        rl_kernel, rl_bytes, rl_n = ("expert GEMV, batch 1, one launch: gate/up + SwiGLU + down + combine",
-                                     gv_bytes, gu_n)
-    else:
-        ach = gate_up_bytes / (gu_ms * 1e-3) / 1e9 if gu_ms else None
-        ach_dn = down_bytes / (dn_ms * 1e-3) / 1e9 if dn_ms else None
-        kernels.get("gate_up", {})["achieved_gbs"] = round(ach, 1) if ach else None
-        kernels.get("down_combine", {})["achieved_gbs"] = round(ach_dn, 1) if ach_dn else None
-        hbm = {"gate_up": round(ach, 1) if ach else None, "down_combine": round(ach_dn, 1) if ach_dn else None}
-        rl_kernel, rl_bytes, rl_n = "gate_up (expert GEMV: gate+up rows, SwiGLU)", gate_up_bytes, gu_n
-    tr = _traffic("expert_gemv_fused" if fused else "gate_up")
-    roofline = {"kernel": rl_kernel, "bound": "hbm",
-                "achieved": round(ach, 1) if ach else None, "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4) if ach else None, "peak_source": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": round(rl_bytes / max(1, rl_n)),
-                "traffic": tr}
-    launches_per_layer = 3 if fused else 4
-    # the decode path as a whole: expert-weight bytes the evaluation reads per token over the
-    # timed time per token (control, fills and evaluation included)
-    wbytes_tok = cache["gpu_experts_per_token"] * 6 * H * w.inter
-    layer_rl = {"scope": "whole decode step (all kernels, fills included): expert weight bytes per token / time per token",
-                "bound": "hbm", "achieved": round(wbytes_tok / (tmax / args.steps) / 1e9, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(wbytes_tok / (tmax / args.steps) / 1e9 / peak, 4)}
-
-    # end to end through the host-buffer C-ABI call (H2D inputs, D2H outputs, every step)
-    n_e2e = min(args.e2e_steps, args.steps)
-    xh = torch.empty((L, Bt, H), dtype=torch.int16).pin_memory()
-    zh = torch.empty((L, Bt, E), dtype=torch.float32).pin_memory()
-    ch = torch.empty((L, Bt, k, H), dtype=torch.float32).pin_memory()
-    oh = torch.empty((L, Bt, H), dtype=torch.float32).pin_memory()
-    cp_host = cp_all[: min(n_tr, 64)].cpu()
-    F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)   # capture the cached graph
-    t_e2e = 0.0
-    for i in range(n_e2e):
-        s = (args.warmup + args.steps + n_prof + i) % n_tr
-        xh.copy_(torch.from_numpy(xs[s].view(np.int16)))
-        zh.copy_(torch.from_numpy(zs[s]))
-        ch.copy_(cp_host[s % cp_host.shape[0]])
-        t0 = time.perf_counter()
-        F.ft_moe_decode_layers_host(h, 0, L, Bt, xh, zh, ch, oh, True)
-        t_e2e += time.perf_counter() - t0
-    e2e_v, _ = aggregate(n_e2e * Bt, t_e2e, d)
-    h2d = L * Bt * (H * 2 + E * 4 + k * H * 4)
-    d2h = L * Bt * H * 4
-    e2e = {"value": round(e2e_v, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": n_e2e, "api": "ft_moe_decode_layers_host (pinned host buffers, cached graph)"}
-    F.ft_graph_destroy(g)
-    F.ft_moe_destroy(h)
-    del x_all, z_all, cp_all
+    head = run_decode(args, d, dev, stream, w, banks, shared, "headline", args.cache_warm, args.steps, args.warmup,
+                      args.profile_steps, e2e_steps=min(args.e2e_steps, args.steps), want_clocks=True)
+    extra = {}
+    solo = d.world == 1
+    if solo and not args.only_headline:
+        # the same workload with the split taken from B_P measured on this machine
+        wm = w.with_(bp_gbps=round(bp_measured, 1))
+        extra["decode_bf16_measured_bp"] = run_decode(args, d, dev, stream, wm, banks, shared, "measured B_P",
+                                                      args.cache_warm, args.steps, args.warmup,
+                                                      min(16, args.profile_steps))
+    _release_host(banks)
+    banks = shared = pool = None
+    gc.collect()
     cpu_baseline = None
-    if d.rank == 0 and d.world == 1 and not args.no_cpu_baseline:
-        n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, args.cpu_tokens, args.cpu_budget)
-        cpu_baseline = {"value": round(n / sec, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
-                        "kind": "oracle",
-                        "sample": f"{n} tokens x {L} layers of the same trace (float64 numpy oracle, "
-                                  f"cache simulation included), {sec:.1f} s on {os.cpu_count()} host cores"}
-    prefill = None
-    if not args.no_prefill:
-        banks = shared = pool = None
-        import gc
-
+    if d.rank == 0 and solo and not args.no_cpu_baseline:
+        cb = cpu_baselines(args)
+        allc = cb.get("all_cores", {})
+        if "value" in allc:
+            cpu_baseline = {"value": allc["value"], "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                            "cpu_model": _cpu_model(),
+                            "sample": f"{allc['tokens']} tokens x {w.n_layers} layers of the same trace (float64 "
+                                      f"numpy oracle, cache simulation included), {allc['seconds']} s",
+                            "single_thread": cb.get("single_thread"), "all_cores": allc}
+    if solo and not args.only_headline and not args.no_fp8:
+        wf = synth.decode_fp8(batch=1)
+        poolf = synth.ExpertPool(wf)
+        banksf = poolf.routed_banks(empty=_host_empty(args))
+        for Bt, st in ((1, min(args.steps, args.fp8_steps)), (8, min(args.steps, args.fp8_steps_b8))):
+            wb = wf.with_(batch=Bt)
+            extra[f"decode_fp8_b{Bt}"] = run_decode(args, d, dev, stream, wb, banksf, None, f"FP8 batch {Bt}",
+                                                    args.fp8_warm, st, args.warmup, min(8, args.profile_steps))
+        _release_host(banksf)
+        banksf = poolf = None
         gc.collect()
+    prefill = None
+    if solo and not args.no_prefill:
         prefill = run_prefill(args, d, dev, stream)
 
-    out = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded: locality trace, N(0,1) BF16 activations, generated expert banks)",
-           "config": {**_config_desc(w), "parallelism": f"replicas x{d.world}" if d.world > 1 else "single GPU"},
-           "hbm_gbs_expert_weights": hbm,
-           "roofline": roofline, "decode_step_roofline": layer_rl, "prefill": prefill, "e2e": e2e, "gpu_launches": args.steps * L * launches_per_layer, "clocks": clk,
-           "cache": cache, "kernels": kernels, "bp_measured_gbps": round(bp_measured, 1), "bp_after_timed_gbps": round(bp_after, 1),
-           "fill_observed_gbs": round(fill_gbs, 1) if fill_gbs else None,
-           "setup_s": round(setup_s, 1)}
+    out = {"metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded: locality trace, N(0,1) BF16 activations, generated expert banks)",
+           "config": {**head["config"], "parallelism": f"replicas x{d.world}" if d.world > 1 else "single GPU",
+                      "timed_miss_rate": head["cache"]["miss_rate"]},
+           "roofline": head.get("roofline"), "decode_step_roofline": head["decode_step_roofline"],
+           "hbm_gbs_expert_weights": head["hbm_gbs_expert_weights"],
+           "e2e": head.get("e2e"),
+           "gpu_launches": args.steps * w.n_layers * head["launches_per_layer"],
+           "clocks": head["clocks"], "cache": head["cache"], "kernels": head["kernels"],
+           "bp_measured_gbps": round(bp_measured, 1), "setup_s": head["setup_s"],
+           "decode_configs": {k: {kk: v for kk, v in r.items() if kk not in ("clocks",)} for k, r in extra.items()},
+           "prefill": prefill}
+    if out["roofline"] is not None:
+        out["roofline"]["traffic"] = _traffic("expert_gemv_fused")
     if cpu_baseline is not None:
         out["cpu_baseline"] = cpu_baseline
     return out
@@ -471,7 +653,7 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
                     cache_slots=max(2 * w.n_experts, synth.capacity_slots(0.37, nl, w.n_experts)))
     L, T, H, E, I, k = w.n_layers, w.prefill_tokens, w.hidden, w.n_experts, w.inter, w.top_k
     pool = synth.ExpertPool(w)
-    banks = pool.routed_banks()
+    banks = pool.routed_banks(empty=_host_empty(args))
     abl_sizes = () if args.no_prefill_ablation else (4096, 8192, 16384)
     cfg = F.make_config(L, H, I, E, k, False, F.FT_W_BF16, 1, w.cache_slots, w.bp_gbps, w.bh_gbps,
                         max_prefill_tokens=max((T,) + abl_sizes), device=d.local, compute_stream=stream.cuda_stream)
@@ -529,6 +711,7 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
             del xa, za, oa
     st = F.ft_moe_get_stats(h)
     F.ft_moe_destroy(h)
+    _release_host(banks)
     del banks, pool
     gc.collect()
     flop_layer = T * k * 6.0 * I * H                  # gate+up (4IH) and down (2IH) per routed pair
@@ -546,7 +729,7 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
     hbm, _ = _peaks()
     bound_s = {"tensor": L * flop_layer / (tc_peak * 1e12), "hbm_weights": stream_bytes / (hbm * 1e9),
                "host_link": stream_bytes / (bp * 1e9)}
-    return {"workload": "prefill_chunk_35B-A3B-shape: T 8192 x 40 layers, H 2048, I 512, E 256 top-8, "
+    return {"workload": f"prefill_chunk_35B-A3B-shape: T {T} x {L} layers, H 2048, I 512, E 256 top-8, "
                         "uniform logits, 3788 slots, full-layer double buffer",
             "value": round(T / chunk_s, 1), "unit": "tok/s", "chunk_s": round(chunk_s, 4),
             "chunks": args.prefill_chunks,
@@ -565,6 +748,47 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
             "error_word": st.error_word}
 
 
+# ------------------------------------------------------------------ sweep
+def run_sweep(args, d: Dist) -> dict:
+    """The batch x capacity x split grid on the 35B-A3B shape (40 layers unless --sweep-layers
+    says otherwise): per point tok/s, miss rate, fills (q summed) and host pairs per token,
+    each after an untimed cache warm prefix; one host pool for every point."""
+    import gc
+
+    import torch
+
+    import synth
+    from serving_router_top_dedupe_gb300 import build as B
+
+    B.build()
+    torch.cuda.set_device(d.local)
+    dev = torch.device("cuda", d.local)
+    stream = torch.cuda.Stream(device=dev)
+    nl = args.sweep_layers
+    w0 = synth.sweep_point(1, 0.37, synth.SWEEP_RATIOS[0]).with_(n_layers=nl)
+    pool = synth.ExpertPool(w0)
+    banks = pool.routed_banks(empty=_pinned_empty)            # page-locked once, used by every point
+    shared = pool.shared_banks()
+    points = []
+    batches = [int(b) for b in args.sweep_batches.split(",")]
+    for Bt in batches:
+        for cap in synth.SWEEP_CAPACITIES:
+            for ratio in synth.SWEEP_RATIOS:
+                w = synth.sweep_point(Bt, cap, ratio).with_(n_layers=nl,
+                                                            cache_slots=synth.capacity_slots(cap, nl, 256))
+                r = run_decode(args, d, dev, stream, w, banks, shared, "sweep", args.sweep_warm, args.sweep_steps,
+                               3, 0)
+                points.append({"batch": Bt, "capacity": cap, "bp_bh": list(ratio), "tok_s": r["value"],
+                               "ms_per_step": r["ms_per_step"], **{kk: r["cache"][kk] for kk in
+                                                                   ("miss_rate", "fills_per_token",
+                                                                    "host_pairs_per_token", "error_word")}})
+                print(json.dumps(points[-1]), file=sys.stderr, flush=True)
+    _release_host(banks)
+    gc.collect()
+    return {"metric": METRIC, "mode": "sweep", "n_layers": nl, "steps_per_point": args.sweep_steps,
+            "cache_warm_prefix_tokens": args.sweep_warm, "points": points}
+
+
 # -------------------------------------------------------------- reference
 def run_reference(args, d: Dist) -> dict | None:
     if d.rank != 0:
@@ -573,21 +797,20 @@ def run_reference(args, d: Dist) -> dict | None:
 
     w = _workload()
     pool = synth.ExpertPool(w)
-    banks, shared = pool.routed_banks(), pool.shared_banks()
     trace = synth.routing_trace(w)
     n_tok = max(1, min(args.steps, args.ref_tokens))
     # three untimed warm-up tokens (~1.4 s each on the host cores): the minimum the timing
     # rules ask for, kept at that so that the arm stays within minutes
     warm = 3
-    oracle_decode_tokens(w, banks, shared, trace, warm, 1e9)
-    n, sec, cpu = oracle_decode_tokens(w, banks, shared, trace, n_tok, args.cpu_budget)
+    oracle_decode_tokens(w, pool, trace, warm, 1e9)
+    n, sec, cpu = oracle_decode_tokens(w, pool, trace, n_tok, args.cpu_budget)
     v = n / sec
     return {"metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": d.world, "steps": n,
             "warmup": warm, "ms_per_step": round(sec * 1e3 / n, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": _config_desc(w), "impl": "reference",
-            "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": max(1, round(cpu / sec)),
-                             "kind": "oracle",
+            "config": {**_config_desc(w), "parallelism": "single host (CPU oracle)"}, "impl": "reference",
+            "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": os.cpu_count(),
+                             "cpu_util": round(cpu / sec, 2), "kind": "oracle", "cpu_model": _cpu_model(),
                              "sample": f"{n} tokens x {w.n_layers} layers (bounded sample of the decode trace)"},
             "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -598,12 +821,20 @@ def main():
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--profile-steps", type=int, default=64)
+    ap.add_argument("--cache-warm", type=int, default=512, help="untimed trace prefix before warm-up (tokens)")
+    ap.add_argument("--profile-steps", type=int, default=32)
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--cpu-tokens", type=int, default=16)
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--host-alloc", choices=["pinned", "register"], default="pinned",
+                    help="host pool: cudaHostAlloc'd by the bench, or malloc'd and registered by the library")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 large-expert decode lines")
+    ap.add_argument("--only-headline", action="store_true", help="decode headline only (no measured-B_P, FP8)")
+    ap.add_argument("--fp8-steps", type=int, default=256)
+    ap.add_argument("--fp8-steps-b8", type=int, default=32)
+    ap.add_argument("--fp8-warm", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-chunks", type=int, default=2)
     ap.add_argument("--no-prefill-ablation", action="store_true", help="skip the second-buffer-off chunks")
@@ -612,14 +843,26 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling only: fewer tokens")
     ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer MoE layers")
     ap.add_argument("--slots", type=int, default=0, help="profiling only: other cache size")
+    ap.add_argument("--sweep", action="store_true", help="time the batch x capacity x split grid instead")
+    ap.add_argument("--sweep-layers", type=int, default=40)
+    ap.add_argument("--sweep-steps", type=int, default=64)
+    ap.add_argument("--sweep-warm", type=int, default=256)
+    ap.add_argument("--sweep-batches", default="1,4,16,64")
+    ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     _OVERRIDE.update(layers=args.layers, slots=args.slots)
+    if args.oracle_child:
+        _oracle_child(args)
+        return
     d = Dist()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         d.init("gloo")
         out = run_reference(args, d)
+    elif args.sweep:
+        d.init("nccl")
+        out = run_sweep(args, d)
     elif args.prefill_only:
         import torch
 

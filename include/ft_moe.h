@@ -147,6 +147,8 @@ typedef struct {
   uint32_t clock;       /* global LRU clock (one tick per layer-step) */
   double bp_gbps, bh_gbps;
   int cache_slots;
+  int32_t batch1_fused; /* 1: batch-1 steps run the persistent one-launch GEMV (its grid fits on
+                           the device, checked at init); 0: they run the batched kernels */
 } ft_stats;
 
 /* Last decode layer-step's decisions, for parity checks.  The caller provides
@@ -176,6 +178,10 @@ typedef struct {
 /* Create the library state: allocates the slot pool (S * slot bytes) and the work
  * buffers in HBM, copies the shared experts to HBM, and registers (pins + maps)
  * each host bank with cudaHostRegister unless it is already pinned.
+ * On any error everything allocated or registered so far is released.  For tests of these
+ * paths, the environment variable FTMOE_INJECT_FAILURE="malloc:<n>" or "register:<n>" makes
+ * the n-th device allocation or bank registration (counted from the moment the variable
+ * took its value) fail as if the runtime had refused it; ft_cache_resize honours "malloc".
  *   cfg      configuration (copied)
  *   host_pool routed-expert banks, caller-owned, must outlive the handle
  *   shared   shared-expert banks (first dim L) or NULL when cfg->has_shared == 0
@@ -331,6 +337,23 @@ ft_status ft_bench_bw(size_t bytes, int iters, double* bp_gbps);
 /* Counters, error word, clock.  Synchronises the library's streams. */
 ft_status ft_moe_get_stats(ft_moe* h, ft_stats* out);
 
+/* Clear the device error word (after a reported FT_DEVERR_* condition has been handled);
+ * counters, state and cache contents are kept.  Synchronises.  Errors: FT_ERR_INVALID (null
+ * handle), FT_ERR_STATE (called during a capture). */
+ft_status ft_moe_reset_error(ft_moe* h);
+
+/* Test controls: they change no result of a correct run and exist so that the error paths
+ * can be exercised without faulting a GPU.
+ *   FT_TEST_HANDOFF_TIMEOUT_NS  value > 0: the batch-1 persistent GEMV waits for one more h
+ *                               row than its CTAs publish, giving up after `value` ns; the
+ *                               step then returns with FT_DEVERR_TIMEOUT set and its outputs
+ *                               undefined, while routing and cache decisions stay valid.
+ *                               0 (default): off.
+ * Takes effect for steps enqueued afterwards (graphs capture the value in force).  Errors:
+ * FT_ERR_INVALID (null handle, unknown control, negative value). */
+typedef enum { FT_TEST_HANDOFF_TIMEOUT_NS = 1 } ft_test_control;
+ft_status ft_moe_test_control(ft_moe* h, int what, long long value);
+
 /* Decisions of the last decode layer-step (see ft_step_trace).  Synchronises. */
 ft_status ft_moe_get_step_trace(ft_moe* h, ft_step_trace* out);
 
@@ -389,6 +412,15 @@ ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, int hidden, i
                                          const void* experts_dev, const void* shared_dev, int batch,
                                          const void* x_bf16, const float* logits, float* out,
                                          float* rows_out, uint32_t* error_word_out, void* stream);
+
+/* Page-locked, device-mapped host memory for expert banks ([FT] "FTW 权重格式与平台适配":
+ * banks are exact-size pinned host arrays).  ft_moe_init uses such memory as it is (no
+ * registration).  `bytes` > 0; *out receives the host address, which kernels can also use
+ * on every device.  Errors: FT_ERR_INVALID, FT_ERR_PIN (the runtime refused; nothing is
+ * allocated).  ft_host_free releases memory from ft_host_alloc (NULL: no-op); the caller
+ * must first destroy every handle using it. */
+ft_status ft_host_alloc(size_t bytes, void** out);
+ft_status ft_host_free(void* p);
 
 /* Thread-local message describing the last error of this thread ("" if none). */
 const char* ft_last_error(void);

@@ -11,8 +11,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <memory>
 #include <string>
 #include <tuple>
@@ -33,6 +35,35 @@ ft_status fail(ft_status s, const char* fmt, ...) {
   va_end(ap);
   g_last_error = buf;
   return s;
+}
+
+// Test hook for the failure paths: FTMOE_INJECT_FAILURE="<kind>:<n>" makes the n-th request
+// (1-based, counted from the moment the variable took its current value) of one kind fail as
+// if the CUDA runtime had refused it.  Kinds: "malloc" (device allocations of a handle: slot
+// pool, shared experts, state, work lists, router, resize buffers) and "register"
+// (cudaHostRegister of a host bank).  Unset or empty: no effect.
+bool injected_failure(const char* kind) {
+  static std::mutex mu;
+  static std::string last;
+  static int count = 0;
+  const char* v = std::getenv("FTMOE_INJECT_FAILURE");
+  std::lock_guard<std::mutex> lock(mu);
+  const std::string cur = v ? v : "";
+  if (cur != last) {
+    last = cur;
+    count = 0;
+  }
+  const size_t colon = cur.find(':');
+  if (cur.empty() || colon == std::string::npos || cur.compare(0, colon, kind) != 0) return false;
+  return ++count == std::atoi(cur.c_str() + colon + 1);
+}
+
+cudaError_t dev_malloc(void** p, size_t bytes) {
+  if (injected_failure("malloc")) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
 }
 
 #define FT_CUDA(call)                                                                        \
@@ -102,6 +133,8 @@ struct ft_moe {
   int32_t* copy_host = nullptr;    // pinned [2*kcap]
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_ctrl = nullptr;
   int grid_eval = 0, grid_fill = 0;
+  bool fused_ok = true;              // the batch-1 persistent GEMV's grid fits (checked at init)
+  uint64_t test_handoff_ns = 0;      // test control: unreachable hand-off target, wait limit (ns)
   // host-buffer staging (lazy)
   uint16_t* stg_x = nullptr;
   float *stg_logits = nullptr, *stg_cp = nullptr, *stg_out = nullptr;
@@ -200,7 +233,7 @@ bool capturing(cudaStream_t s) {
 }
 
 ft_status alloc_dev(ft_moe* h, void** p, size_t bytes) {
-  cudaError_t e = cudaMalloc(p, bytes < 16 ? 16 : bytes);
+  cudaError_t e = dev_malloc(p, bytes < 16 ? 16 : bytes);
   if (e != cudaSuccess) return fail(FT_ERR_NOMEM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
   h->allocs.push_back(*p);
   return FT_OK;
@@ -216,7 +249,9 @@ ft_status register_bank(HostBank& b, const void* p, size_t row, size_t n_rows) {
   bool pinned = e == cudaSuccess && at.type == cudaMemoryTypeHost;
   cudaGetLastError();
   if (!pinned) {
-    e = cudaHostRegister(const_cast<void*>(p), b.bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    e = injected_failure("register")
+            ? cudaErrorMemoryAllocation
+            : cudaHostRegister(const_cast<void*>(p), b.bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return fail(FT_ERR_PIN, "cudaHostRegister(%zu bytes) failed: %s (no fallback path)", b.bytes,
@@ -411,6 +446,9 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   ep.n_sm = chain ? h->n_sm - h->grid_fill : h->n_sm;  // the fill kernel's SMs are left to it
   ep.max_entries = h->kcap + 1;
   ep.pdl = chain;
+  ep.allow_fused = h->fused_ok;
+  ep.wait_extra = h->test_handoff_ns ? 1u : 0u;
+  ep.wait_ns = h->test_handoff_ns ? h->test_handoff_ns : ft::kHandoffWaitNs;
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
   FT_CUDA(ft::launch_gate_up(ep, h->cfg.wtype, h->grid_eval, cs));
   if ((s = prof_end(h, 2, cs, pa)) != FT_OK) return s;
@@ -467,6 +505,28 @@ ft_status check_step(ft_moe* h, int layer, int batch, const void* x, const float
 
 // ============================================================ ABI entry points
 extern "C" {
+
+ft_status ft_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return fail(FT_ERR_INVALID, "ft_host_alloc: null out or zero size");
+  *out = nullptr;
+  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    cudaGetLastError();
+    return fail(FT_ERR_PIN, "cudaHostAlloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  return FT_OK;
+}
+
+ft_status ft_host_free(void* p) {
+  if (!p) return FT_OK;
+  cudaError_t e = cudaFreeHost(p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(FT_ERR_INVALID, "ft_host_free: %s", cudaGetErrorString(e));
+  }
+  return FT_OK;
+}
 
 const char* ft_last_error(void) { return g_last_error.c_str(); }
 
@@ -587,12 +647,12 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
 
   // HBM: slot pool, shared experts, state, work lists
   {
-    cudaError_t e = cudaMalloc(&h->pool, (size_t)h->S * h->lay.stride);
+    cudaError_t e = dev_malloc((void**)&h->pool, (size_t)h->S * h->lay.stride);
     if (e != cudaSuccess)
       return fail(FT_ERR_NOMEM, "slot pool of %d x %zu bytes: %s", h->S, h->lay.stride, cudaGetErrorString(e));
   }
   if (cfg->has_shared) {
-    FT_CUDA(cudaMalloc(&h->shared_w, (size_t)h->L * h->lay.stride));
+    FT_CUDA(dev_malloc((void**)&h->shared_w, (size_t)h->L * h->lay.stride));
     const void* sp[7] = {shared->gate,
                          shared->up,
                          shared->down,
@@ -620,6 +680,10 @@ static ft_status init_body(ft_moe* h, const ft_moe_config* cfg, const ft_banks* 
   FT_CUDA(ft::prepare_kernels(h->cfg.wtype, h->H, h->I));
   FT_CUDA(ft::prepare_control());
   FT_CUDA(ft::prepare_router());
+  // The batch-1 persistent GEMV hands h rows between its CTAs, so every CTA of its grid must
+  // be resident at once: one CTA per SM on the SMs the fill kernel leaves.  When the kernel
+  // does not fit on an SM, batch 1 runs the batched kernels instead (ft_stats.batch1_fused).
+  h->fused_ok = ft::fused_gemv_fits(h->cfg.wtype, h->H, h->I, h->kcap + 1, h->n_sm - h->grid_fill);
   FT_CUDA(cudaDeviceSynchronize());
   return FT_OK;
 }
@@ -672,14 +736,14 @@ ft_status ft_moe_set_router(ft_moe* h, const void* w_router_bf16, int gate) {
   if (w_router_bf16) {
     const size_t bytes = (size_t)h->L * h->E * h->H * sizeof(uint16_t);
     if (!h->router_w) {
-      cudaError_t e = cudaMalloc(&h->router_w, bytes);
+      cudaError_t e = dev_malloc((void**)&h->router_w, bytes);
       if (e != cudaSuccess) {
         h->router_w = nullptr;
         return fail(e == cudaErrorMemoryAllocation ? FT_ERR_NOMEM : FT_ERR_CUDA, "router weights: %s",
                     cudaGetErrorString(e));
       }
       const size_t zb = (size_t)std::max(h->cfg.max_batch, h->cfg.max_prefill_tokens) * h->E * sizeof(float);
-      e = cudaMalloc(&h->router_z, zb);
+      e = dev_malloc((void**)&h->router_z, zb);
       if (e != cudaSuccess) {
         cudaFree(h->router_w);
         h->router_w = nullptr;
@@ -859,6 +923,24 @@ ft_status ft_moe_get_stats(ft_moe* h, ft_stats* out) {
   out->bp_gbps = h->bp_gbps;
   out->bh_gbps = h->bh_gbps;
   out->cache_slots = h->S;
+  out->batch1_fused = h->fused_ok ? 1 : 0;
+  return FT_OK;
+}
+
+ft_status ft_moe_reset_error(ft_moe* h) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (capturing(h->cs)) return fail(FT_ERR_STATE, "reset during capture");
+  ft_status s = ft_moe_synchronize(h);
+  if (s != FT_OK) return s;
+  FT_CUDA(cudaMemset(&h->st->error_word, 0, sizeof(uint32_t)));
+  FT_CUDA(cudaDeviceSynchronize());
+  return FT_OK;
+}
+
+ft_status ft_moe_test_control(ft_moe* h, int what, long long value) {
+  if (!h) return fail(FT_ERR_INVALID, "null handle");
+  if (what != FT_TEST_HANDOFF_TIMEOUT_NS || value < 0) return fail(FT_ERR_INVALID, "unknown test control");
+  h->test_handoff_ns = (uint64_t)value;
   return FT_OK;
 }
 
@@ -1071,10 +1153,22 @@ ft_status ft_cache_resize(ft_moe* h, int new_slots) {
   FT_CUDA(cudaMemcpy(owner.data(), h->owner, (size_t)S * 4, cudaMemcpyDeviceToHost));
   FT_CUDA(cudaMemcpy(stamp.data(), h->stamp, (size_t)S * 4, cudaMemcpyDeviceToHost));
   const size_t stride = h->lay.stride;
+  // every new buffer first: a refused allocation leaves the handle as it was
+  uint8_t* np = nullptr;
+  int32_t* nowner = nullptr;
+  uint32_t* nstamp = nullptr;
+  {
+    cudaError_t e = n >= S ? dev_malloc((void**)&np, (size_t)n * stride) : cudaSuccess;
+    if (e == cudaSuccess) e = dev_malloc((void**)&nowner, (size_t)n * 4);
+    if (e == cudaSuccess) e = dev_malloc((void**)&nstamp, (size_t)n * 4);
+    if (e != cudaSuccess) {
+      if (np) cudaFree(np);
+      if (nowner) cudaFree(nowner);
+      cudaGetLastError();
+      return fail(FT_ERR_NOMEM, "resize to %d slots: %s", n, cudaGetErrorString(e));
+    }
+  }
   if (n >= S) {
-    uint8_t* np = nullptr;
-    cudaError_t e = cudaMalloc(&np, (size_t)n * stride);
-    if (e != cudaSuccess) return fail(FT_ERR_NOMEM, "grow pool to %d slots: %s", n, cudaGetErrorString(e));
     FT_CUDA(cudaMemcpy(np, h->pool, (size_t)S * stride, cudaMemcpyDeviceToDevice));
     cudaFree(h->pool);
     h->pool = np;
@@ -1113,10 +1207,6 @@ ft_status ft_cache_resize(ft_moe* h, int new_slots) {
     stamp.resize(n);
     FT_CUDA(cudaStreamSynchronize(h->cs));
   }
-  int32_t* nowner = nullptr;
-  uint32_t* nstamp = nullptr;
-  FT_CUDA(cudaMalloc(&nowner, (size_t)n * 4));
-  FT_CUDA(cudaMalloc(&nstamp, (size_t)n * 4));
   FT_CUDA(cudaMemcpy(nowner, owner.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
   FT_CUDA(cudaMemcpy(nstamp, stamp.data(), (size_t)n * 4, cudaMemcpyHostToDevice));
   FT_CUDA(cudaMemcpy(h->res, res.data(), nlog * 4, cudaMemcpyHostToDevice));

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
       // every warp waits on its own entries' counters, so the polls run side by side
       if (lane == 0)
         for (int gi = cw; gi < npe; gi += kConsumers)
-          if (!wait_counter(p.ready + pe[gi], (uint32_t)I, abort_flag, p.error_word)) break;
+          if (!wait_counter(p.ready + pe[gi], (uint32_t)I + p.wait_extra, abort_flag, p.error_word, p.wait_ns)) break;
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
       // one flat loop, so that every thread's loads of all the pass's entries are in flight
       // together
@@ -467,6 +467,22 @@ constexpr bool fixed_shape_matches(int H, int I) {
 bool fused_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm) {
   const FusedPlan pl = make_fused_plan(wtype, H, I, max_entries, n_sm);
   return pl.nst >= 2 && fused_smem_bytes(pl) <= kSmemBudget + 4096;
+}
+
+bool fused_gemv_fits(int wtype, int H, int I, int max_entries, int n_sm) {
+  if (!fused_gemv_supported(wtype, H, I, max_entries, n_sm)) return false;
+  const FusedPlan pl = make_fused_plan(wtype, H, I, max_entries, n_sm);
+  int nb = 0;
+  const size_t smem = fused_smem_bytes(pl);
+  cudaError_t e = wtype == FT_W_BF16
+                      ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_BF16, 0, 0>, kThreads, smem)
+                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>,
+                                                                      kThreads, smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return nb >= 1;
 }
 
 cudaError_t launch_fused_gemv(const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s) {

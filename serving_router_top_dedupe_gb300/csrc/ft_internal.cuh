@@ -122,7 +122,14 @@ struct EvalParams {
   int n_sm;                 // CTAs of the batch-1 GEMV (one per SM it may use)
   int max_entries;          // capacity of the entry lists (kcap + 1)
   bool pdl;                 // launched as programmatic dependents
+  bool allow_fused;         // batch 1 may run the persistent one-launch kernel (its grid fits)
+  uint32_t wait_extra;      // added to the batch-1 hand-off target: 0, or 1 in the timeout test
+  unsigned long long wait_ns;  // limit of the batch-1 hand-off wait
 };
+
+// Limit of the batch-1 kernel's wait for the h rows of other CTAs: a lost signal sets
+// FT_DEVERR_TIMEOUT and the kernel returns instead of hanging.
+constexpr unsigned long long kHandoffWaitNs = 2000000000ull;  // 2 s
 
 // Programmatic dependent launch.  Kernels of the decode chain (control -> fill -> gate/up
 // -> down+combine -> next control) are launched with programmatic stream serialization.
@@ -181,6 +188,9 @@ cudaError_t launch_down_combine(const EvalParams& p, int wtype, int grid, cudaSt
 cudaError_t prepare_kernels(int wtype, int H, int I);
 // Batch-1 decode evaluation in one persistent launch (decode_fused.cu).
 bool fused_gemv_supported(int wtype, int H, int I, int max_entries, int n_sm);
+// True when one CTA of the batch-1 kernel fits on an SM (occupancy >= 1), so that its grid of
+// n_sm CTAs can be resident at once on an idle device.
+bool fused_gemv_fits(int wtype, int H, int I, int max_entries, int n_sm);
 cudaError_t launch_fused_gemv(const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s);
 cudaError_t prepare_fused_gemv();
 // Entries of a batch-1 step: at most k routed experts plus the shared expert.

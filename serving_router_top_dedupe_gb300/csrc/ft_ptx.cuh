@@ -66,16 +66,16 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 
 // Bounded wait until *counter >= target, for counters that other CTAs of the same grid
 // raise (every CTA of that grid is resident: one CTA per SM, grid <= SM count).  Gives up
-// after kFlagWaitNs (error word + abort flag) so that a lost signal cannot hang the GPU.
+// after limit_ns (error word + abort flag) so that a lost signal cannot hang the GPU.
 constexpr uint64_t kFlagWaitNs = 2000000000ull;  // 2 s
 __device__ __forceinline__ bool wait_counter(const uint32_t* counter, uint32_t target, volatile int* abort_flag,
-                                             uint32_t* error_word) {
+                                             uint32_t* error_word, uint64_t limit_ns = kFlagWaitNs) {
   if (ld_acquire_gpu(counter) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (ld_acquire_gpu(counter) >= target) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kFlagWaitNs) break;
+    if (globaltimer_ns() - t0 > limit_ns) break;
     __nanosleep(64);
   }
   *abort_flag = 1;

@@ -195,6 +195,9 @@ extern "C" ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, in
   ep.n_sm = su->n_sm;
   ep.max_entries = kcap + 1;
   ep.pdl = false;
+  ep.allow_fused = true;
+  ep.wait_extra = 0;
+  ep.wait_ns = ft::kHandoffWaitNs;
   if (ft::launch_gate_up(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
   if (ft::launch_down_combine(ep, wtype, su->n_sm * 4, s) != cudaSuccess) return FT_ERR_CUDA;
   if (error_word_out) {

@@ -23,6 +23,7 @@ FT_FILL_KERNEL, FT_FILL_MEMCPY = 0, 1
 FT_GATE_SOFTMAX_TOPK, FT_GATE_SOFTMAX_ALL, FT_GATE_SIGMOID_TOPK = 0, 1, 2
 FT_CPU = -1
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_STATE, FT_DEVERR_TIMEOUT, FT_DEVERR_CAPACITY = 1, 2, 4, 8
+FT_TEST_HANDOFF_TIMEOUT_NS = 1
 
 PROFILE_KINDS = ("control", "fill", "gate_up", "down_combine", "prefill_route", "prefill_gemm_gate_up",
                  "prefill_combine", "prefill_copy", "prefill_gemm_down", "router")
@@ -59,7 +60,8 @@ class ft_stats(C.Structure):
                 ("cpu_execs", C.c_uint64), ("evictions", C.c_uint64), ("decode_steps", C.c_uint64),
                 ("prefill_layers", C.c_uint64), ("eval_entries", C.c_uint64), ("eval_pairs", C.c_uint64),
                 ("error_word", C.c_uint32), ("clock", C.c_uint32),
-                ("bp_gbps", C.c_double), ("bh_gbps", C.c_double), ("cache_slots", C.c_int)]
+                ("bp_gbps", C.c_double), ("bh_gbps", C.c_double), ("cache_slots", C.c_int),
+                ("batch1_fused", C.c_int32)]
 
 
 class ft_step_trace(C.Structure):
@@ -101,6 +103,10 @@ _SIGS = {
     "ft_moe_set_stream": [_P, _P],
     "ft_moe_synchronize": [_P],
     "ft_moe_destroy": [_P],
+    "ft_moe_reset_error": [_P],
+    "ft_moe_test_control": [_P, C.c_int, C.c_longlong],
+    "ft_host_alloc": [C.c_size_t, C.POINTER(C.c_void_p)],
+    "ft_host_free": [_P],
     "ft_moe_decode_resident_noalloc": [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, _P, C.c_int, _P, _P, _P, _P,
                                        _P, _P],
 }
@@ -317,6 +323,39 @@ def ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, exper
                                              _ptr(rows_out), _ptr(error_word_out), stream)
     if st != FT_OK:
         raise FtError(st, "ft_moe_decode_resident_noalloc failed")
+
+
+def ft_moe_reset_error(h) -> None:
+    _check(_lib.ft_moe_reset_error(h))
+
+
+def ft_moe_test_control(h, what, value) -> None:
+    _check(_lib.ft_moe_test_control(h, what, value))
+
+
+def ft_host_alloc(nbytes) -> int:
+    """Page-locked, mapped host memory (cudaHostAlloc); returns its address."""
+    p = C.c_void_p()
+    _check(_lib.ft_host_alloc(nbytes, C.byref(p)))
+    return p.value
+
+
+def ft_host_free(addr) -> None:
+    _check(_lib.ft_host_free(addr))
+
+
+def host_array(shape, dtype):
+    """A numpy array over fresh ft_host_alloc memory; release it with free_host_array."""
+    dtype = np.dtype(dtype)
+    n = int(np.prod(shape)) * dtype.itemsize
+    addr = ft_host_alloc(max(n, 16))
+    buf = (C.c_uint8 * max(n, 16)).from_address(addr)
+    return np.frombuffer(buf, dtype=np.uint8, count=n).view(dtype).reshape(shape)
+
+
+def free_host_array(a) -> None:
+    """Release an array that host_array returned (not a slice of it)."""
+    ft_host_free(a.__array_interface__["data"][0])
 
 
 def make_config(n_layers, hidden, inter, n_experts, top_k, has_shared, wtype, max_batch, cache_slots,

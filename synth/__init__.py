@@ -311,8 +311,10 @@ class ExpertPool:
     def shared(self, layer: int) -> dict:
         return self.expert(self.w.n_logical + layer)
 
-    def alloc_banks(self, n_rows: int) -> dict:
-        return {k: np.empty((n_rows,) + self.shapes[k], dtype=self.dtypes[k]) for k in self.shapes}
+    def alloc_banks(self, n_rows: int, empty=np.empty) -> dict:
+        """Uninitialised banks of n_rows experts; `empty(shape, dtype)` allocates each (e.g. in
+        page-locked or huge-page memory)."""
+        return {k: empty((n_rows,) + self.shapes[k], self.dtypes[k]) for k in self.shapes}
 
     def fill_banks(self, banks: dict, first_id: int = 0, threads: int | None = None) -> None:
         """Write experts first_id .. first_id+rows-1 into preallocated banks (rows = first dim)."""
@@ -328,8 +330,8 @@ class ExpertPool:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda lo: work(lo, min(n_rows, lo + step)), range(0, n_rows, step)))
 
-    def routed_banks(self, threads: int | None = None) -> dict:
-        b = self.alloc_banks(self.w.n_logical)
+    def routed_banks(self, threads: int | None = None, empty=np.empty) -> dict:
+        b = self.alloc_banks(self.w.n_logical, empty)
         self.fill_banks(b, 0, threads)
         return b
 

@@ -61,6 +61,34 @@ def test_prefill_35b_expert_shape_sampled_tokens():
         print("max rel err", r.max_err)
 
 
+def test_prefill_35b_full_chunk_second_n_tiles():
+    """The prefill workload's own chunk: 8192 tokens, 35B-A3B expert shape, uniform logits
+    (n_e = 256 +- 16 pairs per expert), 2 layers.  An expert with more than 256 pairs takes
+    two N tiles; its tokens are in ascending order, so its last token's pair sits in the
+    second tile.  The sampled rows hold, for each such expert, its last token (up to 64 of
+    them), plus the first and last token of the chunk and random ones; residency after each
+    layer is compared in full."""
+    import oracle as O
+
+    T = 8192
+    w = synth.prefill().with_(n_layers=2, cache_slots=700, prefill_tokens=T)
+    rng = np.random.default_rng(1)
+    with Run(w, max_prefill_tokens=T) as r:
+        n_second = 0
+        for l in range(w.n_layers):
+            sel, _ = O.route(synth.prefill_logits(w, 0, l, T), w.top_k)
+            n_e = np.bincount(sel.reshape(-1), minlength=w.n_experts)
+            big = np.nonzero(n_e > 256)[0]
+            assert len(big) > 0
+            last = sorted({int(np.nonzero((sel == e).any(axis=1))[0].max()) for e in big})
+            n_second += len(last)
+            pick = rng.choice(last, min(64, len(last)), replace=False).tolist()
+            tokens = sorted(set(pick) | {0, T - 1} | set(rng.choice(T, 16, replace=False).tolist()))
+            prefill_step(r, 0, l, T, check_tokens=tokens)
+        assert r.F.ft_moe_get_stats(r.h).error_word == 0
+        print(f"max rel err {r.max_err:.2e}; experts with a second N tile: {n_second}")
+
+
 def test_prefill_with_shared_expert():
     w = synth.decode_bf16().with_(n_layers=3, n_experts=32, cache_slots=70, logits="uniform", prefill_tokens=300)
     with Run(w, max_prefill_tokens=300) as r:

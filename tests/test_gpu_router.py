@@ -1,8 +1,14 @@
 """GPU parity of the router on hidden states: the router kernel's logits against the
 oracle's float64 logits (within the FP32 accumulation bound, at every launch shape the
 library uses, bitwise reproducible), and the decode and prefill calls that take hidden
-states, for each gate function: every decision compared exactly with the oracle routing
-on the GPU's logits, outputs within the layer tolerance, final residency identical."""
+states, for each gate function.  The oracle routes on its own float64 logits: every
+decision is compared exactly, except that a token whose float64 top-k margin lies inside
+twice the logit error bound (a near tie, where either side is correct) takes the kernel's
+choice once it is shown to lie inside that band; the tests report how many there were.
+Outputs are within the layer tolerance and the final residency is identical.
+
+Edge cases of the top-k itself (equal logits, -0 and +0, -inf, NaN ranked as -inf) run on
+given logits through the decode and prefill routers and are compared in full."""
 import numpy as np
 import pytest
 import torch
@@ -74,7 +80,8 @@ def test_decode_hidden_tiny_every_gate(gate):
             for l in range(w.n_layers):
                 r.step(s, l, check_out=True, hidden=True)
         r.compare_state()
-        print(f"gate {gate}: max rel err {r.max_err:.2e}, fills {r.sim.cnt.fills}, host {r.sim.cnt.cpu_execs}")
+        print(f"gate {gate}: max rel err {r.max_err:.2e}, fills {r.sim.cnt.fills}, host {r.sim.cnt.cpu_execs}, "
+              f"near ties {r.near_ties}")
         assert r.sim.cnt.cpu_execs > 0 and r.sim.cnt.fills > 0
 
 
@@ -89,7 +96,7 @@ def test_decode_hidden_35b_shape(gate, batch, pool35):
             for l in range(w.n_layers):
                 r.step(s, l, check_out=(s % 2 == 0), hidden=True)
         r.compare_state()
-        print(f"gate {gate} batch {batch}: max rel err {r.max_err:.2e}")
+        print(f"gate {gate} batch {batch}: max rel err {r.max_err:.2e}, near ties {r.near_ties}")
 
 
 def test_decode_gate_functions_on_given_logits(pool35):
@@ -146,3 +153,47 @@ def test_router_argument_errors():
         assert e.value.status == F.FT_ERR_INVALID
         s = F.ft_moe_get_stats(r.h)
         assert s.error_word == 0
+
+
+def _edge_logits(B, E, seed):
+    """Logits drawn from a few values, so that equal logits are common, with -0 and +0,
+    -inf and NaN among them; one finite logit of 3.0 per token keeps the gates defined."""
+    rng = np.random.default_rng(seed)
+    vals = np.array([0.0, -0.0, 1.0, 1.0, -1.0, 2.5, -np.inf, np.nan], dtype=np.float32)
+    z = vals[rng.integers(0, len(vals), size=(B, E))]
+    z[np.arange(B), rng.integers(0, E, size=B)] = 3.0
+    return np.ascontiguousarray(z)
+
+
+@pytest.mark.parametrize("shape,batch", [("tiny", 1), ("35B", 1), ("35B", 4)])
+def test_router_edge_cases_decode(shape, batch, pool35):
+    """Ties go to the lower id, -0 equals +0, NaN ranks as -inf (and sets the NaN error
+    bit), a chosen -inf gets gate 0; ids, gates, cache decisions and outputs against the
+    oracle at every step."""
+    if shape == "tiny":
+        w = synth.tiny().with_(steps=6)
+        banks = shared = None
+    else:
+        w = synth.decode_bf16(batch=batch).with_(n_layers=2, steps=4, cache_slots=synth.capacity_slots(0.25, 2, 256))
+        banks, shared = pool35
+    with Run(w, banks, shared) as r:
+        for s in range(w.steps):
+            for l in range(w.n_layers):
+                xb = synth.decode_x(w, s, l)
+                z = _edge_logits(w.batch, w.n_experts, 100 * s + l)
+                r.step(s, l, check_out=True, xz=(xb, z))
+        st = r.F.ft_moe_get_stats(r.h)
+        assert st.error_word == r.F.FT_DEVERR_NAN_LOGIT
+        c = r.sim.cnt
+        assert (st.hits, st.misses, st.fills, st.cpu_execs, st.evictions) == \
+            (c.hits, c.misses, c.fills, c.cpu_execs, c.evictions)
+
+
+def test_router_edge_cases_prefill():
+    """The prefill router on the same kind of logits: 200 tokens, 16 experts top-2."""
+    w = synth.prefill().with_(n_layers=2, n_experts=16, top_k=2, hidden=256, inter=128, cache_slots=40,
+                              prefill_tokens=200)
+    with Run(w, max_prefill_tokens=256) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 200, z=_edge_logits(200, w.n_experts, 7 + l))
+        assert r.F.ft_moe_get_stats(r.h).error_word == r.F.FT_DEVERR_NAN_LOGIT
