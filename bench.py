@@ -146,13 +146,13 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, d: Dist) -> tuple[
 
 
 # ------------------------------------------------------------- host memory
-def _pinned_empty(shape, dtype):
+def _pinned_empty(shape, dtype, flags=0):
     """Page-locked, device-mapped host array from the library's host allocator
-    (ft_host_alloc: exact size, released by _release_host).  ft_moe_init uses such memory
-    as it is and registers nothing."""
+    (ft_host_alloc: cudaHostAlloc by default, released by _release_host).  ft_moe_init uses
+    such memory as it is and registers nothing."""
     from serving_router_top_dedupe_gb300 import ftmoe as F
 
-    a = F.host_array(shape, dtype)
+    a = F.host_array(shape, dtype, flags)
     _PINNED.add(id(a))
     return a
 
@@ -172,7 +172,11 @@ def _release_host(banks):
 
 
 def _host_empty(args):
-    return _pinned_empty if args.host_alloc == "pinned" else (lambda shape, dtype: np.empty(shape, dtype))
+    if args.host_alloc == "pinned":
+        return _pinned_empty
+    if args.host_alloc == "huge":
+        return lambda shape, dtype: _pinned_empty(shape, dtype, 1)
+    return lambda shape, dtype: np.empty(shape, dtype)
 
 
 # ------------------------------------------------------------------ inputs
@@ -218,8 +222,9 @@ def _config_desc(w, args=None, warm=None) -> dict:
     if warm is not None:
         d["cache_warm_prefix_tokens"] = warm
     if args is not None:
-        d["host_pool"] = "cudaHostAlloc (page-locked, mapped)" if args.host_alloc == "pinned" \
-            else "malloc + cudaHostRegister"
+        d["host_pool"] = {"huge": "ft_host_alloc: transparent huge pages, registered (page-locked, mapped)",
+                          "pinned": "ft_host_alloc: cudaHostAlloc (page-locked, mapped)",
+                          "register": "malloc, registered by ft_moe_init"}[args.host_alloc]
     return d
 
 
@@ -827,8 +832,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=8)
-    ap.add_argument("--host-alloc", choices=["pinned", "register"], default="pinned",
-                    help="host pool: cudaHostAlloc'd by the bench, or malloc'd and registered by the library")
+    ap.add_argument("--host-alloc", choices=["pinned", "huge", "register"], default="pinned",
+                    help="host pool: ft_host_alloc with huge pages or cudaHostAlloc, or malloc'd and registered "
+                         "by ft_moe_init")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 large-expert decode lines")
     ap.add_argument("--only-headline", action="store_true", help="decode headline only (no measured-B_P, FP8)")

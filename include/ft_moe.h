@@ -178,10 +178,8 @@ typedef struct {
 /* Create the library state: allocates the slot pool (S * slot bytes) and the work
  * buffers in HBM, copies the shared experts to HBM, and registers (pins + maps)
  * each host bank with cudaHostRegister unless it is already pinned.
- * On any error everything allocated or registered so far is released.  For tests of these
- * paths, the environment variable FTMOE_INJECT_FAILURE="malloc:<n>" or "register:<n>" makes
- * the n-th device allocation or bank registration (counted from the moment the variable
- * took its value) fail as if the runtime had refused it; ft_cache_resize honours "malloc".
+ * On any error everything allocated or registered so far is released (ft_test_inject_failure
+ * makes these paths testable).
  *   cfg      configuration (copied)
  *   host_pool routed-expert banks, caller-owned, must outlive the handle
  *   shared   shared-expert banks (first dim L) or NULL when cfg->has_shared == 0
@@ -354,6 +352,14 @@ ft_status ft_moe_reset_error(ft_moe* h);
 typedef enum { FT_TEST_HANDOFF_TIMEOUT_NS = 1 } ft_test_control;
 ft_status ft_moe_test_control(ft_moe* h, int what, long long value);
 
+/* Failure injection for tests of the error paths, process-wide: after this call the nth
+ * request of the given kind (counted from this call) fails once as if the CUDA runtime had
+ * refused it.  FT_INJECT_MALLOC: device allocations of ft_moe_init, ft_cache_resize and
+ * ft_moe_set_router (the call returns FT_ERR_NOMEM); FT_INJECT_REGISTER: cudaHostRegister of
+ * a host bank in ft_moe_init (FT_ERR_PIN).  nth = 0 disarms.  Errors: FT_ERR_INVALID. */
+typedef enum { FT_INJECT_MALLOC = 1, FT_INJECT_REGISTER = 2 } ft_inject_kind;
+ft_status ft_test_inject_failure(int kind, int nth);
+
 /* Decisions of the last decode layer-step (see ft_step_trace).  Synchronises. */
 ft_status ft_moe_get_step_trace(ft_moe* h, ft_step_trace* out);
 
@@ -415,11 +421,22 @@ ft_status ft_moe_decode_resident_noalloc(int n_experts, int top_k, int hidden, i
 
 /* Page-locked, device-mapped host memory for expert banks ([FT] "FTW 权重格式与平台适配":
  * banks are exact-size pinned host arrays).  ft_moe_init uses such memory as it is (no
- * registration).  `bytes` > 0; *out receives the host address, which kernels can also use
- * on every device.  Errors: FT_ERR_INVALID, FT_ERR_PIN (the runtime refused; nothing is
- * allocated).  ft_host_free releases memory from ft_host_alloc (NULL: no-op); the caller
- * must first destroy every handle using it. */
-ft_status ft_host_alloc(size_t bytes, void** out);
+ * registration of its own).
+ *   FT_HOST_PINNED      cudaHostAlloc (mapped, portable).  The fill kernel reads it fastest:
+ *                       on a GB300 host whose memory a long test run had fragmented, 112 GB/s
+ *                       against 48 GB/s (FT_HOST_HUGE_PAGES) and 40 GB/s (malloc'd banks
+ *                       registered by ft_moe_init).
+ *   FT_HOST_HUGE_PAGES  anonymous memory advised for transparent huge pages, then registered
+ *                       (cudaHostRegister, mapped, portable): the copy engine reads it at the
+ *                       link rate however fragmented host memory is (211 GB/s, against 62 GB/s
+ *                       for registered base pages on the same host).
+ * `bytes` > 0; *out receives the host address, which kernels can also use on every device.
+ * Errors: FT_ERR_INVALID, FT_ERR_NOMEM (no address space), FT_ERR_PIN (the runtime refused to
+ * pin; nothing is kept).  ft_host_free releases memory from ft_host_alloc (NULL: no-op); the
+ * caller must first destroy every handle using it.  Errors: FT_ERR_INVALID (not an
+ * ft_host_alloc address). */
+typedef enum { FT_HOST_PINNED = 0, FT_HOST_HUGE_PAGES = 1 } ft_host_alloc_flags;
+ft_status ft_host_alloc(size_t bytes, int flags, void** out);
 ft_status ft_host_free(void* p);
 
 /* Thread-local message describing the last error of this thread ("" if none). */

@@ -6,6 +6,7 @@
 // validates arguments, enqueues work and moves bytes.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <sys/mman.h>
 
 #include <algorithm>
 #include <cmath>
@@ -37,29 +38,41 @@ ft_status fail(ft_status s, const char* fmt, ...) {
   return s;
 }
 
-// Test hook for the failure paths: FTMOE_INJECT_FAILURE="<kind>:<n>" makes the n-th request
-// (1-based, counted from the moment the variable took its current value) of one kind fail as
-// if the CUDA runtime had refused it.  Kinds: "malloc" (device allocations of a handle: slot
-// pool, shared experts, state, work lists, router, resize buffers) and "register"
-// (cudaHostRegister of a host bank).  Unset or empty: no effect.
-bool injected_failure(const char* kind) {
-  static std::mutex mu;
-  static std::string last;
-  static int count = 0;
-  const char* v = std::getenv("FTMOE_INJECT_FAILURE");
-  std::lock_guard<std::mutex> lock(mu);
-  const std::string cur = v ? v : "";
-  if (cur != last) {
-    last = cur;
-    count = 0;
+// Memory of ft_host_alloc: the registered address -> its mapping (base NULL: cudaHostAlloc).
+struct HostMap {
+  void* base;
+  size_t len;
+};
+std::mutex g_host_mu;
+std::map<void*, HostMap> g_host_maps;
+
+// Transparent huge page size of this host (the PMD size: 2 MB with 4 KB base pages, 512 MB
+// with 64 KB ones); 2 MB when the kernel does not say.
+size_t huge_page_bytes() {
+  size_t v = 0;
+  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    unsigned long long x = 0;
+    if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+    std::fclose(f);
   }
-  const size_t colon = cur.find(':');
-  if (cur.empty() || colon == std::string::npos || cur.compare(0, colon, kind) != 0) return false;
-  return ++count == std::atoi(cur.c_str() + colon + 1);
+  return v >= 4096 && (v & (v - 1)) == 0 ? v : ((size_t)2 << 20);
+}
+
+// Test hook for the failure paths (ft_test_inject_failure): the armed kind's nth request
+// from the moment of arming fails as if the CUDA runtime had refused it, once.
+std::mutex g_inject_mu;
+int g_inject_kind = 0, g_inject_left = 0;
+
+bool injected_failure(int kind) {
+  std::lock_guard<std::mutex> lock(g_inject_mu);
+  if (g_inject_kind != kind || g_inject_left <= 0) return false;
+  if (--g_inject_left > 0) return false;
+  g_inject_kind = 0;
+  return true;
 }
 
 cudaError_t dev_malloc(void** p, size_t bytes) {
-  if (injected_failure("malloc")) {
+  if (injected_failure(FT_INJECT_MALLOC)) {
     *p = nullptr;
     return cudaErrorMemoryAllocation;
   }
@@ -249,7 +262,7 @@ ft_status register_bank(HostBank& b, const void* p, size_t row, size_t n_rows) {
   bool pinned = e == cudaSuccess && at.type == cudaMemoryTypeHost;
   cudaGetLastError();
   if (!pinned) {
-    e = injected_failure("register")
+    e = injected_failure(FT_INJECT_REGISTER)
             ? cudaErrorMemoryAllocation
             : cudaHostRegister(const_cast<void*>(p), b.bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
     if (e != cudaSuccess) {
@@ -506,21 +519,60 @@ ft_status check_step(ft_moe* h, int layer, int batch, const void* x, const float
 // ============================================================ ABI entry points
 extern "C" {
 
-ft_status ft_host_alloc(size_t bytes, void** out) {
+ft_status ft_test_inject_failure(int kind, int nth) {
+  if ((kind != FT_INJECT_MALLOC && kind != FT_INJECT_REGISTER) || nth < 0)
+    return fail(FT_ERR_INVALID, "ft_test_inject_failure: unknown kind or negative count");
+  std::lock_guard<std::mutex> lock(g_inject_mu);
+  g_inject_kind = nth > 0 ? kind : 0;
+  g_inject_left = nth;
+  return FT_OK;
+}
+
+ft_status ft_host_alloc(size_t bytes, int flags, void** out) {
   if (!out || bytes == 0) return fail(FT_ERR_INVALID, "ft_host_alloc: null out or zero size");
+  if (flags != FT_HOST_HUGE_PAGES && flags != FT_HOST_PINNED) return fail(FT_ERR_INVALID, "ft_host_alloc: flags");
   *out = nullptr;
-  cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess) {
-    *out = nullptr;
-    cudaGetLastError();
-    return fail(FT_ERR_PIN, "cudaHostAlloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+  if (flags == FT_HOST_PINNED) {
+    cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      *out = nullptr;
+      cudaGetLastError();
+      return fail(FT_ERR_PIN, "cudaHostAlloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    g_host_maps[*out] = HostMap{nullptr, 0};
+    return FT_OK;
   }
+  const size_t huge = huge_page_bytes();
+  const size_t span = (bytes + huge - 1) / huge * huge, len = span + huge;
+  void* raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (raw == MAP_FAILED) return fail(FT_ERR_NOMEM, "ft_host_alloc: mmap of %zu bytes failed", len);
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + huge - 1) / huge * huge);
+  madvise(p, span, MADV_HUGEPAGE);  // no transparent huge pages: base pages, still correct
+  cudaError_t e = cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    munmap(raw, len);
+    return fail(FT_ERR_PIN, "cudaHostRegister(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  g_host_maps[p] = HostMap{raw, len};
+  *out = p;
   return FT_OK;
 }
 
 ft_status ft_host_free(void* p) {
   if (!p) return FT_OK;
-  cudaError_t e = cudaFreeHost(p);
+  HostMap m{};
+  {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    auto it = g_host_maps.find(p);
+    if (it == g_host_maps.end()) return fail(FT_ERR_INVALID, "ft_host_free: not an ft_host_alloc address");
+    m = it->second;
+    g_host_maps.erase(it);
+  }
+  cudaError_t e = m.base ? cudaHostUnregister(p) : cudaFreeHost(p);
+  if (m.base) munmap(m.base, m.len);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(FT_ERR_INVALID, "ft_host_free: %s", cudaGetErrorString(e));

@@ -15,8 +15,10 @@
 // order of each (token, expert) dot product is fixed (lane-strided chunks, then an xor
 // butterfly), independent of slot, batch composition or split, so outputs are identical
 // across cache capacities.  FP8 E4M3 rows are decoded with the hardware e4m3x2->f16x2
-// conversion; each 128-element block's partial dot is multiplied by its FP32 scale once
-// ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2, post-scaling).  The block-FP4 formats named in
+// conversion; each 1x128 block's dot product is summed over the 8 lanes holding its chunks
+// and then multiplied by its FP32 scale once ("OSDI'26 | 双路 CPU + 两张 5090…", §4.2,
+// post-scaling).  FP8 and FP4 activations enter as F16 after an exact per-token
+// power-of-two prescale (act_shift), undone on the finished sum.  The block-FP4 formats named in
 // "FreeToken 完全拆解" (section 主结果) take the same order: E2M1 pairs are decoded with the
 // hardware e2m1x2->f16x2 conversion, each block's partial dot (16 elements for NVFP4, 32 for
 // MXFP4) is multiplied by its scale (E4M3, or E8M0 = 2^(code-127)), and NVFP4's per-bank FP32
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
   const int row_chunks = H / EPC;
   // x tile: BF16 path keeps raw bf16 (2 B); FP8 and FP4 paths keep f16 (2 B) -> H*2 bytes per token
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  __shared__ int s_shift[TG];  // FP8 / FP4: per-token power-of-two prescale of x (act_shift)
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int g = item / rbs, rb = item - g * rbs;
@@ -140,22 +143,23 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
     for (int t0 = 0; t0 < np; t0 += TG) {
       const int nt = min(TG, np - t0);
       __syncthreads();
+      if (WT != FT_W_BF16) {  // one warp per token: the exponent of its largest |x|
+        for (int tt = warp; tt < nt; tt += kEvalThreads / 32) {
+          const int pr = p.g_pair[p0 + t0 + tt];
+          const uint16_t* xr = p.x + (size_t)(shared_entry ? pr : pr / p.k) * H;
+          uint32_t m = 0;
+          for (int c8 = lane; c8 < H / 8; c8 += 32) m = bf16x8_maxbits(*reinterpret_cast<const uint4*>(xr + c8 * 8), m);
+          m = __reduce_max_sync(0xffffffffu, m);
+          if (lane == 0) s_shift[tt] = act_shift(m);
+        }
+        __syncthreads();
+      }
       for (int idx = threadIdx.x; idx < nt * (H / 8); idx += blockDim.x) {
         const int tt = idx / (H / 8), c8 = idx - tt * (H / 8);
         const int pr = p.g_pair[p0 + t0 + tt];
         const int tok = shared_entry ? pr : pr / p.k;
         uint4 v = *reinterpret_cast<const uint4*>(p.x + (size_t)tok * H + c8 * 8);
-        if (WT != FT_W_BF16) {  // bf16 -> f16 (exact for the f16 normal range)
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float lo = __uint_as_float(in[q] << 16), hi = __uint_as_float(in[q] & 0xffff0000u);
-            __half2 hh = __floats2half2_rn(lo, hi);
-            o[q] = *reinterpret_cast<uint32_t*>(&hh);
-          }
-          v = make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        if (WT != FT_W_BF16) v = bf16x8_to_f16x8_scaled(v, pow2i(-s_shift[tt]));  // exact
         *reinterpret_cast<uint4*>(xs + (size_t)tt * H + c8 * 8) = v;
       }
       __syncthreads();
@@ -192,8 +196,9 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
                 if (tt < nt) {
                   const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)tt * H + c * 16);
                   const uint4 xa = xp[0], xb = xp[1];
-                  acc_a[tt] = fmaf(dot_e4m3_f16(wa[s], xa, xb), scg, acc_a[tt]);
-                  acc_b[tt] = fmaf(dot_e4m3_f16(wb[s], xa, xb), scu, acc_b[tt]);
+                  // the 1x128 block's dot product over its 8 lanes, then its scale once
+                  acc_a[tt] = fmaf(group8_sum(dot_e4m3_f16(wa[s], xa, xb)), scg, acc_a[tt]);
+                  acc_b[tt] = fmaf(group8_sum(dot_e4m3_f16(wb[s], xa, xb)), scu, acc_b[tt]);
                 }
               }
             } else if (WT == FT_W_MXFP4) {
@@ -231,8 +236,10 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
       const float tsb = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(W + p.lay.ts) + 1) : 1.f;
 #pragma unroll
       for (int tt = 0; tt < TG; ++tt) {
-        const float a = warp_sum(acc_a[tt]);
-        const float b = warp_sum(acc_b[tt]);
+        // FP8: every lane of a block group holds the group's sum; FP8 / FP4: undo the prescale
+        const float xsc = WT == FT_W_BF16 ? 1.f : pow2i(tt < nt ? s_shift[tt] : 0);
+        const float a = (WT == FT_W_FP8_E4M3_B128 ? groups_sum(acc_a[tt]) : warp_sum(acc_a[tt])) * xsc;
+        const float b = (WT == FT_W_FP8_E4M3_B128 ? groups_sum(acc_b[tt]) : warp_sum(acc_b[tt])) * xsc;
         if (lane == 0 && tt < nt)
           p.h[(size_t)(p0 + t0 + tt) * I + i] = WT == FT_W_NVFP4 ? silu_mul(a * tsa, b * tsb) : silu_mul(a, b);
       }
@@ -294,6 +301,25 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
 #pragma unroll
         for (int s = 0; s < SEG; ++s) {
           const int c = c0 + s * 32 + lane;
+          if (WT == FT_W_FP8_E4M3_B128) {
+            // row_chunks is a multiple of 8, so a block's 8 lanes are all live or all idle;
+            // the shuffles of the block sum run on every lane of the warp
+            if (c0 + s * 32 >= row_chunks) break;
+            const bool cv = c < row_chunks;
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+              const float sc = cv ? __ldg(reinterpret_cast<const float*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 128) +
+                                          c / 8)
+                                  : 0.f;
+#pragma unroll
+              for (int tt = 0; tt < TG; ++tt)
+                if (tt < nt) {
+                  const float d = group8_sum(cv ? dot_e4m3_f32(wv[r][s], hs + (size_t)tt * I + c * 16) : 0.f);
+                  acc[r][tt] = fmaf(d, sc, acc[r][tt]);
+                }
+            }
+            continue;
+          }
           if (c < row_chunks) {
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
@@ -301,11 +327,6 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
 #pragma unroll
                 for (int tt = 0; tt < TG; ++tt)
                   if (tt < nt) acc[r][tt] = dot_bf16_f32(wv[r][s], hs + (size_t)tt * I + c * 8, acc[r][tt]);
-              } else if (WT == FT_W_FP8_E4M3_B128) {
-                const float sc = __ldg(reinterpret_cast<const float*>(W + p.lay.ds) + (size_t)(j0 + r) * (I / 128) + c / 8);
-#pragma unroll
-                for (int tt = 0; tt < TG; ++tt)
-                  if (tt < nt) acc[r][tt] = fmaf(dot_e4m3_f32(wv[r][s], hs + (size_t)tt * I + c * 16), sc, acc[r][tt]);
               } else if (WT == FT_W_MXFP4) {
                 const float sd = e8m0_to_float(__ldg(W + p.lay.ds + (size_t)(j0 + r) * (I / 32) + c));
 #pragma unroll
@@ -335,7 +356,8 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int tt = 0; tt < TG; ++tt) {
-          const float y = WT == FT_W_NVFP4 ? warp_sum(acc[r][tt]) * tsd : warp_sum(acc[r][tt]);
+          const float y = WT == FT_W_NVFP4 ? warp_sum(acc[r][tt]) * tsd
+                                           : (WT == FT_W_FP8_E4M3_B128 ? groups_sum(acc[r][tt]) : warp_sum(acc[r][tt]));
           if (lane == 0 && tt < nt) {
             const int pr = p.g_pair[p0 + t0 + tt];
             if (shared_entry) p.shared_rows[(size_t)pr * H + j0 + r] = y;

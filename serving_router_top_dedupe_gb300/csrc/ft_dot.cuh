@@ -1,7 +1,7 @@
 // Dot-product building blocks of the decode GEMV kernels.  Every (token, expert) dot is
 // formed the same way in every kernel that uses these: 16-byte chunks strided over the
-// lanes, accumulated in FP32 in chunk order, FP8 blocks scaled after their partial dot,
-// then an xor butterfly across the warp.
+// lanes, accumulated in FP32 in chunk order, then an xor butterfly across the warp; an FP8
+// block's dot product is first summed over the 8 lanes holding it and then scaled once.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -204,6 +204,59 @@ __device__ __forceinline__ float dot_e4m3_f32v(uint4 w, const float4 (&xv)[4]) {
     d = fmaf(f23.y, xv[q].w, d);
   }
   return d;
+}
+
+// FP8 rows are read as 16-byte chunks strided over the lanes, 32 consecutive chunks per
+// step, so the 8 chunks of one 1x128 block sit in the 8 lanes 8m .. 8m+7.  group8_sum adds a
+// value over those 8 lanes (xor butterfly, the same sum in each of them): the block's dot
+// product, formed before its scale multiplies it once.  groups_sum then adds the 4 groups'
+// values (each held by all 8 lanes of its group).
+__device__ __forceinline__ float group8_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  return v;
+}
+
+__device__ __forceinline__ float groups_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+// 2^s as a float, for -126 <= s <= 127 (built from the exponent field: exact).
+__device__ __forceinline__ float pow2i(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
+
+// Activations of the FP8 and FP4 paths enter the products as F16.  BF16 reaches far beyond
+// F16's range, so each token is first scaled by an exact power of two 2^-s chosen from its
+// largest magnitude: that magnitude lands in [2^14, 2^15), every BF16 value within 2^28 of
+// it converts to F16 exactly, and only values below 2^-39 of it are lost.  The finished sum
+// is multiplied by 2^s (exact).  `maxbits` is the largest (bf16 bits & 0x7fff) of the token
+// (BF16 magnitudes order like their bit patterns).
+__device__ __forceinline__ int act_shift(uint32_t maxbits) {
+  if (maxbits == 0) return 0;
+  const int s = (int)(maxbits >> 7) - 127 - 14;
+  return s < -126 ? -126 : (s > 113 ? 113 : s);
+}
+
+// max over the 8 BF16 magnitudes of a 16-byte vector and `m` (halfword-wise, then folded)
+__device__ __forceinline__ uint32_t bf16x8_maxbits(uint4 v, uint32_t m) {
+  const uint32_t k = 0x7fff7fffu;
+  uint32_t a = __vmaxu2(__vmaxu2(v.x & k, v.y & k), __vmaxu2(v.z & k, v.w & k));
+  a = a > 0xffffu ? max(a >> 16, a & 0xffffu) : a;
+  return max(m, a);
+}
+
+// 8 BF16 values (one 16-byte vector) times 2^-s, as 8 F16 values
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float scale) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __half2 hh = __floats2half2_rn(__uint_as_float(in[q] << 16) * scale, __uint_as_float(in[q] & 0xffff0000u) * scale);
+    o[q] = *reinterpret_cast<uint32_t*>(&hh);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

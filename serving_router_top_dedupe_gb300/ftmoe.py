@@ -24,6 +24,8 @@ FT_GATE_SOFTMAX_TOPK, FT_GATE_SOFTMAX_ALL, FT_GATE_SIGMOID_TOPK = 0, 1, 2
 FT_CPU = -1
 FT_DEVERR_NAN_LOGIT, FT_DEVERR_BAD_STATE, FT_DEVERR_TIMEOUT, FT_DEVERR_CAPACITY = 1, 2, 4, 8
 FT_TEST_HANDOFF_TIMEOUT_NS = 1
+FT_INJECT_MALLOC, FT_INJECT_REGISTER = 1, 2
+FT_HOST_PINNED, FT_HOST_HUGE_PAGES = 0, 1
 
 PROFILE_KINDS = ("control", "fill", "gate_up", "down_combine", "prefill_route", "prefill_gemm_gate_up",
                  "prefill_combine", "prefill_copy", "prefill_gemm_down", "router")
@@ -104,8 +106,9 @@ _SIGS = {
     "ft_moe_synchronize": [_P],
     "ft_moe_destroy": [_P],
     "ft_moe_reset_error": [_P],
+    "ft_test_inject_failure": [C.c_int, C.c_int],
     "ft_moe_test_control": [_P, C.c_int, C.c_longlong],
-    "ft_host_alloc": [C.c_size_t, C.POINTER(C.c_void_p)],
+    "ft_host_alloc": [C.c_size_t, C.c_int, C.POINTER(C.c_void_p)],
     "ft_host_free": [_P],
     "ft_moe_decode_resident_noalloc": [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, _P, _P, C.c_int, _P, _P, _P, _P,
                                        _P, _P],
@@ -325,6 +328,10 @@ def ft_moe_decode_resident_noalloc(n_experts, top_k, hidden, inter, wtype, exper
         raise FtError(st, "ft_moe_decode_resident_noalloc failed")
 
 
+def ft_test_inject_failure(kind, nth) -> None:
+    _check(_lib.ft_test_inject_failure(kind, nth))
+
+
 def ft_moe_reset_error(h) -> None:
     _check(_lib.ft_moe_reset_error(h))
 
@@ -333,10 +340,10 @@ def ft_moe_test_control(h, what, value) -> None:
     _check(_lib.ft_moe_test_control(h, what, value))
 
 
-def ft_host_alloc(nbytes) -> int:
-    """Page-locked, mapped host memory (cudaHostAlloc); returns its address."""
+def ft_host_alloc(nbytes, flags=FT_HOST_PINNED) -> int:
+    """Page-locked, mapped host memory for expert banks; returns its address."""
     p = C.c_void_p()
-    _check(_lib.ft_host_alloc(nbytes, C.byref(p)))
+    _check(_lib.ft_host_alloc(nbytes, flags, C.byref(p)))
     return p.value
 
 
@@ -344,11 +351,11 @@ def ft_host_free(addr) -> None:
     _check(_lib.ft_host_free(addr))
 
 
-def host_array(shape, dtype):
+def host_array(shape, dtype, flags=FT_HOST_PINNED):
     """A numpy array over fresh ft_host_alloc memory; release it with free_host_array."""
     dtype = np.dtype(dtype)
     n = int(np.prod(shape)) * dtype.itemsize
-    addr = ft_host_alloc(max(n, 16))
+    addr = ft_host_alloc(max(n, 16), flags)
     buf = (C.c_uint8 * max(n, 16)).from_address(addr)
     return np.frombuffer(buf, dtype=np.uint8, count=n).view(dtype).reshape(shape)
 

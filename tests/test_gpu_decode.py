@@ -273,3 +273,35 @@ def test_host_hook_evaluates_the_c_set_in_step():
         hooked.compare_state()
         F.ft_graph_destroy(g)
         F.ft_moe_set_host_hook(hooked.h, None)
+
+
+def _scaled_x(xb, factor, mixed=False):
+    """BF16 activations times `factor` (rounded to BF16); mixed: alternate elements keep
+    their N(0, 1) size, so one token spans ~1e5 to ~1e-6 of its largest value."""
+    x = O.bf16_to_f64(xb)
+    f = np.full(x.shape, float(factor))
+    if mixed:
+        f[..., 1::2] = 1e-6
+    return synth.f32_to_bf16_bits((x * f).astype(np.float32)).reshape(xb.shape)
+
+
+@pytest.mark.parametrize("wtype,batch", [(synth.W_FP8_E4M3_B128, 1), (synth.W_FP8_E4M3_B128, 4),
+                                         (synth.W_NVFP4, 1), (synth.W_MXFP4, 4)])
+@pytest.mark.parametrize("factor,mixed", [(1e5, False), (1e-6, False), (1e5, True)])
+def test_fp8_fp4_activation_magnitudes(wtype, batch, factor, mixed):
+    """FP8 and FP4 products take the activations as F16.  BF16 activations far outside F16's
+    range (~1e5 and ~1e-6, and both within one token) still match the oracle: each token is
+    scaled by an exact power of two before the narrowing and back after the sum."""
+    if wtype == synth.W_FP8_E4M3_B128:
+        w = synth.decode_fp8(batch=batch).with_(n_layers=2, n_experts=16, hidden=1024, inter=256, steps=4,
+                                                cache_slots=12)
+    else:
+        w = synth.tiny().with_(wtype=wtype, batch=batch, steps=4)
+    tr = synth.routing_trace(w) if w.logits == "trace" else None
+    with Run(w) as r:
+        for s in range(w.steps):
+            for l in range(w.n_layers):
+                xb, z = r.inputs(s, l, tr)
+                r.step(s, l, tr, check_out=True, xz=(_scaled_x(xb, factor, mixed), z))
+        r.compare_state()
+        print(f"factor {factor} mixed {mixed}: max rel err {r.max_err:.2e}")

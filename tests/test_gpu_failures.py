@@ -1,6 +1,6 @@
 """Failure detection without faulting the GPU.
 
-- Host-side injection: FTMOE_INJECT_FAILURE makes the n-th device allocation or host-bank
+- Host-side injection: ft_test_inject_failure makes the n-th device allocation or host-bank
   registration of ft_moe_init / ft_cache_resize fail as if the runtime refused it.  The call
   returns FT_ERR_NOMEM / FT_ERR_PIN, releases what it had taken (device memory back to where
   it was, banks unregistered), and a resize that fails leaves the handle as it was.
@@ -9,8 +9,6 @@
   FT_DEVERR_TIMEOUT in the error word (routing and cache decisions still valid), and after
   ft_moe_reset_error the same handle runs correct steps again.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -30,11 +28,17 @@ def _lib():
 
 @pytest.fixture()
 def inject():
+    from serving_router_top_dedupe_gb300 import ftmoe as F
+
     def set_(v):
-        os.environ["FTMOE_INJECT_FAILURE"] = v
+        kind, _, n = v.partition(":")
+        if not v:
+            F.ft_test_inject_failure(F.FT_INJECT_MALLOC, 0)
+            return
+        F.ft_test_inject_failure(F.FT_INJECT_MALLOC if kind == "malloc" else F.FT_INJECT_REGISTER, int(n))
 
     yield set_
-    os.environ.pop("FTMOE_INJECT_FAILURE", None)
+    set_("")
 
 
 def _cfg(F, w, max_batch=1):
