@@ -66,11 +66,13 @@ typedef enum {
  *                       nibble), one E4M3 scale per 1x16 block along the reduction
  *                       dimension applied after the block's dot product, then one FP32
  *                       tensor scale per bank of each expert ([FT] 主结果 names NVFP4
- *                       experts).  Decode only; prefill is BF16.
+ *                       experts).
  *   FT_W_MXFP4          E2M1 weights packed as for NVFP4, one E8M0 scale (2^(code-127))
  *                       per 1x32 block along the reduction dimension, applied after the
  *                       block's dot product; no tensor scale ([FT] 主结果: MXFP4 checkpoints).
- *                       Decode only. */
+ * Prefill decodes FP8 and FP4 weights to BF16 in shared memory (each weight times its block
+ * scale in FP32, rounded once) before the tensor-core product: the block-scaled tensor-core
+ * forms take FP8 / FP4 activations, and the activations here are BF16. */
 typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1, FT_W_NVFP4 = 2, FT_W_MXFP4 = 3 } ft_wtype;
 
 /* How a decode step moves F-set experts from the host pool into their slots.

@@ -1097,7 +1097,6 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   if (n_tokens < 1 || n_tokens > h->cfg.max_prefill_tokens)
     return fail(FT_ERR_INVALID, "n_tokens %d outside [1, max_prefill_tokens=%d]", n_tokens, h->cfg.max_prefill_tokens);
   if (!x_bf16 || !logits || !out) return fail(FT_ERR_INVALID, "null x/logits/out");
-  if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
   if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
   FT_CUDA(cudaSetDevice(h->dev));
   ft::PrefillCtx c{};
@@ -1119,7 +1118,9 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   c.owner = h->owner;
   c.stamp = h->stamp;
   c.st = h->st;
-  for (int j = 0; j < 3; ++j) {
+  c.n_banks = h->n_banks;
+  c.wtype = h->cfg.wtype;
+  for (int j = 0; j < h->n_banks; ++j) {
     c.bank_host[j] = h->bank[j].host;
     c.bank_row[j] = h->bank[j].row;
   }
@@ -1154,7 +1155,6 @@ ft_status ft_moe_prefill_chunk_hidden(ft_moe* h, int layer, int n_tokens, const 
     return fail(FT_ERR_INVALID, "n_tokens %d above max_prefill_tokens=%d", n_tokens, h->cfg.max_prefill_tokens);
   if (!out) return fail(FT_ERR_INVALID, "null out");
   // the checks of ft_moe_prefill_chunk that do not depend on the logits, before any work
-  if (h->cfg.wtype != FT_W_BF16) return fail(FT_ERR_INVALID, "prefill grouped GEMM is built for BF16 experts only");
   if (capturing(h->cs)) return fail(FT_ERR_STATE, "prefill chunks are not capturable");
   FT_CUDA(cudaSetDevice(h->dev));
   if ((s = enqueue_router(h, layer, n_tokens, x_bf16, h->router_z, false)) != FT_OK) return s;

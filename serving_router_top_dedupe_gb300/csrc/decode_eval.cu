@@ -418,8 +418,7 @@ cudaError_t launch_fill(const FillParams& p, int grid, cudaStream_t s) {
 }
 
 bool eval_fused(const EvalParams& p, int wtype) {
-  // the persistent batch-1 kernel is built for BF16 and FP8; the FP4 formats run the batched kernels
-  return p.B == 1 && p.allow_fused && (wtype == FT_W_BF16 || wtype == FT_W_FP8_E4M3_B128) &&
+  return p.B == 1 && p.allow_fused &&
          fused_gemv_supported(wtype, p.H, p.I, batch1_entries(p), p.n_sm);
 }
 

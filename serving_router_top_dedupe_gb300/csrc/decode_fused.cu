@@ -1,5 +1,6 @@
 // Decode expert evaluation at batch 1 in one persistent launch: gate/up GEMV + SwiGLU,
-// down GEMV and the fixed-order combine.
+// down GEMV and the fixed-order combine, for BF16, FP8 (E4M3, 1x128 FP32 block scales) and the
+// block-FP4 formats (NVFP4, MXFP4).
 //
 // A decode layer reads every byte of its G-set experts once (about 1 FLOP per byte), so
 // it is bound by HBM, and at batch 1 a layer is only ~10 us of traffic: what costs is
@@ -30,8 +31,10 @@
 // Per (entry, row) the lane-strided 16-byte chunk order and the xor butterfly are those of
 // the batched decode kernels, so results are bit-identical to them.
 //
-// FP8 E4M3 weights: each 128-element block's dot product is formed first and then
-// multiplied by the block's FP32 scale ("OSDI'26 | 双路 CPU + 两张 5090 …", §4.2).
+// FP8 E4M3 weights: each 1x128 block's dot product is formed first (its 8 chunks sit in 8
+// lanes and are summed across them) and then multiplied by the block's FP32 scale once
+// ("OSDI'26 | 双路 CPU + 两张 5090 …", §4.2).  The token enters the FP8 products as F16 after
+// an exact per-token power-of-two prescale, undone on the finished sums.
 #include "ft_dot.cuh"
 #include "ft_internal.cuh"
 #include "ft_ptx.cuh"
@@ -41,6 +44,9 @@ namespace {
 
 using namespace dot;
 using namespace ptx;
+
+// E8M0 scale code -> 2^(code - 127) (code 0: the subnormal 2^-127; 255 is never written)
+__device__ __forceinline__ float e8m0_float(uint32_t code) { return __uint_as_float(code ? code << 23 : 0x00400000u); }
 
 constexpr int kConsumers = 8;
 constexpr int kThreads = 32 * (kConsumers + 1);
@@ -60,8 +66,9 @@ struct FusedPlan {
 };
 
 __host__ __device__ inline FusedPlan make_fused_plan(int wtype, int H, int I, int max_entries, int n_cta) {
-  const size_t esz = wtype == FT_W_BF16 ? 2 : 1;
-  const size_t rh = (size_t)H * esz, ri = (size_t)I * esz;
+  // stored bytes per row: 2 per element (BF16), 1 (FP8), 1/2 (NVFP4, MXFP4)
+  const size_t epc = wtype == FT_W_BF16 ? 8 : (wtype == FT_W_FP8_E4M3_B128 ? 16 : 32);  // elements per 16 B
+  const size_t rh = (size_t)H / epc * 16, ri = (size_t)I / epc * 16;
   FusedPlan pl;
   pl.stage = kStageTarget;
   if (pl.stage < 2 * rh) pl.stage = 2 * rh;
@@ -105,12 +112,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
   int4* meta = reinterpret_cast<int4*>(empty + kMaxStages);  // per stage: phase, first row, rows
   volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + kMaxStages);
 
-  constexpr int ESZ = WT == FT_W_BF16 ? 2 : 1;
-  constexpr int EPC = 16 / ESZ;  // weights per 16-byte chunk
+  constexpr int EPC = WT == FT_W_BF16 ? 8 : (WT == FT_W_FP8_E4M3_B128 ? 16 : 32);  // weights per 16-byte chunk
+  constexpr bool kFP4 = WT == FT_W_NVFP4 || WT == FT_W_MXFP4;
   const int ne = p.counts[C_NENTRIES];
   // compile-time shapes make the unit and row index arithmetic constant as well
   const int H = HC > 0 ? HC * 32 * EPC : p.H, I = IC > 0 ? IC * 32 * EPC : p.I, k = p.k;
-  const size_t rh = (size_t)H * ESZ, ri = (size_t)I * ESZ;
+  const size_t rh = (size_t)H / EPC * 16, ri = (size_t)I / EPC * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // Entries split into two passes: those resident before this step (pass 0) and those the
@@ -205,20 +212,29 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
     // ------------------------------------------------------------- consumers
     const int cw = warp - 1;
     const int ct = threadIdx.x - 32;  // 0..255
-    // the token as bf16 (BF16 weights) or f16 (FP8 weights)
+    // the token as bf16 (BF16 weights) or f16 after an exact power-of-two prescale (FP8, FP4)
+    int xshift = 0;
+    if (WT != FT_W_BF16) {
+      __shared__ uint32_t s_xmax[kConsumers];
+      uint32_t m = 0;
+      for (int idx = ct; idx < H / 8; idx += 32 * kConsumers)
+        m = bf16x8_maxbits(*reinterpret_cast<const uint4*>(p.x + (size_t)idx * 8), m);
+      m = __reduce_max_sync(0xffffffffu, m);
+      if (lane == 0) s_xmax[cw] = m;
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
+      m = 0;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) m = max(m, s_xmax[w]);
+      xshift = act_shift(m);
+    }
     for (int idx = ct; idx < H / 8; idx += 32 * kConsumers) {
       uint4 v = *reinterpret_cast<const uint4*>(p.x + (size_t)idx * 8);
-      if (WT == FT_W_FP8_E4M3_B128) {
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          __half2 hh = __floats2half2_rn(__uint_as_float(in[q] << 16), __uint_as_float(in[q] & 0xffff0000u));
-          o[q] = *reinterpret_cast<uint32_t*>(&hh);
-        }
-        v = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      *reinterpret_cast<uint4*>(xs + (size_t)idx * 8) = v;
+      if (WT != FT_W_BF16) v = bf16x8_to_f16x8_scaled(v, pow2i(-xshift));
+      // plane layout: piece q (8 elements) of chunk c at plane q, so that each lane's 16-byte
+      // pieces of consecutive chunks lie side by side (no bank conflicts)
+      constexpr int kXP = EPC / 8;  // x pieces (planes) per chunk
+      const int c = idx / kXP, q = idx - c * kXP;
+      *reinterpret_cast<uint4*>(xs + (size_t)q * (H / kXP) + (size_t)c * 8) = v;
     }
     asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
 
@@ -247,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
       const int npe = s_np[pass];
       if (npe == 0) continue;
       const int* pe = s_pe[pass];
-      if (WT == FT_W_FP8_E4M3_B128 && pass == 1) pdl_wait();  // block scales of filled slots are read directly
+      if (WT != FT_W_BF16 && pass == 1) pdl_wait();  // block scales of filled slots are read directly
       const long long R0 = (long long)npe * I;
       const int v0 = (int)(R0 * blockIdx.x / gridDim.x);
       const int n0 = (int)(R0 * (blockIdx.x + 1) / gridDim.x) - v0;
@@ -278,20 +294,54 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
               a = dot_bf16_bf16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), xv, a);
               b = dot_bf16_bf16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), xv, b);
             }
+          } else if (kFP4) {
+            // a chunk holds 32 elements: two NVFP4 blocks or one MXFP4 block, each block's dot
+            // product taken first and multiplied by its scale (as in the batched kernels)
+            const int sb = WT == FT_W_NVFP4 ? H / 16 : H / 32;  // scale bytes per row
+            const uint8_t* bg = p.g_w[g] + p.lay.gs + (size_t)i * sb;
+            const uint8_t* bu = p.g_w[g] + p.lay.us + (size_t)i * sb;
+            for (int c16 = lane; c16 < H / EPC; c16 += 32) {
+              const uint4 x0 = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
+              const uint4 x1 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 4 + (size_t)c16 * 8);
+              const uint4 x2 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 2 + (size_t)c16 * 8);
+              const uint4 x3 = *reinterpret_cast<const uint4*>(xs + (size_t)3 * H / 4 + (size_t)c16 * 8);
+              const uint4 wa = *reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16);
+              const uint4 wb = *reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16);
+              if (WT == FT_W_NVFP4) {
+                const float2 ga = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(bg) + c16));
+                const float2 gb = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(bu) + c16));
+                a = fmaf(dot16_e2m1_f16(wa.x, wa.y, x0, x1), ga.x, a);
+                a = fmaf(dot16_e2m1_f16(wa.z, wa.w, x2, x3), ga.y, a);
+                b = fmaf(dot16_e2m1_f16(wb.x, wb.y, x0, x1), gb.x, b);
+                b = fmaf(dot16_e2m1_f16(wb.z, wb.w, x2, x3), gb.y, b);
+              } else {
+                const float da = dot16_e2m1_f16(wa.x, wa.y, x0, x1) + dot16_e2m1_f16(wa.z, wa.w, x2, x3);
+                const float db = dot16_e2m1_f16(wb.x, wb.y, x0, x1) + dot16_e2m1_f16(wb.z, wb.w, x2, x3);
+                a = fmaf(da, e8m0_float(__ldg(bg + c16)), a);
+                b = fmaf(db, e8m0_float(__ldg(bu + c16)), b);
+              }
+            }
           } else {
             const float* sg = reinterpret_cast<const float*>(p.g_w[g] + p.lay.gs) + (size_t)i * (H / 128);
             const float* su = reinterpret_cast<const float*>(p.g_w[g] + p.lay.us) + (size_t)i * (H / 128);
+            // H / 16 is a multiple of 32: every lane runs every step.  Each 1x128 block's dot
+            // product is summed over its 8 lanes, then multiplied by the block's scale once.
 #pragma unroll 4
             for (int c16 = lane; c16 < H / EPC; c16 += 32) {
-              const uint4* xp = reinterpret_cast<const uint4*>(xs + (size_t)c16 * 16);
-              const uint4 x0 = xp[0], x1 = xp[1];
-              a = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), x0, x1), __ldg(sg + c16 / 8),
-                       a);
-              b = fmaf(dot_e4m3_f16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), x0, x1), __ldg(su + c16 / 8),
-                       b);
+              const uint4 x0 = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
+              const uint4 x1 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 2 + (size_t)c16 * 8);
+              const float da = group8_sum(dot_e4m3_f16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), x0, x1));
+              const float db = group8_sum(dot_e4m3_f16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), x0, x1));
+              a = fmaf(da, __ldg(sg + c16 / 8), a);
+              b = fmaf(db, __ldg(su + c16 / 8), b);
             }
           }
-          const float ab2[2] = {warp_sum(a), warp_sum(b)};
+          const float xsc = WT == FT_W_BF16 ? 1.f : pow2i(xshift);
+          // NVFP4: the banks' FP32 tensor scales multiply the finished sums
+          const float tsa = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts)) : 1.f;
+          const float tsb = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts) + 1) : 1.f;
+          const float ab2[2] = {(WT == FT_W_FP8_E4M3_B128 ? groups_sum(a) : warp_sum(a)) * xsc * tsa,
+                                (WT == FT_W_FP8_E4M3_B128 ? groups_sum(b) : warp_sum(b)) * xsc * tsb};
           if (lane == 0) p.h[(size_t)g * I + i] = silu_mul(ab2[0], ab2[1]);
         }
         __syncwarp();
@@ -327,7 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
       for (int idx = ct; idx < npe * (I / 4); idx += 32 * kConsumers) {
         const int gi = idx / (I / 4), i4 = idx - gi * (I / 4);
         const size_t off = (size_t)pe[gi] * (I / 4) + i4;
-        reinterpret_cast<float4*>(hs)[off] = __ldcg(reinterpret_cast<const float4*>(p.h) + off);
+        // per entry, float4 piece q of chunk c at plane q (planes of I / EPC float4)
+        constexpr int kHP = EPC / 4;  // h pieces per chunk
+        const int c = i4 / kHP, q = i4 - c * kHP;
+        reinterpret_cast<float4*>(hs)[(size_t)pe[gi] * (I / 4) + (size_t)q * (I / EPC) + c] =
+            __ldcg(reinterpret_cast<const float4*>(p.h) + off);
       }
       asm volatile("bar.sync 1, %0;" ::"r"(32 * kConsumers) : "memory");
 
@@ -358,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
 #pragma unroll
             for (int cc = 0; cc < IC; ++cc) {
               const int c16 = lane + 32 * cc;
-              h0[cc] = *reinterpret_cast<const float4*>(hv + c16 * EPC);
-              h1[cc] = *reinterpret_cast<const float4*>(hv + c16 * EPC + 4);
+              h0[cc] = reinterpret_cast<const float4*>(hv)[c16];
+              h1[cc] = reinterpret_cast<const float4*>(hv)[I / EPC + c16];
             }
             const uint8_t* wrow[kRowsILP];
 #pragma unroll
@@ -392,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           float acc[kRowsILP];
           const float* hv[kRowsILP];
           const float* sc[kRowsILP];
+          const uint8_t* sb4[kRowsILP];
+          float ts4[kRowsILP];
           int yi[kRowsILP];
           bool ok[kRowsILP];
 #pragma unroll
@@ -401,23 +457,70 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
             const int t = m.y + (ok[r] ? qq : q), gi = t / nj, jl = t - gi * nj, g = pe[gi];
             yi[r] = g * nj + jl;
             hv[r] = hs + (size_t)g * I;
-            sc[r] = WT == FT_W_BF16 ? nullptr
-                                    : reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128);
+            sc[r] = WT == FT_W_FP8_E4M3_B128
+                        ? reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128)
+                        : nullptr;
+            sb4[r] = kFP4 ? p.g_w[g] + p.lay.ds + (size_t)(j0 + jl) * (WT == FT_W_NVFP4 ? I / 16 : I / 32) : nullptr;
+            ts4[r] = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts) + 2) : 1.f;
             acc[r] = 0.f;
           }
+          if (WT == FT_W_BF16) {
 #pragma unroll 4
-          for (int c16 = lane; c16 < I / EPC; c16 += 32) {
+            for (int c16 = lane; c16 < I / EPC; c16 += 32) {
 #pragma unroll
-            for (int r = 0; r < kRowsILP; ++r) {
-              if (!ok[r]) continue;
-              const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16);
-              if (WT == FT_W_BF16) acc[r] = dot_bf16_f32(wv, hv[r] + c16 * EPC, acc[r]);
-              else acc[r] = fmaf(dot_e4m3_f32(wv, hv[r] + c16 * EPC), __ldg(sc[r] + c16 / 8), acc[r]);
+              for (int r = 0; r < kRowsILP; ++r) {
+                if (!ok[r]) continue;
+                const uint4 wv =
+                    *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16);
+                const float4* h4 = reinterpret_cast<const float4*>(hv[r]);
+                acc[r] = dot_bf16_f32v(wv, h4[c16], h4[I / EPC + c16], acc[r]);
+              }
+            }
+          } else if (kFP4) {
+            for (int c16 = lane; c16 < I / EPC; c16 += 32) {
+#pragma unroll
+              for (int r = 0; r < kRowsILP; ++r) {
+                if (!ok[r]) continue;
+                const uint4 wv =
+                    *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16);
+                const float4* h4 = reinterpret_cast<const float4*>(hv[r]);
+                float hv32[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) *reinterpret_cast<float4*>(hv32 + 4 * q) = h4[(size_t)q * (I / EPC) + c16];
+                if (WT == FT_W_NVFP4) {
+                  const float2 sd = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(sb4[r]) + c16));
+                  acc[r] = fmaf(dot16_e2m1_f32(wv.x, wv.y, hv32), sd.x, acc[r]);
+                  acc[r] = fmaf(dot16_e2m1_f32(wv.z, wv.w, hv32 + 16), sd.y, acc[r]);
+                } else {
+                  const float d = dot16_e2m1_f32(wv.x, wv.y, hv32) + dot16_e2m1_f32(wv.z, wv.w, hv32 + 16);
+                  acc[r] = fmaf(d, e8m0_float(__ldg(sb4[r] + c16)), acc[r]);
+                }
+              }
+            }
+          } else {
+            // I / 16 is a multiple of 8: a block's 8 lanes are all live or all idle, and the
+            // block-sum shuffles run on every lane
+            for (int cb = 0; cb < I / EPC; cb += 32) {
+              const int c16 = cb + lane;
+              const bool cv = c16 < I / EPC;
+#pragma unroll
+              for (int r = 0; r < kRowsILP; ++r) {
+                if (!ok[r]) continue;  // the same for every lane
+                float d = 0.f;
+                if (cv) {
+                  const float4* h4 = reinterpret_cast<const float4*>(hv[r]);
+                  const float4 hq[4] = {h4[c16], h4[I / EPC + c16], h4[2 * (I / EPC) + c16], h4[3 * (I / EPC) + c16]};
+                  d = dot_e4m3_f32v(
+                      *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16), hq);
+                }
+                d = group8_sum(d);
+                if (cv) acc[r] = fmaf(d, __ldg(sc[r] + c16 / 8), acc[r]);
+              }
             }
           }
 #pragma unroll
           for (int r = 0; r < kRowsILP; ++r) {
-            const float v = warp_sum(acc[r]);
+            const float v = (WT == FT_W_FP8_E4M3_B128 ? groups_sum(acc[r]) : warp_sum(acc[r])) * ts4[r];
             if (ok[r] && lane == 0) ybuf[yi[r]] = v;  // [entry][jl]
           }
         }
@@ -456,7 +559,8 @@ cudaError_t launch_fused_t(const EvalParams& p, int n_sm, int max_entries, cudaS
   return launch_k(fused_gemv_kernel<WT, HC, IC>, dim3(n_sm), dim3(kThreads), fused_smem_bytes(pl), s, p.pdl, p, pl);
 }
 
-// Shapes compiled with fixed chunk counts: the 35B-A3B expert shape (H 2048, I 512, BF16).
+// Shapes compiled with fixed chunk counts: the 35B-A3B expert shape (H 2048, I 512, BF16)
+// and the large FP8 expert shape (H 7168, I 2048, E4M3).
 template <int WT, int HC, int IC>
 constexpr bool fixed_shape_matches(int H, int I) {
   return H == HC * 32 * (WT == FT_W_BF16 ? 8 : 16) && I == IC * 32 * (WT == FT_W_BF16 ? 8 : 16);
@@ -474,10 +578,22 @@ bool fused_gemv_fits(int wtype, int H, int I, int max_entries, int n_sm) {
   const FusedPlan pl = make_fused_plan(wtype, H, I, max_entries, n_sm);
   int nb = 0;
   const size_t smem = fused_smem_bytes(pl);
-  cudaError_t e = wtype == FT_W_BF16
-                      ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_BF16, 0, 0>, kThreads, smem)
-                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>,
-                                                                      kThreads, smem);
+  cudaError_t e;
+  switch (wtype) {
+    case FT_W_BF16:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_BF16, 0, 0>, kThreads, smem);
+      break;
+    case FT_W_FP8_E4M3_B128:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>, kThreads,
+                                                        smem);
+      break;
+    case FT_W_NVFP4:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_NVFP4, 0, 0>, kThreads, smem);
+      break;
+    default:
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fused_gemv_kernel<FT_W_MXFP4, 0, 0>, kThreads, smem);
+      break;
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return false;
@@ -488,20 +604,29 @@ bool fused_gemv_fits(int wtype, int H, int I, int max_entries, int n_sm) {
 cudaError_t launch_fused_gemv(const EvalParams& p, int wtype, int n_sm, int max_entries, cudaStream_t s) {
   if (wtype == FT_W_BF16 && fixed_shape_matches<FT_W_BF16, 8, 2>(p.H, p.I))
     return launch_fused_t<FT_W_BF16, 8, 2>(p, n_sm, max_entries, s);
-  return wtype == FT_W_BF16 ? launch_fused_t<FT_W_BF16, 0, 0>(p, n_sm, max_entries, s)
-                            : launch_fused_t<FT_W_FP8_E4M3_B128, 0, 0>(p, n_sm, max_entries, s);
+  if (wtype == FT_W_FP8_E4M3_B128 && fixed_shape_matches<FT_W_FP8_E4M3_B128, 14, 4>(p.H, p.I))
+    return launch_fused_t<FT_W_FP8_E4M3_B128, 14, 4>(p, n_sm, max_entries, s);
+  switch (wtype) {
+    case FT_W_BF16: return launch_fused_t<FT_W_BF16, 0, 0>(p, n_sm, max_entries, s);
+    case FT_W_FP8_E4M3_B128: return launch_fused_t<FT_W_FP8_E4M3_B128, 0, 0>(p, n_sm, max_entries, s);
+    case FT_W_NVFP4: return launch_fused_t<FT_W_NVFP4, 0, 0>(p, n_sm, max_entries, s);
+    default: return launch_fused_t<FT_W_MXFP4, 0, 0>(p, n_sm, max_entries, s);
+  }
 }
 
 cudaError_t prepare_fused_gemv() {
   const int lim = (int)(kSmemBudget + 4096);
-  cudaError_t e =
-      cudaFuncSetAttribute(fused_gemv_kernel<FT_W_BF16, 8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_BF16, 0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             lim);
-  return e;
+  const void* k[] = {(const void*)fused_gemv_kernel<FT_W_BF16, 8, 2>,
+                     (const void*)fused_gemv_kernel<FT_W_FP8_E4M3_B128, 14, 4>,
+                     (const void*)fused_gemv_kernel<FT_W_BF16, 0, 0>,
+                     (const void*)fused_gemv_kernel<FT_W_FP8_E4M3_B128, 0, 0>,
+                     (const void*)fused_gemv_kernel<FT_W_NVFP4, 0, 0>,
+                     (const void*)fused_gemv_kernel<FT_W_MXFP4, 0, 0>};
+  for (const void* f : k) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace ft

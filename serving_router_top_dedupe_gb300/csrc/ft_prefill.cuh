@@ -19,8 +19,10 @@ struct PrefillCtx {
   int32_t* owner;
   uint32_t* stamp;
   DevState* st;
-  const uint8_t* bank_host[3];  // gate, up, down host banks (pinned)
-  size_t bank_row[3];
+  const uint8_t* bank_host[7];  // host banks (pinned): gate, up, down, then the scale banks
+  size_t bank_row[7];           // bytes per logical id in each bank
+  int n_banks;
+  int wtype;                    // ft_wtype of the experts
   bool prof;
   bool overlap;  // stream layer l+1 while layer l computes (the double buffer)
   int gate;      // FT_GATE_*
@@ -42,13 +44,21 @@ struct GemmDesc {
   uint16_t* h;               // [P][I] BF16 (gate/up output)
   uint16_t* rows;            // [P][H] BF16 (down output)
   uint32_t* error_word;
+  // FP8 / FP4 experts: where the dequantising warps find each weight row's block scales
+  const uint8_t* pool;       // slot pool (routed experts)
+  const uint8_t* shared_w;   // shared experts, one slot-layout row block per layer
+  size_t stride;             // slot stride in bytes
+  size_t off_gs, off_us, off_ds, off_ts;  // scale-bank offsets within a slot
 };
 
 // Tensor maps and launch of the grouped GEMM.  mode 0: gate/up + SwiGLU from the token
-// rows in pair order (xp); mode 1: down + gate weighting from h.
+// rows in pair order (xp); mode 1: down + gate weighting from h.  wtype picks the weight
+// form: BF16 tiles go straight to the tensor cores; FP8 and FP4 tiles are decoded to BF16
+// in shared memory first.
 struct GemmMaps;
 cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
-                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs);
+                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs, int wtype,
+                             const SlotLayout& lay);
 void gemm_maps_destroy(GemmMaps* m);
 cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, int T, const GemmDesc& d, int grid,
                                 cudaStream_t s);

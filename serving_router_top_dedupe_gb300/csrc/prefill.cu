@@ -284,35 +284,68 @@ struct PrefillState {
   cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr}, ev_restore = nullptr;
   bool free_recorded[2] = {false, false};
   cudaStream_t cs = nullptr, ts = nullptr;
+  // a second transfer stream of the library's own: a layer's copies alternate between the two,
+  // so one copy engine's per-copy gaps are covered by the other's copy
+  cudaStream_t ts2 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // what a restore copy needs
   uint8_t* pool = nullptr;
   SlotLayout lay{};
-  const uint8_t* bank_host[3] = {nullptr, nullptr, nullptr};
-  size_t bank_row[3] = {0, 0, 0};
+  const uint8_t* bank_host[7] = {};
+  size_t bank_row[7] = {};
+  int n_banks = 3;
+  int wtype = FT_W_BF16;
 };
 
 namespace {
 
-// Copy every expert of `layer` from the host banks into the slots `slots` (on ts).
-// Runs of consecutive slots become one 2-D copy per bank.
+// Byte offset of bank j within a slot: gate, up, down, then the scale banks.
+size_t bank_offset(const SlotLayout& l, int j) {
+  const size_t off[7] = {l.gate, l.up, l.down, l.gs, l.us, l.ds, l.ts};
+  return off[j];
+}
+
+}  // namespace
+
+namespace {
+
+// Where the decoding warps of the FP8 / FP4 grouped GEMM find the block scales.
+void set_weight_info(GemmDesc& d, const PrefillCtx& c) {
+  d.pool = c.pool;
+  d.shared_w = c.shared_w;
+  d.stride = c.lay.stride;
+  d.off_gs = c.lay.gs;
+  d.off_us = c.lay.us;
+  d.off_ds = c.lay.ds;
+  d.off_ts = c.lay.ts;
+}
+
+// Copy every expert of `layer` from the host banks into the slots `slots`, ordered after
+// the work already on ts and completed in ts's order.  Runs of consecutive slots become one
+// 2-D copy per bank; the copies alternate between ts and the state's second transfer
+// stream, which joins ts at the end.
 cudaError_t copy_layer(PrefillState* p, int layer, const std::vector<int>& slots, cudaStream_t ts) {
-  const size_t seg[3] = {p->lay.gate, p->lay.up, p->lay.down};
   const int E = p->E;
-  int e = 0;
+  cudaError_t err;
+  if ((err = cudaEventRecord(p->ev_fork, ts)) != cudaSuccess || (err = cudaStreamWaitEvent(p->ts2, p->ev_fork, 0)))
+    return err;
+  int e = 0, n = 0;
   while (e < E) {
     int run = 1;
     while (e + run < E && slots[e + run] == slots[e] + run) ++run;
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < p->n_banks; ++j, ++n) {
       const uint8_t* src = p->bank_host[j] + ((size_t)layer * E + e) * p->bank_row[j];
-      uint8_t* dst = p->pool + (size_t)slots[e] * p->lay.stride + seg[j];
-      cudaError_t err = run == 1 ? cudaMemcpyAsync(dst, src, p->bank_row[j], cudaMemcpyHostToDevice, ts)
-                                 : cudaMemcpy2DAsync(dst, p->lay.stride, src, p->bank_row[j], p->bank_row[j], run,
-                                                     cudaMemcpyHostToDevice, ts);
+      uint8_t* dst = p->pool + (size_t)slots[e] * p->lay.stride + bank_offset(p->lay, j);
+      cudaStream_t s = (n & 1) ? p->ts2 : ts;
+      err = run == 1 ? cudaMemcpyAsync(dst, src, p->bank_row[j], cudaMemcpyHostToDevice, s)
+                     : cudaMemcpy2DAsync(dst, p->lay.stride, src, p->bank_row[j], p->bank_row[j], run,
+                                         cudaMemcpyHostToDevice, s);
       if (err != cudaSuccess) return err;
     }
     e += run;
   }
-  return cudaSuccess;
+  if ((err = cudaEventRecord(p->ev_join, p->ts2)) != cudaSuccess) return err;
+  return cudaStreamWaitEvent(ts, p->ev_join, 0);
 }
 
 // Enqueue the load of `layer` into buffer b on the transfer stream, after the compute
@@ -362,7 +395,9 @@ cudaError_t route_chunk(PrefillState* p, const PrefillCtx& c, int T, const uint1
 
 cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   if (c.S > kPickMaxSlots) return cudaErrorInvalidValue;
-  if (c.lay.stride != c.lay.used || c.H % 128 || c.I % 64) return cudaErrorInvalidValue;
+  // BF16 tiles are read through 2-D maps over the whole pool (slot stride = the three banks);
+  // FP8 / FP4 tiles through 3-D maps (any stride)
+  if ((c.wtype == FT_W_BF16 && c.lay.stride != c.lay.used) || c.H % 128 || c.I % 64) return cudaErrorInvalidValue;
   PrefillState* p = new PrefillState();
   p->T_max = c.max_tokens;
   p->E = c.E;
@@ -376,7 +411,9 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   p->n_sm = c.n_sm;
   p->pool = c.pool;
   p->lay = c.lay;
-  for (int j = 0; j < 3; ++j) {
+  p->n_banks = c.n_banks;
+  p->wtype = c.wtype;
+  for (int j = 0; j < c.n_banks; ++j) {
     p->bank_host[j] = c.bank_host[j];
     p->bank_row[j] = c.bank_row[j];
   }
@@ -403,10 +440,14 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_free[b], cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_restore, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->ts2, cudaStreamNonBlocking);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pick_buffers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kPickMaxSlots * (int)sizeof(unsigned long long));
-  if (e == cudaSuccess) e = gemm_maps_create(&p->maps, c.pool, c.S, c.shared_w, c.L, c.H, c.I, p->h, p->xp, (int)P);
+  if (e == cudaSuccess)
+    e = gemm_maps_create(&p->maps, c.pool, c.S, c.shared_w, c.L, c.H, c.I, p->h, p->xp, (int)P, c.wtype, c.lay);
   if (e != cudaSuccess) {
     prefill_destroy(p);
     return e;
@@ -430,6 +471,12 @@ void prefill_destroy(PrefillState* p) {
     if (p->ev_free[b]) cudaEventDestroy(p->ev_free[b]);
   }
   if (p->ev_restore) cudaEventDestroy(p->ev_restore);
+  if (p->ts2) {
+    cudaStreamSynchronize(p->ts2);
+    cudaStreamDestroy(p->ts2);
+  }
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
   gemm_maps_destroy(p->maps);
   delete p;
 }
@@ -528,6 +575,7 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   d.h = p->h;
   d.rows = p->rows;
   d.error_word = &c.st->error_word;
+  set_weight_info(d, c);
   e = timed(5, [&]() -> cudaError_t {
     d.mt = p->I / 64;
     d.kb = p->H / 64;
@@ -644,7 +692,6 @@ cudaError_t prefill_layer_on_demand(PrefillState* p, const PrefillCtx& c, int la
   }
 
   // ---- waves
-  const size_t seg[3] = {p->lay.gate, p->lay.up, p->lay.down};
   const int n_waves = misses.empty() ? 1 : ((int)misses.size() + width - 1) / width;
   std::vector<int32_t> toff(n_ent + 1);
   for (int w = 0; w < n_waves; ++w) {
@@ -663,9 +710,10 @@ cudaError_t prefill_layer_on_demand(PrefillState* p, const PrefillCtx& c, int la
       in_wave[u - base] = 1;
       slot_of[u - base] = v;
       // after the previous wave's GEMMs (same stream), which read this slot
-      for (int j = 0; j < 3; ++j)
-        if ((e = cudaMemcpyAsync(p->pool + (size_t)v * p->lay.stride + seg[j], p->bank_host[j] + (size_t)u * p->bank_row[j],
-                                 p->bank_row[j], cudaMemcpyHostToDevice, c.cs)) != cudaSuccess)
+      for (int j = 0; j < p->n_banks; ++j)
+        if ((e = cudaMemcpyAsync(p->pool + (size_t)v * p->lay.stride + bank_offset(p->lay, j),
+                                 p->bank_host[j] + (size_t)u * p->bank_row[j], p->bank_row[j], cudaMemcpyHostToDevice,
+                                 c.cs)) != cudaSuccess)
           return e;
     }
     toff[0] = 0;
@@ -691,6 +739,7 @@ cudaError_t prefill_layer_on_demand(PrefillState* p, const PrefillCtx& c, int la
     d.h = p->h;
     d.rows = p->rows;
     d.error_word = &c.st->error_word;
+    set_weight_info(d, c);
     e = timed(5, [&]() -> cudaError_t {
       d.mt = p->I / 64;
       d.kb = p->H / 64;

@@ -21,7 +21,9 @@
 // issuing work, drains its outstanding copies (bounded) and frees TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
+#include "ft_dot.cuh"
 #include "ft_prefill.cuh"
 
 namespace ft {
@@ -31,12 +33,28 @@ constexpr int BM = 128, BK = 64, BN_MAX = 256, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_BYTES = BN_MAX * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+// FP8 / FP4 weights: each stage also holds the raw tile (BM rows x BK elements as stored),
+// which four dequantising warps turn into the BF16 A tile; three stages fit.
+constexpr int STAGES_Q = 3;
+constexpr int RAW_BYTES = BM * BK;         // FP8: 8 KB (FP4: half of it used)
+constexpr int STAGE_BYTES_Q = A_BYTES + B_BYTES + RAW_BYTES;
+constexpr int DQ_WARPS = 4;
 constexpr int EPI_COLS = 16;               // TMEM columns drained per step
 constexpr int STG_PITCH = EPI_COLS + 1;    // staging row pitch (floats), bank-conflict free
 constexpr int SB_BYTES = EPI_COLS * BM * 2;  // BF16 output tile of one epilogue step
 constexpr int EPI_HALF_BYTES = BM * STG_PITCH * 4 + SB_BYTES;
 constexpr int EPI_WARPS = 8;              // two epilogue warps per TMEM lane quarter
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int GEMM_THREADS_Q = GEMM_THREADS + 32 * DQ_WARPS;
+
+template <int WT>
+struct WCfg {
+  static constexpr bool q = WT != FT_W_BF16;                                  // decoded in shared memory
+  static constexpr int stages = q ? STAGES_Q : STAGES;
+  static constexpr int stage_bytes = q ? STAGE_BYTES_Q : STAGE_BYTES;
+  static constexpr int threads = q ? GEMM_THREADS_Q : GEMM_THREADS;
+  static constexpr int raw_row = WT == FT_W_FP8_E4M3_B128 ? BK : BK / 2;    // stored bytes of BK elements
+};
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -87,6 +105,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(map), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// 3-D TMA tile load (x innermost) completing on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
       : "memory");
 }
 
@@ -155,6 +183,46 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return (uint16_t)(b >> 16);
 }
 
+// Two decoded weights (as floats) times the scale, as a BF16 pair (element 0 low): one
+// rounding of the scaled product.
+__device__ __forceinline__ uint32_t scaled_bf16x2(float2 f, float sc) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 16 stored E4M3 codes (element 0 in the low byte) times sc -> 16 BF16 (two 16-byte pieces)
+__device__ __forceinline__ void e4m3x16_to_bf16(uint4 w, float sc, uint4& lo, uint4& hi) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    o[2 * q] = scaled_bf16x2(dot::e4m3x2_to_float2((uint16_t)(in[q] & 0xffffu)), sc);
+    o[2 * q + 1] = scaled_bf16x2(dot::e4m3x2_to_float2((uint16_t)(in[q] >> 16)), sc);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// 8 stored bytes of E2M1 codes (16 elements, element 2j in the low nibble of byte j) times sc
+// -> 16 BF16 (two 16-byte pieces)
+__device__ __forceinline__ void e2m1x16_to_bf16(uint32_t w0, uint32_t w1, float sc, uint4& lo, uint4& hi) {
+  const uint32_t in[2] = {w0, w1};
+  uint32_t o[8];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t h2 = dot::e2m1x2_to_f16x2((in[q] >> (8 * b)) & 0xffu);
+      o[4 * q + b] = scaled_bf16x2(__half22float2(*reinterpret_cast<const __half2*>(&h2)), sc);
+    }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__device__ __forceinline__ float e8m0_value(uint32_t code) {
+  return __uint_as_float(code ? code << 23 : 0x00400000u);
+}
+
 struct TileInfo {
   int e, m, nvalid, N, pbase;
 };
@@ -172,28 +240,33 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmDesc& d, int g) {
   return t;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+template <int MODE, int WT>
+__global__ void __launch_bounds__(WCfg<WT>::threads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAs,
                         const __grid_constant__ CUtensorMap tmB, const GemmDesc d) {
+  using C = WCfg<WT>;
+  constexpr int NST = C::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  // per epilogue half: FP32 staging [BM][STG_PITCH], then a BF16 output tile [EPI_COLS][BM]
-  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  // per stage: A tile (BF16, SW128) | B tile | raw weight tile (FP8 / FP4 only); then per
+  // epilogue half: FP32 staging [BM][STG_PITCH] and a BF16 output tile [EPI_COLS][BM]
+  uint8_t* epi = smem + NST * C::stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * EPI_HALF_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint64_t* done = bars + 2 * STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* full = bars;                 // TMA bytes landed (raw or A, and B)
+  uint64_t* empty = bars + NST;          // MMAs of the stage done
+  uint64_t* afull = bars + 2 * NST;      // A tile decoded (FP8 / FP4)
+  uint64_t* tfull = bars + 3 * NST;
+  uint64_t* tempty = bars + 3 * NST + 2;
+  uint64_t* done = bars + 3 * NST + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NST + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
+      mbar_init(smem_u32(afull + s), DQ_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(tfull + b), 1);
@@ -221,9 +294,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
-    int last_par[STAGES];
+    int last_par[NST];
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+    for (int s = 0; s < NST; ++s) last_par[s] = -1;
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
       const TileInfo t = decode_tile(d, g);
       if (t.nvalid <= 0) continue;
@@ -231,7 +304,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const CUtensorMap* mA = sh ? &tmAs : &tmA;
       const int wbase = sh ? d.layer : __ldg(d.buf_slots + t.e);
       int arow0, arow1 = 0;
-      if (MODE == 0) {
+      if (C::q) {  // 3-D maps: (byte within the row, row within the slot's bank, slot)
+        arow0 = MODE == 0 ? t.m * 64 : t.m * BM;
+        arow1 = arow0 + d.I;                // up rows follow the gate rows
+      } else if (MODE == 0) {
         arow0 = wbase * 3 * d.I + t.m * 64;  // gate rows
         arow1 = arow0 + d.I;                 // up rows
       } else {
@@ -245,23 +321,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           ok = false;
           break;
         }
-        const uint32_t a_dst = smem_base + stage * STAGE_BYTES, b_dst = a_dst + A_BYTES;
+        const uint32_t a_dst = smem_base + stage * C::stage_bytes, b_dst = a_dst + A_BYTES;
+        const uint32_t raw_dst = b_dst + B_BYTES;
         const uint32_t fb = smem_u32(full + stage);
         if (lane == 0) {
           // the token box is always BN_MAX rows (rows past the tile belong to the next entry
           // or lie beyond the buffer and are zero-filled; the epilogue ignores them)
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          if (MODE == 0) {
-            tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
-            tma_load_2d_hint(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb, pol_w);
+          if (C::q) {
+            mbar_arrive_expect_tx(fb, BM * C::raw_row + B_BYTES);
+            if (MODE == 0) {
+              tma_load_3d_hint(raw_dst, mA, kb * C::raw_row, arow0, wbase, fb, pol_w);
+              tma_load_3d_hint(raw_dst + 64 * C::raw_row, mA, kb * C::raw_row, arow1, wbase, fb, pol_w);
+            } else {
+              tma_load_3d_hint(raw_dst, mA, kb * C::raw_row, arow0, wbase, fb, pol_w);
+            }
           } else {
-            tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
+            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+            if (MODE == 0) {
+              tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
+              tma_load_2d_hint(a_dst + A_BYTES / 2, mA, kb * BK, arow1, fb, pol_w);
+            } else {
+              tma_load_2d_hint(a_dst, mA, kb * BK, arow0, fb, pol_w);
+            }
           }
           tma_load_2d_hint(b_dst, &tmB, kb * BK, t.pbase, fb, pol_x);
         }
         __syncwarp();
         last_par[stage] = (int)phase;
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1u;
         }
@@ -269,7 +356,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
     }
     if (*abort_flag && lane == 0) {  // drain copies still in flight before the CTA exits
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < NST; ++s)
         if (last_par[s] >= 0)
           for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(smem_u32(full + s), (uint32_t)last_par[s]); ++i) {
           }
@@ -288,17 +375,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_MAX);
         const uint32_t idesc = bf16_idesc(BM, t.N);
         for (int kb = 0; kb < d.kb; ++kb) {
-          if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, d.error_word)) {
+          // FP8 / FP4: the decoded tile (its warps waited for the TMA bytes, so B has landed too)
+          if (!mbar_wait(smem_u32((C::q ? afull : full) + stage), phase, abort_flag, d.error_word)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_base + stage * STAGE_BYTES, b_addr = a_addr + A_BYTES;
+          const uint32_t a_addr = smem_base + stage * C::stage_bytes, b_addr = a_addr + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(d_tmem, sw128_desc(a_addr + 32 * k), sw128_desc(b_addr + 32 * k), idesc, (kb | k) != 0);
           umma_commit(smem_u32(empty + stage));
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -316,7 +404,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + EPI_WARPS) {
     // --------------------------------------------------------------- epilogue
     const int half = (threadIdx.x - 64) >> 7;  // the two halves take alternate column steps
     const int et = (threadIdx.x - 64) & 127;   // 0..127 within the half
@@ -380,6 +468,87 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+  } else if (C::q) {
+    // ---------------------------------------------------------- weight decoding
+    // Thread r decodes row r of the A tile: each of its BK stored weights times the scale of
+    // its block (FP8: one FP32 scale per 1x128 block; NVFP4: E4M3 scale per 16 elements times
+    // the bank's FP32 tensor scale; MXFP4: E8M0 scale per 32 elements), rounded once to BF16
+    // and written in the 128-byte-swizzled K-major layout the MMA reads.
+    const int r = threadIdx.x - GEMM_THREADS;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+      const TileInfo t = decode_tile(d, g);
+      if (t.nvalid <= 0) continue;
+      const bool sh = t.e >= d.E;
+      const uint8_t* slot = sh ? d.shared_w + (size_t)d.layer * d.stride
+                               : d.pool + (size_t)__ldg(d.buf_slots + t.e) * d.stride;
+      const int K = MODE == 0 ? d.H : d.I;                      // reduction length of the row
+      const int row = MODE == 0 ? t.m * 64 + (r & 63) : t.m * BM + r;
+      const size_t soff = MODE == 0 ? (r < 64 ? d.off_gs : d.off_us) : d.off_ds;
+      const int bank = MODE == 0 ? (r < 64 ? 0 : 1) : 2;
+      const float tsc = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(slot + d.off_ts) + bank) : 1.f;
+      for (int kb = 0; kb < d.kb; ++kb) {
+        if (!mbar_wait(smem_u32(full + stage), phase, abort_flag, d.error_word)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = smem + stage * C::stage_bytes;
+        const uint4* src = reinterpret_cast<const uint4*>(st + A_BYTES + B_BYTES + r * C::raw_row);
+        uint8_t* arow = const_cast<uint8_t*>(st) + r * 128;
+        auto put = [&](int ch, uint4 v) { *reinterpret_cast<uint4*>(arow + ((ch ^ (r & 7)) << 4)) = v; };
+        if (WT == FT_W_FP8_E4M3_B128) {
+          const float sc = __ldg(reinterpret_cast<const float*>(slot + soff) + (size_t)row * (K / 128) + kb / 2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 lo, hi;
+            e4m3x16_to_bf16(src[q], sc, lo, hi);
+            put(2 * q, lo);
+            put(2 * q + 1, hi);
+          }
+        } else if (WT == FT_W_NVFP4) {
+          // four E4M3 block scales for the BK = 64 elements of this step
+          const uint32_t sc4 = __ldg(reinterpret_cast<const uint32_t*>(slot + soff + (size_t)row * (K / 16)) + kb);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint4 w = src[q];
+            const float2 s01 = dot::e4m3x2_to_float2((uint16_t)(q == 0 ? (sc4 & 0xffffu) : (sc4 >> 16)));
+            uint4 lo, hi;
+            e2m1x16_to_bf16(w.x, w.y, s01.x * tsc, lo, hi);
+            put(4 * q, lo);
+            put(4 * q + 1, hi);
+            e2m1x16_to_bf16(w.z, w.w, s01.y * tsc, lo, hi);
+            put(4 * q + 2, lo);
+            put(4 * q + 3, hi);
+          }
+        } else {
+          // two E8M0 block scales for the BK = 64 elements of this step
+          const uint32_t sc2 =
+              __ldg(reinterpret_cast<const uint16_t*>(slot + soff + (size_t)row * (K / 32)) + kb);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint4 w = src[q];
+            const float sc = e8m0_value(q == 0 ? (sc2 & 0xffu) : (sc2 >> 8));
+            uint4 lo, hi;
+            e2m1x16_to_bf16(w.x, w.y, sc, lo, hi);
+            put(4 * q, lo);
+            put(4 * q + 1, hi);
+            e2m1x16_to_bf16(w.z, w.w, sc, lo, hi);
+            put(4 * q + 2, lo);
+            put(4 * q + 3, hi);
+          }
+        }
+        // the MMA reads the tile through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(afull + stage));
+        if (++stage == NST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -421,7 +590,43 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-size_t gemm_smem_bytes() { return 1024 + STAGES * STAGE_BYTES + 2 * EPI_HALF_BYTES + 16 * 8 + 16; }
+// 3-D byte tensor (stored weights of one bank per slot): dims {row bytes, rows, slots},
+// unswizzled boxes {box_bytes, box_rows, 1}.
+cudaError_t make_map_raw3d(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
+                           uint64_t slot_stride, uint32_t box_bytes, uint32_t box_rows) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {row_bytes, rows, slots};
+  const cuuint64_t strides[2] = {row_bytes, slot_stride};
+  const cuuint32_t box[3] = {box_bytes, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int WT>
+size_t gemm_smem_bytes() {
+  return 1024 + WCfg<WT>::stages * WCfg<WT>::stage_bytes + 2 * EPI_HALF_BYTES + (3 * WCfg<WT>::stages + 5) * 8 + 16;
+}
+
+template <int WT>
+cudaError_t set_gemm_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<0, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemm_smem_bytes<WT>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<1, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm_smem_bytes<WT>());
+  return e;
+}
+
+template <int WT>
+void launch_t(int mode, const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b, const GemmDesc& d, int grid,
+              cudaStream_t s) {
+  if (mode == 0) grouped_gemm_kernel<0, WT><<<grid, WCfg<WT>::threads, gemm_smem_bytes<WT>(), s>>>(a, as, b, d);
+  else grouped_gemm_kernel<1, WT><<<grid, WCfg<WT>::threads, gemm_smem_bytes<WT>(), s>>>(a, as, b, d);
+}
 
 }  // namespace
 
@@ -430,30 +635,50 @@ struct GemmMaps {
   CUtensorMap a_dn, a_dn_sh;    // weight rows of width I (down)
   CUtensorMap h_map;            // h [P][I]
   CUtensorMap x_map;            // token rows in pair order [P][H]
-  int H, I;
-  bool attr_set = false;
+  int H, I, wtype;
 };
 
 cudaError_t gemm_maps_create(GemmMaps** out, const uint8_t* pool, int S, const uint8_t* shared_w, int L, int H,
-                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs) {
+                             int I, const uint16_t* h_buf, const uint16_t* xp_buf, int max_pairs, int wtype,
+                             const SlotLayout& lay) {
   GemmMaps* m = new GemmMaps();
   m->H = H;
   m->I = I;
-  // a slot is gate [I][H] | up [I][H] | down [H][I]: 3I rows of width H, or 3H rows of width I
-  cudaError_t e = make_map(&m->a_gu, pool, H, (uint64_t)S * 3 * I, (uint64_t)H * 2, BK, 64);
-  if (e == cudaSuccess) e = make_map(&m->a_dn, pool, I, (uint64_t)S * 3 * H, (uint64_t)I * 2, BK, BM);
+  m->wtype = wtype;
   const void* sh = shared_w ? (const void*)shared_w : (const void*)pool;
   const uint64_t sh_rows = shared_w ? (uint64_t)L : (uint64_t)S;
-  if (e == cudaSuccess) e = make_map(&m->a_gu_sh, sh, H, sh_rows * 3 * I, (uint64_t)H * 2, BK, 64);
-  if (e == cudaSuccess) e = make_map(&m->a_dn_sh, sh, I, sh_rows * 3 * H, (uint64_t)I * 2, BK, BM);
+  cudaError_t e = cudaSuccess;
+  if (wtype == FT_W_BF16) {
+    // a slot is gate [I][H] | up [I][H] | down [H][I]: 3I rows of width H, or 3H rows of width I
+    e = make_map(&m->a_gu, pool, H, (uint64_t)S * 3 * I, (uint64_t)H * 2, BK, 64);
+    if (e == cudaSuccess) e = make_map(&m->a_dn, pool, I, (uint64_t)S * 3 * H, (uint64_t)I * 2, BK, BM);
+    if (e == cudaSuccess) e = make_map(&m->a_gu_sh, sh, H, sh_rows * 3 * I, (uint64_t)H * 2, BK, 64);
+    if (e == cudaSuccess) e = make_map(&m->a_dn_sh, sh, I, sh_rows * 3 * H, (uint64_t)I * 2, BK, BM);
+  } else {
+    // stored weights, one 3-D map per bank kind: (byte in row, row, slot); gate and up rows
+    // are contiguous, so one map covers both (rows 0..2I-1)
+    const uint64_t div = wtype == FT_W_FP8_E4M3_B128 ? 1 : 2;  // elements per stored byte
+    const uint32_t raw = (uint32_t)(BK / div);
+    const uint8_t* shb = static_cast<const uint8_t*>(sh);
+    e = make_map_raw3d(&m->a_gu, pool + lay.gate, (uint64_t)H / div, 2 * (uint64_t)I, (uint64_t)S, lay.stride, raw,
+                       64);
+    if (e == cudaSuccess)
+      e = make_map_raw3d(&m->a_dn, pool + lay.down, (uint64_t)I / div, (uint64_t)H, (uint64_t)S, lay.stride, raw, BM);
+    if (e == cudaSuccess)
+      e = make_map_raw3d(&m->a_gu_sh, shb + lay.gate, (uint64_t)H / div, 2 * (uint64_t)I, sh_rows, lay.stride, raw,
+                         64);
+    if (e == cudaSuccess)
+      e = make_map_raw3d(&m->a_dn_sh, shb + lay.down, (uint64_t)I / div, (uint64_t)H, sh_rows, lay.stride, raw, BM);
+  }
   if (e == cudaSuccess) e = make_map(&m->h_map, h_buf, I, (uint64_t)max_pairs, (uint64_t)I * 2, BK, BN_MAX);
   if (e == cudaSuccess) e = make_map(&m->x_map, xp_buf, H, (uint64_t)max_pairs, (uint64_t)H * 2, BK, BN_MAX);
   if (e == cudaSuccess) {
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm_smem_bytes());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)gemm_smem_bytes());
+    switch (wtype) {
+      case FT_W_BF16: e = set_gemm_attrs<FT_W_BF16>(); break;
+      case FT_W_FP8_E4M3_B128: e = set_gemm_attrs<FT_W_FP8_E4M3_B128>(); break;
+      case FT_W_NVFP4: e = set_gemm_attrs<FT_W_NVFP4>(); break;
+      default: e = set_gemm_attrs<FT_W_MXFP4>(); break;
+    }
   }
   if (e != cudaSuccess) {
     delete m;
@@ -469,8 +694,15 @@ cudaError_t launch_grouped_gemm(int mode, const GemmMaps* m, const uint16_t* x, 
                                 cudaStream_t s) {
   (void)x;
   (void)T;
-  if (mode == 0) grouped_gemm_kernel<0><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_gu, m->a_gu_sh, m->x_map, d);
-  else grouped_gemm_kernel<1><<<grid, GEMM_THREADS, gemm_smem_bytes(), s>>>(m->a_dn, m->a_dn_sh, m->h_map, d);
+  const CUtensorMap& a = mode == 0 ? m->a_gu : m->a_dn;
+  const CUtensorMap& as = mode == 0 ? m->a_gu_sh : m->a_dn_sh;
+  const CUtensorMap& b = mode == 0 ? m->x_map : m->h_map;
+  switch (m->wtype) {
+    case FT_W_BF16: launch_t<FT_W_BF16>(mode, a, as, b, d, grid, s); break;
+    case FT_W_FP8_E4M3_B128: launch_t<FT_W_FP8_E4M3_B128>(mode, a, as, b, d, grid, s); break;
+    case FT_W_NVFP4: launch_t<FT_W_NVFP4>(mode, a, as, b, d, grid, s); break;
+    default: launch_t<FT_W_MXFP4>(mode, a, as, b, d, grid, s); break;
+  }
   return cudaGetLastError();
 }
 

@@ -259,7 +259,7 @@ def prefill_step(r: Run, chunk: int, layer: int, T: int, check_tokens=None, hidd
     out = out_d.cpu().numpy()
     tokens = range(T) if check_tokens is None else check_tokens
     ref = O.prefill_outputs(layer, sel, gates, xb, r.expert, w.n_experts, tokens=list(tokens),
-                            shared=r.shared_expert(layer))
+                            shared=r.shared_expert(layer), fp8=r.fp8)
     err = O.rel_err_rows(out[list(tokens)], ref)
     r.max_err = max(r.max_err, err)
     assert err <= OUT_TOL, f"prefill layer {layer}: relative error {err:.3e}"

@@ -157,3 +157,46 @@ def test_prefill_double_buffer_off_same_results():
             r.compare_state()
     for l in range(w.n_layers):
         np.testing.assert_array_equal(outs[True, l], outs[False, l])
+
+
+QUANT = [synth.W_FP8_E4M3_B128, synth.W_NVFP4, synth.W_MXFP4]
+
+
+@pytest.mark.parametrize("wtype", QUANT)
+def test_prefill_quantized_small_every_token_then_decode(wtype):
+    """FP8 / NVFP4 / MXFP4 experts through the prefill grouped GEMM: weights are decoded and
+    block-scaled into BF16 tiles in shared memory before the tensor-core product.  4 layers,
+    16 experts top-2, 200 tokens (ragged tiles), H 512, I 128, 40 slots; every output row
+    against the float64 oracle, residency after every layer; decode steps afterwards."""
+    w = synth.prefill().with_(wtype=wtype, n_layers=4, n_experts=16, top_k=2, hidden=512, inter=128,
+                              cache_slots=40, prefill_tokens=200)
+    with Run(w, max_prefill_tokens=256) as r:
+        for l in range(w.n_layers):
+            prefill_step(r, 0, l, 200)
+        r.w = w.with_(logits="normal")
+        for s in range(3):
+            for l in range(w.n_layers):
+                r.step(s, l, check_out=True)
+        r.compare_state()
+        print(f"wtype {wtype}: max rel err {r.max_err:.2e}")
+
+
+@pytest.mark.parametrize("wtype,T", [(synth.W_FP8_E4M3_B128, 8192), (synth.W_NVFP4, 1024)])
+def test_prefill_quantized_35b_expert_shape(wtype, T):
+    """The prefill chunk's expert shape (H 2048, I 512, 256 experts top-8, uniform logits)
+    with FP8 (the full 8192-token chunk, so routed experts take two N tiles) and NVFP4
+    experts, 2 layers; sampled rows include each two-tile expert's last token."""
+    import oracle as O
+
+    w = synth.prefill().with_(wtype=wtype, n_layers=2, cache_slots=700, prefill_tokens=T)
+    rng = np.random.default_rng(2)
+    with Run(w, max_prefill_tokens=T) as r:
+        for l in range(w.n_layers):
+            sel, _ = O.route(synth.prefill_logits(w, 0, l, T), w.top_k)
+            n_e = np.bincount(sel.reshape(-1), minlength=w.n_experts)
+            last = sorted({int(np.nonzero((sel == e).any(axis=1))[0].max()) for e in np.nonzero(n_e > 256)[0]})
+            pick = rng.choice(last, min(32, len(last)), replace=False).tolist() if last else []
+            tokens = sorted(set(pick) | {0, T - 1} | set(rng.choice(T, 16, replace=False).tolist()))
+            prefill_step(r, 0, l, T, check_tokens=tokens)
+        assert r.F.ft_moe_get_stats(r.h).error_word == 0
+        print(f"wtype {wtype} T {T}: max rel err {r.max_err:.2e}")
