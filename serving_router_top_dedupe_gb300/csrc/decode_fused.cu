@@ -126,19 +126,30 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
   // output row j0 + t % nj) are this CTA's output rows of every entry of the pass.
   __shared__ int s_pe[2][kMaxK + 2];
   __shared__ int s_np[2];
+  // the entries' weight bases, read once: the producer would otherwise wait on a global load
+  // before every copy it issues
+  __shared__ const uint8_t* s_gw[kMaxK + 2];
   const int j0 = (int)((long long)H * blockIdx.x / gridDim.x);
   const int nj = (int)((long long)H * (blockIdx.x + 1) / gridDim.x) - j0;
 
-  if (threadIdx.x == 0) {
+  __shared__ int s_fill[kMaxK + 2];
+  if (threadIdx.x < ne && threadIdx.x < kMaxK + 2) {  // one thread per entry: the loads overlap
+    s_fill[threadIdx.x] = p.g_fill[threadIdx.x];
+    s_gw[threadIdx.x] = p.g_w[threadIdx.x];
+  }
+  if (threadIdx.x == 32) {
     for (int s = 0; s < pl.nst; ++s) {
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), kConsumers);
     }
     *abort_flag = 0;
     mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
     int n[2] = {0, 0};
     for (int g = 0; g < ne && g < kMaxK + 2; ++g) {
-      const int ps = p.g_fill[g] != 0 ? 1 : 0;
+      const int ps = s_fill[g] != 0 ? 1 : 0;
       s_pe[ps][n[ps]++] = g;
     }
     s_np[0] = n[0];
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           if (!mbar_wait(smem_u32(empty + s), (uint32_t)(use & 1) ^ 1u, abort_flag, p.error_word)) break;
           meta[s] = make_int4(0, v, nr, pass);
           const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
-          const uint8_t* src = p.g_w[g] + p.lay.gate + (size_t)i * rh;
+          const uint8_t* src = s_gw[g] + p.lay.gate + (size_t)i * rh;
           mbar_arrive_expect_tx(fb, (uint32_t)(2 * nr * rh));
           bulk_g2s_hint(dst, src, (uint32_t)(nr * rh), fb, pol);
           bulk_g2s_hint(dst + (uint32_t)(nr * rh), src + (size_t)I * rh, (uint32_t)(nr * rh), fb, pol);
@@ -193,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           for (int tt = t; tt < t + nr;) {
             const int gi = tt / nj, jl = tt - gi * nj;
             const int seg = min(t + nr, (gi + 1) * nj) - tt;
-            bulk_g2s_hint(dst + off, p.g_w[pe[gi]] + p.lay.down + (size_t)(j0 + jl) * ri, (uint32_t)(seg * ri), fb,
+            bulk_g2s_hint(dst + off, s_gw[pe[gi]] + p.lay.down + (size_t)(j0 + jl) * ri, (uint32_t)(seg * ri), fb,
                           pol);
             off += (uint32_t)(seg * ri);
             tt += seg;
@@ -298,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
             // a chunk holds 32 elements: two NVFP4 blocks or one MXFP4 block, each block's dot
             // product taken first and multiplied by its scale (as in the batched kernels)
             const int sb = WT == FT_W_NVFP4 ? H / 16 : H / 32;  // scale bytes per row
-            const uint8_t* bg = p.g_w[g] + p.lay.gs + (size_t)i * sb;
-            const uint8_t* bu = p.g_w[g] + p.lay.us + (size_t)i * sb;
+            const uint8_t* bg = s_gw[g] + p.lay.gs + (size_t)i * sb;
+            const uint8_t* bu = s_gw[g] + p.lay.us + (size_t)i * sb;
             for (int c16 = lane; c16 < H / EPC; c16 += 32) {
               const uint4 x0 = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
               const uint4 x1 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 4 + (size_t)c16 * 8);
@@ -322,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
               }
             }
           } else {
-            const float* sg = reinterpret_cast<const float*>(p.g_w[g] + p.lay.gs) + (size_t)i * (H / 128);
-            const float* su = reinterpret_cast<const float*>(p.g_w[g] + p.lay.us) + (size_t)i * (H / 128);
+            const float* sg = reinterpret_cast<const float*>(s_gw[g] + p.lay.gs) + (size_t)i * (H / 128);
+            const float* su = reinterpret_cast<const float*>(s_gw[g] + p.lay.us) + (size_t)i * (H / 128);
             // H / 16 is a multiple of 32: every lane runs every step.  Each 1x128 block's dot
             // product is summed over its 8 lanes, then multiplied by the block's scale once.
 #pragma unroll 4
@@ -338,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           }
           const float xsc = WT == FT_W_BF16 ? 1.f : pow2i(xshift);
           // NVFP4: the banks' FP32 tensor scales multiply the finished sums
-          const float tsa = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts)) : 1.f;
-          const float tsb = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts) + 1) : 1.f;
+          const float tsa = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(s_gw[g] + p.lay.ts)) : 1.f;
+          const float tsb = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(s_gw[g] + p.lay.ts) + 1) : 1.f;
           const float ab2[2] = {(WT == FT_W_FP8_E4M3_B128 ? groups_sum(a) : warp_sum(a)) * xsc * tsa,
                                 (WT == FT_W_FP8_E4M3_B128 ? groups_sum(b) : warp_sum(b)) * xsc * tsb};
           if (lane == 0) p.h[(size_t)g * I + i] = silu_mul(ab2[0], ab2[1]);
@@ -458,10 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
             yi[r] = g * nj + jl;
             hv[r] = hs + (size_t)g * I;
             sc[r] = WT == FT_W_FP8_E4M3_B128
-                        ? reinterpret_cast<const float*>(p.g_w[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128)
+                        ? reinterpret_cast<const float*>(s_gw[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128)
                         : nullptr;
-            sb4[r] = kFP4 ? p.g_w[g] + p.lay.ds + (size_t)(j0 + jl) * (WT == FT_W_NVFP4 ? I / 16 : I / 32) : nullptr;
-            ts4[r] = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(p.g_w[g] + p.lay.ts) + 2) : 1.f;
+            sb4[r] = kFP4 ? s_gw[g] + p.lay.ds + (size_t)(j0 + jl) * (WT == FT_W_NVFP4 ? I / 16 : I / 32) : nullptr;
+            ts4[r] = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(s_gw[g] + p.lay.ts) + 2) : 1.f;
             acc[r] = 0.f;
           }
           if (WT == FT_W_BF16) {
