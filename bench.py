@@ -186,9 +186,11 @@ _OVERRIDE: dict = {}
 def _workload():
     import synth
 
-    w = synth.decode_bf16()
-    if _OVERRIDE.get("layers"):
-        w = w.with_(n_layers=_OVERRIDE["layers"], cache_slots=synth.capacity_slots(0.37, _OVERRIDE["layers"], 256))
+    w = synth.decode_fp8(batch=1) if _OVERRIDE.get("fp8") else synth.decode_bf16()
+    if _OVERRIDE.get("layers") or _OVERRIDE.get("experts"):
+        frac = w.cache_slots / w.n_logical
+        nl, ne = _OVERRIDE.get("layers") or w.n_layers, _OVERRIDE.get("experts") or w.n_experts
+        w = w.with_(n_layers=nl, n_experts=ne, cache_slots=synth.capacity_slots(frac, nl, ne))
     if _OVERRIDE.get("slots"):
         w = w.with_(cache_slots=_OVERRIDE["slots"])
     return w
@@ -206,11 +208,12 @@ def _expert_bytes(w) -> int:
 def _config_desc(w, args=None, warm=None) -> dict:
     import synth
 
-    reduced = _OVERRIDE.get("layers") or _OVERRIDE.get("slots")
+    reduced = _OVERRIDE.get("layers") or _OVERRIDE.get("slots") or _OVERRIDE.get("experts")
+    tag = " (reduced, profiling only)" if reduced else ""
     if w.wtype == synth.W_BF16:
-        name = "decode_bf16_35B-A3B-shape" + (" (reduced, profiling only)" if reduced else "")
+        name = "decode_bf16_35B-A3B-shape" + tag
     else:
-        name = "decode_fp8_large-expert"
+        name = "decode_fp8_large-expert" + tag
     d = {"workload": name, "n_layers": w.n_layers, "hidden": w.hidden,
          "expert_inter": w.inter, "n_experts": w.n_experts, "top_k": w.top_k, "shared_expert": w.has_shared,
          "weights": "bf16" if w.wtype == synth.W_BF16 else "fp8_e4m3 + fp32 scale per 1x128 block",
@@ -849,6 +852,9 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=0, help="profiling only: fewer tokens")
     ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer MoE layers")
     ap.add_argument("--slots", type=int, default=0, help="profiling only: other cache size")
+    ap.add_argument("--experts", type=int, default=0, help="profiling only: fewer routed experts per layer")
+    ap.add_argument("--fp8-headline", action="store_true",
+                    help="profiling only: the FP8 large-expert workload in place of the BF16 one")
     ap.add_argument("--sweep", action="store_true", help="time the batch x capacity x split grid instead")
     ap.add_argument("--sweep-layers", type=int, default=40)
     ap.add_argument("--sweep-steps", type=int, default=64)
@@ -856,7 +862,7 @@ def main():
     ap.add_argument("--sweep-batches", default="1,4,16,64")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    _OVERRIDE.update(layers=args.layers, slots=args.slots)
+    _OVERRIDE.update(layers=args.layers, slots=args.slots, experts=args.experts, fp8=args.fp8_headline)
     if args.oracle_child:
         _oracle_child(args)
         return

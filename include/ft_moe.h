@@ -248,10 +248,12 @@ ft_status ft_graph_destroy(ft_graph* g);
 
 /* One prefill layer of a chunk ([FT] "全层双缓冲"): a call that does not continue
  * the previous prefill layer starts a chunk and takes the 2E least recently used
- * slots as two full-layer buffers (host-synchronising once).  Layer l's experts are
- * in buffer (l - first) mod 2; the whole of layer l+1 is copied into the other
- * buffer with cudaMemcpyAsync on the transfer stream while layer l's routing and
- * grouped GEMM run on the compute stream.  All pairs run on the GPU.
+ * slots as two full-layer buffers (chosen on the device; the transfer stream waits for
+ * the choice).  Layer l's experts are in buffer (l - first) mod 2; the whole of layer
+ * l+1 is copied into the other buffer while layer l's routing and grouped GEMMs run on
+ * the compute stream: a copy kernel on the transfer stream (16 SMs) reads the mapped
+ * pinned banks over the host link, and the GEMMs take the other SMs meanwhile.  All
+ * pairs run on the GPU.
  * When the pool cannot hold two full layers (S < 2E), experts are loaded on demand
  * instead, after the layer's routing: the chunk's resident experts are hits, the
  * others go (ascending id) into the least recently used slots outside the hits, in

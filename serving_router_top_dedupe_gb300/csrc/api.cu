@@ -1122,6 +1122,7 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
   c.wtype = h->cfg.wtype;
   for (int j = 0; j < h->n_banks; ++j) {
     c.bank_host[j] = h->bank[j].host;
+    c.bank_dev[j] = static_cast<const uint8_t*>(h->bank[j].dev);
     c.bank_row[j] = h->bank[j].row;
   }
   c.prof = h->prof;

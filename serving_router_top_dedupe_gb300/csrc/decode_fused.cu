@@ -61,20 +61,35 @@ struct FusedPlan {
   int pairs;     // phase-0 (gate, up) row pairs per stage
   int drows;     // phase-1 down rows per stage
   int nst;       // ring stages
+  int sbh, sbi;  // block-scale bytes of an H row / an I row carried in the ring (0: read from HBM)
   size_t stage;  // bytes per stage
   size_t xs, hs, ybuf, cb;
 };
+
+// Block-scale bytes per row of H (or I) elements: FP32 per 128 (FP8), E4M3 per 16 (NVFP4),
+// E8M0 per 32 (MXFP4).
+__host__ __device__ inline int scale_row_bytes(int wtype, int n) {
+  return wtype == FT_W_FP8_E4M3_B128 ? n / 128 * 4 : (wtype == FT_W_NVFP4 ? n / 16 : (wtype == FT_W_MXFP4 ? n / 32 : 0));
+}
 
 __host__ __device__ inline FusedPlan make_fused_plan(int wtype, int H, int I, int max_entries, int n_cta) {
   // stored bytes per row: 2 per element (BF16), 1 (FP8), 1/2 (NVFP4, MXFP4)
   const size_t epc = wtype == FT_W_BF16 ? 8 : (wtype == FT_W_FP8_E4M3_B128 ? 16 : 32);  // elements per 16 B
   const size_t rh = (size_t)H / epc * 16, ri = (size_t)I / epc * 16;
   FusedPlan pl;
+  // The block scales of a stage's rows travel in the same stage (one bulk copy per run of
+  // rows), so the consumers read them from shared memory instead of waiting on HBM for them;
+  // that needs 16-byte multiples per row (bulk copies move 16-byte units).
+  const int sh = scale_row_bytes(wtype, H), si = scale_row_bytes(wtype, I);
+  const bool carry = sh > 0 && sh % 16 == 0 && si % 16 == 0;
+  pl.sbh = carry ? sh : 0;
+  pl.sbi = carry ? si : 0;
+  const size_t ph = rh + pl.sbh, pi = ri + pl.sbi;  // ring bytes per H row / per I row
   pl.stage = kStageTarget;
-  if (pl.stage < 2 * rh) pl.stage = 2 * rh;
-  if (pl.stage < ri) pl.stage = ri;
-  pl.pairs = (int)(pl.stage / (2 * rh));
-  pl.drows = (int)(pl.stage / ri);
+  if (pl.stage < 2 * ph) pl.stage = 2 * ph;
+  if (pl.stage < pi) pl.stage = pi;
+  pl.pairs = (int)(pl.stage / (2 * ph));
+  pl.drows = (int)(pl.stage / pi);
   pl.xs = round128((size_t)H * 2);
   pl.hs = round128((size_t)max_entries * I * 4);
   const int jpc = (H + n_cta - 1) / n_cta;
@@ -179,9 +194,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           meta[s] = make_int4(0, v, nr, pass);
           const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
           const uint8_t* src = s_gw[g] + p.lay.gate + (size_t)i * rh;
-          mbar_arrive_expect_tx(fb, (uint32_t)(2 * nr * rh));
+          mbar_arrive_expect_tx(fb, (uint32_t)(2 * nr * (rh + pl.sbh)));
           bulk_g2s_hint(dst, src, (uint32_t)(nr * rh), fb, pol);
           bulk_g2s_hint(dst + (uint32_t)(nr * rh), src + (size_t)I * rh, (uint32_t)(nr * rh), fb, pol);
+          if (pl.sbh) {  // gate scales, then up scales, behind the rows
+            const uint32_t sdst = dst + (uint32_t)(2 * nr * rh);
+            bulk_g2s_hint(sdst, s_gw[g] + p.lay.gs + (size_t)i * pl.sbh, (uint32_t)(nr * pl.sbh), fb, pol);
+            bulk_g2s_hint(sdst + (uint32_t)(nr * pl.sbh), s_gw[g] + p.lay.us + (size_t)i * pl.sbh,
+                          (uint32_t)(nr * pl.sbh), fb, pol);
+          }
           v += nr;
           ++c;
         }
@@ -198,14 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
           const int nr = min(p1_rows, n1 - t);
           meta[s] = make_int4(1, t, nr, pass);
           const uint32_t fb = smem_u32(full + s), dst = smem_u32(stages + (size_t)s * pl.stage);
-          mbar_arrive_expect_tx(fb, (uint32_t)(nr * ri));
-          // a stage may span entries: one bulk copy per entry segment (its rows are contiguous)
+          mbar_arrive_expect_tx(fb, (uint32_t)(nr * (ri + pl.sbi)));
+          // a stage may span entries: one bulk copy per entry segment (its rows are contiguous),
+          // and one for the segment's block scales behind all the stage's rows
           uint32_t off = 0;
           for (int tt = t; tt < t + nr;) {
             const int gi = tt / nj, jl = tt - gi * nj;
             const int seg = min(t + nr, (gi + 1) * nj) - tt;
             bulk_g2s_hint(dst + off, s_gw[pe[gi]] + p.lay.down + (size_t)(j0 + jl) * ri, (uint32_t)(seg * ri), fb,
                           pol);
+            if (pl.sbi)
+              bulk_g2s_hint(dst + (uint32_t)(nr * ri) + (uint32_t)((tt - t) * pl.sbi),
+                            s_gw[pe[gi]] + p.lay.ds + (size_t)(j0 + jl) * pl.sbi, (uint32_t)(seg * pl.sbi), fb, pol);
             off += (uint32_t)(seg * ri);
             tt += seg;
           }
@@ -309,8 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
             // a chunk holds 32 elements: two NVFP4 blocks or one MXFP4 block, each block's dot
             // product taken first and multiplied by its scale (as in the batched kernels)
             const int sb = WT == FT_W_NVFP4 ? H / 16 : H / 32;  // scale bytes per row
-            const uint8_t* bg = s_gw[g] + p.lay.gs + (size_t)i * sb;
-            const uint8_t* bu = s_gw[g] + p.lay.us + (size_t)i * sb;
+            // the stage's copy of the scales when the ring carries them (generic loads serve both)
+            const uint8_t* bg = pl.sbh ? st + (size_t)2 * m.z * rh + (size_t)q * sb : s_gw[g] + p.lay.gs + (size_t)i * sb;
+            const uint8_t* bu = pl.sbh ? st + (size_t)2 * m.z * rh + (size_t)(m.z + q) * sb
+                                       : s_gw[g] + p.lay.us + (size_t)i * sb;
             for (int c16 = lane; c16 < H / EPC; c16 += 32) {
               const uint4 x0 = *reinterpret_cast<const uint4*>(xs + (size_t)c16 * 8);
               const uint4 x1 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 4 + (size_t)c16 * 8);
@@ -319,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
               const uint4 wa = *reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16);
               const uint4 wb = *reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16);
               if (WT == FT_W_NVFP4) {
-                const float2 ga = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(bg) + c16));
-                const float2 gb = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(bu) + c16));
+                const float2 ga = e4m3x2_to_float2(reinterpret_cast<const uint16_t*>(bg)[c16]);
+                const float2 gb = e4m3x2_to_float2(reinterpret_cast<const uint16_t*>(bu)[c16]);
                 a = fmaf(dot16_e2m1_f16(wa.x, wa.y, x0, x1), ga.x, a);
                 a = fmaf(dot16_e2m1_f16(wa.z, wa.w, x2, x3), ga.y, a);
                 b = fmaf(dot16_e2m1_f16(wb.x, wb.y, x0, x1), gb.x, b);
@@ -328,13 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
               } else {
                 const float da = dot16_e2m1_f16(wa.x, wa.y, x0, x1) + dot16_e2m1_f16(wa.z, wa.w, x2, x3);
                 const float db = dot16_e2m1_f16(wb.x, wb.y, x0, x1) + dot16_e2m1_f16(wb.z, wb.w, x2, x3);
-                a = fmaf(da, e8m0_float(__ldg(bg + c16)), a);
-                b = fmaf(db, e8m0_float(__ldg(bu + c16)), b);
+                a = fmaf(da, e8m0_float(bg[c16]), a);
+                b = fmaf(db, e8m0_float(bu[c16]), b);
               }
             }
           } else {
-            const float* sg = reinterpret_cast<const float*>(s_gw[g] + p.lay.gs) + (size_t)i * (H / 128);
-            const float* su = reinterpret_cast<const float*>(s_gw[g] + p.lay.us) + (size_t)i * (H / 128);
+            const float* sg = pl.sbh ? reinterpret_cast<const float*>(st + (size_t)2 * m.z * rh) + (size_t)q * (H / 128)
+                                     : reinterpret_cast<const float*>(s_gw[g] + p.lay.gs) + (size_t)i * (H / 128);
+            const float* su = pl.sbh
+                                  ? reinterpret_cast<const float*>(st + (size_t)2 * m.z * rh) + (size_t)(m.z + q) * (H / 128)
+                                  : reinterpret_cast<const float*>(s_gw[g] + p.lay.us) + (size_t)i * (H / 128);
             // H / 16 is a multiple of 32: every lane runs every step.  Each 1x128 block's dot
             // product is summed over its 8 lanes, then multiplied by the block's scale once.
 #pragma unroll 4
@@ -343,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
               const uint4 x1 = *reinterpret_cast<const uint4*>(xs + (size_t)H / 2 + (size_t)c16 * 8);
               const float da = group8_sum(dot_e4m3_f16(*reinterpret_cast<const uint4*>(rg + (size_t)c16 * 16), x0, x1));
               const float db = group8_sum(dot_e4m3_f16(*reinterpret_cast<const uint4*>(ru + (size_t)c16 * 16), x0, x1));
-              a = fmaf(da, __ldg(sg + c16 / 8), a);
-              b = fmaf(db, __ldg(su + c16 / 8), b);
+              a = fmaf(da, sg[c16 / 8], a);
+              b = fmaf(db, su[c16 / 8], b);
             }
           }
           const float xsc = WT == FT_W_BF16 ? 1.f : pow2i(xshift);
@@ -468,10 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
             const int t = m.y + (ok[r] ? qq : q), gi = t / nj, jl = t - gi * nj, g = pe[gi];
             yi[r] = g * nj + jl;
             hv[r] = hs + (size_t)g * I;
-            sc[r] = WT == FT_W_FP8_E4M3_B128
-                        ? reinterpret_cast<const float*>(s_gw[g] + p.lay.ds) + (size_t)(j0 + jl) * (I / 128)
-                        : nullptr;
-            sb4[r] = kFP4 ? s_gw[g] + p.lay.ds + (size_t)(j0 + jl) * (WT == FT_W_NVFP4 ? I / 16 : I / 32) : nullptr;
+            // block scales: the stage's copy when the ring carries them, else the slot's
+            const uint8_t* sbase = pl.sbi ? st + (size_t)m.z * ri + (size_t)(ok[r] ? qq : q) * pl.sbi
+                                          : s_gw[g] + p.lay.ds + (size_t)(j0 + jl) * scale_row_bytes(WT, I);
+            sc[r] = WT == FT_W_FP8_E4M3_B128 ? reinterpret_cast<const float*>(sbase) : nullptr;
+            sb4[r] = kFP4 ? sbase : nullptr;
             ts4[r] = WT == FT_W_NVFP4 ? __ldg(reinterpret_cast<const float*>(s_gw[g] + p.lay.ts) + 2) : 1.f;
             acc[r] = 0.f;
           }
@@ -499,12 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
 #pragma unroll
                 for (int q = 0; q < 8; ++q) *reinterpret_cast<float4*>(hv32 + 4 * q) = h4[(size_t)q * (I / EPC) + c16];
                 if (WT == FT_W_NVFP4) {
-                  const float2 sd = e4m3x2_to_float2(__ldg(reinterpret_cast<const uint16_t*>(sb4[r]) + c16));
+                  const float2 sd = e4m3x2_to_float2(reinterpret_cast<const uint16_t*>(sb4[r])[c16]);
                   acc[r] = fmaf(dot16_e2m1_f32(wv.x, wv.y, hv32), sd.x, acc[r]);
                   acc[r] = fmaf(dot16_e2m1_f32(wv.z, wv.w, hv32 + 16), sd.y, acc[r]);
                 } else {
                   const float d = dot16_e2m1_f32(wv.x, wv.y, hv32) + dot16_e2m1_f32(wv.z, wv.w, hv32 + 16);
-                  acc[r] = fmaf(d, e8m0_float(__ldg(sb4[r] + c16)), acc[r]);
+                  acc[r] = fmaf(d, e8m0_float(sb4[r][c16]), acc[r]);
                 }
               }
             }
@@ -525,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_gemv_kernel(EvalParams p, F
                       *reinterpret_cast<const uint4*>(st + (size_t)(q + r * kConsumers) * ri + (size_t)c16 * 16), hq);
                 }
                 d = group8_sum(d);
-                if (cv) acc[r] = fmaf(d, __ldg(sc[r] + c16 / 8), acc[r]);
+                if (cv) acc[r] = fmaf(d, sc[r][c16 / 8], acc[r]);
               }
             }
           }

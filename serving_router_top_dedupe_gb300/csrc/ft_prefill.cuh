@@ -20,6 +20,7 @@ struct PrefillCtx {
   uint32_t* stamp;
   DevState* st;
   const uint8_t* bank_host[7];  // host banks (pinned): gate, up, down, then the scale banks
+  const uint8_t* bank_dev[7];   // the same banks as the device addresses them (mapped)
   size_t bank_row[7];           // bytes per logical id in each bank
   int n_banks;
   int wtype;                    // ft_wtype of the experts

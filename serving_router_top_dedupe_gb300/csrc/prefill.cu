@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <cstring>
 
+#include "ft_dot.cuh"
 #include "ft_prefill.cuh"
 #include "ft_route.cuh"
 
@@ -22,7 +23,65 @@ namespace {
 
 constexpr int kPickThreads = 1024;
 constexpr int kPickMaxSlots = 16384;  // slots sorted in shared memory when a chunk starts
-constexpr int kTileN = 256;
+constexpr int kTileN = 256;  // token rows of one grouped-GEMM tile at most
+
+// Layer copy: SM loads of the mapped host banks.  One CTA step moves a 64 KB piece of one
+// expert's bank (512 threads x 8 loads of 16 bytes in flight).  16 CTAs already hold the host
+// link at its read rate (~200 GB/s for SM loads; the copy engine managed 110-150 GB/s on the
+// scattered 2 MB pieces of a layer); each reserves enough shared memory that no grouped-GEMM
+// CTA shares its SM, and the GEMMs run on the other SMs meanwhile.
+constexpr int kCopySms = 16;
+constexpr int kCopyThreads = 512;
+constexpr int kCopyUnroll = 8;
+constexpr size_t kCopyPiece = (size_t)kCopyThreads * kCopyUnroll * 16;
+constexpr size_t kCopySmemReserve = 120 * 1024;
+
+struct LayerCopyArgs {
+  const uint8_t* src[7];  // device view of the host banks
+  size_t row[7];          // bytes per logical id in bank j (a multiple of 16)
+  size_t off[7];          // byte offset of bank j within a slot
+  uint32_t pieces[7];     // 64 KB pieces per expert in bank j
+  uint32_t per_expert;    // sum of pieces[]
+  int n_banks, E, layer;
+  const int32_t* slots;   // [E] destination slot of each expert of the layer
+  uint8_t* pool;
+  size_t stride;
+};
+
+__global__ void __launch_bounds__(kCopyThreads) layer_copy_kernel(const LayerCopyArgs a) {
+  const size_t total = (size_t)a.E * a.per_expert;
+  for (size_t c = blockIdx.x; c < total; c += gridDim.x) {
+    const int e = (int)(c / a.per_expert);
+    uint32_t r = (uint32_t)(c - (size_t)e * a.per_expert);
+    const uint8_t* sb = a.src[0];
+    size_t row = a.row[0], off = a.off[0];
+    uint32_t np = a.pieces[0];
+#pragma unroll
+    for (int j = 1; j < 7; ++j)
+      if (r >= np && j < a.n_banks) {
+        r -= np;
+        sb = a.src[j];
+        row = a.row[j];
+        off = a.off[j];
+        np = a.pieces[j];
+      }
+    const size_t lo = (size_t)r * kCopyPiece;
+    const size_t n16 = (row - lo < kCopyPiece ? row - lo : kCopyPiece) / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(sb + ((size_t)a.layer * a.E + e) * row + lo);
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + (size_t)__ldg(a.slots + e) * a.stride + off + lo);
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const size_t i = threadIdx.x + (size_t)u * kCopyThreads;
+      if (i < n16) v[u] = dot::ld_host(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const size_t i = threadIdx.x + (size_t)u * kCopyThreads;
+      if (i < n16) dst[i] = v[u];
+    }
+  }
+}
 
 // Sorts all slots by (stamp, slot) in shared memory (bitonic), writes the 2E least
 // recently used to out[] in order and evicts their occupants.
@@ -271,7 +330,7 @@ struct PrefillState {
   int T_max = 0, E = 0, K = 0, H = 0, I = 0, L = 0, S = 0, W = 0, has_shared = 0, n_sm = 0;
   // routing and GEMM buffers
   int32_t *sel = nullptr, *wpre = nullptr, *entry_off = nullptr, *tile_off = nullptr;
-  int32_t *pair_tok = nullptr, *pos_of = nullptr, *buf_dev = nullptr, *pick_dev = nullptr, *pick_host = nullptr;
+  int32_t *pair_tok = nullptr, *pos_of = nullptr, *buf_dev = nullptr, *pick_dev = nullptr;
   float *gates = nullptr, *pair_gate = nullptr;
   uint32_t* masks = nullptr;
   uint16_t *h = nullptr, *rows = nullptr, *xp = nullptr;
@@ -280,18 +339,15 @@ struct PrefillState {
   // chunk state (host)
   bool active = false;
   int first = 0, next_layer = -1, pending = -1;
-  std::vector<int> buf[2];
   cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr}, ev_restore = nullptr;
+  cudaEvent_t ev_pick = nullptr;  // the chunk's buffer slots are in buf_dev (the copies read them)
   bool free_recorded[2] = {false, false};
   cudaStream_t cs = nullptr, ts = nullptr;
-  // a second transfer stream of the library's own: a layer's copies alternate between the two,
-  // so one copy engine's per-copy gaps are covered by the other's copy
-  cudaStream_t ts2 = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // what a restore copy needs
   uint8_t* pool = nullptr;
   SlotLayout lay{};
   const uint8_t* bank_host[7] = {};
+  const uint8_t* bank_dev[7] = {};
   size_t bank_row[7] = {};
   int n_banks = 3;
   int wtype = FT_W_BF16;
@@ -320,32 +376,26 @@ void set_weight_info(GemmDesc& d, const PrefillCtx& c) {
   d.off_ts = c.lay.ts;
 }
 
-// Copy every expert of `layer` from the host banks into the slots `slots`, ordered after
-// the work already on ts and completed in ts's order.  Runs of consecutive slots become one
-// 2-D copy per bank; the copies alternate between ts and the state's second transfer
-// stream, which joins ts at the end.
-cudaError_t copy_layer(PrefillState* p, int layer, const std::vector<int>& slots, cudaStream_t ts) {
-  const int E = p->E;
-  cudaError_t err;
-  if ((err = cudaEventRecord(p->ev_fork, ts)) != cudaSuccess || (err = cudaStreamWaitEvent(p->ts2, p->ev_fork, 0)))
-    return err;
-  int e = 0, n = 0;
-  while (e < E) {
-    int run = 1;
-    while (e + run < E && slots[e + run] == slots[e] + run) ++run;
-    for (int j = 0; j < p->n_banks; ++j, ++n) {
-      const uint8_t* src = p->bank_host[j] + ((size_t)layer * E + e) * p->bank_row[j];
-      uint8_t* dst = p->pool + (size_t)slots[e] * p->lay.stride + bank_offset(p->lay, j);
-      cudaStream_t s = (n & 1) ? p->ts2 : ts;
-      err = run == 1 ? cudaMemcpyAsync(dst, src, p->bank_row[j], cudaMemcpyHostToDevice, s)
-                     : cudaMemcpy2DAsync(dst, p->lay.stride, src, p->bank_row[j], p->bank_row[j], run,
-                                         cudaMemcpyHostToDevice, s);
-      if (err != cudaSuccess) return err;
-    }
-    e += run;
+// Copy every expert of `layer` from the host banks into the slots of buffer b (slot ids in
+// buf_dev), ordered after the work already on ts and completed in ts's order.
+cudaError_t copy_layer(PrefillState* p, int layer, int b, cudaStream_t ts) {
+  LayerCopyArgs a{};
+  a.per_expert = 0;
+  for (int j = 0; j < p->n_banks; ++j) {
+    a.src[j] = p->bank_dev[j];
+    a.row[j] = p->bank_row[j];
+    a.off[j] = bank_offset(p->lay, j);
+    a.pieces[j] = (uint32_t)((p->bank_row[j] + kCopyPiece - 1) / kCopyPiece);
+    a.per_expert += a.pieces[j];
   }
-  if ((err = cudaEventRecord(p->ev_join, p->ts2)) != cudaSuccess) return err;
-  return cudaStreamWaitEvent(ts, p->ev_join, 0);
+  a.n_banks = p->n_banks;
+  a.E = p->E;
+  a.layer = layer;
+  a.slots = p->buf_dev + (size_t)b * p->E;
+  a.pool = p->pool;
+  a.stride = p->lay.stride;
+  layer_copy_kernel<<<kCopySms, kCopyThreads, kCopySmemReserve, ts>>>(a);
+  return cudaGetLastError();
 }
 
 // Enqueue the load of `layer` into buffer b on the transfer stream, after the compute
@@ -359,7 +409,7 @@ cudaError_t load_buffer(PrefillState* p, int layer, int b, ProfEvents* prof) {
     cudaEventCreate(&z);
     cudaEventRecord(a, p->ts);
   }
-  if ((e = copy_layer(p, layer, p->buf[b], p->ts)) != cudaSuccess) return e;
+  if ((e = copy_layer(p, layer, b, p->ts)) != cudaSuccess) return e;
   if (prof) {
     cudaEventRecord(z, p->ts);
     prof->push_back({7, {a, z}});
@@ -415,6 +465,7 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   p->wtype = c.wtype;
   for (int j = 0; j < c.n_banks; ++j) {
     p->bank_host[j] = c.bank_host[j];
+    p->bank_dev[j] = c.bank_dev[j];
     p->bank_row[j] = c.bank_row[j];
   }
   const size_t T = c.max_tokens, k = c.K, P = T * k + (c.has_shared ? T : 0);
@@ -434,15 +485,14 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   if (e == cudaSuccess) e = dev_alloc(&p->rows, P * c.H);
   if (e == cudaSuccess) e = dev_alloc(&p->buf_dev, (size_t)2 * c.E);
   if (e == cudaSuccess) e = dev_alloc(&p->pick_dev, (size_t)2 * c.E);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->pick_host), sizeof(int32_t) * 2 * c.E, 0);
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
     e = cudaEventCreateWithFlags(&p->ev_loaded[b], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_free[b], cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_restore, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->ts2, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pick, cudaEventDisableTiming);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(layer_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCopySmemReserve);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pick_buffers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kPickMaxSlots * (int)sizeof(unsigned long long));
@@ -465,18 +515,12 @@ void prefill_destroy(PrefillState* p) {
                   p->pair_gate, p->pos_of, p->h, p->rows, p->xp, p->tiles, p->buf_dev, p->pick_dev};
   for (void* b : bufs)
     if (b) cudaFree(b);
-  if (p->pick_host) cudaFreeHost(p->pick_host);
   for (int b = 0; b < 2; ++b) {
     if (p->ev_loaded[b]) cudaEventDestroy(p->ev_loaded[b]);
     if (p->ev_free[b]) cudaEventDestroy(p->ev_free[b]);
   }
   if (p->ev_restore) cudaEventDestroy(p->ev_restore);
-  if (p->ts2) {
-    cudaStreamSynchronize(p->ts2);
-    cudaStreamDestroy(p->ts2);
-  }
-  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
-  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  if (p->ev_pick) cudaEventDestroy(p->ev_pick);
   gemm_maps_destroy(p->maps);
   delete p;
 }
@@ -489,7 +533,7 @@ void prefill_interrupt(PrefillState* p) {
     const int b = (p->pending - p->first) & 1;
     const int back = p->pending - 2;
     if (back >= p->first) {
-      copy_layer(p, back, p->buf[b], p->ts);
+      copy_layer(p, back, b, p->ts);
     }
     cudaEventRecord(p->ev_restore, p->ts);
     cudaStreamWaitEvent(p->cs, p->ev_restore, 0);
@@ -527,14 +571,9 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
         c.res, c.owner, c.stamp, c.S, 2 * E, p->pick_dev);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaMemcpyAsync(p->buf_dev, p->pick_dev, sizeof(int32_t) * 2 * E, cudaMemcpyDeviceToDevice, c.cs)) !=
-        cudaSuccess)
+            cudaSuccess ||
+        (e = cudaEventRecord(p->ev_pick, c.cs)) != cudaSuccess || (e = cudaStreamWaitEvent(c.ts, p->ev_pick, 0)))
       return e;
-    if ((e = cudaMemcpyAsync(p->pick_host, p->pick_dev, sizeof(int32_t) * 2 * E, cudaMemcpyDeviceToHost, c.cs)) !=
-        cudaSuccess)
-      return e;
-    if ((e = cudaStreamSynchronize(c.cs)) != cudaSuccess) return e;
-    p->buf[0].assign(p->pick_host, p->pick_host + E);
-    p->buf[1].assign(p->pick_host + E, p->pick_host + 2 * E);
     p->active = true;
     p->first = layer;
     p->pending = -1;
@@ -576,16 +615,18 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   d.rows = p->rows;
   d.error_word = &c.st->error_word;
   set_weight_info(d, c);
+  // while the next layer's copy runs, its CTAs hold kCopySms SMs: the GEMMs take the others
+  const int grid = p->pending == layer + 1 ? std::max(1, p->n_sm - kCopySms) : p->n_sm;
   e = timed(5, [&]() -> cudaError_t {
     d.mt = p->I / 64;
     d.kb = p->H / 64;
-    return launch_grouped_gemm(0, p->maps, x, T, d, p->n_sm, c.cs);
+    return launch_grouped_gemm(0, p->maps, x, T, d, grid, c.cs);
   });
   if (e == cudaSuccess)
     e = timed(8, [&]() -> cudaError_t {
       d.mt = p->H / 128;
       d.kb = p->I / 64;
-      return launch_grouped_gemm(1, p->maps, x, T, d, p->n_sm, c.cs);
+      return launch_grouped_gemm(1, p->maps, x, T, d, grid, c.cs);
     });
   if (e != cudaSuccess) {
     if (err) *err = "grouped GEMM launch";
