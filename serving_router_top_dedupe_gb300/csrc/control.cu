@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ int s_miss[kMaxE];
   __shared__ int s_gidx[kMaxE];
   __shared__ int s_victims[kMaxE];
+  __shared__ int s_cand[kTour];                // LRU candidates taken before the dependency wait
   __shared__ int s_res[kMaxE];                 // res[] of this layer's experts
   __shared__ unsigned long long s_tok[kMaxE];  // tokens routed to each expert of this layer
   __shared__ int s_goff[kMaxE + 1];
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ uint32_t s_wsum[kWarps + 1];
   __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_err, s_clock, s_lo, s_hi;
-  __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand, s_kk, s_done;
+  __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand, s_kk, s_done, s_npre;
   __shared__ unsigned long long s_prefix;
   extern __shared__ unsigned long long s_dyn[];
   unsigned long long* s_vkeys = s_dyn;                              // [kMaxE]
@@ -142,6 +143,89 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     s_hi = 0;
     s_ncand = 0;
     s_done = 0;
+  }
+  const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
+  // Small K (batch 1-2): the `want` (<= kTour) smallest keys (stamp << sbits | slot) over the
+  // slots with stamp < clock, ascending, into out[]; returns how many (fewer when fewer
+  // slots qualify), or -1 when the gather overflows its buffer (the radix select then
+  // runs).  Each thread's smallest key is found in one scan; the want-th smallest of those
+  // per-thread minima bounds the want-th smallest key overall, since they are distinct
+  // keys.  A warp tournament over the minima finds that bound T, a second scan gathers every
+  // key <= T, and rank counting orders them.  Every thread calls it.
+  auto small_k_select = [&](int want, int* out) -> int {
+    const uint32_t clk = s_clock;
+    const int nit = S > tid ? (S - tid + kThreads - 1) / kThreads : 0;  // slots tid + j*kThreads
+    unsigned long long mk = ~0ull;
+    for (int j = 0; j < nit; ++j) {
+      const int sl = tid + j * kThreads;
+      const uint32_t st = s_stamp[sl];
+      const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
+      if (st < clk && key < mk) mk = key;
+    }
+    int r = 0;
+    for (; r < want; ++r) {  // this warp's `want` smallest minima, ascending
+      const unsigned long long win = warp_min_u64(mk);
+      if (win == ~0ull) break;
+      if (mk == win) mk = ~0ull;
+      if (lane == 0) s_vkeys[warp * kTour + r] = win;
+    }
+    if (lane == 0) s_wcnt[warp] = r;
+    if (tid == 0) s_nv = 0;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t taken = 0;
+      unsigned long long kth = ~0ull - 1ull;  // fewer than `want` minima: every key qualifies
+      for (int n = 0; n < want; ++n) {
+        unsigned long long m2 = ~0ull;
+        int mj = 0;
+        for (int j = 0; j < kWarps * kTour / 32; ++j) {
+          const int it = lane + 32 * j, w = it / kTour, rr = it - w * kTour;
+          if (rr < s_wcnt[w] && !((taken >> j) & 1u) && s_vkeys[it] < m2) {
+            m2 = s_vkeys[it];
+            mj = j;
+          }
+        }
+        const unsigned long long win = warp_min_u64(m2);
+        if (win == ~0ull) break;
+        if (m2 == win) taken |= 1u << mj;
+        if (n == want - 1) kth = win;
+      }
+      if (lane == 0) s_prefix = kth;
+    }
+    __syncthreads();
+    const unsigned long long bound = s_prefix;
+    for (int j = 0; j < nit; ++j) {
+      const int sl = tid + j * kThreads;
+      const uint32_t st = s_stamp[sl];
+      const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
+      if (st < clk && key <= bound) {
+        const int i = atomicAdd(&s_nv, 1);
+        if (i < kMaxE) s_vkeys[i] = key;
+      }
+    }
+    __syncthreads();
+    const int nc = s_nv;
+    if (nc > kMaxE) return -1;
+    const unsigned long long smask = (1ull << sbits) - 1ull;
+    for (int i = tid; i < nc; i += kThreads) {
+      const unsigned long long ki = s_vkeys[i];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += s_vkeys[j] < ki;
+      if (rank < want) out[rank] = (int)(ki & smask);
+    }
+    return min(nc, want);
+  };
+  // Victim candidates before the wait (the slot stamps are final: only the previous control
+  // kernel writes them, and this kernel's own hits come later).  Hits of this step can
+  // remove at most kcap of them, so the 2*kcap least recently used slots always hold the
+  // kcap victims; after the wait only the hits are filtered out.  This takes the victim
+  // scan off the step's critical path, while the previous layer's evaluation still runs
+  // (launched as a programmatic dependent; otherwise nothing runs beside the prologue).
+  if (tid == 0) s_npre = -1;
+  if (p.pdl && in_smem && 2 * p.kcap <= kTour) {
+    __syncthreads();  // stamps staged, s_clock set
+    const int n = small_k_select(2 * p.kcap, s_cand);
+    if (tid == 0) s_npre = n;
   }
   // The logits may be written by the kernel right before this one, so they are read only
   // after the wait; an L2 prefetch of their lines now is safe (the L2 is coherent and a
@@ -224,77 +308,26 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   const int kcap = p.kcap;
   // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
   if (q > 0) {
-    const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
     bool picked = false;
-    if (in_smem && kcap <= kTour) {
-      // Small K (batch 1-2).  Each thread's smallest key (stamp, slot) is found in one scan;
-      // the K-th smallest of those per-thread minima bounds the K-th smallest key overall,
-      // since they are K distinct keys.  A warp tournament over the minima finds that bound
-      // T, a second scan gathers every key <= T, and rank counting orders them.  A rare
-      // gather larger than the key buffer falls through to the radix select.
-      const int nit = S > tid ? (S - tid + kThreads - 1) / kThreads : 0;  // slots tid + j*kThreads
-      unsigned long long mk = ~0ull;
-      for (int j = 0; j < nit; ++j) {
-        const int sl = tid + j * kThreads;
-        const uint32_t st = s_stamp[sl];
-        const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
-        if (st < clock && key < mk) mk = key;
-      }
-      int r = 0;
-      for (; r < kcap; ++r) {  // this warp's K smallest minima, ascending
-        const unsigned long long win = warp_min_u64(mk);
-        if (win == ~0ull) break;
-        if (mk == win) mk = ~0ull;
-        if (lane == 0) s_vkeys[warp * kTour + r] = win;
-      }
-      if (lane == 0) s_wcnt[warp] = r;
-      if (tid == 0) s_nv = 0;
-      __syncthreads();
+    if (s_npre >= 0) {
+      // candidates taken before the wait, minus this step's hits (now stamped with clock)
       if (warp == 0) {
-        uint32_t taken = 0;
-        unsigned long long kth = ~0ull - 1ull;  // fewer than K minima: every key qualifies
-        for (int n = 0; n < kcap; ++n) {
-          unsigned long long m2 = ~0ull;
-          int mj = 0;
-          for (int j = 0; j < kWarps * kTour / 32; ++j) {
-            const int it = lane + 32 * j, w = it / kTour, rr = it - w * kTour;
-            if (rr < s_wcnt[w] && !((taken >> j) & 1u) && s_vkeys[it] < m2) {
-              m2 = s_vkeys[it];
-              mj = j;
-            }
-          }
-          const unsigned long long win = warp_min_u64(m2);
-          if (win == ~0ull) break;
-          if (m2 == win) taken |= 1u << mj;
-          if (n == kcap - 1) kth = win;
-        }
-        if (lane == 0) s_prefix = kth;
+        const int v = lane < s_npre ? s_cand[lane] : -1;
+        const bool ok = v >= 0 && s_stamp[v] < clock;
+        const uint32_t okb = __ballot_sync(0xffffffffu, ok);
+        const int rank = __popc(okb & ((1u << lane) - 1u));
+        if (ok && rank < kcap) s_victims[rank] = v;
+        if (lane == 0) s_nv = min(__popc(okb), kcap);
       }
+      picked = true;
       __syncthreads();
-      const unsigned long long bound = s_prefix;
-      for (int j = 0; j < nit; ++j) {
-        const int sl = tid + j * kThreads;
-        const uint32_t st = s_stamp[sl];
-        const unsigned long long key = ((unsigned long long)st << sbits) | (unsigned)sl;
-        if (st < clock && key <= bound) {
-          const int i = atomicAdd(&s_nv, 1);
-          if (i < kMaxE) s_vkeys[i] = key;
-        }
-      }
-      __syncthreads();
-      const int nc = s_nv;
-      if (nc <= kMaxE) {
-        const unsigned long long smask = (1ull << sbits) - 1ull;
-        for (int i = tid; i < nc; i += kThreads) {
-          const unsigned long long ki = s_vkeys[i];
-          int rank = 0;
-          for (int j = 0; j < nc; ++j) rank += s_vkeys[j] < ki;
-          if (rank < kcap) s_victims[rank] = (int)(ki & smask);
-        }
+    } else if (in_smem && kcap <= kTour) {
+      const int n = small_k_select(kcap, s_victims);
+      __syncthreads();  // every thread has read the gather count before it is overwritten
+      if (n >= 0) {
         picked = true;
+        if (tid == 0) s_nv = n;
       }
-      __syncthreads();
-      if (tid == 0) s_nv = picked ? min(nc, kcap) : 0;
       __syncthreads();
     }
     if (!picked) {
