@@ -268,8 +268,9 @@ ft_status ft_moe_prefill_chunk(ft_moe* h, int layer, int n_tokens, const void* x
 /* Ablation switch for the prefill double buffer ([FT] "全层双缓冲" measures the loss
  * when the second buffer is off).  on = 1 (default): layer l+1 streams into the other
  * buffer while layer l computes.  on = 0: each layer's weights are copied at the start
- * of its own call and the computation waits for them; residency decisions and outputs
- * are identical either way.  Takes effect at the next prefill call.
+ * of its own call, after all compute enqueued before it (as into a single buffer), and
+ * the computation waits for them; residency decisions and outputs are identical either
+ * way.  Takes effect at the next prefill call.
  * Errors: FT_ERR_INVALID (null handle). */
 ft_status ft_moe_set_prefill_overlap(ft_moe* h, int on);
 

@@ -130,6 +130,7 @@ struct ft_moe {
   std::vector<std::pair<ft_moe*, std::pair<int, int>>> hook_ctx;  // (handle, (layer, batch)), stable
   ft::SlotLayout lay{};
   int S = 0, L = 0, E = 0, K = 0, H = 0, I = 0, kcap = 0;
+  bool logits_early_next = false;  // the next control kernel may read its logits before its wait
   long long bp_mbs = 0, bh_mbs = 0;
   double bp_gbps = 0, bh_gbps = 0;
   HostBank bank[7];
@@ -372,6 +373,8 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
   // compute stream; the memcpy mode hands the fill to the transfer stream and back.
   const bool chain = h->cfg.fill_mode == FT_FILL_KERNEL;
   cp.pdl = chain;
+  cp.logits_early = h->logits_early_next;
+  h->logits_early_next = false;
   cudaEvent_t pa;
   ft_status s;
   if ((s = prof_begin(h, cs, &pa)) != FT_OK) return s;
@@ -840,9 +843,12 @@ ft_status ft_moe_decode_layers(ft_moe* h, int first_layer, int n_layers, int bat
   const size_t H = h->H, E = h->E, K = h->K;
   for (int i = 0; i < n_layers; ++i) {
     const size_t b = (size_t)i * batch;
+    // layers after the first: their logits were written before this call's first kernel
+    h->logits_early_next = i > 0;
     ft_status s = ft_moe_decode_step(
         h, first_layer + i, batch, static_cast<const uint16_t*>(x_bf16) + b * H, logits + b * E,
         c_partial ? c_partial + b * K * H : nullptr, out + b * H, rows_out ? rows_out + b * K * H : nullptr);
+    h->logits_early_next = false;
     if (s != FT_OK) return s;
   }
   return FT_OK;

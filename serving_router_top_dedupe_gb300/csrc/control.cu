@@ -229,9 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   }
   // The logits may be written by the kernel right before this one, so they are read only
   // after the wait; an L2 prefetch of their lines now is safe (the L2 is coherent and a
-  // prefetch returns no data) and takes the DRAM latency off the routing step.
-  for (int i = tid * 32; i < B * E; i += kThreads * 32)
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.logits + i));
+  // prefetch returns no data) and takes the DRAM latency off the routing step.  When they
+  // were complete before the previous kernel started (p.logits_early), each routing warp
+  // loads its token's logits into registers now.
+  const bool early = p.logits_early && B <= kWarps;
+  float zpre[NPL];
+  if (early) {
+    if (warp < B) load_logits_warp<NPL>(p.logits + (size_t)warp * E, E, lane, zpre);
+  } else {
+    for (int i = tid * 32; i < B * E; i += kThreads * 32)
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.logits + i));
+  }
   // logits and the work lists belong to the kernel right before this one
   pdl_wait();
   pdl_trigger();
@@ -240,14 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
 
   // ---- 1. route: one warp per token
   for (int t = warp; t < B; t += kWarps) {
-    route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, p.gate, lane, &s_err, [&](int e, float g, int rank) {
+    auto emit = [&](int e, float g, int rank) {
       const int idx = t * k + rank;
       p.w.sel[idx] = e;
       p.w.gates[idx] = g;
       s_sel[idx] = e;
       atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
       atomicOr(reinterpret_cast<uint32_t*>(&s_tok[e]) + (t >> 5), 1u << (t & 31));  // 32-bit half of the mask
-    });
+    };
+    if (early) route_token_warp_loaded<NPL>(zpre, E, k, p.gate, lane, &s_err, emit);
+    else route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, p.gate, lane, &s_err, emit);
   }
   __syncthreads();
 

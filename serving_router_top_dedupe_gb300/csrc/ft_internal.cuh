@@ -86,6 +86,9 @@ struct CtrlParams {
   size_t slot_stride;
   const uint8_t* shared_w;  // shared expert of this layer, or nullptr
   bool pdl;                 // launched as a programmatic dependent
+  // the logits were complete before the kernel right before this one started (a later layer
+  // of one multi-layer call): they may be read before the dependency wait
+  bool logits_early;
 };
 
 struct FillParams {

@@ -30,11 +30,22 @@ __device__ __forceinline__ float route_key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// This lane's logits of one token: experts lane, lane+32, ... (-inf past E).
+template <int NPL>
+__device__ __forceinline__ void load_logits_warp(const float* z, int E, int lane, float (&raw)[NPL]) {
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int e = lane + 32 * j;
+    raw[j] = e < E ? __ldg(z + e) : -INFINITY;
+  }
+}
+
 // Calls emit(e, gate, rank) once for each of the token's k choices, from the lane that
-// holds expert e; rank is e's position among the k choices in ascending expert id.
+// holds expert e; rank is e's position among the k choices in ascending expert id.  The
+// logits come as this lane's raw values (load_logits_warp).
 template <int NPL, typename F>  // logits held per lane: E <= 32*NPL
-__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int gate, int lane, uint32_t* err,
-                                                 F&& emit) {
+__device__ __forceinline__ void route_token_warp_loaded(const float (&raw)[NPL], int E, int k, int gate, int lane,
+                                                        uint32_t* err, F&& emit) {
   constexpr uint32_t kFull = 0xffffffffu;
   float v[NPL];
   uint32_t key[NPL];
@@ -45,7 +56,7 @@ __device__ __forceinline__ void route_token_warp(const float* z, int E, int k, i
     float x = -INFINITY;
     key[j] = 0u;  // not an expert: below every logit, never chosen (k <= E)
     if (e < E) {
-      x = __ldg(z + e);
+      x = raw[j];
       if (x != x) {
         x = -INFINITY;
         atomicOr(err, FT_DEVERR_NAN_LOGIT);
@@ -109,6 +120,14 @@ __device__ __forceinline__ void route_token_warp(const float* z, int E, int k, i
     if ((taken >> j) & 1u) emit(lane + 32 * j, ex[j] / sum, (int)(below + __popc(b & ((1u << lane) - 1u))));
     below += __popc(b);
   }
+}
+
+template <int NPL, typename F>
+__device__ __forceinline__ void route_token_warp(const float* z, int E, int k, int gate, int lane, uint32_t* err,
+                                                 F&& emit) {
+  float raw[NPL];
+  load_logits_warp<NPL>(z, E, lane, raw);
+  route_token_warp_loaded<NPL>(raw, E, k, gate, lane, err, emit);
 }
 
 // Dispatch on E (the number of logits each lane holds).

@@ -341,6 +341,7 @@ struct PrefillState {
   int first = 0, next_layer = -1, pending = -1;
   cudaEvent_t ev_loaded[2] = {nullptr, nullptr}, ev_free[2] = {nullptr, nullptr}, ev_restore = nullptr;
   cudaEvent_t ev_pick = nullptr;  // the chunk's buffer slots are in buf_dev (the copies read them)
+  cudaEvent_t ev_serial = nullptr;  // second buffer off: this layer's copy waits for all prior compute
   bool free_recorded[2] = {false, false};
   cudaStream_t cs = nullptr, ts = nullptr;
   // what a restore copy needs
@@ -491,6 +492,7 @@ cudaError_t prefill_create(PrefillState** out, const PrefillCtx& c) {
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_restore, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_pick, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_serial, cudaEventDisableTiming);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(layer_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCopySmemReserve);
   if (e == cudaSuccess)
@@ -521,6 +523,7 @@ void prefill_destroy(PrefillState* p) {
   }
   if (p->ev_restore) cudaEventDestroy(p->ev_restore);
   if (p->ev_pick) cudaEventDestroy(p->ev_pick);
+  if (p->ev_serial) cudaEventDestroy(p->ev_serial);
   gemm_maps_destroy(p->maps);
   delete p;
 }
@@ -581,8 +584,14 @@ cudaError_t prefill_layer(PrefillState* p, const PrefillCtx& c, int layer, int T
   }
   const int b = (layer - p->first) & 1;
 
-  // ---- this layer's weights: already streaming (prefetched) or load now
-  if (p->pending != layer && (e = load_buffer(p, layer, b, prof)) != cudaSuccess) return e;
+  // ---- this layer's weights: already streaming (prefetched) or load now.  With the second
+  // buffer off the copy also waits for the previous layer's compute, as a single buffer would.
+  if (p->pending != layer) {
+    if (!c.overlap && ((e = cudaEventRecord(p->ev_serial, c.cs)) != cudaSuccess ||
+                       (e = cudaStreamWaitEvent(c.ts, p->ev_serial, 0)) != cudaSuccess))
+      return e;
+    if ((e = load_buffer(p, layer, b, prof)) != cudaSuccess) return e;
+  }
   p->pending = -1;
   if ((e = cudaStreamWaitEvent(c.cs, p->ev_loaded[b], 0)) != cudaSuccess) return e;
   install_layer_kernel<<<1, 1024, 0, c.cs>>>(layer, E, p->buf_dev + (size_t)b * E, c.res, c.owner, c.stamp, c.st);
