@@ -193,6 +193,8 @@ def _workload():
         w = w.with_(n_layers=nl, n_experts=ne, cache_slots=synth.capacity_slots(frac, nl, ne))
     if _OVERRIDE.get("slots"):
         w = w.with_(cache_slots=_OVERRIDE["slots"])
+    if _OVERRIDE.get("batch"):
+        w = w.with_(batch=_OVERRIDE["batch"])
     return w
 
 
@@ -208,7 +210,8 @@ def _expert_bytes(w) -> int:
 def _config_desc(w, args=None, warm=None) -> dict:
     import synth
 
-    reduced = _OVERRIDE.get("layers") or _OVERRIDE.get("slots") or _OVERRIDE.get("experts")
+    reduced = (_OVERRIDE.get("layers") or _OVERRIDE.get("slots") or _OVERRIDE.get("experts")
+               or _OVERRIDE.get("batch"))
     tag = " (reduced, profiling only)" if reduced else ""
     if w.wtype == synth.W_BF16:
         name = "decode_bf16_35B-A3B-shape" + tag
@@ -618,9 +621,11 @@ def run_ours(args, d: Dist) -> dict | None:
         _release_host(banksf)
         banksf = poolf = None
         gc.collect()
-    prefill = None
+    prefill = prefill_fp8 = None
     if solo and not args.no_prefill:
         prefill = run_prefill(args, d, dev, stream)
+        if not args.no_prefill_fp8:
+            prefill_fp8 = run_prefill(args, d, dev, stream, fp8=True)
 
     out = {"metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": d.world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
@@ -635,7 +640,7 @@ def run_ours(args, d: Dist) -> dict | None:
            "clocks": head["clocks"], "cache": head["cache"], "kernels": head["kernels"],
            "bp_measured_gbps": round(bp_measured, 1), "setup_s": head["setup_s"],
            "decode_configs": {k: {kk: v for kk, v in r.items() if kk not in ("clocks",)} for k, r in extra.items()},
-           "prefill": prefill}
+           "prefill": prefill, "prefill_fp8": prefill_fp8}
     if out["roofline"] is not None:
         out["roofline"]["traffic"] = _traffic("expert_gemv_fused")
     if cpu_baseline is not None:
@@ -644,9 +649,11 @@ def run_ours(args, d: Dist) -> dict | None:
 
 
 # ---------------------------------------------------------------- prefill
-def run_prefill(args, d: Dist, dev, stream) -> dict:
+def run_prefill(args, d: Dist, dev, stream, fp8: bool = False) -> dict:
     """Prefill chunks of the 35B-A3B shape: T = 8192 tokens x 40 layers, 256 experts top-8,
-    uniform router logits, full-layer double buffering from the pinned host pool."""
+    uniform router logits, full-layer double buffering from the pinned host pool.  fp8: the
+    same chunk with E4M3 experts (one FP32 scale per 1x128 block), decoded to BF16 tiles in
+    shared memory for the tensor cores."""
     import gc
 
     import torch
@@ -655,6 +662,8 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
     from serving_router_top_dedupe_gb300 import ftmoe as F
 
     w = synth.prefill()
+    if fp8:
+        w = w.with_(wtype=synth.W_FP8_E4M3_B128)
     if args.prefill_layers or args.prefill_tokens:   # profiling captures only: smaller chunk
         nl = args.prefill_layers or w.n_layers
         w = w.with_(n_layers=nl, prefill_tokens=args.prefill_tokens or w.prefill_tokens,
@@ -662,8 +671,8 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
     L, T, H, E, I, k = w.n_layers, w.prefill_tokens, w.hidden, w.n_experts, w.inter, w.top_k
     pool = synth.ExpertPool(w)
     banks = pool.routed_banks(empty=_host_empty(args))
-    abl_sizes = () if args.no_prefill_ablation else (4096, 8192, 16384)
-    cfg = F.make_config(L, H, I, E, k, False, F.FT_W_BF16, 1, w.cache_slots, w.bp_gbps, w.bh_gbps,
+    abl_sizes = () if args.no_prefill_ablation or fp8 else (4096, 8192, 16384)
+    cfg = F.make_config(L, H, I, E, k, False, w.wtype, 1, w.cache_slots, w.bp_gbps, w.bh_gbps,
                         max_prefill_tokens=max((T,) + abl_sizes), device=d.local, compute_stream=stream.cuda_stream)
     h = F.ft_moe_init(cfg, banks)
     # activations: two distinct layers' x, reused alternately (routing, which sets the work,
@@ -691,6 +700,12 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
         F.ft_moe_get_profile(h, reset=True)
         chunk()
         prof = F.ft_moe_get_profile(h, reset=True)
+        # the same chunk with the second buffer off: each layer's GEMMs run alone on every SM
+        # (no copy kernel beside them)
+        F.ft_moe_set_prefill_overlap(h, False)
+        chunk()
+        prof_alone = F.ft_moe_get_profile(h, reset=True)
+        F.ft_moe_set_prefill_overlap(h, True)
         F.ft_moe_set_profiling(h, 0)
         # ablation: second buffer off (each layer's copy at its own call, compute waits)
         ablation = {}
@@ -726,19 +741,26 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
     gu_ms, dn_ms = prof["prefill_gemm_gate_up"][1], prof["prefill_gemm_down"][1]
     gemm_ms = gu_ms + dn_ms
     copy_n, copy_ms = prof["prefill_copy"]
-    stream_bytes = L * E * 6.0 * I * H                # whole pool streamed per chunk
+    stream_bytes = float(L * E * _expert_bytes(w))   # whole pool streamed per chunk
     try:
         pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
         tc_peak, tc_src = float(pk["bf16_tflops_sustained"]), "measured bf16_tflops_sustained"
     except (OSError, ValueError, KeyError):
         tc_peak, tc_src = 1700.0, "fallback sustained"
     gemm_tflops = L * flop_layer / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    gu_a, dn_a = prof_alone["prefill_gemm_gate_up"][1], prof_alone["prefill_gemm_down"][1]
+    # algorithmic HBM bytes of the two GEMMs per layer: every weight once, the token rows in pair
+    # order read, h written and read back, the BF16 pair rows written
+    P = T * k
+    gemm_bytes = E * float(_expert_bytes(w)) + P * H * 2.0 + P * I * 4.0 + P * H * 2.0
+    alone_tflops = L * flop_layer / ((gu_a + dn_a) * 1e-3) / 1e12 if gu_a + dn_a else None
     bp = F.ft_bench_bw(256 << 20, 8)
     hbm, _ = _peaks()
     bound_s = {"tensor": L * flop_layer / (tc_peak * 1e12), "hbm_weights": stream_bytes / (hbm * 1e9),
                "host_link": stream_bytes / (bp * 1e9)}
     return {"workload": f"prefill_chunk_35B-A3B-shape: T {T} x {L} layers, H 2048, I 512, E 256 top-8, "
-                        "uniform logits, 3788 slots, full-layer double buffer",
+                        "uniform logits, 3788 slots, full-layer double buffer"
+                        + (", FP8 E4M3 experts (1x128 FP32 block scales) decoded to BF16 tiles" if fp8 else ""),
             "value": round(T / chunk_s, 1), "unit": "tok/s", "chunk_s": round(chunk_s, 4),
             "chunks": args.prefill_chunks,
             "grouped_gemm": {"tflops": round(gemm_tflops, 1) if gemm_tflops else None, "peak": tc_peak,
@@ -746,7 +768,17 @@ def run_prefill(args, d: Dist, dev, stream) -> dict:
                              "peak_source": tc_src, "bound": "tensor",
                              "flop_per_layer": flop_layer, "avg_us_per_layer": round(1e3 * gemm_ms / L, 2),
                              "gate_up_tflops": round(L * T * k * 4.0 * I * H / (gu_ms * 1e-3) / 1e12, 1) if gu_ms else None,
-                             "down_tflops": round(L * T * k * 2.0 * I * H / (dn_ms * 1e-3) / 1e12, 1) if dn_ms else None},
+                             "down_tflops": round(L * T * k * 2.0 * I * H / (dn_ms * 1e-3) / 1e12, 1) if dn_ms else None,
+                             "timed_as": "in the double-buffered chunk: 136 SMs, beside the next layer's copy kernel",
+                             "hbm_bytes_per_layer": gemm_bytes,
+                             "hbm_frac": round(gemm_bytes / (hbm * 1e9) / (gemm_ms * 1e-3 / L), 4) if gemm_ms else None},
+            "grouped_gemm_alone": {"tflops": round(alone_tflops, 1) if alone_tflops else None,
+                                   "frac": round(alone_tflops / tc_peak, 4) if alone_tflops else None,
+                                   "gate_up_tflops": round(L * T * k * 4.0 * I * H / (gu_a * 1e-3) / 1e12, 1) if gu_a else None,
+                                   "down_tflops": round(L * T * k * 2.0 * I * H / (dn_a * 1e-3) / 1e12, 1) if dn_a else None,
+                                   "timed_as": "second buffer off: all 152 SMs, no copy beside the GEMMs",
+                                   "hbm_frac": round(gemm_bytes / (hbm * 1e9) / ((gu_a + dn_a) * 1e-3 / L), 4)
+                                   if gu_a + dn_a else None},
             "layer_copy_gbs": round(stream_bytes / (copy_ms * 1e-3) / 1e9, 1) if copy_ms else None,
             "bp_gbps": round(bp, 1),
             "chunk_bound_s": {kk: round(v, 4) for kk, v in bound_s.items()},
@@ -846,6 +878,9 @@ def main():
     ap.add_argument("--fp8-warm", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-chunks", type=int, default=2)
+    ap.add_argument("--no-prefill-fp8", action="store_true", help="skip the FP8-expert prefill chunk")
+    ap.add_argument("--prefill-fp8-only", action="store_true",
+                    help="with --prefill-only: the FP8-expert chunk instead of the BF16 one")
     ap.add_argument("--no-prefill-ablation", action="store_true", help="skip the second-buffer-off chunks")
     ap.add_argument("--prefill-only", action="store_true", help="profiling: run only the prefill measurement")
     ap.add_argument("--prefill-layers", type=int, default=0, help="profiling only: fewer layers")
@@ -853,6 +888,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer MoE layers")
     ap.add_argument("--slots", type=int, default=0, help="profiling only: other cache size")
     ap.add_argument("--experts", type=int, default=0, help="profiling only: fewer routed experts per layer")
+    ap.add_argument("--batch", type=int, default=0, help="profiling only: another batch size")
     ap.add_argument("--fp8-headline", action="store_true",
                     help="profiling only: the FP8 large-expert workload in place of the BF16 one")
     ap.add_argument("--sweep", action="store_true", help="time the batch x capacity x split grid instead")
@@ -862,7 +898,8 @@ def main():
     ap.add_argument("--sweep-batches", default="1,4,16,64")
     ap.add_argument("--oracle-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    _OVERRIDE.update(layers=args.layers, slots=args.slots, experts=args.experts, fp8=args.fp8_headline)
+    _OVERRIDE.update(layers=args.layers, slots=args.slots, experts=args.experts, fp8=args.fp8_headline,
+                     batch=args.batch)
     if args.oracle_child:
         _oracle_child(args)
         return
@@ -883,7 +920,9 @@ def main():
         B.build()
         torch.cuda.set_device(d.local)
         dev = torch.device("cuda", d.local)
-        out = {"metric": METRIC, "prefill": run_prefill(args, d, dev, torch.cuda.Stream(device=dev)),
+        ps = torch.cuda.Stream(device=dev)
+        out = {"metric": METRIC, "prefill": None if args.prefill_fp8_only else run_prefill(args, d, dev, ps),
+               "prefill_fp8": run_prefill(args, d, dev, ps, fp8=True) if args.prefill_fp8_only else None,
                "note": "prefill-only profiling run"}
     else:
         d.init("nccl")

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ int s_gidx[kMaxE];
   __shared__ int s_victims[kMaxE];
   __shared__ int s_cand[kTour];                // LRU candidates taken before the dependency wait
+  __shared__ float s_gate[kMaxPairs];          // gates of the routed pairs
+  __shared__ int s_gent[kMaxE];                // expert (index in the layer) of evaluation entry g
   __shared__ int s_res[kMaxE];                 // res[] of this layer's experts
   __shared__ unsigned long long s_tok[kMaxE];  // tokens routed to each expert of this layer
   __shared__ int s_goff[kMaxE + 1];
@@ -221,18 +223,22 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   // kcap victims; after the wait only the hits are filtered out.  This takes the victim
   // scan off the step's critical path, while the previous layer's evaluation still runs
   // (launched as a programmatic dependent; otherwise nothing runs beside the prologue).
+  // When the logits were complete before the previous kernel started (p.logits_early: a
+  // later layer of one multi-layer call), every decision of the step is taken before the
+  // dependency wait, while the previous layer's evaluation still runs: the residency state
+  // is final (only the previous control kernel writes it), and the decisions write only
+  // that state and shared memory.  The work lists, which the previous fill and evaluation
+  // kernels read, are published after the wait.  Otherwise the logits may be written by
+  // the kernel right before this one, so the decisions follow the wait.
+  const bool early = p.logits_early && B <= kWarps;
   if (tid == 0) s_npre = -1;
-  if (p.pdl && in_smem && 2 * p.kcap <= kTour) {
+  if (!early && p.pdl && in_smem && 2 * p.kcap <= kTour) {
     __syncthreads();  // stamps staged, s_clock set
     const int n = small_k_select(2 * p.kcap, s_cand);
     if (tid == 0) s_npre = n;
   }
-  // The logits may be written by the kernel right before this one, so they are read only
-  // after the wait; an L2 prefetch of their lines now is safe (the L2 is coherent and a
-  // prefetch returns no data) and takes the DRAM latency off the routing step.  When they
-  // were complete before the previous kernel started (p.logits_early), each routing warp
-  // loads its token's logits into registers now.
-  const bool early = p.logits_early && B <= kWarps;
+  // an L2 prefetch of the logits is safe before the wait (the L2 is coherent and a prefetch
+  // returns no data) and takes the DRAM latency off the routing step
   float zpre[NPL];
   if (early) {
     if (warp < B) load_logits_warp<NPL>(p.logits + (size_t)warp * E, E, lane, zpre);
@@ -240,275 +246,299 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     for (int i = tid * 32; i < B * E; i += kThreads * 32)
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.logits + i));
   }
-  // logits and the work lists belong to the kernel right before this one
+
+  auto decide = [&]() {
+    const uint32_t clock = s_clock;
+    // ---- 1. route: one warp per token
+    for (int t = warp; t < B; t += kWarps) {
+      auto emit = [&](int e, float g, int rank) {
+        const int idx = t * k + rank;
+        s_gate[idx] = g;
+        s_sel[idx] = e;
+        atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
+        atomicOr(reinterpret_cast<uint32_t*>(&s_tok[e]) + (t >> 5), 1u << (t & 31));  // 32-bit half of the mask
+      };
+      if (early) route_token_warp_loaded<NPL>(zpre, E, k, p.gate, lane, &s_err, emit);
+      else route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, p.gate, lane, &s_err, emit);
+    }
+    __syncthreads();
+
+    // ---- 2. dedupe + classify (warp 0; A is at most min(B*k, E) ids, ascending)
+    if (warp == 0) {
+      const int nwords = (E + 31) / 32;
+      int nact = 0, nh = 0, nm = 0;
+      for (int c = 0; c < nwords; c += 32) {
+        uint32_t word = c + lane < nwords ? s_bitmap[c + lane] : 0u;
+        const int cnt = __popc(word);
+        int incl = cnt;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int pos = nact + incl - cnt;
+        while (word) {
+          const int b = __ffs(word) - 1;
+          word &= word - 1;
+          s_active[pos++] = base_u + (c + lane) * 32 + b;
+        }
+        nact += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      for (int c = 0; c < nact; c += 32) {
+        const int i = c + lane;
+        const bool valid = i < nact;
+        const int u = valid ? s_active[i] : -1;
+        int slot = valid ? s_res[u - base_u] : -1;
+        if (slot >= S) {  // cannot happen with a consistent table
+          atomicOr(&s_err, FT_DEVERR_BAD_STATE);
+          slot = -1;
+        }
+        const bool hit = valid && slot >= 0;
+        const uint32_t hb = __ballot_sync(0xffffffffu, hit);
+        const uint32_t mb = __ballot_sync(0xffffffffu, valid && !hit);
+        const uint32_t lt = (1u << lane) - 1u;
+        if (hit) {
+          s_hit[nh + __popc(hb & lt)] = u;
+          p.stamp[slot] = clock;  // a hit refreshes recency
+          stv[slot] = clock;
+        } else if (valid) {
+          s_miss[nm + __popc(mb & lt)] = u;
+        }
+        nh += __popc(hb);
+        nm += __popc(mb);
+      }
+      if (lane == 0) {
+        s_nactive = nact;
+        s_nhit = nh;
+        s_nmiss = nm;
+        s_q = split_q(nm, p.bp_mbs, p.bh_mbs, S - nh);
+      }
+    }
+    __syncthreads();
+
+    const int q = s_q;
+    const int kcap = p.kcap;
+    // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
+    if (q > 0) {
+      bool picked = false;
+      if (s_npre >= 0) {
+        // candidates taken before the wait, minus this step's hits (now stamped with clock)
+        if (warp == 0) {
+          const int v = lane < s_npre ? s_cand[lane] : -1;
+          const bool ok = v >= 0 && s_stamp[v] < clock;
+          const uint32_t okb = __ballot_sync(0xffffffffu, ok);
+          const int rank = __popc(okb & ((1u << lane) - 1u));
+          if (ok && rank < kcap) s_victims[rank] = v;
+          if (lane == 0) s_nv = min(__popc(okb), kcap);
+        }
+        picked = true;
+        __syncthreads();
+      } else if (in_smem && kcap <= kTour) {
+        const int n = small_k_select(kcap, s_victims);
+        __syncthreads();  // every thread has read the gather count before it is overwritten
+        if (n >= 0) {
+          picked = true;
+          if (tid == 0) s_nv = n;
+        }
+        __syncthreads();
+      }
+      if (!picked) {
+        // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
+        uint32_t lo = UINT_MAX, hi = 0;
+        int nc = 0;
+        for (int s = tid; s < S; s += kThreads) {
+          const uint32_t st = stv[s];
+          if (st < clock) {
+            lo = min(lo, st);
+            hi = max(hi, st);
+            ++nc;
+          }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+          hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+          nc += __shfl_xor_sync(0xffffffffu, nc, o);
+        }
+        if (lane == 0) {
+          atomicMin(&s_lo, lo);
+          atomicMax(&s_hi, hi);
+          atomicAdd(&s_ncand, nc);
+        }
+        __syncthreads();
+        const uint32_t st_lo = s_lo;
+        const int ncand = s_ncand;
+        const int want = min(kcap, ncand);
+        const uint32_t range = s_hi - st_lo;
+        const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
+        // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
+        unsigned long long thresh = ~0ull;
+        if (want < ncand) {
+          // radix select of the want-th smallest key, most significant digit first.  Digits are
+          // taken from the top of the key's actual width, so the first pass spreads the keys
+          // over all kBins bins (few shared-memory atomics collide).
+          if (tid == 0) {
+            s_prefix = 0;
+            s_kk = want;
+          }
+          for (int hi_bit = width; hi_bit > 0;) {
+            const int shift = hi_bit > kDigit ? hi_bit - kDigit : 0;
+            const int dbits = hi_bit - shift;
+            s_hist[tid] = 0;
+            __syncthreads();
+            const unsigned long long pre = s_prefix;
+            for (int s = tid; s < S; s += kThreads) {
+              const uint32_t st = stv[s];
+              if (st >= clock) continue;
+              const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+              if ((key >> hi_bit) == pre) atomicAdd(&s_hist[(key >> shift) & ((1u << dbits) - 1u)], 1u);
+            }
+            __syncthreads();
+            const uint32_t h = s_hist[tid];
+            const uint32_t kk = (uint32_t)s_kk;
+            uint32_t total;
+            const uint32_t excl = block_excl_scan(h, s_wsum, &total);
+            if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
+              s_prefix = (pre << dbits) | (unsigned long long)tid;
+              s_kk = (int)(kk - excl);
+              s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
+            }
+            __syncthreads();
+            if (s_done || shift == 0) {
+              thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
+              break;
+            }
+            hi_bit = shift;
+          }
+        }
+        // collect the `want` smallest keys (keys are unique), then order them
+        for (int s = tid; s < S; s += kThreads) {
+          const uint32_t st = stv[s];
+          if (st >= clock) continue;
+          const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
+          if (key <= thresh) {
+            const int i = atomicAdd(&s_nv, 1);
+            if (i < kMaxE) s_vkeys[i] = key;
+          }
+        }
+        __syncthreads();
+        const int nv = min(s_nv, want);
+        const unsigned long long smask = (1ull << sbits) - 1ull;
+        for (int i = tid; i < nv; i += kThreads) {
+          const unsigned long long ki = s_vkeys[i];
+          int rank = 0;
+          for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
+          s_victims[rank] = (int)(ki & smask);
+        }
+        __syncthreads();
+        if (tid == 0) s_nv = nv;
+      }
+
+      // ---- 4. install F = first q misses into the first q victims
+      for (int i = tid; i < q; i += kThreads) {
+        const int v = s_victims[i];
+        const int u = s_miss[i];
+        const int old = own_smem ? s_owner[v] : p.owner[v];
+        if (old >= 0) {
+          p.res[old] = -1;
+          atomicAdd(&s_evict, 1);
+        }
+        p.owner[v] = u;
+        p.res[u] = v;
+        s_res[u - base_u] = v;
+        s_fflag[u - base_u] = 1;
+        p.stamp[v] = clock;
+      }
+    }
+    __syncthreads();
+
+    // ---- 5. G = resident part of A (ascending u): evaluation entries and pair offsets
+    if (warp == 0) {
+      const int nact = s_nactive;
+      int ng = 0, carry = 0;
+      for (int c = 0; c < nact; c += 32) {
+        const int i = c + lane;
+        const int e = i < nact ? s_active[i] - base_u : -1;
+        const int slot = e >= 0 ? s_res[e] : -1;
+        const bool in = slot >= 0;
+        const int cnt = in ? __popcll(s_tok[e]) : 0;
+        int incl = cnt;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const int g = ng + __popc(b & ((1u << lane) - 1u));
+          s_gidx[e] = g;
+          s_gent[g] = e;
+          s_goff[g] = carry + incl - cnt;
+        }
+        ng += __popc(b);
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        s_ng = ng;
+        s_goff[ng] = carry;
+      }
+    }
+    __syncthreads();
+  };  // decide
+
+  if (early) {
+    __syncthreads();  // stamps and residency staged, s_clock set
+    decide();
+  }
+  // the work lists belong to the kernels right before this one (and the logits, unless early)
   pdl_wait();
   pdl_trigger();
   __syncthreads();
+  if (!early) decide();
+
+  // ---- publish the step's lists
   const uint32_t clock = s_clock;
-
-  // ---- 1. route: one warp per token
-  for (int t = warp; t < B; t += kWarps) {
-    auto emit = [&](int e, float g, int rank) {
-      const int idx = t * k + rank;
-      p.w.sel[idx] = e;
-      p.w.gates[idx] = g;
-      s_sel[idx] = e;
-      atomicOr(&s_bitmap[e >> 5], 1u << (e & 31));
-      atomicOr(reinterpret_cast<uint32_t*>(&s_tok[e]) + (t >> 5), 1u << (t & 31));  // 32-bit half of the mask
-    };
-    if (early) route_token_warp_loaded<NPL>(zpre, E, k, p.gate, lane, &s_err, emit);
-    else route_token_warp<NPL>(p.logits + (size_t)t * E, E, k, p.gate, lane, &s_err, emit);
-  }
-  __syncthreads();
-
-  // ---- 2. dedupe + classify (warp 0; A is at most min(B*k, E) ids, ascending)
-  if (warp == 0) {
-    const int nwords = (E + 31) / 32;
-    int nact = 0, nh = 0, nm = 0;
-    for (int c = 0; c < nwords; c += 32) {
-      uint32_t word = c + lane < nwords ? s_bitmap[c + lane] : 0u;
-      const int cnt = __popc(word);
-      int incl = cnt;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int pos = nact + incl - cnt;
-      while (word) {
-        const int b = __ffs(word) - 1;
-        word &= word - 1;
-        s_active[pos++] = base_u + (c + lane) * 32 + b;
-      }
-      nact += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    __syncwarp();
-    for (int c = 0; c < nact; c += 32) {
-      const int i = c + lane;
-      const bool valid = i < nact;
-      const int u = valid ? s_active[i] : -1;
-      int slot = valid ? s_res[u - base_u] : -1;
-      if (slot >= S) {  // cannot happen with a consistent table
-        atomicOr(&s_err, FT_DEVERR_BAD_STATE);
-        slot = -1;
-      }
-      const bool hit = valid && slot >= 0;
-      const uint32_t hb = __ballot_sync(0xffffffffu, hit);
-      const uint32_t mb = __ballot_sync(0xffffffffu, valid && !hit);
-      const uint32_t lt = (1u << lane) - 1u;
-      if (hit) {
-        s_hit[nh + __popc(hb & lt)] = u;
-        p.stamp[slot] = clock;  // a hit refreshes recency
-        stv[slot] = clock;
-      } else if (valid) {
-        s_miss[nm + __popc(mb & lt)] = u;
-      }
-      nh += __popc(hb);
-      nm += __popc(mb);
-    }
-    if (lane == 0) {
-      s_nactive = nact;
-      s_nhit = nh;
-      s_nmiss = nm;
-      s_q = split_q(nm, p.bp_mbs, p.bh_mbs, S - nh);
-    }
-  }
-  __syncthreads();
-
   const int q = s_q;
   const int kcap = p.kcap;
-  // ---- 3. one-pass K-LRU victim scan over slots not touched in this step
-  if (q > 0) {
-    bool picked = false;
-    if (s_npre >= 0) {
-      // candidates taken before the wait, minus this step's hits (now stamped with clock)
-      if (warp == 0) {
-        const int v = lane < s_npre ? s_cand[lane] : -1;
-        const bool ok = v >= 0 && s_stamp[v] < clock;
-        const uint32_t okb = __ballot_sync(0xffffffffu, ok);
-        const int rank = __popc(okb & ((1u << lane) - 1u));
-        if (ok && rank < kcap) s_victims[rank] = v;
-        if (lane == 0) s_nv = min(__popc(okb), kcap);
-      }
-      picked = true;
-      __syncthreads();
-    } else if (in_smem && kcap <= kTour) {
-      const int n = small_k_select(kcap, s_victims);
-      __syncthreads();  // every thread has read the gather count before it is overwritten
-      if (n >= 0) {
-        picked = true;
-        if (tid == 0) s_nv = n;
-      }
-      __syncthreads();
-    }
-    if (!picked) {
-      // range of candidate stamps (stamp < clock: hits of this step are excluded) and count
-      uint32_t lo = UINT_MAX, hi = 0;
-      int nc = 0;
-      for (int s = tid; s < S; s += kThreads) {
-        const uint32_t st = stv[s];
-        if (st < clock) {
-          lo = min(lo, st);
-          hi = max(hi, st);
-          ++nc;
-        }
-      }
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        nc += __shfl_xor_sync(0xffffffffu, nc, o);
-      }
-      if (lane == 0) {
-        atomicMin(&s_lo, lo);
-        atomicMax(&s_hi, hi);
-        atomicAdd(&s_ncand, nc);
-      }
-      __syncthreads();
-      const uint32_t st_lo = s_lo;
-      const int ncand = s_ncand;
-      const int want = min(kcap, ncand);
-      const uint32_t range = s_hi - st_lo;
-      const int width = (range ? 32 - __clz(range) : 0) + sbits;  // <= 52 bits
-      // key = (stamp - lowest candidate stamp, slot): unique, ordered like (stamp, slot)
-      unsigned long long thresh = ~0ull;
-      if (want < ncand) {
-        // radix select of the want-th smallest key, most significant digit first.  Digits are
-        // taken from the top of the key's actual width, so the first pass spreads the keys
-        // over all kBins bins (few shared-memory atomics collide).
-        if (tid == 0) {
-          s_prefix = 0;
-          s_kk = want;
-        }
-        for (int hi_bit = width; hi_bit > 0;) {
-          const int shift = hi_bit > kDigit ? hi_bit - kDigit : 0;
-          const int dbits = hi_bit - shift;
-          s_hist[tid] = 0;
-          __syncthreads();
-          const unsigned long long pre = s_prefix;
-          for (int s = tid; s < S; s += kThreads) {
-            const uint32_t st = stv[s];
-            if (st >= clock) continue;
-            const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
-            if ((key >> hi_bit) == pre) atomicAdd(&s_hist[(key >> shift) & ((1u << dbits) - 1u)], 1u);
-          }
-          __syncthreads();
-          const uint32_t h = s_hist[tid];
-          const uint32_t kk = (uint32_t)s_kk;
-          uint32_t total;
-          const uint32_t excl = block_excl_scan(h, s_wsum, &total);
-          if (excl < kk && excl + h >= kk) {  // exactly one thread: the bin holding the kk-th key
-            s_prefix = (pre << dbits) | (unsigned long long)tid;
-            s_kk = (int)(kk - excl);
-            s_done = excl + h == kk;  // every key of the bin is wanted: no finer digit needed
-          }
-          __syncthreads();
-          if (s_done || shift == 0) {
-            thresh = (s_prefix << shift) | ((1ull << shift) - 1ull);
-            break;
-          }
-          hi_bit = shift;
-        }
-      }
-      // collect the `want` smallest keys (keys are unique), then order them
-      for (int s = tid; s < S; s += kThreads) {
-        const uint32_t st = stv[s];
-        if (st >= clock) continue;
-        const unsigned long long key = ((unsigned long long)(st - st_lo) << sbits) | (unsigned)s;
-        if (key <= thresh) {
-          const int i = atomicAdd(&s_nv, 1);
-          if (i < kMaxE) s_vkeys[i] = key;
-        }
-      }
-      __syncthreads();
-      const int nv = min(s_nv, want);
-      const unsigned long long smask = (1ull << sbits) - 1ull;
-      for (int i = tid; i < nv; i += kThreads) {
-        const unsigned long long ki = s_vkeys[i];
-        int rank = 0;
-        for (int j = 0; j < nv; ++j) rank += s_vkeys[j] < ki;
-        s_victims[rank] = (int)(ki & smask);
-      }
-      __syncthreads();
-      if (tid == 0) s_nv = nv;
-    }
-
-    // ---- 4. install F = first q misses into the first q victims
-    for (int i = tid; i < q; i += kThreads) {
-      const int v = s_victims[i];
-      const int u = s_miss[i];
-      const int old = own_smem ? s_owner[v] : p.owner[v];
-      if (old >= 0) {
-        p.res[old] = -1;
-        atomicAdd(&s_evict, 1);
-      }
-      p.owner[v] = u;
-      p.res[u] = v;
-      s_res[u - base_u] = v;
-      s_fflag[u - base_u] = 1;
-      p.stamp[v] = clock;
-      p.w.copy_u[i] = u;
-      p.w.copy_slot[i] = v;
-    }
+  const int ng = s_ng, carry = s_goff[ng];
+  const int npairs = B * k;
+  for (int i = tid; i < npairs; i += kThreads) {
+    p.w.sel[i] = s_sel[i];
+    p.w.gates[i] = s_gate[i];
   }
-  __syncthreads();
-
-  // ---- 5. G = resident part of A (ascending u): evaluation entries and pair offsets
-  if (warp == 0) {
-    const int nact = s_nactive;
-    int ng = 0, carry = 0;
-    for (int c = 0; c < nact; c += 32) {
-      const int i = c + lane;
-      const int e = i < nact ? s_active[i] - base_u : -1;
-      const int slot = e >= 0 ? s_res[e] : -1;
-      const bool in = slot >= 0;
-      const int cnt = in ? __popcll(s_tok[e]) : 0;
-      int incl = cnt;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t b = __ballot_sync(0xffffffffu, in);
-      if (in) {
-        const int g = ng + __popc(b & ((1u << lane) - 1u));
-        s_gidx[e] = g;
-        s_goff[g] = carry + incl - cnt;
-        p.w.g_w[g] = p.pool + (size_t)slot * p.slot_stride;
-        p.w.g_fill[g] = s_fflag[e];
-        p.w.g_off[g] = carry + incl - cnt;
-      }
-      ng += __popc(b);
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      s_ng = ng;
-      s_goff[ng] = carry;
-      p.w.g_off[ng] = carry;
-      int ne = ng;
-      if (p.has_shared) {
-        p.w.g_w[ng] = p.shared_w;
-        p.w.g_fill[ng] = 0;
-        p.w.g_off[ng + 1] = carry + B;
-        ne = ng + 1;
-      }
-      int* cnt = p.w.counts;
-      cnt[C_NACTIVE] = nact;
-      cnt[C_NHIT] = s_nhit;
-      cnt[C_NMISS] = s_nmiss;
-      cnt[C_Q] = q;
-      cnt[C_NVICT] = q > 0 ? s_nv : 0;
-      cnt[C_NG] = ng;
-      cnt[C_NENTRIES] = ne;
-      cnt[C_NGPAIRS] = carry;
-      cnt[C_LAYER] = p.layer;
-      cnt[C_BATCH] = B;
-      cnt[C_CLOCK] = (int)clock;
-      cnt[C_EVICT] = s_evict;
-    }
+  for (int i = tid; i < q; i += kThreads) {
+    p.w.copy_u[i] = s_miss[i];
+    p.w.copy_slot[i] = s_victims[i];
   }
-  __syncthreads();
-
+  for (int g = tid; g < ng; g += kThreads) {
+    const int e = s_gent[g];
+    p.w.g_w[g] = p.pool + (size_t)s_res[e] * p.slot_stride;
+    p.w.g_fill[g] = s_fflag[e];
+    p.w.g_off[g] = s_goff[g];
+  }
+  if (tid == 0) {
+    p.w.g_off[ng] = carry;
+    int ne = ng;
+    if (p.has_shared) {
+      p.w.g_w[ng] = p.shared_w;
+      p.w.g_fill[ng] = 0;
+      p.w.g_off[ng + 1] = carry + B;
+      ne = ng + 1;
+    }
+    int* cnt = p.w.counts;
+    cnt[C_NACTIVE] = s_nactive;
+    cnt[C_NHIT] = s_nhit;
+    cnt[C_NMISS] = s_nmiss;
+    cnt[C_Q] = q;
+    cnt[C_NVICT] = q > 0 ? s_nv : 0;
+    cnt[C_NG] = ng;
+    cnt[C_NENTRIES] = ne;
+    cnt[C_NGPAIRS] = carry;
+    cnt[C_LAYER] = p.layer;
+    cnt[C_BATCH] = B;
+    cnt[C_CLOCK] = (int)clock;
+    cnt[C_EVICT] = s_evict;
+  }
   // rewrite pairs to slots / FT_CPU and place them: within an entry, ascending pair id
   // (= ascending token, since a token routes to an expert at most once)
-  const int npairs = B * k;
   for (int pi = tid; pi < npairs; pi += kThreads) {
     const int e = s_sel[pi];
     const int g = s_gidx[e];
@@ -519,10 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
       p.w.g_pair[s_goff[g] + pos] = pi;
     }
   }
-  if (p.has_shared) {
-    const int base = s_goff[s_ng];
-    for (int t = tid; t < B; t += kThreads) p.w.g_pair[base + t] = t;
-  }
+  if (p.has_shared)
+    for (int t = tid; t < B; t += kThreads) p.w.g_pair[carry + t] = t;
   for (int i = tid; i <= kcap; i += kThreads) p.w.ready[i] = 0u;
   // lists for traces
   for (int i = tid; i < s_nactive; i += kThreads) p.w.active[i] = s_active[i];
@@ -540,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     atomicAdd(&st->cpu_execs, (unsigned long long)(s_nmiss - q));
     atomicAdd(&st->evictions, (unsigned long long)s_evict);
     atomicAdd(&st->decode_steps, 1ull);
-    atomicAdd(&st->eval_entries, (unsigned long long)(s_ng + (p.has_shared ? 1 : 0)));
-    atomicAdd(&st->eval_pairs, (unsigned long long)(s_goff[s_ng] + (p.has_shared ? B : 0)));
+    atomicAdd(&st->eval_entries, (unsigned long long)(ng + (p.has_shared ? 1 : 0)));
+    atomicAdd(&st->eval_pairs, (unsigned long long)(carry + (p.has_shared ? B : 0)));
     if (s_err) atomicOr(&st->error_word, s_err);
   }
 }
