@@ -332,10 +332,12 @@ ft_status alloc_work(ft_moe* h) {
   A(w.rows, npair * h->H);
   A(w.shared_rows, (size_t)B * h->H);
   A(w.blk_count, (size_t)h->H / ft::kRowsPerItem2);
+  A(w.ecopy, (size_t)2 * (2 + 2 * kc));
 #undef A
   w.kmax = kc;
   FT_CUDA(cudaMemset(w.blk_count, 0, sizeof(uint32_t) * (h->H / ft::kRowsPerItem2)));
   FT_CUDA(cudaMemset(w.counts, 0, sizeof(int32_t) * ft::C_NCOUNTS));
+  FT_CUDA(cudaMemset(w.ecopy, 0, sizeof(int32_t) * 2 * (2 + 2 * kc)));  // clock 0: no step
   return FT_OK;
 }
 
@@ -403,6 +405,9 @@ ft_status enqueue_layer(ft_moe* h, int layer, int batch, const void* x, const fl
     fp.lay = h->lay;
     fp.n_banks = h->n_banks;
     fp.pdl = !hooked;  // after the host branch's copies the fill follows a plain dependency
+    fp.ecopy = h->w.ecopy;
+    fp.st = h->st;
+    fp.kmax = h->kcap;
     for (int j = 0; j < h->n_banks; ++j) {
       fp.src[j] = h->bank[j].dev;
       fp.src_row[j] = h->bank[j].row;

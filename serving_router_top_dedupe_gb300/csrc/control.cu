@@ -19,6 +19,7 @@
 #include <climits>
 
 #include "ft_internal.cuh"
+#include "ft_ptx.cuh"
 #include "ft_route.cuh"
 
 namespace ft {
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   __shared__ int s_wcnt[kWarps];
   __shared__ uint32_t s_err, s_clock, s_lo, s_hi;
   __shared__ int s_nactive, s_nhit, s_nmiss, s_q, s_nv, s_ng, s_evict, s_ncand, s_kk, s_done, s_npre;
+  __shared__ int s_free;  // no victim was touched by the previous layer-step (its kernels may still run)
   __shared__ unsigned long long s_prefix;
   extern __shared__ unsigned long long s_dyn[];
   unsigned long long* s_vkeys = s_dyn;                              // [kMaxE]
@@ -145,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
     s_hi = 0;
     s_ncand = 0;
     s_done = 0;
+    s_free = 1;
   }
   const int sbits = S > 1 ? 32 - __clz((unsigned)(S - 1)) : 1;
   // Small K (batch 1-2): the `want` (<= kTour) smallest keys (stamp << sbits | slot) over the
@@ -437,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
       for (int i = tid; i < q; i += kThreads) {
         const int v = s_victims[i];
         const int u = s_miss[i];
+        // the previous layer-step stamped its entries and victims with clock - 1
+        if (stv[v] + 1u >= clock) s_free = 0;
         const int old = own_smem ? s_owner[v] : p.owner[v];
         if (old >= 0) {
           p.res[old] = -1;
@@ -487,10 +492,27 @@ __global__ void __launch_bounds__(kThreads, 1) control_kernel(CtrlParams p) {
   if (early) {
     __syncthreads();  // stamps and residency staged, s_clock set
     decide();
+    // The fill may start now when no victim slot belongs to the previous layer-step, whose
+    // evaluation (and fill) may still read (and write) its slots: the copy list goes out
+    // tagged with the step's clock, released after its entries, and the fill kernel is let
+    // launch.  It still waits for this kernel before it lets the evaluation start.
+    const int q = s_q;
+    if (p.w.ecopy != nullptr && q > 0 && s_free) {
+      const uint32_t clock = s_clock;
+      int32_t* el = p.w.ecopy + (size_t)(clock & 1u) * (2 + 2 * p.w.kmax);
+      for (int i = tid; i < q; i += kThreads) {
+        el[2 + i] = s_miss[i];
+        el[2 + p.w.kmax + i] = s_victims[i];
+      }
+      if (tid == 0) el[1] = q;
+      __syncthreads();
+      if (tid == 0) ptx::st_release_gpu(reinterpret_cast<uint32_t*>(el), clock);
+    }
+    pdl_trigger();
   }
   // the work lists belong to the kernels right before this one (and the logits, unless early)
   pdl_wait();
-  pdl_trigger();
+  if (!early) pdl_trigger();
   __syncthreads();
   if (!early) decide();
 

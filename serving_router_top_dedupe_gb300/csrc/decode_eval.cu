@@ -73,10 +73,46 @@ __device__ __forceinline__ void copy_segment(const uint4* __restrict__ src, uint
   }
 }
 
+// The kernel is launched while the control kernel right before still runs.  When that kernel
+// took its decisions early and none of its victim slots belongs to the previous layer-step,
+// it has released a copy list tagged with this step's clock: the copy starts at once, while
+// warp 0 waits for the control kernel to complete and only then lets the evaluation kernel
+// launch (whose prologue reads the control kernel's lists).  Otherwise every thread waits and
+// the list comes from the published work lists.  Both lists hold the same entries.
 __global__ void __launch_bounds__(kFillThreads) fill_kernel(FillParams p) {
-  pdl_wait();  // the copy list comes from the control kernel right before
-  pdl_trigger();
-  const int q = p.counts[C_Q];
+  __shared__ int s_early;  // 0, or 1 + the parity of the early list
+  if (threadIdx.x == 0) {
+    int e = 0;
+    if (p.pdl && p.ecopy != nullptr) {
+      const uint32_t expect = *reinterpret_cast<const volatile uint32_t*>(&p.st->clock) + 1u;
+      const int32_t* l = p.ecopy + (size_t)(expect & 1u) * (2 + 2 * p.kmax);
+      if (ptx::ld_acquire_gpu(reinterpret_cast<const uint32_t*>(l)) == expect) e = 1 + (int)(expect & 1u);
+    }
+    s_early = e;
+  }
+  __syncthreads();
+  // warp 0 lets the evaluation launch once the control kernel is done; the other warps copy.
+  // The copy's split over threads is the same on both paths, since CTAs of one launch can
+  // take different paths (a CTA that starts after the control kernel published its clock
+  // finds no early list).
+  if (threadIdx.x < 32) {
+    pdl_wait();
+    pdl_trigger();
+    return;
+  }
+  const int early = s_early;
+  const int ct = threadIdx.x - 32, nct = blockDim.x - 32;  // copying threads
+  const int32_t *copy_u = p.copy_u, *copy_slot = p.copy_slot;
+  int q;
+  if (early) {
+    const int32_t* l = p.ecopy + (size_t)(early - 1) * (2 + 2 * p.kmax);
+    q = l[1];
+    copy_u = l + 2;
+    copy_slot = l + 2 + p.kmax;
+  } else {
+    pdl_wait();  // the copy list comes from the control kernel right before
+    q = p.counts[C_Q];
+  }
   if (q <= 0) return;
   const int nseg = q * p.n_banks;
   const int G = gridDim.x;
@@ -96,10 +132,10 @@ __global__ void __launch_bounds__(kFillThreads) fill_kernel(FillParams p) {
       case 5: nbytes = p.src_row[5]; doff = p.lay.ds; sb = p.src[5]; break;
       default: nbytes = p.src_row[6]; doff = p.lay.ts; sb = p.src[6]; break;
     }
-    const int uid = p.copy_u[i];
+    const int uid = copy_u[i];
     const uint4* src = reinterpret_cast<const uint4*>(sb + (size_t)uid * nbytes);
-    uint4* dst = reinterpret_cast<uint4*>(p.pool + (size_t)p.copy_slot[i] * p.lay.stride + doff);
-    copy_segment(src, dst, nbytes / 16, (size_t)part * blockDim.x + threadIdx.x, (size_t)nparts * blockDim.x);
+    uint4* dst = reinterpret_cast<uint4*>(p.pool + (size_t)copy_slot[i] * p.lay.stride + doff);
+    copy_segment(src, dst, nbytes / 16, (size_t)part * nct + ct, (size_t)nparts * nct);
     if (nseg < G) break;  // one segment share per CTA
   }
 }
@@ -395,15 +431,41 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
   }
 }
 
+// The batched kernels loop over their items (item += gridDim.x), so a grid larger than what
+// the SMs hold at once leaves a second, partial wave of CTAs that start only as the first ones
+// finish.  The grid is therefore the CTAs resident at once (occupancy x the SMs the kernel may
+// use, p.n_sm: the fill kernel's SMs are left to it), at most the requested grid.  Occupancy is
+// queried once per kernel instantiation (per_sm, cached by the caller) and shared-memory size.
+template <typename K>
+int resident_grid(K kernel, size_t smem, int n_sm, int grid, int& per_sm, size_t& per_sm_smem) {
+  if (per_sm < 0 || per_sm_smem != smem) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kEvalThreads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      nb = 0;
+    }
+    per_sm = nb;
+    per_sm_smem = smem;
+  }
+  return per_sm > 0 ? std::max(1, std::min(grid, per_sm * n_sm)) : grid;
+}
+
 template <int WT, int SEG, int TG>
 cudaError_t gate_up_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  return launch_k(gate_up_kernel<WT, SEG, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.H * 2, s, p.pdl, p);
+  static int per_sm = -1;
+  static size_t per_sm_smem = 0;
+  const size_t smem = (size_t)TG * p.H * 2;
+  grid = resident_grid(gate_up_kernel<WT, SEG, TG>, smem, p.n_sm, grid, per_sm, per_sm_smem);
+  return launch_k(gate_up_kernel<WT, SEG, TG>, dim3(grid), dim3(kEvalThreads), smem, s, p.pdl, p);
 }
 
 template <int WT, int TG>
 cudaError_t down_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  return launch_k(down_combine_kernel<WT, 4, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.I * 4, s, p.pdl,
-                  p);
+  static int per_sm = -1;
+  static size_t per_sm_smem = 0;
+  const size_t smem = (size_t)TG * p.I * 4;
+  grid = resident_grid(down_combine_kernel<WT, 4, TG>, smem, p.n_sm, grid, per_sm, per_sm_smem);
+  return launch_k(down_combine_kernel<WT, 4, TG>, dim3(grid), dim3(kEvalThreads), smem, s, p.pdl, p);
 }
 
 template <typename F>

@@ -59,6 +59,9 @@ struct DecodeWork {
   float* rows;             // [maxB*k*H] GPU pair rows when the caller gives no rows_out
   float* shared_rows;      // [maxB*H]
   uint32_t* blk_count;     // [H / kRowsPerItem2] combine arrival counters (self-resetting)
+  // Copy list taken before the control kernel's dependency wait, two buffers by the parity of
+  // the step's clock: {clock (written last, release), q, ids[kmax], slots[kmax]}
+  int32_t* ecopy;
   int kmax;                // capacity of the per-expert lists
 };
 
@@ -101,6 +104,9 @@ struct FillParams {
   size_t src_row[7];        // bytes per logical id in each bank
   int n_banks;
   bool pdl;
+  const int32_t* ecopy;     // DecodeWork::ecopy (nullptr: no early start)
+  const DevState* st;       // the step clock: st->clock + 1 while the step's control kernel runs
+  int kmax;
 };
 
 struct EvalParams {
