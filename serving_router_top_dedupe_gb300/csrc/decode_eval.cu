@@ -431,41 +431,15 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
   }
 }
 
-// The batched kernels loop over their items (item += gridDim.x), so a grid larger than what
-// the SMs hold at once leaves a second, partial wave of CTAs that start only as the first ones
-// finish.  The grid is therefore the CTAs resident at once (occupancy x the SMs the kernel may
-// use, p.n_sm: the fill kernel's SMs are left to it), at most the requested grid.  Occupancy is
-// queried once per kernel instantiation (per_sm, cached by the caller) and shared-memory size.
-template <typename K>
-int resident_grid(K kernel, size_t smem, int n_sm, int grid, int& per_sm, size_t& per_sm_smem) {
-  if (per_sm < 0 || per_sm_smem != smem) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kEvalThreads, smem) != cudaSuccess) {
-      cudaGetLastError();
-      nb = 0;
-    }
-    per_sm = nb;
-    per_sm_smem = smem;
-  }
-  return per_sm > 0 ? std::max(1, std::min(grid, per_sm * n_sm)) : grid;
-}
-
 template <int WT, int SEG, int TG>
 cudaError_t gate_up_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  static int per_sm = -1;
-  static size_t per_sm_smem = 0;
-  const size_t smem = (size_t)TG * p.H * 2;
-  grid = resident_grid(gate_up_kernel<WT, SEG, TG>, smem, p.n_sm, grid, per_sm, per_sm_smem);
-  return launch_k(gate_up_kernel<WT, SEG, TG>, dim3(grid), dim3(kEvalThreads), smem, s, p.pdl, p);
+  return launch_k(gate_up_kernel<WT, SEG, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.H * 2, s, p.pdl, p);
 }
 
 template <int WT, int TG>
 cudaError_t down_launch(const EvalParams& p, int grid, cudaStream_t s) {
-  static int per_sm = -1;
-  static size_t per_sm_smem = 0;
-  const size_t smem = (size_t)TG * p.I * 4;
-  grid = resident_grid(down_combine_kernel<WT, 4, TG>, smem, p.n_sm, grid, per_sm, per_sm_smem);
-  return launch_k(down_combine_kernel<WT, 4, TG>, dim3(grid), dim3(kEvalThreads), smem, s, p.pdl, p);
+  return launch_k(down_combine_kernel<WT, 4, TG>, dim3(grid), dim3(kEvalThreads), (size_t)TG * p.I * 4, s, p.pdl,
+                  p);
 }
 
 template <typename F>
