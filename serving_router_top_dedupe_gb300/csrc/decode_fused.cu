@@ -51,6 +51,10 @@ __device__ __forceinline__ float e8m0_float(uint32_t code) { return __uint_as_fl
 constexpr int kConsumers = 8;
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxStages = 8;
+// Ring stage size: 48 KB for BF16 rows (four stages; measured 22.7 against 23.2 us per
+// 35B-shape layer with 32 KB stages), 32 KB for the FP8 / FP4 rows, whose h and activation
+// planes leave less room for the ring.
+constexpr size_t kStageTargetBF16 = 48 * 1024;
 constexpr size_t kStageTarget = 32 * 1024;
 constexpr size_t kSmemBudget = 220 * 1024;  // largest ring
 constexpr int kRowsILP = 4;                 // phase-1 rows a consumer warp forms at once
@@ -85,7 +89,7 @@ __host__ __device__ inline FusedPlan make_fused_plan(int wtype, int H, int I, in
   pl.sbh = carry ? sh : 0;
   pl.sbi = carry ? si : 0;
   const size_t ph = rh + pl.sbh, pi = ri + pl.sbi;  // ring bytes per H row / per I row
-  pl.stage = kStageTarget;
+  pl.stage = wtype == FT_W_BF16 ? kStageTargetBF16 : kStageTarget;
   if (pl.stage < 2 * ph) pl.stage = 2 * ph;
   if (pl.stage < pi) pl.stage = pi;
   pl.pairs = (int)(pl.stage / (2 * ph));
