@@ -15,10 +15,12 @@
  *    the fill count q, finds the K least recently used victims in one pass and
  *    rewrites routed ids to slots or FT_CPU ([FT] "Device-side 缓存控制").
  *  - q = round(m * B_P / B_H), at least one fill when m > 0 ([FT] "q* 策略").
- *    The F set is copied host->slots on the transfer stream; the C set's
- *    gate-weighted rows are an INPUT (c_partial): no host executor lives here.
- *  - G = H u F is evaluated by SwiGLU GEMV kernels (BF16, or FP8 E4M3 with one
- *    FP32 scale per 1x128 block applied after the block's dot product, [P3] §4.2),
+ *    The F set is copied host->slots by a copy kernel (or, in FT_FILL_MEMCPY mode, by
+ *    copies on the transfer stream); the C set's gate-weighted rows are an INPUT
+ *    (c_partial): no host executor lives here.
+ *  - G = H u F is evaluated by SwiGLU GEMV kernels (BF16; FP8 E4M3 with one FP32
+ *    scale per 1x128 block applied after the block's dot product, [P3] §4.2; NVFP4
+ *    and MXFP4),
  *    then a combine sums, per token, the shared expert and the k pair rows in
  *    ascending expert id (fixed order), so outputs do not depend on cache size or
  *    on the F/C split ([FT] "q* 策略").
@@ -76,9 +78,12 @@ typedef enum {
 typedef enum { FT_W_BF16 = 0, FT_W_FP8_E4M3_B128 = 1, FT_W_NVFP4 = 2, FT_W_MXFP4 = 3 } ft_wtype;
 
 /* How a decode step moves F-set experts from the host pool into their slots.
- * FT_FILL_KERNEL: one fixed-shape copy kernel on the transfer stream reads the
- *   device-resident copy list and pulls bytes from the mapped host pool; the
- *   whole step can be captured into a CUDA graph.
+ * FT_FILL_KERNEL: one fixed-shape copy kernel on the compute stream, between the
+ *   control kernel and the evaluation, reads the device-resident copy list and pulls
+ *   bytes from the mapped host pool (16 CTAs of SM loads); the whole step can be
+ *   captured into a CUDA graph.  In a multi-layer call the copy can start while the
+ *   previous layer's evaluation still runs, when none of its victim slots belongs to
+ *   the previous layer-step.
  * FT_FILL_MEMCPY: the host waits for the control kernel, reads the copy list and
  *   issues one cudaMemcpyAsync per bank per filled expert on the transfer stream.
  *   One host synchronisation per layer; not capturable. */
@@ -226,7 +231,11 @@ ft_status ft_moe_decode_step(ft_moe* h, int layer, int batch, const void* x_bf16
 /* n_layers consecutive decode layer-steps (layers first_layer .. first_layer+n-1,
  * one token batch), with per-layer inputs packed layer-major:
  * x [n][batch][H], logits [n][batch][E], c_partial [n][batch][k][H], out [n][batch][H],
- * rows_out [n][batch][k][H] or NULL.  Same semantics as n calls of ft_moe_decode_step. */
+ * rows_out [n][batch][k][H] or NULL.  Same results as n calls of ft_moe_decode_step.
+ * Every layer's logits are an input of the call, complete in stream order before it (a
+ * kernel enqueued earlier on the compute stream may write them): the control kernel of a
+ * layer after the first takes its routing and cache decisions from them before its
+ * dependency wait, while the previous layer is still evaluated. */
 ft_status ft_moe_decode_layers(ft_moe* h, int first_layer, int n_layers, int batch, const void* x_bf16,
                                const float* logits, const float* c_partial, float* out, float* rows_out);
 
