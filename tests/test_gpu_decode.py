@@ -94,6 +94,46 @@ def test_outputs_identical_across_capacity_and_split():
             assert r.sim.cnt.cpu_execs > 0
 
 
+@pytest.mark.parametrize("batch,slots", [(1, 20), (1, 60), (4, 40)])
+def test_multilayer_call_matches_per_layer_calls(batch, slots):
+    """ft_moe_decode_layers takes the decisions of every layer after the first before the
+    control kernel's dependency wait, and starts a fill early when no victim slot belongs to
+    the previous layer-step; per-layer ft_moe_decode_step calls take them after the wait.
+    Outputs and the residency state must agree bit for bit, with caches small enough that
+    victims often belong to the previous layer-step (the fill then takes its ordinary path)."""
+    w = synth.decode_bf16(batch=batch).with_(n_layers=5, n_experts=64, steps=8, cache_slots=slots)
+    tr = synth.routing_trace(w)
+    pool = synth.ExpertPool(w)
+    banks, shared = pool.routed_banks(), pool.shared_banks()
+    L, B, H, E, k = w.n_layers, w.batch, w.hidden, w.n_experts, w.top_k
+    dev = torch.device("cuda:0")
+    x = torch.empty((L, B, H), dtype=torch.int16, device=dev)
+    z = torch.empty((L, B, E), dtype=torch.float32, device=dev)
+    cp = torch.zeros((L, B, k, H), dtype=torch.float32, device=dev)
+    out_m = torch.empty((L, B, H), dtype=torch.float32, device=dev)
+    out_s = torch.empty_like(out_m)
+    with Run(w, banks, shared) as rm, Run(w, banks, shared) as rs:
+        F = rm.F
+        g = F.ft_moe_graph_capture_decode(rm.h, 0, L, B, x, z, cp, out_m)
+        for s in range(w.steps):
+            for l in range(L):
+                xb, zz = rm.inputs(s, l, tr)
+                x[l].copy_(torch.from_numpy(xb.view(np.int16)))
+                z[l].copy_(torch.from_numpy(zz))
+            F.ft_graph_launch(g)
+            F.ft_moe_synchronize(rm.h)
+            for l in range(L):
+                F.ft_moe_decode_step(rs.h, l, B, x[l], z[l], cp[l], out_s[l])
+            F.ft_moe_synchronize(rs.h)
+            assert torch.equal(out_m, out_s), f"token {s}"
+        sm = F.ft_moe_get_state(rm.h, w.n_logical, w.cache_slots)
+        ss = F.ft_moe_get_state(rs.h, w.n_logical, w.cache_slots)
+        for key in ("res", "owner", "stamp"):
+            assert np.array_equal(sm[key], ss[key]), key
+        assert F.ft_moe_get_stats(rm.h).error_word == 0 and F.ft_moe_get_stats(rs.h).error_word == 0
+        assert F.ft_moe_get_stats(rm.h).fills > 0
+
+
 def test_graph_replay_matches_eager():
     w = synth.decode_bf16(batch=2).with_(n_layers=4, n_experts=64, steps=6, cache_slots=60)
     tr = synth.routing_trace(w)
