@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
   const uint64_t pol = ptx::l2_evict_first();
   pdl_trigger();
   __shared__ int s_last;
+  __shared__ uint8_t s_gpu_pair[kMaxPairs];  // combine: pair evaluated on the GPU (else host row)
   const int ne = p.counts[C_NENTRIES];
   const int I = p.I, H = p.H, k = p.k, B = p.B;
   constexpr int R2 = 8 * RPW;
@@ -461,18 +462,26 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
     __syncthreads();
     if (s_last) {
       __threadfence();
+      // which pairs run on the GPU, read once; then per output the k rows' loads are issued
+      // together (L2 loads of the other CTAs' rows) and summed in the fixed order: the shared
+      // row, then r ascending
+      for (int i = threadIdx.x; i < B * k; i += blockDim.x) s_gpu_pair[i] = p.slot_of_pair[i] >= 0;
+      __syncthreads();
       for (int idx = threadIdx.x; idx < B * R2; idx += blockDim.x) {
         const int t = idx / R2, j = rb * R2 + (idx - t * R2);
-        float o = p.has_shared ? ld_cg_f32(p.shared_rows + (size_t)t * H + j) : 0.f;
+        float o = p.has_shared ? __ldcg(p.shared_rows + (size_t)t * H + j) : 0.f;
+#pragma unroll 4
         for (int r = 0; r < k; ++r) {
           const int pr = t * k + r;
-          if (p.slot_of_pair[pr] >= 0) {
-            o += ld_cg_f32(p.rows + (size_t)pr * H + j);
+          float v = 0.f;
+          if (s_gpu_pair[pr]) {
+            v = __ldcg(p.rows + (size_t)pr * H + j);
           } else if (p.c_partial) {
-            o += p.c_partial[(size_t)pr * H + j];
+            v = p.c_partial[(size_t)pr * H + j];
           } else if (j == 0) {
             atomicOr(p.error_word, FT_DEVERR_CAPACITY);
           }
+          o += v;
         }
         p.out[(size_t)t * H + j] = o;
       }
