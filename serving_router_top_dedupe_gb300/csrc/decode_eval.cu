@@ -360,31 +360,50 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
     const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
     const bool shared_entry = p.has_shared && g == ne - 1;
     const int j0 = rb * R2 + warp * RPW;
+    constexpr int SEG = WT == FT_W_BF16 ? 2 : 4;
+    // BF16 rows of one K segment (I <= 512) are loaded once per item, before h is staged:
+    // their HBM latency then overlaps the staging, and every token chunk reuses them
+    const bool early_w = WT == FT_W_BF16 && row_chunks <= 32 * SEG;
+    uint4 wv[RPW][SEG];
+    if (early_w) {
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int s = 0; s < SEG; ++s) {
+          const int c = s * 32 + lane;
+          if (c < row_chunks)
+            wv[r][s] = ld_stream(W + p.lay.down + (size_t)(j0 + r) * row_chunks * 16 + (size_t)c * 16, pol);
+        }
+    }
     for (int t0 = 0; t0 < np; t0 += TG) {
       const int nt = min(TG, np - t0);
+      // lane tt holds the chunk's pair tt and its gate, loaded while h is staged
+      int my_pr = 0;
+      if (lane < nt) my_pr = p.g_pair[p0 + t0 + lane];
       __syncthreads();
       for (int idx = threadIdx.x; idx < nt * (I / 4); idx += blockDim.x) {
         const int tt = idx / (I / 4), c4 = idx - tt * (I / 4);
         *reinterpret_cast<float4*>(hs + (size_t)tt * I + c4 * 4) =
             *reinterpret_cast<const float4*>(p.h + (size_t)(p0 + t0 + tt) * I + c4 * 4);
       }
+      const float my_gate = lane < nt && !shared_entry ? p.gates[my_pr] : 0.f;
       __syncthreads();
       float acc[RPW][TG];
 #pragma unroll
       for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int tt = 0; tt < TG; ++tt) acc[r][tt] = 0.f;
-      constexpr int SEG = WT == FT_W_BF16 ? 2 : 4;
       for (int c0 = 0; c0 < row_chunks; c0 += 32 * SEG) {
-        uint4 wv[RPW][SEG];
+        if (!early_w) {
 #pragma unroll
-        for (int r = 0; r < RPW; ++r)
+          for (int r = 0; r < RPW; ++r)
 #pragma unroll
-          for (int s = 0; s < SEG; ++s) {
-            const int c = c0 + s * 32 + lane;
-            if (c < row_chunks)
-              wv[r][s] = ld_stream(W + p.lay.down + (size_t)(j0 + r) * row_chunks * 16 + (size_t)c * 16, pol);
-          }
+            for (int s = 0; s < SEG; ++s) {
+              const int c = c0 + s * 32 + lane;
+              if (c < row_chunks)
+                wv[r][s] = ld_stream(W + p.lay.down + (size_t)(j0 + r) * row_chunks * 16 + (size_t)c * 16, pol);
+            }
+        }
 #pragma unroll
         for (int s = 0; s < SEG; ++s) {
           const int c = c0 + s * 32 + lane;
@@ -445,10 +464,11 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
         for (int tt = 0; tt < TG; ++tt) {
           const float y = WT == FT_W_NVFP4 ? warp_sum(acc[r][tt]) * tsd
                                            : (WT == FT_W_FP8_E4M3_B128 ? groups_sum(acc[r][tt]) : warp_sum(acc[r][tt]));
+          const int pr = __shfl_sync(0xffffffffu, my_pr, tt);
+          const float gate = __shfl_sync(0xffffffffu, my_gate, tt);
           if (lane == 0 && tt < nt) {
-            const int pr = p.g_pair[p0 + t0 + tt];
             if (shared_entry) p.shared_rows[(size_t)pr * H + j0 + r] = y;
-            else p.rows[(size_t)pr * H + j0 + r] = p.gates[pr] * y;
+            else p.rows[(size_t)pr * H + j0 + r] = gate * y;
           }
         }
     }
