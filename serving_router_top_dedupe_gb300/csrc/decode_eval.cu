@@ -355,7 +355,10 @@ __global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p
   float* hs = reinterpret_cast<float*>(smem);  // [TG][I]
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int g = item / nrb, rb = item - g * nrb;
+    // entries in the order ne-1, 0, 1, ..: the shared expert, which takes all B tokens and so
+    // the longest items, goes first instead of forming the tail
+    const int gi = item / nrb, rb = item - gi * nrb;
+    const int g = gi == 0 ? ne - 1 : gi - 1;
     const uint8_t* W = p.g_w[g];
     const int p0 = p.g_off[g], np = p.g_off[g + 1] - p0;
     const bool shared_entry = p.has_shared && g == ne - 1;
