@@ -642,7 +642,9 @@ def run_ours(args, d: Dist) -> dict | None:
            "decode_configs": {k: {kk: v for kk, v in r.items() if kk not in ("clocks",)} for k, r in extra.items()},
            "prefill": prefill, "prefill_fp8": prefill_fp8}
     if out["roofline"] is not None:
-        out["roofline"]["traffic"] = _traffic("expert_gemv_fused")
+        # ncu DRAM bytes are recorded for the batch-1 GEMV only
+        fused = "expert_gemv_fused" in head["kernels"]["mixed"]
+        out["roofline"]["traffic"] = _traffic("expert_gemv_fused") if fused else None
     if cpu_baseline is not None:
         out["cpu_baseline"] = cpu_baseline
     return out

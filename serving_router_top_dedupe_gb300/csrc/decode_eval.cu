@@ -336,7 +336,9 @@ __global__ void __launch_bounds__(kEvalThreads) gate_up_kernel(EvalParams p) {
 // here: 514 against 416 us at batch 64, 136 against 129 at batch 16, with one combine arrival
 // per chunk.)
 template <int WT, int RPW, int TG>
-__global__ void __launch_bounds__(kEvalThreads) down_combine_kernel(EvalParams p) {
+// BF16: registers capped for three CTAs per SM (80, no spill; the uncapped build took 116 and
+// two CTAs: batch 16 down 122 -> 117 us); the FP8 / FP4 forms keep two CTAs per SM
+__global__ void __launch_bounds__(kEvalThreads, WT == FT_W_BF16 ? 3 : 2) down_combine_kernel(EvalParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_wait();
   const uint64_t pol = ptx::l2_evict_first();
