@@ -252,7 +252,14 @@ ft_status ft_moe_decode_layers_host(ft_moe* h, int first_layer, int n_layers, in
 ft_status ft_moe_graph_capture_decode(ft_moe* h, int first_layer, int n_layers, int batch,
                                       const void* x_bf16, const float* logits, const float* c_partial,
                                       float* out, float* rows_out, ft_graph** g);
-ft_status ft_graph_launch(ft_graph* g);  /* enqueue one replay on the compute stream */
+/* Enqueue one replay on the handle's compute stream (no host synchronisation).  A prefill
+ * chunk in progress on the handle is ended first (the next prefill call starts a new
+ * chunk).  Errors: FT_ERR_INVALID (null graph),
+ * FT_ERR_STATE (the handle was destroyed, or resized after the capture: capture again),
+ * FT_ERR_CUDA (the launch failed). */
+ft_status ft_graph_launch(ft_graph* g);
+/* Free a captured graph (NULL is a no-op).  Replays already enqueued are not waited for:
+ * CUDA keeps an executing graph alive until it completes.  Always returns FT_OK. */
 ft_status ft_graph_destroy(ft_graph* g);
 
 /* One prefill layer of a chunk ([FT] "全层双缓冲"): a call that does not continue
@@ -346,7 +353,8 @@ ft_status ft_split_misses(int m, double bp_gbps, double bh_gbps, int evictable, 
  * [FT] "q* 策略", "ft bench bw").  Allocates and frees its own buffers; synchronises. */
 ft_status ft_bench_bw(size_t bytes, int iters, double* bp_gbps);
 
-/* Counters, error word, clock.  Synchronises the library's streams. */
+/* Counters, error word, clock.  Synchronises the library's streams.  Errors: FT_ERR_INVALID
+ * (null handle or out), FT_ERR_CUDA (a CUDA call failed, e.g. after a device fault). */
 ft_status ft_moe_get_stats(ft_moe* h, ft_stats* out);
 
 /* Clear the device error word (after a reported FT_DEVERR_* condition has been handled);
@@ -389,13 +397,19 @@ ft_status ft_moe_get_state(ft_moe* h, int32_t* res, int32_t* owner, uint32_t* st
 ft_status ft_moe_set_profiling(ft_moe* h, int enable);
 ft_status ft_moe_get_profile(ft_moe* h, ft_profile* out, int reset);
 
-/* Replace the compute stream (e.g. to follow a framework's current stream). */
+/* Replace the compute stream (e.g. to follow a framework's current stream): waits for the
+ * handle's work, then uses compute_stream (caller-owned, must outlive its use) or, for
+ * NULL, a new library-owned stream.  Graphs captured before are replayed on the new
+ * stream.  Errors: FT_ERR_INVALID (null handle), FT_ERR_CUDA. */
 ft_status ft_moe_set_stream(ft_moe* h, void* compute_stream);
 
-/* Wait for all work the handle has enqueued. */
+/* Wait for all work the handle has enqueued (transfer stream, then compute stream).
+ * Errors: FT_ERR_INVALID (null handle), FT_ERR_CUDA (an enqueued kernel or copy failed). */
 ft_status ft_moe_synchronize(ft_moe* h);
 
-/* Release device memory, streams and host registrations.  Synchronises. */
+/* Release device memory, streams and host registrations (NULL is a no-op).  Synchronises.
+ * Graphs captured on the handle stay valid objects but can no longer be launched
+ * (FT_ERR_STATE); free them with ft_graph_destroy.  Always returns FT_OK. */
 ft_status ft_moe_destroy(ft_moe* h);
 
 /* Allocation-free layer evaluation.  The pages have no counterpart: this entry point is
