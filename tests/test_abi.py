@@ -122,3 +122,21 @@ def test_null_handle_calls_fail_cleanly(F):
     with pytest.raises(F.FtError):
         F.ft_moe_get_stats(None)
     F.ft_moe_destroy(None)
+
+
+def test_binding_without_the_library_fails_loudly(tmp_path):
+    """The binding has no fallback: a copy of the package without the built library
+    raises at import."""
+    import shutil
+    import subprocess
+    import sys
+
+    pkg = tmp_path / "serving_router_top_dedupe_gb300"
+    pkg.mkdir()
+    for fn in ("__init__.py", "ftmoe.py"):
+        shutil.copy(os.path.join(ROOT, "serving_router_top_dedupe_gb300", fn), pkg / fn)
+    r = subprocess.run([sys.executable, "-c", "import serving_router_top_dedupe_gb300.ftmoe"], cwd=tmp_path,
+                       capture_output=True, text=True, timeout=120,
+                       env={**os.environ, "PYTHONPATH": str(tmp_path)})
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libftmoe.so is missing" in r.stderr
